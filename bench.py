@@ -1,0 +1,429 @@
+#!/usr/bin/env python
+"""Throughput of the routed-expert MoE layer (libmoe) on GB300.
+
+Default workload: single-token decode of the guide's layer (H 4096, I 2048,
+256 MXFP4 experts, top-6 sqrt-softplus router, w_scale 1.5): every step is
+one T = 1 layer call (route + permute + quantise + gate/up + down + combine)
+on a fresh token with fresh logits, so the experts touched vary and the
+3.4 GB expert set is far larger than L2.  --config 2/3/4 time the batched
+decode, pp512 and 8192-token prefill workloads instead.
+
+One JSON line on rank 0.  Under torchrun every rank runs an independent
+replica on its own GPU (no collective in the layer); the time is the max over
+ranks and `value` counts the tokens of all ranks.
+
+--impl reference times the fp64 CPU oracle on the host cores on the same
+workload (time-bounded; rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "routed-MoE layer tokens/s"
+UNIT = "tokens/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=None)
+    ap.add_argument("--warmup", type=int, default=None)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
+    ap.add_argument("--path", choices=["auto", "cc", "tc"], default="auto")
+    ap.add_argument("--graph-chunk", type=int, default=256, help="steps per CUDA graph")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    return ap.parse_args()
+
+
+def default_steps(cfg):
+    # long enough (~1 s) for the clock samples to fall inside the timed region
+    return {1: 32768, 2: 1024, 3: 256, 4: 32}[cfg.index]
+
+
+def config_json(cfg, args, world):
+    return {"workload": cfg.name, "hidden": cfg.H, "inter": cfg.I, "experts": cfg.E,
+            "top_k": cfg.k, "tokens_per_step": cfg.T, "router": cfg.router,
+            "shared_expert": cfg.shared, "weights": "MXFP4 e2m1 + UE8M0 /32",
+            "activations": "MXFP8 e4m3 + UE8M0 /32", "gemm_path": args.path,
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+            "l2": "inputs larger than L2 (3.4 GB expert set; fresh tokens each step)"}
+
+
+def algorithmic_bytes(cfg, touched, rows):
+    """Bytes one layer call must move at least: the touched experts' MXFP4
+    weights (payload + scales) and the activation rows in and out."""
+    H, I = cfg.H, cfg.I
+    w_gu = 2 * (I * H // 2 + I * H // 32)
+    w_dn = H * I // 2 + H * I // 32
+    act_gu = rows * (H + H // 32) + rows * (I + I // 32)
+    act_dn = rows * (I + I // 32) + rows * H * 4
+    return {"gateup": touched * w_gu + act_gu, "down": touched * w_dn + act_dn}
+
+
+# ------------------------------------------------------------------ clocks --
+def gpu_uuid(dev):
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(dev).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid):
+        self.uuid = uuid
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is not None:
+            self.p.terminate()
+            try:
+                self.p.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.p.kill()
+        self.f.flush()
+        self.f.seek(0)
+        rows = []
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) != 10:
+                continue
+            if self.uuid and parts[1] != self.uuid:
+                continue
+            rows.append(parts)
+        os.unlink(self.f.name)
+        return rows
+
+    @staticmethod
+    def summary(rows):
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        sm = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in rows if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": float(np.median(sm)) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons, "samples": len(rows)}
+
+
+# --------------------------------------------------------------- our path --
+def run_ours(args, cfg, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    import block_quantized_expert_gb300 as bqe
+    from workloads import make_hash_table, make_tokens, make_weights
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=dev)
+    K = args.steps if args.steps is not None else default_steps(cfg)
+    W = args.warmup if args.warmup is not None else (64 if cfg.T == 1 else 3)
+    W = max(W, 3)
+
+    w = make_weights(cfg)
+    dw = {n: torch.from_numpy(np.ascontiguousarray(getattr(w, n))).to(dev)
+          for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
+                    "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")
+          if getattr(w, n) is not None}
+    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, cfg.T, cfg.shared, cfg.w_scale)
+    layer = bqe.moe_create(mc, dw)
+    del dw
+    bqe.moe_set_gemm_path(layer, {"auto": 0, "cc": 1, "tc": 2}[args.path])
+
+    # distinct inputs: one token per step for decode, else a few batches cycled
+    S = (K + W) if cfg.T == 1 else min(K + W, 4)
+    tk = make_tokens(cfg, seed=cfg.default_seed + 7919 * rank, n=S * cfg.T)
+    x_all = torch.from_numpy(tk.x_bits.view(np.int16).reshape(S, cfg.T, cfg.H).copy()).to(dev)
+    lg_all = torch.from_numpy(tk.logits.reshape(S, cfg.T, cfg.E).copy()).to(dev)
+    hashed = cfg.router == "hash"
+    if hashed:
+        tab = torch.from_numpy(make_hash_table(cfg)).to(dev)
+        tok_all = torch.from_numpy(tk.token_ids.reshape(S, cfg.T).copy()).to(dev)
+    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+    wt = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+    out = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device=dev)
+
+    def step(i):
+        j = i % S
+        if hashed:
+            bqe.moe_route_hash(layer, tok_all[j], tab, ids, wt)
+        else:
+            bqe.moe_route(layer, lg_all[j], ids, wt)
+        bqe.moe_forward(layer, x_all[j], ids, wt, out)
+
+    # experts touched per input batch (for the algorithmic byte count)
+    touched, rows = [], cfg.T * cfg.k
+    for j in range(min(S, 64)):
+        step(j)
+        touched.append(len(np.unique(ids.cpu().numpy())))
+    avg_touched = float(np.mean(touched))
+    for i in range(W):
+        step(i)
+    bqe.moe_check(layer)
+
+    # the timed region: K steps as chunked CUDA graphs; stage events on every
+    # ev_every-th step
+    stream = torch.cuda.Stream(device=dev)
+    ev_every = max(1, K // 256)
+    stage_events = []
+    graphs = []
+    launches0 = bqe.moe_kernel_launches(layer)
+    with torch.cuda.stream(stream):
+        for c0 in range(0, K, args.graph_chunk):
+            g = torch.cuda.CUDAGraph()
+            evs_chunk = []
+            for i in range(c0, min(K, c0 + args.graph_chunk)):
+                if i % ev_every == 0:
+                    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
+                    for e in evs:
+                        e.record(stream)
+                    evs_chunk.append(evs)
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                n_ev = 0
+                for i in range(c0, min(K, c0 + args.graph_chunk)):
+                    if i % ev_every == 0:
+                        bqe.moe_set_stage_events(layer, evs_chunk[n_ev])
+                        n_ev += 1
+                    step(W + i)
+            graphs.append(g)
+            stage_events.extend(evs_chunk)
+    launches = bqe.moe_kernel_launches(layer) - launches0   # kernels per replay of all graphs
+    for g in graphs[:2]:
+        g.replay()
+    torch.cuda.synchronize()
+
+    sampler = ClockSampler(gpu_uuid(dev))
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for g in graphs:
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    clk_rows = sampler.stop()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tm = torch.tensor([ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    bqe.moe_check(layer)
+
+    # per-stage device times from the sampled steps
+    names = ["permute", "quantize", "gateup", "down", "combine"]
+    st = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(5)] for evs in stage_events])
+    stage_ms = dict(zip(names, st.mean(0).tolist()))
+    byts = algorithmic_bytes(cfg, avg_touched, rows)
+    dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
+    achieved = byts[dom] / (stage_ms[dom] * 1e-3) / 1e9
+    peaks = {}
+    try:
+        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        pass
+    peak = peaks.get("hbm_gbs", 6800.0)
+    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+
+    tokens = K * cfg.T
+    value = world * tokens / (ms * 1e-3)
+    # rows in the timed region within the clock sampling
+    in_region = [r for r in clk_rows if _ts_in(r[0], wall0, wall1)]
+    clocks = ClockSampler.summary(in_region if in_region else clk_rows)
+    clocks["window"] = "timed region" if in_region else "around the timed region"
+
+    res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+           "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
+           "scaling": "weak", "vs_baseline": None,
+           "dtype": "mxfp4 x mxfp8 -> f32 accumulate", "data": "synthetic (seeded)",
+           "config": config_json(cfg, args, world),
+           "gpu_launches": int(launches),
+           "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
+           "experts_touched_per_step": avg_touched,
+           "roofline": {"bound": "hbm", "kernel": f"{dom} GEMM", "achieved": round(achieved, 1),
+                        "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
+                        "traffic": None, "algorithmic_bytes_per_launch": int(byts[dom]),
+                        "peak_source": peak_src,
+                        "hbm_frac_whole_step": round(
+                            (byts["gateup"] + byts["down"]) / (ms / K * 1e-3) / 1e9 / peak, 4)},
+           "clocks": clocks}
+
+    if not args.no_e2e:
+        res["e2e"] = run_e2e(args, cfg, layer, tk, S, K, W, world, dev)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(cfg, w, tk, args.cpu_seconds)
+    layer.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return res
+
+
+def _ts_in(ts, a, b):
+    try:
+        t = time.mktime(time.strptime(ts.split(".")[0], "%Y/%m/%d %H:%M:%S"))
+        return a - 1.0 <= t <= b + 1.0
+    except Exception:
+        return False
+
+
+def run_e2e(args, cfg, layer, tk, S, K, W, world, dev):
+    """Same steps through moe_forward_host: each step copies its x and logits
+    from page-locked host memory and reads the layer output back."""
+    import torch
+    import torch.distributed as dist
+
+    import block_quantized_expert_gb300 as bqe
+
+    if cfg.router == "hash":
+        return {"value": None, "unit": UNIT, "note": "host entry covers the learned router only"}
+    xh = torch.from_numpy(tk.x_bits.view(np.int16).reshape(S, cfg.T, cfg.H).copy()).pin_memory()
+    lh = torch.from_numpy(tk.logits.reshape(S, cfg.T, cfg.E).copy()).pin_memory()
+    oh = torch.empty((cfg.T, cfg.H), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.Stream(device=dev)
+    graphs = []
+    with torch.cuda.stream(stream):
+        for i in range(W):
+            bqe.moe_forward_host(layer, xh[i % S], lh[i % S], oh)
+        stream.synchronize()
+        for c0 in range(0, K, args.graph_chunk):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(c0, min(K, c0 + args.graph_chunk)):
+                    j = (W + i) % S
+                    bqe.moe_forward_host(layer, xh[j], lh[j], oh)
+            graphs.append(g)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for g in graphs:
+            g.replay()
+        t1.record(stream)
+    torch.cuda.synchronize()
+    ms = t0.elapsed_time(t1)
+    if world > 1:
+        tm = torch.tensor([ms], device=dev)
+        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+        ms = float(tm.item())
+    return {"value": round(world * K * cfg.T / (ms * 1e-3), 1), "unit": UNIT,
+            "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
+            "d2h_bytes_per_step": cfg.T * cfg.H * 4,
+            "path": "moe_forward_host (pinned host in/out, CUDA graphs)"}
+
+
+# ------------------------------------------------------------- CPU oracle --
+def oracle_rate(cfg, w, tk, seconds):
+    """Tokens/s of the fp64 oracle (route + layer) on the host cores, on a
+    sample sized to about `seconds` of work."""
+    from oracle import oracle as orc
+
+    for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
+        np.asarray(getattr(w, n)).sum()   # page the weights in before timing
+    T = cfg.T
+    n_all = tk.logits.shape[0]
+
+    def run(n):
+        tok = min(n, n_all)
+        lg, xb = tk.logits[:tok], tk.x_bits[:tok]
+        t = time.perf_counter()
+        ids, wt = orc.route_learned(lg, cfg.k, cfg.w_scale)
+        orc.layer_forward(w, xb, ids, wt)
+        return tok, time.perf_counter() - t
+
+    n0, t0 = run(min(4, n_all))
+    per = t0 / n0
+    n = int(max(4, min(n_all, seconds / max(per, 1e-9))))
+    n, t = run(n)
+    return n, t, orc.max_threads(), T
+
+
+def cpu_baseline(cfg, w, tk, seconds):
+    n, t, cores, T = oracle_rate(cfg, w, tk, seconds)
+    return {"value": round(n / t, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
+            "sample": f"{n} tokens of the {cfg.name} workload (tokens are independent; "
+                      f"route + layer per token), {t:.1f} s"}
+
+
+def run_reference(args, cfg, rank, world):
+    if rank != 0:
+        return None
+    from workloads import make_tokens, make_weights
+
+    K = args.steps if args.steps is not None else default_steps(cfg)
+    W = args.warmup if args.warmup is not None else 3
+    w = make_weights(cfg)
+    tk = make_tokens(cfg, n=min(cfg.T * (K + W), 4096) if cfg.T == 1 else cfg.T)
+    budget = 60.0
+    n, t, cores, T = oracle_rate(cfg, w, tk, budget)
+    value = n / t
+    steps_done = max(1, n // cfg.T)
+    res = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+           "steps": steps_done, "warmup": 1, "ms_per_step": 1e3 * t / steps_done,
+           "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+           "data": "synthetic (seeded)", "config": config_json(cfg, args, world),
+           "impl": "reference",
+           "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
+                            "kind": "oracle",
+                            "sample": f"{n} tokens ({steps_done} of {K} steps, time-bounded "
+                                      f"~{budget:.0f} s) of the {cfg.name} workload"},
+           "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                   "d2h_bytes_per_step": 0}}
+    return res
+
+
+def main():
+    args = parse()
+    from workloads import CONFIGS
+
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    local_rank = int(os.environ.get("LOCAL_RANK", 0))
+    cfg = CONFIGS[args.config]
+    if args.impl == "reference":
+        res = run_reference(args, cfg, rank, world)
+    else:
+        res = run_ours(args, cfg, rank, world, local_rank)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+
+
+if __name__ == "__main__":
+    main()

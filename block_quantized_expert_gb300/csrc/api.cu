@@ -1,0 +1,364 @@
+// api.cu -- the C ABI of libmoe (include/moe.h): argument checks, the layer
+// object and its workspace, and the sequence of kernels of one layer call.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <new>
+
+#include "common.cuh"
+#include "layer.h"
+
+namespace {
+
+thread_local char g_tls_error[256] = "";
+
+moe_status fail(moe_layer* L, moe_status st, const char* fmt, ...) {
+    char* buf = L ? L->last_error : g_tls_error;
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, 256, fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+moe_status cuda_fail(moe_layer* L, cudaError_t e, const char* what) {
+    return fail(L, MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+size_t round_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+struct Sizes {
+    size_t R, Rp, Tpad;
+};
+
+Sizes sizes_of(const moe_config& c) {
+    Sizes z;
+    z.R = (size_t)c.max_tokens * c.top_k;
+    size_t nz = z.R < (size_t)c.n_experts ? z.R : (size_t)c.n_experts;
+    z.Rp = round_up(z.R + nz * (moe::kRowTile - 1), moe::kRowTile);
+    z.Tpad = round_up((size_t)c.max_tokens, moe::kRowTile);
+    return z;
+}
+
+const char* check_config(const moe_config* c) {
+    if (!c) return "config is NULL";
+    if (c->hidden <= 0 || c->hidden % 128) return "hidden must be a positive multiple of 128";
+    if (c->inter <= 0 || c->inter % 128) return "inter must be a positive multiple of 128";
+    if (c->n_experts < 1 || c->n_experts > moe::kMaxExperts) return "n_experts must be in [1, 1024]";
+    if (c->top_k < 1 || c->top_k > moe::kMaxTopK || c->top_k > c->n_experts)
+        return "top_k must be in [1, min(n_experts, 8)]";
+    if (c->max_tokens < 1 || (long long)c->max_tokens * c->top_k > (1LL << 30))
+        return "max_tokens out of range";
+    if (c->hidden > 8192 || c->inter > 8192) return "hidden/inter larger than 8192";
+    if (!std::isfinite(c->w_scale)) return "w_scale must be finite";
+    return nullptr;
+}
+
+// Workspace byte count: every device buffer moe_create allocates besides the
+// weight copies.
+size_t workspace_bytes(const moe_config& c) {
+    Sizes z = sizes_of(c);
+    const size_t H = c.hidden, I = c.inter, E = c.n_experts, T = c.max_tokens, k = c.top_k;
+    size_t b = 0;
+    b += 5 * (E + 1) * 4;                        // counts, offsets, poff, tile_scan, chunk_scan
+    b += 3 * z.R * 4 + z.Rp * 4 + 8 * 4;         // row_src, row_dst, row_pos, pos_row, sh_desc
+    b += z.Rp * H + z.Rp * H / 32;               // xq, xs
+    b += z.Rp * I + z.Rp * I / 32;               // hq, hs
+    b += z.R * H * 4;                            // y
+    if (c.has_shared) {
+        b += z.Tpad * H + z.Tpad * H / 32 + z.Tpad * I + z.Tpad * I / 32 + T * H * 4;
+    }
+    b += T * H * 2 + T * E * 4 + T * H * 4 + 2 * T * k * 4;  // staging
+    b += 256;                                    // error word
+    return b;
+}
+
+template <typename P>
+cudaError_t dalloc(P** p, size_t bytes, size_t* total) {
+    *total += bytes;
+    return cudaMalloc((void**)p, bytes ? bytes : 1);
+}
+
+void free_all(moe_layer* L) {
+    void* ptrs[] = {L->gate_q, L->gate_s, L->up_q, L->up_s, L->down_q, L->down_s,
+                    L->sh_gate_q, L->sh_gate_s, L->sh_up_q, L->sh_up_s, L->sh_down_q, L->sh_down_s,
+                    L->gate_sf, L->up_sf, L->down_sf, L->sh_gate_sf, L->sh_up_sf, L->sh_down_sf,
+                    L->counts, L->offsets, L->poff, L->tile_scan, L->chunk_scan, L->row_src,
+                    L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->xq, L->xs, L->xq_tok,
+                    L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
+                    L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err};
+    for (void* p : ptrs)
+        if (p) cudaFree(p);
+    moe::tc_free(L);
+}
+
+moe_status check_T(moe_layer* L, int T) {
+    if (T < 1 || T > L->cfg.max_tokens)
+        return fail(L, MOE_ERR_INVALID_ARG, "T=%d outside [1, max_tokens=%d]", T, L->cfg.max_tokens);
+    return MOE_OK;
+}
+
+// The GEMM steps (gate/up + SwiGLU + requant, down; routed and shared);
+// `mid` (if set) is recorded after the routed gate/up launch.
+cudaError_t run_gemms(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {
+    if (L->gemm_path == 1 || L->tc == nullptr) return moe::launch_gemm_cc(L, T, s, mid);
+    return moe::launch_gemm_tc(L, T, s, mid);
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t moe_workspace_bytes(const moe_config* cfg) {
+    if (check_config(cfg)) return 0;
+    return workspace_bytes(*cfg);
+}
+
+const char* moe_last_error(const moe_layer* layer) {
+    return layer ? layer->last_error : g_tls_error;
+}
+
+moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t stream,
+                      moe_layer** out) {
+    if (!out) return fail(nullptr, MOE_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    if (const char* why = check_config(cfg)) return fail(nullptr, MOE_ERR_INVALID_ARG, "%s", why);
+    if (!w) return fail(nullptr, MOE_ERR_INVALID_ARG, "weights is NULL");
+    if (!w->gate_q || !w->gate_s || !w->up_q || !w->up_s || !w->down_q || !w->down_s)
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "a routed-expert weight pointer is NULL");
+    if (cfg->has_shared && (!w->sh_gate_q || !w->sh_gate_s || !w->sh_up_q || !w->sh_up_s ||
+                            !w->sh_down_q || !w->sh_down_s))
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "has_shared set but a shared weight pointer is NULL");
+
+    moe_layer* L = new (std::nothrow) moe_layer;
+    if (!L) return fail(nullptr, MOE_ERR_OOM, "host allocation failed");
+    std::memset(L, 0, sizeof(*L));
+    L->cfg = *cfg;
+    L->cfg.has_shared = cfg->has_shared ? 1 : 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    cudaError_t e = cudaGetDevice(&L->device);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&L->num_sms, cudaDevAttrMultiProcessorCount, L->device);
+    if (e != cudaSuccess) {
+        moe_status st = cuda_fail(nullptr, e, "device query");
+        delete L;
+        return st;
+    }
+    const moe_config& c = L->cfg;
+    const size_t H = c.hidden, I = c.inter, E = c.n_experts, T = c.max_tokens, k = c.top_k;
+    Sizes z = sizes_of(c);
+    L->R_max = (int)z.R;
+    L->Rp_max = (int)z.Rp;
+    size_t total = 0;
+    const size_t gq = E * I * H / 2, gs = E * I * H / 32, dq = E * H * I / 2, ds = E * H * I / 32;
+    cudaError_t a = cudaSuccess;
+    auto A = [&](auto** p, size_t bytes) { if (a == cudaSuccess) a = dalloc(p, bytes, &total); };
+    A(&L->gate_q, gq); A(&L->gate_s, gs); A(&L->up_q, gq); A(&L->up_s, gs);
+    A(&L->down_q, dq); A(&L->down_s, ds);
+    A(&L->gate_sf, gs); A(&L->up_sf, gs); A(&L->down_sf, ds);
+    if (c.has_shared) {
+        A(&L->sh_gate_q, I * H); A(&L->sh_gate_s, (I / 128) * (H / 128));
+        A(&L->sh_up_q, I * H); A(&L->sh_up_s, (I / 128) * (H / 128));
+        A(&L->sh_down_q, H * I); A(&L->sh_down_s, (H / 128) * (I / 128));
+        A(&L->sh_gate_sf, I * H / 32); A(&L->sh_up_sf, I * H / 32); A(&L->sh_down_sf, H * I / 32);
+    }
+    A(&L->counts, E * 4); A(&L->offsets, (E + 1) * 4); A(&L->poff, (E + 1) * 4);
+    A(&L->tile_scan, (E + 1) * 4); A(&L->chunk_scan, (E + 1) * 4);
+    A(&L->row_src, z.R * 4); A(&L->row_dst, z.R * 4); A(&L->row_pos, z.R * 4);
+    A(&L->pos_row, z.Rp * 4); A(&L->sh_desc, 8 * 4);
+    A(&L->xq, z.Rp * H); A(&L->xs, z.Rp * H / 32);
+    A(&L->hq, z.Rp * I); A(&L->hs, z.Rp * I / 32);
+    A(&L->y, z.R * H * 4);
+    if (c.has_shared) {
+        A(&L->xq_tok, z.Tpad * H); A(&L->xs_tok, z.Tpad * H / 32);
+        A(&L->hq_sh, z.Tpad * I); A(&L->hs_sh, z.Tpad * I / 32);
+        A(&L->y_sh, T * H * 4);
+    }
+    A(&L->x_stage, T * H * 2); A(&L->logits_stage, T * E * 4); A(&L->out_stage, T * H * 4);
+    A(&L->ids_stage, T * k * 4); A(&L->w_stage, T * k * 4);
+    A(&L->d_err, 256);
+    if (a != cudaSuccess) {
+        cudaGetLastError();
+        free_all(L);
+        delete L;
+        return fail(nullptr, MOE_ERR_OOM, "device allocation of %zu bytes failed: %s", total,
+                    cudaGetErrorString(a));
+    }
+    // weights: copy, then repack the block scales for the tensor-core kernels
+    auto C = [&](void* dst, const void* src, size_t n) {
+        if (a == cudaSuccess) a = cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, s);
+    };
+    C(L->gate_q, w->gate_q, gq); C(L->gate_s, w->gate_s, gs);
+    C(L->up_q, w->up_q, gq); C(L->up_s, w->up_s, gs);
+    C(L->down_q, w->down_q, dq); C(L->down_s, w->down_s, ds);
+    if (c.has_shared) {
+        C(L->sh_gate_q, w->sh_gate_q, I * H); C(L->sh_gate_s, w->sh_gate_s, (I / 128) * (H / 128));
+        C(L->sh_up_q, w->sh_up_q, I * H); C(L->sh_up_s, w->sh_up_s, (I / 128) * (H / 128));
+        C(L->sh_down_q, w->sh_down_q, H * I); C(L->sh_down_s, w->sh_down_s, (H / 128) * (I / 128));
+    }
+    if (a == cudaSuccess) a = moe::repack_sf(L->gate_s, L->gate_sf, (int)E, (int)I, (int)H, s);
+    if (a == cudaSuccess) a = moe::repack_sf(L->up_s, L->up_sf, (int)E, (int)I, (int)H, s);
+    if (a == cudaSuccess) a = moe::repack_sf(L->down_s, L->down_sf, (int)E, (int)H, (int)I, s);
+    if (c.has_shared) {
+        if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_gate_s, L->sh_gate_sf, (int)I, (int)H, s);
+        if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_up_s, L->sh_up_sf, (int)I, (int)H, s);
+        if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_down_s, L->sh_down_sf, (int)H, (int)I, s);
+    }
+    // a defined workspace: padding rows of the activation buffers read as zero
+    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row};
+    size_t zn[] = {z.Rp * H, z.Rp * H / 32, z.Rp * I, z.Rp * I / 32, 256, z.Rp * 4};
+    for (int i = 0; i < 6 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
+    if (c.has_shared) {
+        void* zs[] = {L->xq_tok, L->xs_tok, L->hq_sh, L->hs_sh};
+        size_t zsn[] = {z.Tpad * H, z.Tpad * H / 32, z.Tpad * I, z.Tpad * I / 32};
+        for (int i = 0; i < 4 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zs[i], 0, zsn[i], s);
+    }
+    if (a == cudaSuccess) a = cudaStreamSynchronize(s);
+    if (a == cudaSuccess) a = moe::kernels_init();
+    if (a == cudaSuccess) a = moe::cc_init();
+    if (a == cudaSuccess) a = moe::tc_init(L);
+    if (a != cudaSuccess) {
+        moe_status st = cuda_fail(nullptr, a, "moe_create");
+        cudaGetLastError();
+        free_all(L);
+        delete L;
+        return st;
+    }
+    L->gemm_path = 0;
+    *out = L;
+    return MOE_OK;
+}
+
+moe_status moe_destroy(moe_layer* layer) {
+    if (!layer) return MOE_OK;
+    free_all(layer);
+    delete layer;
+    return MOE_OK;
+}
+
+moe_status moe_set_stage_events(moe_layer* L, void* const* events, int n) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!events) { L->stage_ev_set = 0; return MOE_OK; }
+    if (n != 6) return fail(L, MOE_ERR_INVALID_ARG, "n must be 6");
+    for (int i = 0; i < 6; ++i) {
+        if (!events[i]) return fail(L, MOE_ERR_INVALID_ARG, "event %d is NULL", i);
+        L->stage_ev[i] = (cudaEvent_t)events[i];
+    }
+    L->stage_ev_set = 1;
+    return MOE_OK;
+}
+
+unsigned long long moe_kernel_launches(const moe_layer* L) { return L ? L->launches : 0ull; }
+
+moe_status moe_set_gemm_path(moe_layer* L, int path) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (path < 0 || path > 2) return fail(L, MOE_ERR_INVALID_ARG, "path must be 0, 1 or 2");
+    if (path == 2 && !L->tc) return fail(L, MOE_ERR_UNSUPPORTED, "tensor-core path unavailable");
+    L->gemm_path = path;
+    return MOE_OK;
+}
+
+moe_status moe_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,
+                     moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!logits || !ids || !w) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaError_t e = moe::launch_route(L, logits, T, ids, w, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_route");
+}
+
+moe_status moe_route_hash(moe_layer* L, const int32_t* token_ids, const int32_t* tid2eid, int V,
+                          int T, int32_t* ids, float* w, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!token_ids || !tid2eid || !ids || !w) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (V <= 0) return fail(L, MOE_ERR_INVALID_ARG, "V must be positive");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaError_t e = moe::launch_route_hash(L, token_ids, tid2eid, V, T, ids, w, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_route_hash");
+}
+
+moe_status moe_permute(moe_layer* L, const int32_t* ids, int T, int32_t* offsets, int32_t* row_src,
+                       int32_t* row_dst, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!ids || !offsets || !row_src || !row_dst) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaError_t e = moe::launch_permute(L, ids, T, offsets, row_src, row_dst, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_permute");
+}
+
+moe_status moe_quantize(moe_layer* L, const uint16_t* x, int T, uint8_t* q, uint8_t* s,
+                        moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!x || !q || !s) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(x, 16) || !aligned(q, 8))
+        return fail(L, MOE_ERR_INVALID_ARG, "x must be 16-byte and q 8-byte aligned");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaError_t e = moe::launch_quantize_canonical(L, x, T, q, s, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_quantize");
+}
+
+moe_status moe_forward(moe_layer* L, const uint16_t* x, int T, const int32_t* ids, const float* w,
+                       float* out, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!x || !ids || !w || !out) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(x, 16) || !aligned(out, 16))
+        return fail(L, MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const bool ev = L->stage_ev_set != 0;
+    L->stage_ev_set = 0;
+    auto mark = [&](int i, cudaError_t e) {
+        return (ev && e == cudaSuccess) ? cudaEventRecord(L->stage_ev[i], s) : e;
+    };
+    cudaError_t e = mark(0, cudaSuccess);
+    if (e == cudaSuccess) e = mark(1, moe::launch_permute(L, ids, T, L->offsets, L->row_src, L->row_dst, s));
+    if (e == cudaSuccess) e = mark(2, moe::launch_quantize_scatter(L, x, T, s));
+    if (e == cudaSuccess) e = run_gemms(L, T, s, ev ? L->stage_ev[3] : nullptr);
+    if (e == cudaSuccess) e = mark(4, cudaSuccess);
+    if (e == cudaSuccess) e = mark(5, moe::launch_combine(L, ids, w, T, out, s));
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward");
+}
+
+moe_status moe_forward_host(moe_layer* L, const uint16_t* x, const float* logits, int T,
+                            float* out, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!x || !logits || !out) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaStream_t s = (cudaStream_t)stream;
+    const size_t H = L->cfg.hidden, E = L->cfg.n_experts;
+    cudaError_t e = cudaMemcpyAsync(L->x_stage, x, (size_t)T * H * 2, cudaMemcpyHostToDevice, s);
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(L->logits_stage, logits, (size_t)T * E * 4, cudaMemcpyHostToDevice, s);
+    if (e != cudaSuccess) return cuda_fail(L, e, "moe_forward_host: input copy");
+    moe_status st = moe_route(L, L->logits_stage, T, L->ids_stage, L->w_stage, stream);
+    if (st == MOE_OK) st = moe_forward(L, L->x_stage, T, L->ids_stage, L->w_stage, L->out_stage, stream);
+    if (st != MOE_OK) return st;
+    e = cudaMemcpyAsync(out, L->out_stage, (size_t)T * H * 4, cudaMemcpyDeviceToHost, s);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward_host: output copy");
+}
+
+moe_status moe_hidden(moe_layer* L, int T, uint8_t* hq, uint8_t* hs, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!hq || !hs) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (moe_status st = check_T(L, T)) return st;
+    cudaError_t e = moe::launch_hidden_gather(L, T, hq, hs, (cudaStream_t)stream);
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_hidden");
+}
+
+moe_status moe_check(moe_layer* L, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    cudaError_t e = cudaStreamSynchronize((cudaStream_t)stream);
+    uint32_t flags = 0;
+    if (e == cudaSuccess) e = cudaMemcpy(&flags, L->d_err, 4, cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess && flags) e = cudaMemset(L->d_err, 0, 4);
+    if (e != cudaSuccess) return cuda_fail(L, e, "moe_check");
+    if (flags & moe::ERR_TIMEOUT)
+        return fail(L, MOE_ERR_TIMEOUT, "a device-side wait ran out of iterations");
+    if (flags & moe::ERR_BAD_ID)
+        return fail(L, MOE_ERR_INVALID_ARG, "an expert or token id was out of range");
+    return MOE_OK;
+}
+
+}  // extern "C"

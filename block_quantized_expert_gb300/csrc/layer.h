@@ -1,0 +1,93 @@
+// layer.h -- the moe_layer object behind the C ABI and the launchers of its
+// kernels.  Everything here is library-internal.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/moe.h"
+
+struct moe_layer {
+    moe_config cfg;
+    int device;
+    int num_sms;
+    int gemm_path;  // 0 auto, 1 CUDA cores, 2 tcgen05
+
+    // -------- weights (library-owned copies, canonical layout) --------
+    uint8_t *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
+    uint8_t *sh_gate_q, *sh_gate_s, *sh_up_q, *sh_up_s, *sh_down_q, *sh_down_s;
+    // block scales repacked into 512-byte atoms for the tensor-core kernels
+    uint8_t *gate_sf, *up_sf, *down_sf;          // [E][rows/128][K/128][512]
+    uint8_t *sh_gate_sf, *sh_up_sf, *sh_down_sf;  // [rows/128][K/128][512]
+
+    // -------- workspace (sized by max_tokens) --------
+    int R_max;        // max_tokens * k
+    int Rp_max;       // padded permuted rows (segments start at multiples of 128)
+    int32_t* counts;      // [E]   rows per expert
+    int32_t* offsets;     // [E+1] unpadded segment starts
+    int32_t* poff;        // [E+1] padded segment starts (multiples of 128)
+    int32_t* tile_scan;   // [E+1] 128-row tiles before expert e
+    int32_t* chunk_scan;  // [E+1] CUDA-core token chunks before expert e
+    int32_t* row_src;     // [R]
+    int32_t* row_dst;     // [R]
+    int32_t* row_pos;     // [R]  padded position of row r (-1 if dropped)
+    int32_t* pos_row;     // [Rp] row at padded position p (-1 = padding)
+    int32_t* sh_desc;     // shared-expert segment: counts[1], poff[2], tiles[2], chunks[2]
+    uint8_t* xq;          // [Rp][H]   MXFP8 codes of x, permuted rows
+    uint8_t* xs;          // atoms of [Rp][H/32]
+    uint8_t* xq_tok;      // [T][H]    MXFP8 codes of x, token order (shared expert)
+    uint8_t* xs_tok;      // atoms of [T_pad][H/32]
+    uint8_t* hq;          // [Rp][I]   MXFP8 codes of h
+    uint8_t* hs;          // atoms
+    uint8_t* hq_sh;       // [T_pad][I] shared expert h
+    uint8_t* hs_sh;
+    float* y;             // [R][H]   down output of row r (unweighted)
+    float* y_sh;          // [T][H]   shared expert output
+    uint16_t* x_stage;    // [T][H]   moe_forward_host staging
+    float* logits_stage;  // [T][E]
+    float* out_stage;     // [T][H]
+    int32_t* ids_stage;   // [T][k]
+    float* w_stage;       // [T][k]
+    uint32_t* d_err;      // sticky device error flags
+
+    void* tc;             // tensor-core kernel state (tensor maps), or null
+    unsigned long long launches;  // kernels enqueued so far
+    cudaEvent_t stage_ev[6];  // one-shot stage events for the next forward
+    int stage_ev_set;
+
+    char last_error[256];
+};
+
+namespace moe {
+
+constexpr int kChunk = 4;  // tokens per CUDA-core GEMM work item
+
+// Launchers; each returns the launch error (cudaSuccess on success).
+cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,
+                         cudaStream_t s);
+cudaError_t launch_route_hash(moe_layer* L, const int32_t* tok, const int32_t* tab, int V,
+                              int T, int32_t* ids, float* w, cudaStream_t s);
+// Counting sort into the given outputs plus the layer's padded bookkeeping.
+cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* offsets,
+                           int32_t* row_src, int32_t* row_dst, cudaStream_t s);
+cudaError_t launch_quantize_canonical(moe_layer* L, const uint16_t* x, int T, uint8_t* q,
+                                      uint8_t* sc, cudaStream_t s);
+cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cudaStream_t s);
+cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int T,
+                           float* out, cudaStream_t s);
+cudaError_t launch_hidden_gather(moe_layer* L, int T, uint8_t* hq, uint8_t* hs,
+                                 cudaStream_t s);
+cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid);
+cudaError_t kernels_init();
+cudaError_t cc_init();
+
+// Tensor-core path.
+cudaError_t tc_init(moe_layer* L);
+void tc_free(moe_layer* L);
+cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid);
+cudaError_t repack_sf(const uint8_t* src, uint8_t* dst, int mats, int rows, int K,
+                      cudaStream_t s);
+cudaError_t expand_tile_sf(const uint8_t* src, uint8_t* dst, int rows, int K, cudaStream_t s);
+
+}  // namespace moe

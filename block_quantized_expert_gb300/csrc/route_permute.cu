@@ -1,0 +1,478 @@
+// route_permute.cu -- the integer and element-wise steps of the layer:
+// learned and hash routing, the token -> expert counting sort, MXFP8
+// quantisation of activations (scattered into the permuted row space), the
+// fixed-order combine, and the one-time block-scale repack of the weights.
+#include <climits>
+#include <cmath>
+
+#include "common.cuh"
+#include "layer.h"
+
+namespace moe {
+
+// ------------------------------------------------------------------ route --
+// One warp per token.  The top-k by score s = sqrt(softplus(logit)) is the
+// top-k by logit (s is strictly increasing), so the selection compares the
+// fp32 logits exactly: k warp-wide argmax passes, equal values to the lower
+// expert index (guide, section 1: SQRT_SOFTPLUS gating, top-k).  The k
+// selected scores and the weights w_j = w_scale * s_j / sum s (guide,
+// section 3.2) are evaluated in fp64 and rounded once to fp32.
+__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
+                                               int k, float w_scale, int32_t* __restrict__ ids,
+                                               float* __restrict__ w, uint32_t* err) {
+    const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    const float* row = logits + (size_t)t * E;
+    uint32_t taken = 0;  // bit i <-> expert lane + 32 i
+    int sel[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        sel[j] = -1;
+        if (j < k) {
+            float best = -INFINITY;
+            int bi = INT_MAX;
+            for (int i = 0, e = lane; e < E; ++i, e += 32) {
+                if ((taken >> i) & 1u) continue;
+                float v = __ldg(row + e);
+                if (v > best || (v == best && e < bi)) { best = v; bi = e; }
+            }
+#pragma unroll
+            for (int o = 16; o; o >>= 1) {
+                float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+                int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+                if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+            }
+            if (bi < E) {
+                sel[j] = bi;
+                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+            }
+        }
+    }
+    if (lane == 0) {
+        double s[kMaxTopK], sum = 0.0;
+        bool ok = true;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k) {
+                if (sel[j] < 0) { ok = false; s[j] = 0.0; continue; }
+                double l = (double)row[sel[j]];
+                s[j] = sqrt((l > 0.0 ? l : 0.0) + log1p(exp(-fabs(l))));
+                sum += s[j];
+            }
+        }
+        if (!ok) raise_flag(err, ERR_BAD_ID);
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j < k) {
+                ids[(size_t)t * k + j] = sel[j];
+                w[(size_t)t * k + j] = ok ? (float)((double)w_scale * s[j] / sum) : 0.0f;
+            }
+        }
+    }
+}
+
+cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,
+                         cudaStream_t s) {
+    const int warps_per_block = 8;
+    dim3 grid((T + warps_per_block - 1) / warps_per_block);
+    k_route<<<grid, 32 * warps_per_block, 0, s>>>(logits, T, L->cfg.n_experts, L->cfg.top_k,
+                                                  L->cfg.w_scale, ids, w, L->d_err);
+    L->launches += 1;
+    return cudaGetLastError();
+}
+
+// Hash-routed layers (guide, section 1: tid2eid maps a token id to its k
+// experts; flat weights w_scale / k).
+__global__ void k_route_hash(const int32_t* __restrict__ tok, const int32_t* __restrict__ tab,
+                             int V, int T, int k, int E, float w_each, int32_t* __restrict__ ids,
+                             float* __restrict__ w, uint32_t* err) {
+    int t = blockIdx.x * blockDim.x + threadIdx.x;
+    if (t >= T) return;
+    int id = tok[t];
+    bool ok = id >= 0 && id < V;
+    for (int j = 0; j < k; ++j) {
+        int e = ok ? tab[(size_t)id * k + j] : -1;
+        if (e < 0 || e >= E) { e = -1; ok = false; }
+        ids[(size_t)t * k + j] = e;
+        w[(size_t)t * k + j] = w_each;
+    }
+    if (!ok) raise_flag(err, ERR_BAD_ID);
+}
+
+cudaError_t launch_route_hash(moe_layer* L, const int32_t* tok, const int32_t* tab, int V,
+                              int T, int32_t* ids, float* w, cudaStream_t s) {
+    float w_each = L->cfg.w_scale / (float)L->cfg.top_k;
+    k_route_hash<<<(T + 127) / 128, 128, 0, s>>>(tok, tab, V, T, L->cfg.top_k, L->cfg.n_experts,
+                                                 w_each, ids, w, L->d_err);
+    L->launches += 1;
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------- permute --
+// Block-wide exclusive scan of 4 ints per thread (1024 threads).
+struct Int4Scan { int a, b, c, d; };
+
+__device__ Int4Scan block_exclusive_scan4(Int4Scan v, Int4Scan* warp_tot, Int4Scan* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    Int4Scan inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        int a = __shfl_up_sync(0xFFFFFFFFu, inc.a, o), b = __shfl_up_sync(0xFFFFFFFFu, inc.b, o);
+        int c = __shfl_up_sync(0xFFFFFFFFu, inc.c, o), d = __shfl_up_sync(0xFFFFFFFFu, inc.d, o);
+        if (lane >= o) { inc.a += a; inc.b += b; inc.c += c; inc.d += d; }
+    }
+    if (lane == 31) warp_tot[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        Int4Scan x = warp_tot[lane], xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            int a = __shfl_up_sync(0xFFFFFFFFu, xi.a, o), b = __shfl_up_sync(0xFFFFFFFFu, xi.b, o);
+            int c = __shfl_up_sync(0xFFFFFFFFu, xi.c, o), d = __shfl_up_sync(0xFFFFFFFFu, xi.d, o);
+            if (lane >= o) { xi.a += a; xi.b += b; xi.c += c; xi.d += d; }
+        }
+        warp_tot[lane] = {xi.a - x.a, xi.b - x.b, xi.c - x.c, xi.d - x.d};
+        if (lane == 31) *total = xi;
+    }
+    __syncthreads();
+    Int4Scan base = warp_tot[warp];
+    return {base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c, base.d + inc.d - v.d};
+}
+
+// Stable counting sort of the rows r = t*k + j by expert, in one CTA of 1024
+// threads: histogram, scan, then the rows in chunks of 1024 in ascending r,
+// each row's rank = rows of the same expert in earlier chunks (cursor) +
+// in earlier warps of this chunk (per-warp counts) + in earlier lanes
+// (match_any).  Integer atomics only count, so the result is deterministic.
+// Besides the ABI outputs it fills the padded bookkeeping of the GEMMs:
+// every expert segment starts at a multiple of 128 rows.
+__global__ void __launch_bounds__(1024) k_permute(
+    const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
+    int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
+    int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
+    int T, uint32_t* err) {
+    extern __shared__ int dyn[];  // cnt, cursor, s_off, s_poff [E] each; then wc [32][E] bytes
+    int* cnt = dyn;
+    int* cursor = dyn + E;
+    int* s_off = dyn + 2 * E;
+    int* s_poff = dyn + 3 * E;
+    uint8_t* wc = reinterpret_cast<uint8_t*>(dyn + 4 * E);
+    __shared__ Int4Scan warp_tot[32];
+    __shared__ Int4Scan total;
+    __shared__ int bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+
+    for (int e = tid; e < E; e += 1024) { cnt[e] = 0; cursor[e] = 0; }
+    if (tid == 0) bad = 0;
+    __syncthreads();
+    for (int r = tid; r < R; r += 1024) {
+        int e = ids[r];
+        if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
+        else bad = 1;
+    }
+    __syncthreads();
+
+    Int4Scan v = {0, 0, 0, 0};
+    if (tid < E) {
+        int n = cnt[tid];
+        v = {n, (n + kRowTile - 1) / kRowTile * kRowTile, (n + kRowTile - 1) / kRowTile,
+             (n + kChunk - 1) / kChunk};
+    }
+    Int4Scan ex = block_exclusive_scan4(v, warp_tot, &total);
+    if (tid < E) {
+        s_off[tid] = ex.a;
+        s_poff[tid] = ex.b;
+        offsets[tid] = ex.a;
+        counts[tid] = v.a;
+        poff[tid] = ex.b;
+        tile_scan[tid] = ex.c;
+        chunk_scan[tid] = ex.d;
+    }
+    if (tid == 0) {
+        offsets[E] = total.a;
+        poff[E] = total.b;
+        tile_scan[E] = total.c;
+        chunk_scan[E] = total.d;
+        if (sh_desc) {  // the shared expert's single segment: all T tokens
+            sh_desc[0] = T;
+            sh_desc[1] = 0;
+            sh_desc[2] = (T + kRowTile - 1) / kRowTile * kRowTile;
+            sh_desc[3] = 0;
+            sh_desc[4] = (T + kRowTile - 1) / kRowTile;
+            sh_desc[5] = 0;
+            sh_desc[6] = (T + kChunk - 1) / kChunk;
+        }
+        if (bad) raise_flag(err, ERR_BAD_ID);
+    }
+    __syncthreads();
+    const int Rp = total.b;
+    for (int p = tid; p < Rp; p += 1024) pos_row[p] = -1;
+
+    for (int base = 0; base < R; base += 1024) {
+        for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
+        __syncthreads();
+        const int r = base + tid;
+        int e = (r < R) ? ids[r] : -1;
+        if (e >= E) e = -1;
+        const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
+        const int rank = __popc(grp & ((1u << lane) - 1u));
+        if (e >= 0 && rank == 0) wc[warp * E + e] = (uint8_t)__popc(grp);
+        __syncthreads();
+        if (e >= 0) {
+            int before = cursor[e] + rank;
+            for (int w2 = 0; w2 < warp; ++w2) before += wc[w2 * E + e];
+            const int p = s_off[e] + before, pp = s_poff[e] + before;
+            row_src[p] = r;
+            row_dst[r] = p;
+            row_pos[r] = pp;
+            pos_row[pp] = r;
+        } else if (r < R) {
+            row_dst[r] = -1;
+            row_pos[r] = -1;
+        }
+        __syncthreads();
+        for (int e2 = tid; e2 < E; e2 += 1024) {
+            int add = 0;
+            for (int w2 = 0; w2 < 32; ++w2) add += wc[w2 * E + e2];
+            cursor[e2] += add;
+        }
+        __syncthreads();
+    }
+}
+
+cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* offsets,
+                           int32_t* row_src, int32_t* row_dst, cudaStream_t s) {
+    const int R = T * L->cfg.top_k;
+    const size_t smem = (size_t)48 * L->cfg.n_experts;
+    k_permute<<<1, 1024, smem, s>>>(ids, R, L->cfg.n_experts, offsets, row_src, row_dst, L->counts,
+                                 L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
+                                 L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err);
+    L->launches += 1;
+    return cudaGetLastError();
+}
+
+cudaError_t kernels_init() {
+    return cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                48 * kMaxExperts);
+}
+
+// --------------------------------------------------------------- quantise --
+// MXFP8 of bf16 rows.  A group of 4 lanes owns one 32-block (8 elements per
+// lane, one 16-byte load); the block amax is a 2-step shuffle max, the scale
+// exponent comes from its fp32 exponent field, and the codes are the
+// hardware's round-to-nearest-even, saturating e4m3 conversion of v * 2^-ex.
+struct QuantDst {
+    uint8_t* q;              // canonical [T][H] ...
+    uint8_t* s;              // ... and [T][H/32]            (mode 0)
+    uint8_t* xq;             // permuted rows [Rp][H] + atoms (mode 1)
+    uint8_t* xs;
+    const int32_t* row_pos;  // [T*k]
+    int k;
+    uint8_t* xq_tok;         // token-order rows [T][H] + atoms, or null
+    uint8_t* xs_tok;
+};
+
+template <int kMode>
+__global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x, int T, int H,
+                                                  QuantDst d) {
+    const int lane = threadIdx.x & 31;
+    const int tasks_per_row = (H + 255) / 256;
+    const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (task >= T * tasks_per_row) return;
+    const int t = task / tasks_per_row;
+    const int b = (task % tasks_per_row) * 8 + (lane >> 2);  // 32-block index
+    const int part = lane & 3;
+    const bool active = b < H / 32;
+    const int h = b * 32 + part * 8;
+    float v[8];
+    float amax = 0.0f;
+    if (active) {
+        uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
+        uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(wv[i] << 16);
+            v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    }
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    if (!active) return;
+    const int ex = mxfp8_exponent(amax);
+    uint32_t lo = 0, hi = 0;
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+        lo |= f32x2_to_e4m3x2(scale_pow2(v[2 * i], ex), scale_pow2(v[2 * i + 1], ex)) << (16 * i);
+        hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
+    }
+    const uint2 codes = make_uint2(lo, hi);
+    const uint8_t sbyte = (uint8_t)(ex + 127);
+    if (kMode == 0) {
+        *reinterpret_cast<uint2*>(d.q + (size_t)t * H + h) = codes;
+        if (part == 0) d.s[(size_t)t * (H / 32) + b] = sbyte;
+    } else {
+        for (int j = 0; j < d.k; ++j) {
+            const int p = d.row_pos[(size_t)t * d.k + j];
+            if (p < 0) continue;
+            *reinterpret_cast<uint2*>(d.xq + (size_t)p * H + h) = codes;
+            if (part == 0) d.xs[sf_atom_offset(p, b, H)] = sbyte;
+        }
+        if (d.xq_tok) {
+            *reinterpret_cast<uint2*>(d.xq_tok + (size_t)t * H + h) = codes;
+            if (part == 0) d.xs_tok[sf_atom_offset(t, b, H)] = sbyte;
+        }
+    }
+}
+
+static cudaError_t quantize_launch(int mode, const uint16_t* x, int T, int H, QuantDst d,
+                                   cudaStream_t s) {
+    const long long tasks = (long long)T * ((H + 255) / 256);
+    const int threads = 256;
+    const long long blocks = (tasks * 32 + threads - 1) / threads;
+    if (mode == 0) k_quantize<0><<<(unsigned)blocks, threads, 0, s>>>(x, T, H, d);
+    else k_quantize<1><<<(unsigned)blocks, threads, 0, s>>>(x, T, H, d);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_canonical(moe_layer* L, const uint16_t* x, int T, uint8_t* q,
+                                      uint8_t* sc, cudaStream_t s) {
+    L->launches += 1;
+    QuantDst d{};
+    d.q = q;
+    d.s = sc;
+    return quantize_launch(0, x, T, L->cfg.hidden, d, s);
+}
+
+cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cudaStream_t s) {
+    L->launches += 1;
+    QuantDst d{};
+    d.xq = L->xq;
+    d.xs = L->xs;
+    d.row_pos = L->row_pos;
+    d.k = L->cfg.top_k;
+    if (L->cfg.has_shared) {
+        d.xq_tok = L->xq_tok;
+        d.xs_tok = L->xs_tok;
+    }
+    return quantize_launch(1, x, T, L->cfg.hidden, d, s);
+}
+
+// ---------------------------------------------------------------- combine --
+// out[t] = sum over the token's experts in ascending expert order (equal ids
+// in j order) of w * y[row] (+ the shared expert): a fixed fp32 order, no
+// atomics (guide, section 3.2, the FFN output equation).
+__global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids,
+                                                 const float* __restrict__ w,
+                                                 const int32_t* __restrict__ row_pos,
+                                                 const float* __restrict__ y,
+                                                 const float* __restrict__ y_sh, int T, int H,
+                                                 int k, float* __restrict__ out) {
+    const int H4 = H / 4;
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= (long long)T * H4) return;
+    const int t = (int)(i / H4), c = (int)(i % H4) * 4;
+    int order[kMaxTopK];
+    int idv[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        order[j] = j;
+        idv[j] = (j < k) ? ids[(size_t)t * k + j] : INT_MAX;
+    }
+#pragma unroll
+    for (int a = 1; a < kMaxTopK; ++a)
+#pragma unroll
+        for (int b = a; b > 0; --b)
+            if (idv[order[b - 1]] > idv[order[b]]) {
+                int tmp = order[b]; order[b] = order[b - 1]; order[b - 1] = tmp;
+            }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int a = 0; a < kMaxTopK; ++a) {
+        if (a < k) {
+            const int r = t * k + order[a];
+            if (row_pos[r] < 0) continue;
+            const float wt = w[r];
+            const float4 v = *reinterpret_cast<const float4*>(y + (size_t)r * H + c);
+            acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+        }
+    }
+    if (y_sh) {
+        const float4 v = *reinterpret_cast<const float4*>(y_sh + (size_t)t * H + c);
+        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+    }
+    *reinterpret_cast<float4*>(out + (size_t)t * H + c) = acc;
+}
+
+cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int T,
+                           float* out, cudaStream_t s) {
+    const long long n = (long long)T * (L->cfg.hidden / 4);
+    k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
+        ids, w, L->row_pos, L->y, L->cfg.has_shared ? L->y_sh : nullptr, T, L->cfg.hidden,
+        L->cfg.top_k, out);
+    L->launches += 1;
+    return cudaGetLastError();
+}
+
+// ----------------------------------------------------------- test helpers --
+__global__ void k_hidden_gather(const int32_t* __restrict__ row_pos, const uint8_t* __restrict__ hq,
+                                const uint8_t* __restrict__ hs, int R, int I, uint8_t* __restrict__ oq,
+                                uint8_t* __restrict__ os) {
+    const int r = blockIdx.x;
+    if (r >= R) return;
+    const int p = row_pos[r];
+    for (int j = threadIdx.x; j < I; j += blockDim.x)
+        oq[(size_t)r * I + j] = p >= 0 ? hq[(size_t)p * I + j] : 0;
+    for (int b = threadIdx.x; b < I / 32; b += blockDim.x)
+        os[(size_t)r * (I / 32) + b] = p >= 0 ? hs[sf_atom_offset(p, b, I)] : 0;
+}
+
+cudaError_t launch_hidden_gather(moe_layer* L, int T, uint8_t* hq, uint8_t* hs,
+                                 cudaStream_t s) {
+    const int R = T * L->cfg.top_k;
+    k_hidden_gather<<<R, 256, 0, s>>>(L->row_pos, L->hq, L->hs, R, L->cfg.inter, hq, hs);
+    L->launches += 1;
+    return cudaGetLastError();
+}
+
+// Canonical block scales [mats][rows][K/32] -> 512-byte atoms
+// [mats][rows/128][K/128][512] (one thread per byte).
+__global__ void k_repack_sf(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int rows,
+                            int K, long long n) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int KB = K / 32;
+    const long long per_mat = (long long)rows * KB;
+    const long long m = i / per_mat, rem = i % per_mat;
+    const int row = (int)(rem / KB), kb = (int)(rem % KB);
+    dst[m * per_mat + sf_atom_offset(row, kb, K)] = src[i];
+}
+
+cudaError_t repack_sf(const uint8_t* src, uint8_t* dst, int mats, int rows, int K,
+                      cudaStream_t s) {
+    const long long n = (long long)mats * rows * (K / 32);
+    k_repack_sf<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, dst, rows, K, n);
+    return cudaGetLastError();
+}
+
+// 128x128 tile scales [rows/128][K/128] -> atoms where every 32-block of the
+// tile carries the tile's scale.
+__global__ void k_expand_tile_sf(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
+                                 int rows, int K, long long n) {
+    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
+    if (i >= n) return;
+    const int KB = K / 32;
+    const int row = (int)(i / KB), kb = (int)(i % KB);
+    dst[sf_atom_offset(row, kb, K)] = src[(size_t)(row / 128) * (K / 128) + kb / 4];
+}
+
+cudaError_t expand_tile_sf(const uint8_t* src, uint8_t* dst, int rows, int K, cudaStream_t s) {
+    const long long n = (long long)rows * (K / 32);
+    k_expand_tile_sf<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, dst, rows, K, n);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

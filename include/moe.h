@@ -1,0 +1,195 @@
+/*
+ * moe.h -- C ABI of libmoe: the routed-expert FFN layer of a
+ * DeepSeek-V4-Flash-style MoE on one NVIDIA GB300 (sm_103a).
+ *
+ * The layer ("DeepSeek-V4-Flash 284B - Deep-Dive Mathematical & Kernel
+ * Guide", section 3.2, the FFN output equation):
+ *     out(x) = shared(x) + sum_{i=1..k} w_i * expert_{e_i}(x),  sum_i w_i = w_scale
+ * with expert(x) = W_down h, h_j = SiLU(g_j) * u_j, g = W_gate x, u = W_up x
+ * (same guide, section 4).  Routed experts ship as MXFP4 (colibri "DeepSeek
+ * V4 target engine", intro: "routed experts stay native fp4"): e2m1 codes in
+ * 32-element blocks along the contraction axis, two codes per byte with the
+ * even element in the low nibble, one UE8M0 scale byte 2^(c-127) per block.
+ * The optional shared expert ships as fp8 e4m3 with one UE8M0 scale per
+ * 128x128 tile (same page: "the dense set stays fp8-e4m3 with UE8M0 block
+ * scales").  Activations enter every matmul as MXFP8: e4m3 codes in
+ * 32-element blocks with a UE8M0 scale 2^(floor(log2 amax) - 8), rounded to
+ * nearest even, saturating at +-448 (colibri "Linux CUDA tier": the MXFP8
+ * tensor-core path).
+ *
+ * Conventions for every entry point:
+ *  - All tensors are dense and row-major.  Pointers marked "device" must be
+ *    device memory of the layer's GPU; "host" pointers are host memory (page-
+ *    locked for the copies to overlap).  The caller owns every buffer it
+ *    passes; the library never frees or keeps a caller pointer past the call.
+ *  - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
+ *    stream) and is asynchronous: outputs are ready when the stream reaches
+ *    that point.  route/permute/quantize/forward make no allocation and no
+ *    host synchronisation, so they may be captured in a CUDA graph.
+ *  - A layer is not thread-safe: calls on one layer must be serialised, and
+ *    calls that overlap on the GPU (different streams) race on its workspace.
+ *  - Every call returns a status and never aborts.  Invalid arguments that
+ *    the host can see are rejected before anything is enqueued
+ *    (MOE_ERR_INVALID_ARG).  Device-side checks (expert ids outside [0, E),
+ *    token ids outside [0, V), a capped device wait that ran out) cannot be
+ *    seen without a synchronisation: the kernels skip the offending work and
+ *    raise a sticky device flag that moe_check() reports.  CUDA launch or
+ *    runtime errors return MOE_ERR_CUDA.  moe_last_error() gives a message.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st* moe_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = 1, /* bad pointer, size or id                      */
+    MOE_ERR_UNSUPPORTED = 2, /* shape the kernels do not cover               */
+    MOE_ERR_OOM = 3,         /* device allocation failed (create only)       */
+    MOE_ERR_CUDA = 4,        /* CUDA runtime / launch error                  */
+    MOE_ERR_TIMEOUT = 5      /* a capped device-side wait ran out            */
+} moe_status;
+
+/* Shape of one layer.  hidden (H) and inter (I) must be multiples of 128
+ * and at most 8192;
+ * 1 <= top_k (k) <= min(n_experts, 8); 1 <= n_experts (E) <= 1024;
+ * max_tokens bounds T of every later call and sizes the workspace.  The
+ * guide's layer (section 1): H = 4096, I = 2048, E = 256, k = 6,
+ * w_scale = 1.5, one shared expert.                                        */
+typedef struct {
+    int hidden;
+    int inter;
+    int n_experts;
+    int top_k;
+    int max_tokens;
+    int has_shared;  /* 1: the shared-expert pointers of moe_weights are set */
+    float w_scale;   /* routing weights of a token sum to w_scale            */
+} moe_config;
+
+/* Device pointers to the weights, in the canonical shipping layout:
+ *   gate_q, up_q  u8 [E][I][H/2]  e2m1 pairs (even element = low nibble)
+ *   gate_s, up_s  u8 [E][I][H/32] UE8M0 block scales
+ *   down_q        u8 [E][H][I/2]
+ *   down_s        u8 [E][H][I/32]
+ *   sh_gate_q, sh_up_q u8 [I][H] e4m3;  sh_gate_s, sh_up_s u8 [I/128][H/128]
+ *   sh_down_q     u8 [H][I] e4m3;       sh_down_s          u8 [H/128][I/128]
+ * Shared-expert pointers are ignored unless has_shared.                     */
+typedef struct {
+    const uint8_t *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
+    const uint8_t *sh_gate_q, *sh_gate_s, *sh_up_q, *sh_up_s, *sh_down_q, *sh_down_s;
+} moe_weights;
+
+typedef struct moe_layer moe_layer;
+
+/* Build a layer on the current CUDA device.  Copies and repacks the weights
+ * into library-owned device memory (about 3.5 GB for the guide's shape) and
+ * allocates the workspace for max_tokens; synchronises `stream` once, after
+ * which the caller may free its weight buffers.  *out receives the layer, or
+ * NULL on failure.                                                          */
+moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t stream,
+                      moe_layer** out);
+
+/* Free everything the layer owns.  The caller must make sure no work of the
+ * layer is still running (synchronise its streams first).  NULL is a no-op.*/
+moe_status moe_destroy(moe_layer* layer);
+
+/* Learned router (guide, section 1: gating_func = SQRT_SOFTPLUS, top-k over
+ * the routed experts; section 3.2: the k weights sum to w_scale).
+ *   logits  device f32 [T][E]
+ *   ids     device i32 [T][k]  experts by descending score s = sqrt(softplus
+ *           (logit)); equal scores go to the lower expert index
+ *   w       device f32 [T][k]  w_j = w_scale * s_j / sum of the k scores
+ * 1 <= T <= max_tokens.  The top-k is plain (one expert group).             */
+moe_status moe_route(moe_layer* layer, const float* logits, int T, int32_t* ids, float* w,
+                     moe_stream_t stream);
+
+/* Hash router of the first layers (guide, section 1: ffn_gate_tid2eid maps a
+ * token id to its experts; weights flat):
+ *   token_ids device i32 [T] in [0, V); tid2eid device i32 [V][k]
+ *   ids[t][j] = tid2eid[token_ids[t]][j];  w[t][j] = w_scale / k.
+ * A token id outside [0, V) yields ids = -1 for that token and raises the
+ * device flag (MOE_ERR_INVALID_ARG from moe_check).                         */
+moe_status moe_route_hash(moe_layer* layer, const int32_t* token_ids, const int32_t* tid2eid,
+                          int V, int T, int32_t* ids, float* w, moe_stream_t stream);
+
+/* Token -> expert grouping (the grouping MUL_MAT_ID does; guide, section 2):
+ * a stable counting sort of the rows r = t*k + j by expert ids[r].
+ *   ids      device i32 [T][k], values in [0, E)
+ *   offsets  device i32 [E+1]  offsets[e] = rows with expert < e
+ *   row_src  device i32 [T*k]  row placed at sorted position p (ascending r
+ *            within an expert's segment)
+ *   row_dst  device i32 [T*k]  inverse: sorted position of row r
+ * Ids outside [0, E) are left out (row_dst = -1) and raise the device flag. */
+moe_status moe_permute(moe_layer* layer, const int32_t* ids, int T, int32_t* offsets,
+                       int32_t* row_src, int32_t* row_dst, moe_stream_t stream);
+
+/* Activation quantiser, exposed for tests: bf16 rows -> MXFP8.
+ *   x  device u16 [T][H] (bf16 bits);  q device u8 [T][H] e4m3 codes;
+ *   s  device u8 [T][H/32] UE8M0 byte of 2^(floor(log2 amax) - 8) per
+ *      32-block (amax = 0 or a clamped exponent gives -127 -> byte 0).     */
+moe_status moe_quantize(moe_layer* layer, const uint16_t* x, int T, uint8_t* q, uint8_t* s,
+                        moe_stream_t stream);
+
+/* The layer: permute, quantise, SwiGLU gate/up with MXFP8 requantisation of
+ * h, down projection, and the weighted combine in ascending expert order,
+ * plus the shared expert when present.
+ *   x    device u16 [T][H] bf16;  ids device i32 [T][k] in [0, E);
+ *   w    device f32 [T][k];       out device f32 [T][H] (overwritten).     */
+moe_status moe_forward(moe_layer* layer, const uint16_t* x, int T, const int32_t* ids,
+                       const float* w, float* out, moe_stream_t stream);
+
+/* Whole layer from host memory: copies x (host u16 [T][H]) and logits (host
+ * f32 [T][E]) into the layer's staging buffers, runs moe_route and
+ * moe_forward, and copies the result to out (host f32 [T][H]).  Asynchronous
+ * on `stream` (page-locked host buffers make the copies overlap); read out
+ * only after synchronising the stream.                                      */
+moe_status moe_forward_host(moe_layer* layer, const uint16_t* x, const float* logits, int T,
+                            float* out, moe_stream_t stream);
+
+/* Test hook: after moe_forward, the requantised SwiGLU activations of the
+ * rows r = t*k + j of its T tokens, in row order:
+ *   hq device u8 [T*k][I] e4m3;  hs device u8 [T*k][I/32] UE8M0.          */
+moe_status moe_hidden(moe_layer* layer, int T, uint8_t* hq, uint8_t* hs, moe_stream_t stream);
+
+/* Synchronise `stream` and report (then clear) the sticky device flag:
+ * MOE_OK, MOE_ERR_INVALID_ARG (an id was out of range) or MOE_ERR_TIMEOUT. */
+moe_status moe_check(moe_layer* layer, moe_stream_t stream);
+
+/* Bytes of device workspace moe_create allocates for this shape (weights
+ * not included); 0 for an invalid configuration.                           */
+size_t moe_workspace_bytes(const moe_config* cfg);
+
+/* Message of the last failed call on `layer`; for layer == NULL, of the last
+ * failed call in this thread that had no layer (e.g. moe_create).          */
+const char* moe_last_error(const moe_layer* layer);
+
+/* Stage timing: when `events` is non-NULL, the next moe_forward call on
+ * `layer` records events[0..5] on its stream at the stage boundaries
+ * [start, after permute, after quantise, after gate/up, after down (and the
+ * shared expert), after combine] and then forgets the array.  events holds
+ * 6 cudaEvent_t created by the caller; n must be 6.  Recording is stream-
+ * ordered, so it may be captured in a CUDA graph.                         */
+moe_status moe_set_stage_events(moe_layer* layer, void* const* events, int n);
+
+/* Number of CUDA kernels this layer has enqueued since moe_create (a launch
+ * made while a stream is being captured counts once, although every replay
+ * of the graph runs it again).                                             */
+unsigned long long moe_kernel_launches(const moe_layer* layer);
+
+/* Kernel path of the GEMM steps: 0 = automatic, 1 = CUDA-core kernels,
+ * 2 = tcgen05 block-scaled tensor-core kernels.  Both compute the same
+ * layer; the choice only affects speed and the order of fp32 additions.    */
+moe_status moe_set_gemm_path(moe_layer* layer, int path);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -63,7 +63,14 @@ class LayerConfig:
 
     @property
     def default_seed(self) -> int:
+        """Seed of the per-call inputs (logits, x, token ids)."""
         return 1000 + self.index
+
+    @property
+    def weight_seed(self) -> int:
+        """Seed of the expert weights: every configuration with the guide's
+        full layer shape uses one weight set (that of the decode layer)."""
+        return 1000 if (self.H, self.I, self.E) == (256, 128, 16) else 1001
 
 
 CONFIGS = {
@@ -200,13 +207,21 @@ def _cache_dir(cfg: LayerConfig, seed: int) -> Optional[Path]:
     root = os.environ.get("BQE_WORKLOAD_CACHE", str(Path.home() / ".cache" / "bqe_workloads"))
     if root in ("", "0", "off"):
         return None
-    return Path(root) / f"{cfg.name}_H{cfg.H}_I{cfg.I}_E{cfg.E}_s{seed}"
+    return Path(root) / f"H{cfg.H}_I{cfg.I}_E{cfg.E}_s{seed}"
 
 
 def make_weights(cfg: LayerConfig, seed: Optional[int] = None, threads: Optional[int] = None,
                  cache: bool = True) -> Weights:
     """Draw and encode every expert matrix of `cfg` (deterministic in seed)."""
-    seed = cfg.default_seed if seed is None else seed
+    seed = cfg.weight_seed if seed is None else seed
+    if cfg.shared:  # routed experts as without the shared expert, plus its three matrices
+        w = make_weights(dataclasses.replace(cfg, shared=False), seed, threads, cache)
+        w = dataclasses.replace(w, cfg=cfg)
+        sk = _streams(seed)["shared"].spawn(3)
+        w.sh_gate_q, w.sh_gate_s = encode_fp8_tiles(_draw(sk[0], cfg.I, cfg.H))
+        w.sh_up_q, w.sh_up_s = encode_fp8_tiles(_draw(sk[1], cfg.I, cfg.H))
+        w.sh_down_q, w.sh_down_s = encode_fp8_tiles(_draw(sk[2], cfg.H, cfg.I))
+        return w
     H, I, E = cfg.H, cfg.I, cfg.E
     big = E * H * I >= (1 << 28)
     cdir = _cache_dir(cfg, seed) if (cache and big) else None
@@ -237,12 +252,6 @@ def make_weights(cfg: LayerConfig, seed: Optional[int] = None, threads: Optional
     nthr = threads or min(32, os.cpu_count() or 1)
     with ThreadPoolExecutor(nthr) as ex:
         list(ex.map(job, range(3 * E)))
-
-    if cfg.shared:
-        sk = st["shared"].spawn(3)
-        w.sh_gate_q, w.sh_gate_s = encode_fp8_tiles(_draw(sk[0], I, H))
-        w.sh_up_q, w.sh_up_s = encode_fp8_tiles(_draw(sk[1], I, H))
-        w.sh_down_q, w.sh_down_s = encode_fp8_tiles(_draw(sk[2], H, I))
 
     if cdir is not None:
         try:
