@@ -148,7 +148,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     W = max(W, 3)
 
     w = make_weights(cfg)
-    dw = {n: torch.from_numpy(np.ascontiguousarray(getattr(w, n))).to(dev)
+    dw = {n: torch.from_numpy(np.array(getattr(w, n))).to(dev)
           for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
                     "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")
           if getattr(w, n) is not None}

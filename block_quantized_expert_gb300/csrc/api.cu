@@ -104,7 +104,7 @@ moe_status check_T(moe_layer* L, int T) {
 // The GEMM steps (gate/up + SwiGLU + requant, down; routed and shared);
 // `mid` (if set) is recorded after the routed gate/up launch.
 cudaError_t run_gemms(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {
-    if (L->gemm_path == 1 || L->tc == nullptr) return moe::launch_gemm_cc(L, T, s, mid);
+    if (L->gemm_path != 2 || L->tc == nullptr) return moe::launch_gemm_cc(L, T, s, mid);
     return moe::launch_gemm_tc(L, T, s, mid);
 }
 
@@ -309,8 +309,12 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, int T, const int32_t* id
     cudaStream_t s = (cudaStream_t)stream;
     const bool ev = L->stage_ev_set != 0;
     L->stage_ev_set = 0;
+    // external records: inside a stream capture they become timestamped
+    // event nodes of the graph (not capture-internal dependencies)
     auto mark = [&](int i, cudaError_t e) {
-        return (ev && e == cudaSuccess) ? cudaEventRecord(L->stage_ev[i], s) : e;
+        return (ev && e == cudaSuccess)
+                   ? cudaEventRecordWithFlags(L->stage_ev[i], s, cudaEventRecordExternal)
+                   : e;
     };
     cudaError_t e = mark(0, cudaSuccess);
     if (e == cudaSuccess) e = mark(1, moe::launch_permute(L, ids, T, L->offsets, L->row_src, L->row_dst, s));

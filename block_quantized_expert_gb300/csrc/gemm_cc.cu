@@ -189,7 +189,7 @@ cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     a.K = c.hidden; a.N = c.inter;
     a.hq = L->hq; a.hs = L->hs;
     cudaError_t err = cc_launch<0, true>(L, a, s);
-    if (err == cudaSuccess && mid) err = cudaEventRecord(mid, s);
+    if (err == cudaSuccess && mid) err = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
     if (err != cudaSuccess) return err;
     CCArgs d = a;
     d.w1_q = L->down_q; d.w1_s = L->down_s; d.w2_q = nullptr; d.w2_s = nullptr;

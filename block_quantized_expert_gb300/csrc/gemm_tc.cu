@@ -1,18 +1,438 @@
-// gemm_tc.cu -- grouped expert GEMMs on the tcgen05 block-scaled tensor cores.
+// gemm_tc.cu -- grouped expert GEMMs on the sm_103a block-scaled tensor cores
+// (tcgen05.mma kind::mxf8f6f4, one UE8M0 scale per 32 K-elements).
+//
+// Orientation: weights are the MMA's A operand (M = 128 weight rows = output
+// features), the routed tokens of one expert segment its B operand (N = 32..128
+// token rows), so the fp32 accumulator D[feature][token] lives in tensor
+// memory with one feature per TMEM lane.  MXFP4 weights are e2m1 (A format
+// 5), the shared expert's fp8 weights e4m3 (A format 0); activations are
+// e4m3.  Per 128-wide K step a TMA producer fills one pipeline stage with
+// the weight tile(s) (fp4 unpacked by TMA into the 16-byte-aligned form the
+// MMA reads), the token tile and three 512-byte scale-factor atoms; the MMA
+// thread copies the atoms into tensor memory (tcgen05.cp) and issues four
+// K=32 MMAs per accumulator; four epilogue warps read the accumulators back.
+//
+// Gate/up (guide, section 4): two accumulators (gate, up) per tile; the
+// epilogue forms h = SiLU(g) * u in fp32 and requantises it to MXFP8 along
+// the feature axis (32 features = one warp), writing h codes and scale atoms
+// in the padded row space the down GEMM reads.  Down: one accumulator; the
+// epilogue writes fp32 rows y[row][feature] for the fixed-order combine.
+//
+// Persistent grid of one CTA per SM; tiles enumerated (token tile u, weight
+// tile m) with m fastest, so CTAs running together share a token tile and
+// walk one expert's weights (L2 reuse).  Every wait is bounded in wall time:
+// on expiry the CTA raises ERR_TIMEOUT, lets in-flight copies land, frees its
+// tensor memory and exits.
+#include <cuda.h>
+
+#include <new>
+
 #include "common.cuh"
 #include "layer.h"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
+using namespace tc;
+
+// Transaction bytes of one 128x128 e2m1 tile loaded with the 16-byte-aligned
+// 4-bit unpacking: the bytes the copy writes to shared memory.
+constexpr uint32_t kFp4TileTx = 16384;
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+struct TcArgs {
+    int n_seg;
+    const int32_t* counts;     // [n_seg] token rows per segment
+    const int32_t* poff;       // [n_seg+1] padded row starts (multiples of 128)
+    const int32_t* tile_scan;  // [n_seg+1] 128-row token tiles before segment e
+    int K;                     // contraction length (multiple of 128)
+    int N_out;                 // output features (multiple of 128)
+    int seg_rows;              // weight rows per segment (0: one shared matrix)
+    const uint8_t* sfa0;       // weight scale atoms [rows/128][K/128][512]
+    const uint8_t* sfa1;
+    const uint8_t* sfb;        // activation scale atoms [Rp/128][K/128][512]
+    uint8_t* hq;               // gate/up: h codes [Rp][N_out] + atoms
+    uint8_t* hs;
+    float* y;                  // down: y[row][N_out]
+    const int32_t* pos_row;    // down: padded position -> y row (null: identity)
+    uint32_t* err;
+    uint32_t a_tx;             // TMA bytes of one weight tile
+};
+
+template <bool kGateUp>
+struct TcCfg {
+    static constexpr int kNumA = kGateUp ? 2 : 1;
+    static constexpr int kStages = kGateUp ? 4 : 6;
+    static constexpr int kTileBytes = 16384;  // 128 rows x 128 B
+    static constexpr int kSfOff = (kNumA + 1) * kTileBytes;
+    static constexpr int kStageBytes = ((kSfOff + 512 * (kNumA + 1)) + 1023) / 1024 * 1024;
+    static constexpr int kBarOff = kStages * kStageBytes;
+    static constexpr int kSmem = kBarOff + 256 + 1024;  // + barriers + alignment slack
+    static constexpr uint32_t kTmemCols = kGateUp ? 512 : 256;
+    static constexpr uint32_t kAcc1Col = 128;
+    static constexpr uint32_t kSfBase = kGateUp ? 256 : 128;
+    static constexpr uint32_t kSfPerStage = 4 * (kNumA + 1);
+    static_assert(kSfBase + kStages * kSfPerStage <= kTmemCols, "tensor memory budget");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+
+struct Tile {
+    int e, m0, n0, nvalid, nt, arow, p0;
+};
+
+__device__ __forceinline__ Tile decode_tile(const TcArgs& a, int t, int MT) {
+    const int u = t / MT, m = t % MT;
+    int lo = 0, hi = a.n_seg;  // segment with tile_scan[e] <= u < tile_scan[e+1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldg(a.tile_scan + mid) <= u) lo = mid; else hi = mid;
+    }
+    Tile T;
+    T.e = lo;
+    T.n0 = (u - __ldg(a.tile_scan + lo)) * 128;
+    T.nvalid = min(128, __ldg(a.counts + lo) - T.n0);
+    T.nt = (T.nvalid + 31) & ~31;
+    T.m0 = m * 128;
+    T.arow = a.seg_rows * lo + T.m0;
+    T.p0 = __ldg(a.poff + lo) + T.n0;
+    return T;
+}
+
+template <bool kGateUp, uint32_t kAFmt>
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
+          const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
+    using Cfg = TcCfg<kGateUp>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + Cfg::kBarOff);
+    const uint32_t bar0 = smem_u32(bars);
+    auto full_bar = [&](int s) { return bar0 + 8u * s; };
+    auto empty_bar = [&](int s) { return bar0 + 8u * (Cfg::kStages + s); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * Cfg::kStages);
+    const uint32_t tmem_empty = tmem_full + 8u;
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::kStages + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int MT = a.N_out / 128;
+    const int KB = a.K / 128;
+    const int total = __ldg(a.tile_scan + a.n_seg) * MT;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < Cfg::kStages; ++s) {
+            mbar_init(full_bar(s), 1);
+            mbar_init(empty_bar(s), 1);
+        }
+        mbar_init(tmem_full, 1);
+        mbar_init(tmem_empty, 4);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmA0);
+        if (kGateUp) prefetch_tmap(&tmA1);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        raise_flag(a.err, ERR_TIMEOUT);
+    };
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer --
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const Tile T = decode_tile(a, t, MT);
+                const uint32_t tx = Cfg::kNumA * a.a_tx + (uint32_t)T.nt * 128u + 512u * (Cfg::kNumA + 1);
+                const size_t atom_a = (size_t)(T.arow / 128) * KB;
+                const size_t atom_b = (size_t)(T.p0 / 128) * KB;
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * Cfg::kStageBytes;
+                    uint8_t* bt = st + Cfg::kNumA * Cfg::kTileBytes;
+                    uint8_t* sf = st + Cfg::kSfOff;
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, tx);
+                    tma_load_2d(smem_u32(st), &tmA0, kb * 128, T.arow, fb);
+                    if (kGateUp) tma_load_2d(smem_u32(st + Cfg::kTileBytes), &tmA1, kb * 128, T.arow, fb);
+                    for (int i = 0; i < T.nt / 32; ++i)
+                        tma_load_2d(smem_u32(bt + i * 4096), &tmB, kb * 128, T.p0 + 32 * i, fb);
+                    bulk_load(smem_u32(sf), a.sfa0 + (atom_a + kb) * 512, 512, fb);
+                    if (kGateUp) bulk_load(smem_u32(sf + 512), a.sfa1 + (atom_a + kb) * 512, 512, fb);
+                    bulk_load(smem_u32(sf + 512 * Cfg::kNumA), a.sfb + (atom_b + kb) * 512, 512, fb);
+                    if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer --
+        if (lane == 0) {
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            bool ok = true;
+            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
+                const Tile T = decode_tile(a, t, MT);
+                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, kWaitLimitNs, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(smem + stage * Cfg::kStageBytes);
+                    const uint32_t bt = st + Cfg::kNumA * Cfg::kTileBytes;
+                    const uint32_t sf = st + Cfg::kSfOff;
+                    const uint32_t sf_col = tmem + Cfg::kSfBase + stage * Cfg::kSfPerStage;
+                    const uint32_t sfb_col = sf_col + 4 * Cfg::kNumA;
+                    tmem_cp_32x128_x4(sf_col, desc_sf(sf));
+                    if (kGateUp) tmem_cp_32x128_x4(sf_col + 4, desc_sf(sf + 512));
+                    tmem_cp_32x128_x4(sfb_col, desc_sf(sf + 512 * Cfg::kNumA));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t id = idesc_mx(kAFmt, kFmtE4M3, 128, (uint32_t)T.nt, kk, kk);
+                        const uint64_t bd = desc_sw128(bt + 32 * kk);
+                        const uint32_t acc = (kb | kk) ? 1u : 0u;
+                        mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sfb_col, acc);
+                        if (kGateUp)
+                            mma_mx(tmem + Cfg::kAcc1Col, desc_sw128(st + Cfg::kTileBytes + 32 * kk), bd, id,
+                                   sf_col + 4, sfb_col, acc);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tmem_full);
+                acc_phase ^= 1u;
+            }
+        }
+    } else {
+        // ---------------------------------------------------- epilogue --
+        const int q = warp & 3;  // the TMEM lane quarter this warp may access
+        const int fm = 32 * q + lane;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        uint32_t acc_phase = 0;
+        for (int t = blockIdx.x; t < total; t += gridDim.x) {
+            const Tile T = decode_tile(a, t, MT);
+            if (!mbar_wait(tmem_full, acc_phase, kWaitLimitNs, abort_flag)) {
+                if (lane == 0) give_up();
+                break;
+            }
+            tc_fence_after();
+            for (int c0 = 0; c0 < T.nt; c0 += 16) {
+                uint32_t g[16], u[16];
+                tmem_ld16(tq + (uint32_t)c0, g);
+                if (kGateUp) tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
+                tmem_ld_wait();
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    const int n = c0 + i;
+                    if (n >= T.nvalid) break;  // warp-uniform
+                    const int p = T.p0 + n;
+                    if (kGateUp) {
+                        const float h = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
+                        const int ex = mxfp8_exponent(warp_max(fabsf(h)));
+                        const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
+                        a.hq[(size_t)p * a.N_out + T.m0 + fm] = (uint8_t)code;
+                        if (lane == 0)
+                            a.hs[sf_atom_offset(p, (T.m0 + 32 * q) / 32, a.N_out)] = (uint8_t)(ex + 127);
+                    } else {
+                        const int row = a.pos_row ? __ldg(a.pos_row + p) : p;
+                        if (row >= 0) a.y[(size_t)row * a.N_out + T.m0 + fm] = __uint_as_float(g[i]);
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            acc_phase ^= 1u;
+        }
+    }
+
+    __syncthreads();
+    if (*abort_flag) spin_ns(200000);  // copies / MMAs still in flight land first
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------------- host --
+struct TcState {
+    CUtensorMap gate, up, down, sh_gate, sh_up, sh_down, xq, hq, xq_tok, hq_sh;
+    uint32_t fp4_tx;
+};
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*,
+                                   CUtensorMapInterleave, CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+static EncodeTiledFn get_encode() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+// 2-D map over a row-major matrix [rows][cols] of 8-bit (fp4 = false) or
+// packed 4-bit (fp4 = true) elements; box = 128 columns x box_rows rows,
+// 128-byte swizzle.
+static bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows,
+                     bool fp4) {
+    EncodeTiledFn enc = get_encode();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {cols, rows};
+    cuuint64_t strides[1] = {fp4 ? cols / 2 : cols};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
+                     const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS;
+}
+
+template <bool G, uint32_t F>
+static cudaError_t set_smem_attr() {
+    return cudaFuncSetAttribute(k_gemm_tc<G, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                TcCfg<G>::kSmem);
+}
+
 cudaError_t tc_init(moe_layer* L) {
     L->tc = nullptr;
+    int major = 0, minor = 0;
+    cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, L->device);
+    cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, L->device);
+    if (major != 10 || minor != 3) return cudaSuccess;  // kernels are built for sm_103a only
+    TcState* st = new (std::nothrow) TcState;
+    if (!st) return cudaErrorMemoryAllocation;
+    const uint64_t H = L->cfg.hidden, I = L->cfg.inter, E = L->cfg.n_experts;
+    const uint64_t Rp = (uint64_t)L->Rp_max;
+    const uint64_t Tpad = ((uint64_t)L->cfg.max_tokens + 127) / 128 * 128;
+    bool ok = make_map(&st->gate, L->gate_q, H, E * I, 128, true) &&
+              make_map(&st->up, L->up_q, H, E * I, 128, true) &&
+              make_map(&st->down, L->down_q, I, E * H, 128, true) &&
+              make_map(&st->xq, L->xq, H, Rp, 32, false) && make_map(&st->hq, L->hq, I, Rp, 32, false);
+    if (ok && L->cfg.has_shared)
+        ok = make_map(&st->sh_gate, L->sh_gate_q, H, I, 128, false) &&
+             make_map(&st->sh_up, L->sh_up_q, H, I, 128, false) &&
+             make_map(&st->sh_down, L->sh_down_q, I, H, 128, false) &&
+             make_map(&st->xq_tok, L->xq_tok, H, Tpad, 32, false) &&
+             make_map(&st->hq_sh, L->hq_sh, I, Tpad, 32, false);
+    if (!ok) {
+        delete st;
+        return cudaSuccess;  // no tensor-core path; the CUDA-core kernels run instead
+    }
+    st->fp4_tx = kFp4TileTx;
+    cudaError_t e = set_smem_attr<true, kFmtE2M1>();
+    if (e == cudaSuccess) e = set_smem_attr<false, kFmtE2M1>();
+    if (e == cudaSuccess) e = set_smem_attr<true, kFmtE4M3>();
+    if (e == cudaSuccess) e = set_smem_attr<false, kFmtE4M3>();
+    if (e != cudaSuccess) {
+        delete st;
+        return e;
+    }
+    L->tc = st;
     return cudaSuccess;
 }
 
-void tc_free(moe_layer* L) { L->tc = nullptr; }
+void tc_free(moe_layer* L) {
+    delete static_cast<TcState*>(L->tc);
+    L->tc = nullptr;
+}
+
+template <bool G, uint32_t F>
+static cudaError_t tc_launch(moe_layer* L, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
+                             const TcArgs& args, cudaStream_t s) {
+    k_gemm_tc<G, F><<<L->num_sms, kTcThreads, TcCfg<G>::kSmem, s>>>(a0, a1, b, args);
+    L->launches += 1;
+    return cudaGetLastError();
+}
 
 cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {
-    return launch_gemm_cc(L, T, s, mid);
+    (void)T;
+    const TcState* st = static_cast<const TcState*>(L->tc);
+    const moe_config& c = L->cfg;
+    TcArgs g{};
+    g.n_seg = c.n_experts;
+    g.counts = L->counts;
+    g.poff = L->poff;
+    g.tile_scan = L->tile_scan;
+    g.K = c.hidden;
+    g.N_out = c.inter;
+    g.seg_rows = c.inter;
+    g.sfa0 = L->gate_sf;
+    g.sfa1 = L->up_sf;
+    g.sfb = L->xs;
+    g.hq = L->hq;
+    g.hs = L->hs;
+    g.err = L->d_err;
+    g.a_tx = st->fp4_tx;
+    cudaError_t e = tc_launch<true, kFmtE2M1>(L, st->gate, st->up, st->xq, g, s);
+    if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
+    if (e != cudaSuccess) return e;
+    TcArgs d = g;
+    d.K = c.inter;
+    d.N_out = c.hidden;
+    d.seg_rows = c.hidden;
+    d.sfa0 = L->down_sf;
+    d.sfa1 = nullptr;
+    d.sfb = L->hs;
+    d.hq = nullptr;
+    d.hs = nullptr;
+    d.y = L->y;
+    d.pos_row = L->pos_row;
+    e = tc_launch<false, kFmtE2M1>(L, st->down, st->down, st->hq, d, s);
+    if (e != cudaSuccess || !c.has_shared) return e;
+    TcArgs sg = g;
+    sg.n_seg = 1;
+    sg.counts = L->sh_desc;
+    sg.poff = L->sh_desc + 1;
+    sg.tile_scan = L->sh_desc + 3;
+    sg.seg_rows = 0;
+    sg.sfa0 = L->sh_gate_sf;
+    sg.sfa1 = L->sh_up_sf;
+    sg.sfb = L->xs_tok;
+    sg.hq = L->hq_sh;
+    sg.hs = L->hs_sh;
+    sg.a_tx = 16384;
+    e = tc_launch<true, kFmtE4M3>(L, st->sh_gate, st->sh_up, st->xq_tok, sg, s);
+    if (e != cudaSuccess) return e;
+    TcArgs sd = sg;
+    sd.K = c.inter;
+    sd.N_out = c.hidden;
+    sd.sfa0 = L->sh_down_sf;
+    sd.sfa1 = nullptr;
+    sd.sfb = L->hs_sh;
+    sd.hq = nullptr;
+    sd.hs = nullptr;
+    sd.y = L->y_sh;
+    sd.pos_row = nullptr;
+    return tc_launch<false, kFmtE4M3>(L, st->sh_down, st->sh_down, st->hq_sh, sd, s);
 }
 
 }  // namespace moe

@@ -23,7 +23,7 @@ HQ_FLIP_TOL = 1e-3
 
 
 def to_dev(a, dtype=None):
-    a = np.ascontiguousarray(a)
+    a = np.array(a)
     if a.dtype == np.uint16:
         a = a.view(np.int16)
     t = torch.from_numpy(a)

@@ -20,7 +20,7 @@ from workloads import CONFIGS, make_hash_table
 
 pytestmark = pytest.mark.gpu
 
-PATHS = [1]  # GEMM kernel paths under test (1 = CUDA cores, 2 = tcgen05)
+PATHS = [1, 2]  # GEMM kernel paths under test (1 = CUDA cores, 2 = tcgen05)
 
 
 @pytest.fixture(scope="module")
