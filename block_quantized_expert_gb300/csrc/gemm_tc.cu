@@ -36,8 +36,9 @@ namespace moe {
 using namespace tc;
 
 // Transaction bytes of one 128x128 e2m1 tile loaded with the 16-byte-aligned
-// 4-bit unpacking: the bytes the copy writes to shared memory.
-constexpr uint32_t kFp4TileTx = 16384;
+// 4-bit unpacking: the packed bytes read (8192), not the 16 KB footprint in
+// shared memory -- the copy leaves the 8-byte gaps untouched.
+constexpr uint32_t kFp4TileTx = 8192;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 struct TcArgs {
