@@ -23,7 +23,7 @@ _STATUS = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
 EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_permute",
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
-           "moe_kernel_launches")
+           "moe_kernel_launches", "moe_permute_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -75,6 +75,7 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_set_gemm_path": ([vp, i], i),
         "moe_set_stage_events": ([vp, C.POINTER(vp), i], i),
         "moe_kernel_launches": ([vp], C.c_ulonglong),
+        "moe_permute_noalloc": ([vp, i, i, i, vp, vp, vp, vp], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -235,6 +236,20 @@ def moe_permute(layer: Layer, ids, offsets, row_src, row_dst, stream=None):
                                     _ptr(row_src, torch.int32, (R,), "row_src"),
                                     _ptr(row_dst, torch.int32, (R,), "row_dst"), _stream(stream))
     _check(st, layer.ptr)
+
+
+def moe_permute_noalloc(ids, n_experts: int, offsets, row_src, row_dst, stream=None):
+    """The grouping of moe_permute without a layer and without allocating
+    (scratch in a static device array; T * top_k <= 65536)."""
+    import torch
+    T, k = ids.shape
+    R = T * k
+    st = load_library().moe_permute_noalloc(
+        _ptr(ids, torch.int32, (T, k), "ids"), T, k, n_experts,
+        _ptr(offsets, torch.int32, (n_experts + 1,), "offsets"),
+        _ptr(row_src, torch.int32, (R,), "row_src"), _ptr(row_dst, torch.int32, (R,), "row_dst"),
+        _stream(stream))
+    _check(st)
 
 
 def moe_quantize(layer: Layer, x, q, s, stream=None):

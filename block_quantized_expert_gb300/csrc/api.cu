@@ -110,6 +110,10 @@ cudaError_t run_gemms(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {
 
 }  // namespace
 
+namespace moe {
+void set_thread_error(const char* msg) { snprintf(g_tls_error, sizeof(g_tls_error), "%s", msg); }
+}  // namespace moe
+
 extern "C" {
 
 size_t moe_workspace_bytes(const moe_config* cfg) {

@@ -79,7 +79,12 @@ cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int
 cudaError_t launch_hidden_gather(moe_layer* L, int T, uint8_t* hq, uint8_t* hs,
                                  cudaStream_t s);
 cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid);
+cudaError_t launch_permute_raw(const int32_t* ids, int T, int k, int E, int32_t* offsets,
+                               int32_t* row_src, int32_t* row_dst, int32_t* counts, int32_t* poff,
+                               int32_t* tile_scan, int32_t* chunk_scan, int32_t* row_pos,
+                               int32_t* pos_row, cudaStream_t s);
 cudaError_t kernels_init();
+void set_thread_error(const char* msg);
 cudaError_t cc_init();
 
 // Tensor-core path.

@@ -253,6 +253,18 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
     return cudaGetLastError();
 }
 
+// The same counting sort with caller-chosen bookkeeping buffers (no layer):
+// counts [E], poff/tile_scan/chunk_scan [E+1], row_pos [T*k], pos_row [padded rows].
+cudaError_t launch_permute_raw(const int32_t* ids, int T, int k, int E, int32_t* offsets,
+                               int32_t* row_src, int32_t* row_dst, int32_t* counts, int32_t* poff,
+                               int32_t* tile_scan, int32_t* chunk_scan, int32_t* row_pos,
+                               int32_t* pos_row, cudaStream_t s) {
+    const size_t smem = (size_t)48 * E;
+    k_permute<<<1, 1024, smem, s>>>(ids, T * k, E, offsets, row_src, row_dst, counts, poff, tile_scan,
+                                 chunk_scan, row_pos, pos_row, nullptr, T, nullptr);
+    return cudaGetLastError();
+}
+
 cudaError_t kernels_init() {
     return cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 48 * kMaxExperts);

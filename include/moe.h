@@ -188,6 +188,30 @@ unsigned long long moe_kernel_launches(const moe_layer* layer);
  * layer; the choice only affects speed and the order of fp32 additions.    */
 moe_status moe_set_gemm_path(moe_layer* layer, int path);
 
+/* Token -> expert grouping without a layer and without any allocation.
+ * The paper has no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc -- code running inside another framework's memory
+ * arena that forbids foreign allocations, serving loops that freeze device
+ * memory after start-up, or engines that only want the grouping for their
+ * own expert GEMMs and cannot afford moe_create's weight copies.  It runs the
+ * same stable counting sort as moe_permute and gives the same results:
+ *   ids      device i32 [T][top_k];  offsets device i32 [n_experts+1];
+ *   row_src, row_dst device i32 [T*top_k]  (as moe_permute).
+ * Limits: 1 <= T*top_k <= 65536, 1 <= top_k <= 8, 1 <= n_experts <= 1024;
+ * larger sizes return MOE_ERR_INVALID_ARG (message in moe_last_error(NULL)).
+ * The sort's bookkeeping lives in one static device array of 1,060,876 bytes
+ * that every GPU loading the library holds until the process exits; every
+ * call shares it, so calls that overlap on the GPU (several streams or
+ * threads at once) race and must be serialised by the caller.  The first
+ * call on a device looks up that array's address and sets the kernel's
+ * shared-memory limit (with the device current): make it before any stream
+ * capture; later calls only enqueue one kernel and may be captured.  Ids
+ * outside [0, n_experts) are left out (row_dst = -1); with no layer there is
+ * no device flag to report them.                                           */
+moe_status moe_permute_noalloc(const int32_t* ids, int T, int top_k, int n_experts,
+                               int32_t* offsets, int32_t* row_src, int32_t* row_dst,
+                               moe_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
