@@ -73,6 +73,8 @@ size_t workspace_bytes(const moe_config& c) {
     }
     b += T * H * 2 + T * E * 4 + T * H * 4 + 2 * T * k * 4;  // staging
     b += 256;                                    // error word
+    // split-tile counters and partial accumulators (sized for up to 256 SMs)
+    b += (size_t)4 * 256 * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
     return b;
 }
 
@@ -89,7 +91,8 @@ void free_all(moe_layer* L) {
                     L->counts, L->offsets, L->poff, L->tile_scan, L->chunk_scan, L->row_src,
                     L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->xq, L->xs, L->xq_tok,
                     L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
-                    L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err};
+                    L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err,
+                    L->sk_counters, L->sk_partials};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     moe::tc_free(L);
@@ -183,6 +186,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     A(&L->x_stage, T * H * 2); A(&L->logits_stage, T * E * 4); A(&L->out_stage, T * H * 4);
     A(&L->ids_stage, T * k * 4); A(&L->w_stage, T * k * 4);
     A(&L->d_err, 256);
+    A(&L->sk_counters, (size_t)4 * L->num_sms * 4);
+    A(&L->sk_partials, (size_t)L->num_sms * 2 * 2 * 128 * 128 * 4);
     if (a != cudaSuccess) {
         cudaGetLastError();
         free_all(L);
@@ -211,9 +216,10 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_down_s, L->sh_down_sf, (int)H, (int)I, s);
     }
     // a defined workspace: padding rows of the activation buffers read as zero
-    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row};
-    size_t zn[] = {z.Rp * H, z.Rp * H / 32, z.Rp * I, z.Rp * I / 32, 256, z.Rp * 4};
-    for (int i = 0; i < 6 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
+    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters};
+    size_t zn[] = {z.Rp * H, z.Rp * H / 32, z.Rp * I, z.Rp * I / 32, 256, z.Rp * 4,
+                   (size_t)4 * L->num_sms * 4};
+    for (int i = 0; i < 7 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
     if (c.has_shared) {
         void* zs[] = {L->xq_tok, L->xs_tok, L->hq_sh, L->hs_sh};
         size_t zsn[] = {z.Tpad * H, z.Tpad * H / 32, z.Tpad * I, z.Tpad * I / 32};

@@ -58,6 +58,8 @@ struct TcArgs {
     const int32_t* pos_row;    // down: padded position -> y row (null: identity)
     uint32_t* err;
     uint32_t a_tx;             // TMA bytes of one weight tile
+    int32_t* sk_cnt;           // [gridDim] arrival counters of cut tiles, by first CTA (start at 0)
+    float* sk_part;            // [gridDim][2][kNumA][128][128] partial accumulators
 };
 
 template <bool kGateUp>
@@ -73,6 +75,7 @@ struct TcCfg {
     static constexpr uint32_t kAcc1Col = 128;
     static constexpr uint32_t kSfBase = kGateUp ? 256 : 128;
     static constexpr uint32_t kSfPerStage = 4 * (kNumA + 1);
+    static constexpr int kPrefetch = 8;  // weight tiles prefetched into L2 ahead of the loads
     static_assert(kSfBase + kStages * kSfPerStage <= kTmemCols, "tensor memory budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -101,6 +104,80 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs& a, int t, int MT) {
     return T;
 }
 
+// The work of one CTA: a sequence of (tile, K-stage range) segments.  With at
+// least four waves of tiles, CTA c takes whole tiles c, c+G, ... (CTAs that
+// run together share token tiles and one expert's weights in L2).  With
+// fewer (decode), the tiles x K-stages space is cut into G equal contiguous
+// ranges (stream-K), so every SM streams the same number of weight bytes; a
+// tile cut between CTAs is finished by whichever of them arrives last,
+// summing the partial accumulators in CTA (= K) order, so the result does
+// not depend on arrival order.  A CTA range holds at most two cut pieces
+// (its first and last segment), parked in slots 0 and 1.
+struct Seg {
+    int tile, kb0, kb1;
+    int first_cta, last_cta;  // CTAs sharing this tile (equal: whole tile here)
+};
+
+struct SegIter {
+    int tiles, KB, G, c;
+    bool split;
+    long long total, g, gend;
+    int t;
+
+    __device__ void init(int tiles_, int KB_, int G_, int c_) {
+        tiles = tiles_; KB = KB_; G = G_; c = c_;
+        total = (long long)tiles * KB;
+        // fewer than four waves of whole tiles would leave SMs idle: split,
+        // as long as every CTA still gets at least 4 K-stages
+        split = tiles < 4 * G && total >= 4LL * G;
+        if (split) { g = (long long)c * total / G; gend = (long long)(c + 1) * total / G; }
+        t = c;
+    }
+    __device__ int owner(long long gs) const {  // CTA whose range holds global stage gs
+        return (int)(((gs + 1) * G + total - 1) / total - 1);
+    }
+    __device__ long long range_begin(int cc) const { return (long long)cc * total / G; }
+    __device__ bool next(Seg& s) {
+        if (split) {
+            if (g >= gend) return false;
+            s.tile = (int)(g / KB);
+            s.kb0 = (int)(g % KB);
+            s.kb1 = (int)min((long long)KB, s.kb0 + (gend - g));
+            s.first_cta = owner((long long)s.tile * KB);
+            s.last_cta = owner((long long)s.tile * KB + KB - 1);
+            g += s.kb1 - s.kb0;
+            return true;
+        }
+        if (t >= tiles) return false;
+        s.tile = t; s.kb0 = 0; s.kb1 = KB; s.first_cta = s.last_cta = c;
+        t += G;
+        return true;
+    }
+    // partial-accumulator slot of CTA cc's piece of `tile` (0: its first segment)
+    __device__ int slot(int cc, int tile) const {
+        return (int)(range_begin(cc) / KB) == tile ? 0 : 1;
+    }
+};
+
+template <bool kGateUp>
+__device__ __forceinline__ void emit_token(const TcArgs& a, const Tile& T, int n, int q, int lane,
+                                           float g, float u) {
+    const int p = T.p0 + n;
+    const int fm = 32 * q + lane;
+    if (kGateUp) {
+        const float h = silu_mul(g, u);
+        const int ex = mxfp8_exponent(warp_max(fabsf(h)));
+        const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
+        a.hq[(size_t)p * a.N_out + T.m0 + fm] = (uint8_t)code;
+        if (lane == 0) a.hs[sf_atom_offset(p, (T.m0 + 32 * q) / 32, a.N_out)] = (uint8_t)(ex + 127);
+    } else {
+        const int row = a.pos_row ? __ldg(a.pos_row + p) : p;
+        if (row >= 0) a.y[(size_t)row * a.N_out + T.m0 + fm] = g;
+    }
+}
+
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
 template <bool kGateUp, uint32_t kAFmt>
 __global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
@@ -117,11 +194,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
     const uint32_t tmem_empty = tmem_full + 8u;
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::kStages + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int MT = a.N_out / 128;
     const int KB = a.K / 128;
-    const int total = __ldg(a.tile_scan + a.n_seg) * MT;
+    const int tiles = __ldg(a.tile_scan + a.n_seg) * MT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
@@ -146,18 +224,29 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
         *abort_flag = 1;
         raise_flag(a.err, ERR_TIMEOUT);
     };
+    SegIter it;
+    it.init(tiles, KB, (int)gridDim.x, (int)blockIdx.x);
+    Seg sg;
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const Tile T = decode_tile(a, t, MT);
+            while (ok && it.next(sg)) {
+                const Tile T = decode_tile(a, sg.tile, MT);
                 const uint32_t tx = Cfg::kNumA * a.a_tx + (uint32_t)T.nt * 128u + 512u * (Cfg::kNumA + 1);
                 const size_t atom_a = (size_t)(T.arow / 128) * KB;
                 const size_t atom_b = (size_t)(T.p0 / 128) * KB;
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = sg.kb0; kb < min(sg.kb1, sg.kb0 + Cfg::kPrefetch); ++kb) {
+                    prefetch_tile_l2(&tmA0, kb * 128, T.arow);
+                    if (kGateUp) prefetch_tile_l2(&tmA1, kb * 128, T.arow);
+                }
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (kb + Cfg::kPrefetch < sg.kb1) {
+                        prefetch_tile_l2(&tmA0, (kb + Cfg::kPrefetch) * 128, T.arow);
+                        if (kGateUp) prefetch_tile_l2(&tmA1, (kb + Cfg::kPrefetch) * 128, T.arow);
+                    }
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
                         give_up();
                         ok = false;
@@ -184,14 +273,14 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             bool ok = true;
-            for (int t = blockIdx.x; ok && t < total; t += gridDim.x) {
-                const Tile T = decode_tile(a, t, MT);
+            while (ok && it.next(sg)) {
+                const Tile T = decode_tile(a, sg.tile, MT);
                 if (!mbar_wait(tmem_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
-                for (int kb = 0; kb < KB; ++kb) {
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
                     if (!mbar_wait(full_bar(stage), phase, kWaitLimitNs, abort_flag)) {
                         give_up();
                         ok = false;
@@ -210,7 +299,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t id = idesc_mx(kAFmt, kFmtE4M3, 128, (uint32_t)T.nt, kk, kk);
                         const uint64_t bd = desc_sw128(bt + 32 * kk);
-                        const uint32_t acc = (kb | kk) ? 1u : 0u;
+                        const uint32_t acc = (kb > sg.kb0 || kk) ? 1u : 0u;
                         mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sfb_col, acc);
                         if (kGateUp)
                             mma_mx(tmem + Cfg::kAcc1Col, desc_sw128(st + Cfg::kTileBytes + 32 * kk), bd, id,
@@ -229,14 +318,38 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
         const int q = warp & 3;  // the TMEM lane quarter this warp may access
         const int fm = 32 * q + lane;
         const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        const bool leader = warp == 2 && lane == 0;
         uint32_t acc_phase = 0;
-        for (int t = blockIdx.x; t < total; t += gridDim.x) {
-            const Tile T = decode_tile(a, t, MT);
+        while (it.next(sg)) {
+            const Tile T = decode_tile(a, sg.tile, MT);
             if (!mbar_wait(tmem_full, acc_phase, kWaitLimitNs, abort_flag)) {
                 if (lane == 0) give_up();
                 break;
             }
             tc_fence_after();
+            acc_phase ^= 1u;
+            if (sg.first_cta == sg.last_cta) {
+                // whole tile: straight from tensor memory
+                for (int c0 = 0; c0 < T.nt; c0 += 16) {
+                    uint32_t g[16], u[16];
+                    tmem_ld16(tq + (uint32_t)c0, g);
+                    if (kGateUp) tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
+                    tmem_ld_wait();
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) {
+                        if (c0 + i >= T.nvalid) break;  // warp-uniform
+                        emit_token<kGateUp>(a, T, c0 + i, q, lane, __uint_as_float(g[i]),
+                                            kGateUp ? __uint_as_float(u[i]) : 0.f);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(tmem_empty);
+                continue;
+            }
+            // a piece of a split tile: park the partial sums, count arrivals
+            float* part = a.sk_part +
+                          ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * Cfg::kNumA * 128 * 128;
             for (int c0 = 0; c0 < T.nt; c0 += 16) {
                 uint32_t g[16], u[16];
                 tmem_ld16(tq + (uint32_t)c0, g);
@@ -244,26 +357,33 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
-                    const int n = c0 + i;
-                    if (n >= T.nvalid) break;  // warp-uniform
-                    const int p = T.p0 + n;
-                    if (kGateUp) {
-                        const float h = silu_mul(__uint_as_float(g[i]), __uint_as_float(u[i]));
-                        const int ex = mxfp8_exponent(warp_max(fabsf(h)));
-                        const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
-                        a.hq[(size_t)p * a.N_out + T.m0 + fm] = (uint8_t)code;
-                        if (lane == 0)
-                            a.hs[sf_atom_offset(p, (T.m0 + 32 * q) / 32, a.N_out)] = (uint8_t)(ex + 127);
-                    } else {
-                        const int row = a.pos_row ? __ldg(a.pos_row + p) : p;
-                        if (row >= 0) a.y[(size_t)row * a.N_out + T.m0 + fm] = __uint_as_float(g[i]);
-                    }
+                    part[(size_t)(c0 + i) * 128 + fm] = __uint_as_float(g[i]);
+                    if (kGateUp) part[(size_t)(128 + c0 + i) * 128 + fm] = __uint_as_float(u[i]);
                 }
             }
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
-            acc_phase ^= 1u;
+            __threadfence();
+            epi_bar();
+            if (leader) {
+                const int nparts = sg.last_cta - sg.first_cta + 1;
+                *last_flag = (atomicAdd(a.sk_cnt + sg.first_cta, 1) == nparts - 1);
+            }
+            epi_bar();
+            if (!*last_flag) continue;
+            __threadfence();
+            // the last piece to arrive sums all pieces in K order and finishes the tile
+            for (int n = 0; n < T.nvalid; ++n) {
+                float g = 0.f, u = 0.f;
+                for (int cc = sg.first_cta; cc <= sg.last_cta; ++cc) {
+                    const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * Cfg::kNumA * 128 * 128;
+                    g += __ldcg(pp + (size_t)n * 128 + fm);
+                    if (kGateUp) u += __ldcg(pp + (size_t)(128 + n) * 128 + fm);
+                }
+                emit_token<kGateUp>(a, T, n, q, lane, g, u);
+            }
+            if (leader) a.sk_cnt[sg.first_cta] = 0;
         }
     }
 
@@ -393,6 +513,8 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     g.hs = L->hs;
     g.err = L->d_err;
     g.a_tx = st->fp4_tx;
+    g.sk_part = L->sk_partials;
+    g.sk_cnt = L->sk_counters;
     cudaError_t e = tc_launch<true, kFmtE2M1>(L, st->gate, st->up, st->xq, g, s);
     if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
@@ -407,6 +529,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     d.hs = nullptr;
     d.y = L->y;
     d.pos_row = L->pos_row;
+    d.sk_cnt = L->sk_counters + L->num_sms;
     e = tc_launch<false, kFmtE2M1>(L, st->down, st->down, st->hq, d, s);
     if (e != cudaSuccess || !c.has_shared) return e;
     TcArgs sg = g;
@@ -421,6 +544,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     sg.hq = L->hq_sh;
     sg.hs = L->hs_sh;
     sg.a_tx = 16384;
+    sg.sk_cnt = L->sk_counters + 2 * L->num_sms;
     e = tc_launch<true, kFmtE4M3>(L, st->sh_gate, st->sh_up, st->xq_tok, sg, s);
     if (e != cudaSuccess) return e;
     TcArgs sd = sg;
@@ -433,6 +557,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     sd.hs = nullptr;
     sd.y = L->y_sh;
     sd.pos_row = nullptr;
+    sd.sk_cnt = L->sk_counters + 3 * L->num_sms;
     return tc_launch<false, kFmtE4M3>(L, st->sh_down, st->sh_down, st->hq_sh, sd, s);
 }
 

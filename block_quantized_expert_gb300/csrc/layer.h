@@ -50,6 +50,8 @@ struct moe_layer {
     int32_t* ids_stage;   // [T][k]
     float* w_stage;       // [T][k]
     uint32_t* d_err;      // sticky device error flags
+    int32_t* sk_counters; // [4][num_sms] arrival counters of split tiles (zeroed per forward)
+    float* sk_partials;   // [num_sms][2][2][128][128] partial accumulators of split tiles
 
     void* tc;             // tensor-core kernel state (tensor maps), or null
     unsigned long long launches;  // kernels enqueued so far

@@ -14,9 +14,9 @@ namespace moe {
 // One warp per token.  The top-k by score s = sqrt(softplus(logit)) is the
 // top-k by logit (s is strictly increasing), so the selection compares the
 // fp32 logits exactly: k warp-wide argmax passes, equal values to the lower
-// expert index (guide, section 1: SQRT_SOFTPLUS gating, top-k).  The k
-// selected scores and the weights w_j = w_scale * s_j / sum s (guide,
-// section 3.2) are evaluated in fp64 and rounded once to fp32.
+// expert index (guide, section 1: SQRT_SOFTPLUS gating, top-k).  Lane j < k
+// then evaluates s_j in fp32 and every lane sums s_0..s_{k-1} in that order;
+// w_j = w_scale * s_j / sum (guide, section 3.2).
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
                                                int k, float w_scale, int32_t* __restrict__ ids,
                                                float* __restrict__ w, uint32_t* err) {
@@ -25,51 +25,37 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
     if (t >= T) return;
     const float* row = logits + (size_t)t * E;
     uint32_t taken = 0;  // bit i <-> expert lane + 32 i
-    int sel[kMaxTopK];
-#pragma unroll
-    for (int j = 0; j < kMaxTopK; ++j) {
-        sel[j] = -1;
-        if (j < k) {
-            float best = -INFINITY;
-            int bi = INT_MAX;
-            for (int i = 0, e = lane; e < E; ++i, e += 32) {
-                if ((taken >> i) & 1u) continue;
-                float v = __ldg(row + e);
-                if (v > best || (v == best && e < bi)) { best = v; bi = e; }
-            }
-#pragma unroll
-            for (int o = 16; o; o >>= 1) {
-                float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-                int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-                if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-            }
-            if (bi < E) {
-                sel[j] = bi;
-                if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
-            }
+    int my_sel = -1;     // lane j keeps the j-th selection
+    float my_logit = 0.f;
+    bool ok = true;
+    for (int j = 0; j < k; ++j) {
+        float best = -INFINITY;
+        int bi = INT_MAX;
+        for (int i = 0, e = lane; e < E; ++i, e += 32) {
+            if ((taken >> i) & 1u) continue;
+            float v = __ldg(row + e);
+            if (v > best || (v == best && e < bi)) { best = v; bi = e; }
         }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+            float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
+            int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
+            if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
+        }
+        if (bi >= E) { ok = false; bi = -1; }
+        if (lane == j) { my_sel = bi; my_logit = best; }
+        if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     }
-    if (lane == 0) {
-        double s[kMaxTopK], sum = 0.0;
-        bool ok = true;
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < k) {
-                if (sel[j] < 0) { ok = false; s[j] = 0.0; continue; }
-                double l = (double)row[sel[j]];
-                s[j] = sqrt((l > 0.0 ? l : 0.0) + log1p(exp(-fabs(l))));
-                sum += s[j];
-            }
-        }
-        if (!ok) raise_flag(err, ERR_BAD_ID);
-#pragma unroll
-        for (int j = 0; j < kMaxTopK; ++j) {
-            if (j < k) {
-                ids[(size_t)t * k + j] = sel[j];
-                w[(size_t)t * k + j] = ok ? (float)((double)w_scale * s[j] / sum) : 0.0f;
-            }
-        }
+    float s = 0.f;
+    if (lane < k && my_sel >= 0)
+        s = sqrtf(fmaxf(my_logit, 0.f) + log1pf(expf(-fabsf(my_logit))));
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, s, j);
+    if (lane < k) {
+        ids[(size_t)t * k + lane] = ok ? my_sel : -1;
+        w[(size_t)t * k + lane] = ok ? w_scale * s / sum : 0.0f;
     }
+    if (!ok && lane == 0) raise_flag(err, ERR_BAD_ID);
 }
 
 cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,
@@ -152,7 +138,7 @@ __global__ void __launch_bounds__(1024) k_permute(
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
     int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
     int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
-    int T, uint32_t* err) {
+    int T, uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
     extern __shared__ int dyn[];  // cnt, cursor, s_off, s_poff [E] each; then wc [32][E] bytes
     int* cnt = dyn;
     int* cursor = dyn + E;
@@ -165,6 +151,7 @@ __global__ void __launch_bounds__(1024) k_permute(
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
 
     for (int e = tid; e < E; e += 1024) { cnt[e] = 0; cursor[e] = 0; }
+    for (int i = tid; i < n_zero; i += 1024) zero[i] = 0;  // the GEMMs' split-tile counters
     if (tid == 0) bad = 0;
     __syncthreads();
     for (int r = tid; r < R; r += 1024) {
@@ -248,7 +235,8 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
     const size_t smem = (size_t)48 * L->cfg.n_experts;
     k_permute<<<1, 1024, smem, s>>>(ids, R, L->cfg.n_experts, offsets, row_src, row_dst, L->counts,
                                  L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
-                                 L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err);
+                                 L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err,
+                                 L->sk_counters, L->sk_counters ? 4 * L->num_sms : 0);
     L->launches += 1;
     return cudaGetLastError();
 }
@@ -261,7 +249,7 @@ cudaError_t launch_permute_raw(const int32_t* ids, int T, int k, int E, int32_t*
                                int32_t* pos_row, cudaStream_t s) {
     const size_t smem = (size_t)48 * E;
     k_permute<<<1, 1024, smem, s>>>(ids, T * k, E, offsets, row_src, row_dst, counts, poff, tile_scan,
-                                 chunk_scan, row_pos, pos_row, nullptr, T, nullptr);
+                                 chunk_scan, row_pos, pos_row, nullptr, T, nullptr, nullptr, 0);
     return cudaGetLastError();
 }
 

@@ -83,6 +83,12 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
         ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
 }
 
+// Fetch a tile into L2 only (no shared memory, no barrier).
+__device__ __forceinline__ void prefetch_tile_l2(const void* tmap, int x, int y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(tmap), "r"(x), "r"(y) : "memory");
+}
+
 __device__ __forceinline__ void prefetch_tmap(const void* tmap) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }

@@ -48,7 +48,9 @@ def _route_check(layer, logits, k, w_scale=1.5):
     ids, w = G.route_dev(layer, logits, k)
     rid, rw = orc.route_learned(logits, k, w_scale)
     assert np.array_equal(ids.cpu().numpy(), rid)
-    assert np.allclose(w.cpu().numpy(), rw, rtol=2e-7, atol=0)
+    # fp32 evaluation of exp, log1p, sqrt, a k-term sum and one division:
+    # each routing weight (<= w_scale) is within 8 fp32 roundings of the value
+    assert np.abs(w.cpu().numpy() - rw).max() <= 8 * 2.0 ** -24 * w_scale
     return ids, w, rid, rw
 
 
