@@ -171,3 +171,267 @@ extern "C" int probe_mma(const uint8_t* a, const uint8_t* b, const uint8_t* sfa,
     k_probe_mma<<<1, 128>>>(ta, tb, sfa, sfb, mode, a_tx, a_fmt, d_out, sf_dump, flags);
     return (int)cudaDeviceSynchronize();
 }
+
+// ------------------------------------------------------------------------
+// Microbenchmarks (timing only; results are not checked for values).
+// ------------------------------------------------------------------------
+
+// Streams `tiles_per_cta` x KB fp4 weight tiles (128 x 128) per CTA through a
+// `stages`-deep TMA pipeline.  mode bit 0: issue one M=128,N=32 block-scaled
+// MMA group per stage (else the consumer frees the stage at once); bit 1:
+// prefetch tiles into L2 `pf` stages ahead.  CTA 0 records, per stage, the
+// global time the load was issued and the time the consumer saw it land.
+__global__ void __launch_bounds__(64, 1)
+k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int stages, int mode, int pf,
+         unsigned long long* stamps, int* ok_out, int layout, uint32_t box_tx, uint32_t slot) {
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + stages * slot + 16384 + 1024);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * stages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t b0 = smem_u32(bars);
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) { mbar_init(b0 + 8 * s, 1); mbar_init(b0 + 8 * (stages + s), 1); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tslot), 256);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int total = tiles_per_cta * KB;
+    bool ok = true;
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < total && ok; ++i) {
+            const int s = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            const int row = (blockIdx.x + (i / KB) * gridDim.x) * 128, kb = i % KB;
+            if ((mode & 2) && i + pf < total) {
+                const int j = i + pf;
+                prefetch_tile_l2(&tmA, (j % KB) * 128, (blockIdx.x + (j / KB) * gridDim.x) * 128);
+            }
+            if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
+            mbar_arrive_expect_tx(b0 + 8 * s, box_tx);
+            if (blockIdx.x == 0 && i < 256) stamps[2 * i] = globaltimer();
+            if (layout == 1)  // contiguous 8 KB tiles: 64-byte rows back to back
+                tma_load_2d(smem_u32(sm + s * slot), &tmA, 0, (blockIdx.x * tiles_per_cta * KB + i) * 128, b0 + 8 * s);
+            else if (layout == 3)  // 256-row fp4 box (two 128-row tiles per copy)
+                tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row, b0 + 8 * s);
+            else
+                tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row, b0 + 8 * s);
+        }
+    } else if (warp == 1 && lane == 0) {
+        for (int i = 0; i < total && ok; ++i) {
+            const int s = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            if (!mbar_wait(b0 + 8 * s, ph, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
+            if (blockIdx.x == 0 && i < 256) stamps[2 * i + 1] = globaltimer();
+            if (mode & 1) {
+                // bit 2: no tcgen05 fence; bit 3: 16 MMAs per stage; bit 4: N = 128;
+                // bit 5: unscaled kind::f8f6f4 instead of the block-scaled MMA
+                if (!(mode & 4)) tc_fence_after();
+                const uint32_t a = smem_u32(sm + s * slot), b = smem_u32(sm + stages * slot);
+                const uint32_t nn = (mode & 16) ? 128 : 32;
+                const int reps = (mode & 8) ? 4 : 1;
+                for (int rr = 0; rr < reps; ++rr)
+                    for (int kk = 0; kk < 4; ++kk) {
+                        if (mode & 32) {
+                            const uint32_t id = (kFmtE2M1 << 7) | (kFmtE4M3 << 10) | ((nn >> 3) << 17) | (8u << 24) | (1u << 4);
+                            asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+                                         "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}"
+                                         ::"r"(tmem), "l"(desc_sw128(a + 32 * kk)), "l"(desc_sw128(b + 32 * kk)), "r"(id),
+                                           "r"((uint32_t)(kk > 0 || rr > 0)) : "memory");
+                        } else {
+                            mma_mx(tmem, desc_sw128(a + 32 * kk), desc_sw128(b + 32 * kk),
+                                   idesc_mx(kFmtE2M1, kFmtE4M3, 128, nn, kk, kk), tmem + 128, tmem + 132,
+                                   (kk > 0 || rr > 0) ? 1u : 0u);
+                        }
+                    }
+                mma_commit(b0 + 8 * (stages + s));
+            } else {
+                mbar_arrive(b0 + 8 * (stages + s));
+            }
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) { spin_ns(200000); if (threadIdx.x == 0) atomicExch(ok_out, 0); }
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 256); }
+}
+
+// layout 0: fp4 [rows][4096] box 128x128 (rows 2 KB apart); 1: fp4 viewed as
+// contiguous 64-byte rows (each box = 8 KB contiguous); 2: uint8 [rows][4096]
+// box 128x128 (16 KB); 3: fp4 box 128 x 256 rows (16 KB of codes, 32 KB slot).
+extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tiles_per_cta, int stages, int mode,
+                            int pf, unsigned long long* stamps, int* ok, float* ms, int layout) {
+    CUtensorMap ta;
+    int r;
+    uint32_t tx = 8192, slot = 16384;
+    if (layout == 1) r = make_map(&ta, a, 128, (uint64_t)rows * 32, 128, true);
+    else if (layout == 2) { r = make_map(&ta, a, 4096, (uint64_t)rows / 2, 128, false); tx = 16384; }
+    else if (layout == 3) { r = make_map(&ta, a, 4096, (uint64_t)rows, 256, true); tx = 16384; slot = 32768; }
+    else r = make_map(&ta, a, 4096, (uint64_t)rows, 128, true);
+    if (r) return 1000 + r;
+    const long long need = (long long)(grid * (tiles_per_cta - 1) + grid) * 128 + (layout == 3 ? 128 : 0);
+    if (need > (layout == 2 ? rows / 2 : rows)) return 3;
+    if (layout == 1 && (long long)grid * tiles_per_cta * 32 * 128 > rows * 32) return 4;
+    if (slot == 32768 && stages > 6) return 5;
+    // tiles + B tile + barrier offset + barriers/slot + 1024 alignment slack
+    const int smem = stages * (int)slot + 16384 + 1024 + 512 + 1024;
+    cudaFuncSetAttribute(k_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_stream<<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// Plain HBM read stream: every thread sums 16-byte loads, grid-strided.
+__global__ void k_read(const uint4* __restrict__ p, long long n, unsigned int* sink) {
+    unsigned int acc = 0;
+    for (long long i = blockIdx.x * (long long)blockDim.x + threadIdx.x; i < n; i += (long long)gridDim.x * blockDim.x) {
+        const uint4 v = __ldcs(p + i);
+        acc ^= v.x ^ v.y ^ v.z ^ v.w;
+    }
+    if (acc == 0x12345678u) atomicAdd(sink, 1u);
+}
+
+extern "C" int probe_read(const uint8_t* p, long long bytes, int grid, int block, unsigned int* sink, float* ms) {
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_read<<<grid, block>>>(reinterpret_cast<const uint4*>(p), bytes / 16, sink);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// Block-scaled MMA issue rate: one thread per CTA issues `iters` x 4 MMAs of
+// M=128, N=n, K=32 (e2m1 or e4m3 A, e4m3 B) on shared-memory-resident tiles.
+__global__ void __launch_bounds__(64, 1) k_mma_peak(int iters, int n, uint32_t a_fmt, int* ok_out) {
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 16384 + 32768);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < (16384 + 32768) / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sm)[i] = 0x38383838u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (threadIdx.x == 0) { mbar_init(smem_u32(bar), 1); *abort_flag = 0; fence_mbar_init(); }
+    if (warp == 1) tmem_alloc(smem_u32(slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (threadIdx.x == 0) {
+        const uint32_t a = smem_u32(sm), b = smem_u32(sm + 16384);
+        for (int it = 0; it < iters; ++it)
+            for (int kk = 0; kk < 4; ++kk)
+                mma_mx(tmem, desc_sw128(a + 32 * kk), desc_sw128(b + 32 * kk),
+                       idesc_mx(a_fmt, kFmtE4M3, 128, (uint32_t)n, kk, kk), tmem + 256, tmem + 260,
+                       (it | kk) ? 1u : 0u);
+        mma_commit(smem_u32(bar));
+        if (!mbar_wait(smem_u32(bar), 0, 2000000000ull, abort_flag)) { atomicExch(ok_out, 0); spin_ns(200000); }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+extern "C" int probe_mma_peak(int grid, int iters, int n, uint32_t a_fmt, int* ok, float* ms) {
+    const int smem = 16384 + 32768 + 1024 + 64;
+    cudaFuncSetAttribute(k_mma_peak, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_mma_peak<<<grid, 64, smem>>>(iters, n, a_fmt, ok);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// The same stream with the fp4 tiles moved by 128 threads with 8-byte
+// cp.async copies (no TMA) into the 16-byte-aligned unpacked layout (code
+// group c of row r -> slot (c ^ (r % 8)) of the 128-byte row), completion
+// tracked by cp.async.mbarrier.arrive.noinc on the stage's barrier.
+__global__ void __launch_bounds__(160, 1)
+k_stream_lsu(const uint8_t* __restrict__ w, int tiles_per_cta, int KB, int stages, unsigned long long* stamps,
+             int* ok_out) {
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(sm + stages * 16384);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(bars + 2 * stages);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t b0 = smem_u32(bars);
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < stages; ++st) { mbar_init(b0 + 8 * st, 128); mbar_init(b0 + 8 * (stages + st), 1); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    const int total = tiles_per_cta * KB;
+    if (warp < 4) {
+        const int t = threadIdx.x;
+        for (int i = 0; i < total; ++i) {
+            const int st = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            const long long row0 = (long long)(blockIdx.x + (i / KB) * gridDim.x) * 128;
+            const int kb = i % KB;
+            if (!mbar_wait(b0 + 8 * (stages + st), ph ^ 1u, 200000000ull, abort_flag)) { *abort_flag = 1; break; }
+            if (blockIdx.x == 0 && t == 0 && i < 256) stamps[2 * i] = globaltimer();
+            const uint32_t dst0 = smem_u32(sm + st * 16384);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int idx = j * 128 + t, r = idx >> 3, c = idx & 7;
+                const uint8_t* src = w + (row0 + r) * 2048 + kb * 64 + c * 8;
+                const uint32_t dst = dst0 + r * 128 + ((c ^ (r & 7)) << 4);
+                asm volatile("cp.async.ca.shared.global [%0], [%1], 8;" ::"r"(dst), "l"(src) : "memory");
+            }
+            asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(b0 + 8 * st) : "memory");
+        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+    } else if (threadIdx.x == 128) {
+        for (int i = 0; i < total; ++i) {
+            const int st = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            if (!mbar_wait(b0 + 8 * st, ph, 200000000ull, abort_flag)) { *abort_flag = 1; break; }
+            if (blockIdx.x == 0 && i < 256) stamps[2 * i + 1] = globaltimer();
+            mbar_arrive(b0 + 8 * (stages + st));
+        }
+    }
+    __syncthreads();
+    if (*abort_flag) { spin_ns(200000); if (threadIdx.x == 0) atomicExch(ok_out, 0); }
+}
+
+extern "C" int probe_stream_lsu(const uint8_t* a, long long rows, int grid, int tiles_per_cta, int stages,
+                                unsigned long long* stamps, int* ok, float* ms) {
+    if ((long long)(grid * (tiles_per_cta - 1) + grid) * 128 > rows) return 3;
+    const int smem = stages * 16384 + 1024 + 16 * stages + 64;
+    cudaFuncSetAttribute(k_stream_lsu, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_stream_lsu<<<grid, 160, smem>>>(a, tiles_per_cta, 32, stages, stamps, ok);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}

@@ -1,0 +1,107 @@
+#!/usr/bin/env python
+"""Microbenchmarks of the sm_103a building blocks (tests/csrc/tc_probe.cu):
+a plain HBM read stream, the block-scaled MMA issue rate, and TMA weight
+streaming with and without MMAs.  Prints one line per case and writes all
+results as JSON (default gpurun_out/microbench_tc.json).  Timing only.
+
+    python tests/microbench_tc.py [--out PATH]
+"""
+import argparse
+import ctypes as C
+import json
+import os
+import subprocess
+
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+
+
+def load():
+    lib_path = os.path.join(HERE, "_build", "libtcprobe.so")
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
+    subprocess.run(["/usr/local/cuda/bin/nvcc", "-gencode", "arch=compute_103a,code=sm_103a", "-O2",
+                    "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
+                    "-I", os.path.join(ROOT, "block_quantized_expert_gb300", "csrc"),
+                    "-o", lib_path, os.path.join(HERE, "csrc", "tc_probe.cu")], check=True)
+    lib = C.CDLL(lib_path)
+    vp = C.c_void_p
+    lib.probe_read.argtypes = [vp, C.c_longlong, C.c_int, C.c_int, vp, vp]
+    lib.probe_stream.argtypes = [vp, C.c_longlong, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp,
+                                 vp, C.c_int]
+    lib.probe_stream_lsu.argtypes = [vp, C.c_longlong, C.c_int, C.c_int, C.c_int, vp, vp, vp]
+    lib.probe_mma_peak.argtypes = [C.c_int, C.c_int, C.c_int, C.c_uint32, vp, vp]
+    return lib
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "microbench_tc.json"))
+    args = ap.parse_args()
+    lib = load()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    ms = C.c_float()
+    ok = torch.ones(1, dtype=torch.int32, device="cuda")
+    out = {"sms": sms}
+
+    buf = torch.zeros(4 << 30, dtype=torch.uint8, device="cuda")
+    sink = torch.zeros(1, dtype=torch.int32, device="cuda")
+    for grid, block in ((sms * 4, 512), (sms * 8, 512), (sms * 16, 256)):
+        for _ in range(3):
+            rc = lib.probe_read(buf.data_ptr(), buf.numel(), grid, block, sink.data_ptr(), C.byref(ms))
+        out[f"read_{grid}x{block}_GBs"] = round(buf.numel() / ms.value / 1e6, 1)
+        print("read", grid, block, rc, out[f"read_{grid}x{block}_GBs"], flush=True)
+    del buf
+
+    rows = sms * 128 * 16
+    A = torch.zeros(rows * 2048, dtype=torch.uint8, device="cuda")
+    stamps = torch.zeros(512, dtype=torch.int64, device="cuda")
+
+    def stage_stats():
+        st = stamps.cpu().tolist()
+        lat = sorted((st[2 * i + 1] - st[2 * i]) / 1000 for i in range(64, 200))
+        per = sorted((st[2 * i + 3] - st[2 * i + 1]) / 1000 for i in range(64, 200))
+        return lat[len(lat) // 2], per[len(per) // 2]
+
+    # layout: 0 fp4 128-row box, 1 fp4 contiguous tiles, 2 uint8 128-row box, 3 fp4 256-row box
+    # mode: 1 = MMAs (N=32), |8 = 16 MMAs per stage, |16 = N=128, |32 = unscaled kind
+    cases = [(0, 8192, 4, 0), (0, 8192, 8, 0), (1, 8192, 4, 0), (2, 16384, 4, 0), (2, 16384, 8, 0),
+             (3, 16384, 4, 0), (0, 8192, 4, 1), (3, 16384, 4, 1), (0, 8192, 4, 1 | 16),
+             (0, 8192, 4, 1 | 8), (0, 8192, 4, 1 | 32)]
+    for layout, box, stages, mode in cases:
+        for _ in range(2):
+            ok.fill_(1)
+            rc = lib.probe_stream(A.data_ptr(), rows, sms, 8, stages, mode, 0, stamps.data_ptr(),
+                                  ok.data_ptr(), C.byref(ms), layout)
+        lat, per = stage_stats()
+        key = f"tma_layout{layout}_stages{stages}_mode{mode}"
+        out[key] = {"GBs": round(sms * 8 * 32 * box / ms.value / 1e6, 1), "issue_to_land_us": lat,
+                    "us_per_stage": per, "ok": int(ok.item()), "rc": rc}
+        print(key, out[key], flush=True)
+    for stages in (4, 8):
+        ok.fill_(1)
+        for _ in range(2):
+            rc = lib.probe_stream_lsu(A.data_ptr(), rows, sms, 8, stages, stamps.data_ptr(), ok.data_ptr(),
+                                      C.byref(ms))
+        lat, per = stage_stats()
+        out[f"cpasync_stages{stages}"] = {"GBs": round(sms * 8 * 32 * 8192 / ms.value / 1e6, 1),
+                                          "us_per_stage": per, "ok": int(ok.item()), "rc": rc}
+        print(f"cpasync_stages{stages}", out[f"cpasync_stages{stages}"], flush=True)
+    del A
+
+    for fmt in (5, 0):
+        for n in (32, 128, 256):
+            iters = 20000 if n >= 128 else 40000
+            ok.fill_(1)
+            lib.probe_mma_peak(sms, 100, n, fmt, ok.data_ptr(), C.byref(ms))
+            rc = lib.probe_mma_peak(sms, iters, n, fmt, ok.data_ptr(), C.byref(ms))
+            tf = sms * iters * 4 * 2 * 128 * n * 32 / ms.value / 1e9
+            out[f"mma_afmt{fmt}_n{n}_TFs"] = round(tf, 1)
+            print("mma", fmt, n, rc, int(ok.item()), round(tf, 1), flush=True)
+    os.makedirs(os.path.dirname(args.out), exist_ok=True)
+    json.dump(out, open(args.out, "w"), indent=1)
+
+
+if __name__ == "__main__":
+    main()
