@@ -53,6 +53,7 @@ const char* check_config(const moe_config* c) {
     if (c->max_tokens < 1 || (long long)c->max_tokens * c->top_k > (1LL << 30))
         return "max_tokens out of range";
     if (c->hidden > 8192 || c->inter > 8192) return "hidden/inter larger than 8192";
+    if (c->hidden % 256) return "hidden must be a multiple of 256";
     if (!std::isfinite(c->w_scale)) return "w_scale must be finite";
     return nullptr;
 }
@@ -85,9 +86,9 @@ cudaError_t dalloc(P** p, size_t bytes, size_t* total) {
 }
 
 void free_all(moe_layer* L) {
-    void* ptrs[] = {L->gate_q, L->gate_s, L->up_q, L->up_s, L->down_q, L->down_s,
-                    L->sh_gate_q, L->sh_gate_s, L->sh_up_q, L->sh_up_s, L->sh_down_q, L->sh_down_s,
-                    L->gate_sf, L->up_sf, L->down_sf, L->sh_gate_sf, L->sh_up_sf, L->sh_down_sf,
+    void* ptrs[] = {L->gu_q, L->gate_s, L->up_s, L->down_q, L->down_s,
+                    L->sh_gu_q, L->sh_gate_s, L->sh_up_s, L->sh_down_q, L->sh_down_s,
+                    L->gu_sf, L->down_sf, L->sh_gu_sf, L->sh_down_sf,
                     L->counts, L->offsets, L->poff, L->tile_scan, L->chunk_scan, L->row_src,
                     L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->xq, L->xs, L->xq_tok,
                     L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
@@ -162,14 +163,14 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     const size_t gq = E * I * H / 2, gs = E * I * H / 32, dq = E * H * I / 2, ds = E * H * I / 32;
     cudaError_t a = cudaSuccess;
     auto A = [&](auto** p, size_t bytes) { if (a == cudaSuccess) a = dalloc(p, bytes, &total); };
-    A(&L->gate_q, gq); A(&L->gate_s, gs); A(&L->up_q, gq); A(&L->up_s, gs);
+    A(&L->gu_q, 2 * gq); A(&L->gate_s, gs); A(&L->up_s, gs);
     A(&L->down_q, dq); A(&L->down_s, ds);
-    A(&L->gate_sf, gs); A(&L->up_sf, gs); A(&L->down_sf, ds);
+    A(&L->gu_sf, 2 * gs); A(&L->down_sf, ds);
     if (c.has_shared) {
-        A(&L->sh_gate_q, I * H); A(&L->sh_gate_s, (I / 128) * (H / 128));
-        A(&L->sh_up_q, I * H); A(&L->sh_up_s, (I / 128) * (H / 128));
+        A(&L->sh_gu_q, 2 * I * H); A(&L->sh_gate_s, (I / 128) * (H / 128));
+        A(&L->sh_up_s, (I / 128) * (H / 128));
         A(&L->sh_down_q, H * I); A(&L->sh_down_s, (H / 128) * (I / 128));
-        A(&L->sh_gate_sf, I * H / 32); A(&L->sh_up_sf, I * H / 32); A(&L->sh_down_sf, H * I / 32);
+        A(&L->sh_gu_sf, 2 * I * H / 32); A(&L->sh_down_sf, H * I / 32);
     }
     A(&L->counts, E * 4); A(&L->offsets, (E + 1) * 4); A(&L->poff, (E + 1) * 4);
     A(&L->tile_scan, (E + 1) * 4); A(&L->chunk_scan, (E + 1) * 4);
@@ -199,21 +200,30 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     auto C = [&](void* dst, const void* src, size_t n) {
         if (a == cudaSuccess) a = cudaMemcpyAsync(dst, src, n, cudaMemcpyDefault, s);
     };
-    C(L->gate_q, w->gate_q, gq); C(L->gate_s, w->gate_s, gs);
-    C(L->up_q, w->up_q, gq); C(L->up_s, w->up_s, gs);
+    // gate/up codes interleaved per 128 features (gate block, then up block)
+    auto C2 = [&](void* dst, size_t dpitch, const void* src, size_t width, size_t height) {
+        if (a == cudaSuccess)
+            a = cudaMemcpy2DAsync(dst, dpitch, src, width, width, height, cudaMemcpyDefault, s);
+    };
+    const size_t blk = 128 * (H / 2);  // one 128-row block of fp4 codes
+    C2(L->gu_q, 2 * blk, w->gate_q, blk, E * (I / 128));
+    C2(L->gu_q + blk, 2 * blk, w->up_q, blk, E * (I / 128));
+    C(L->gate_s, w->gate_s, gs); C(L->up_s, w->up_s, gs);
     C(L->down_q, w->down_q, dq); C(L->down_s, w->down_s, ds);
     if (c.has_shared) {
-        C(L->sh_gate_q, w->sh_gate_q, I * H); C(L->sh_gate_s, w->sh_gate_s, (I / 128) * (H / 128));
-        C(L->sh_up_q, w->sh_up_q, I * H); C(L->sh_up_s, w->sh_up_s, (I / 128) * (H / 128));
+        C2(L->sh_gu_q, 2 * 128 * H, w->sh_gate_q, 128 * H, I / 128);
+        C2(L->sh_gu_q + 128 * H, 2 * 128 * H, w->sh_up_q, 128 * H, I / 128);
+        C(L->sh_gate_s, w->sh_gate_s, (I / 128) * (H / 128));
+        C(L->sh_up_s, w->sh_up_s, (I / 128) * (H / 128));
         C(L->sh_down_q, w->sh_down_q, H * I); C(L->sh_down_s, w->sh_down_s, (H / 128) * (I / 128));
     }
-    if (a == cudaSuccess) a = moe::repack_sf(L->gate_s, L->gate_sf, (int)E, (int)I, (int)H, s);
-    if (a == cudaSuccess) a = moe::repack_sf(L->up_s, L->up_sf, (int)E, (int)I, (int)H, s);
-    if (a == cudaSuccess) a = moe::repack_sf(L->down_s, L->down_sf, (int)E, (int)H, (int)I, s);
+    if (a == cudaSuccess) a = moe::pack_sf_pairs(L->gate_s, L->up_s, L->gu_sf, (int)E, (int)(I / 128), (int)H, 0, s);
+    if (a == cudaSuccess) a = moe::pack_sf_pairs(L->down_s, nullptr, L->down_sf, (int)E, (int)(H / 256), (int)I, 1, s);
     if (c.has_shared) {
-        if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_gate_s, L->sh_gate_sf, (int)I, (int)H, s);
-        if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_up_s, L->sh_up_sf, (int)I, (int)H, s);
-        if (a == cudaSuccess) a = moe::expand_tile_sf(L->sh_down_s, L->sh_down_sf, (int)H, (int)I, s);
+        if (a == cudaSuccess)
+            a = moe::pack_sf_pairs(L->sh_gate_s, L->sh_up_s, L->sh_gu_sf, 1, (int)(I / 128), (int)H, 2, s);
+        if (a == cudaSuccess)
+            a = moe::pack_sf_pairs(L->sh_down_s, nullptr, L->sh_down_sf, 1, (int)(H / 256), (int)I, 3, s);
     }
     // a defined workspace: padding rows of the activation buffers read as zero
     void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters};

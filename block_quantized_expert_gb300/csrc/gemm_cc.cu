@@ -97,14 +97,18 @@ __global__ void __launch_bounds__(kCCThreads) k_gemm_cc(CCArgs a) {
             float acc1[kChunk], acc2[kChunk];
 #pragma unroll
             for (int n = 0; n < kChunk; ++n) { acc1[n] = 0.f; acc2[n] = 0.f; }
+            // gate/up codes are interleaved per 128 features (gate block, then up
+            // block); down codes are row-major per segment
+            const size_t prow = kGateUp ? (size_t)((kWKind == 0 ? e : 0) * (a.N / 128) + j / 128) * 256 + (j % 128)
+                                        : seg_row0 + j;
             for (int b = lane; b < KB; b += 32) {
                 float w1[32];
-                load_weight_block<kWKind>(a.w1_q, seg_row0 + j, a.K, b, w1);
+                load_weight_block<kWKind>(a.w1_q, prow, a.K, b, w1);
                 const float s1 = weight_scale<kWKind>(a.w1_s, seg_row0, j, a.K, b);
                 float w2[32];
                 float s2 = 0.f;
                 if (kGateUp) {
-                    load_weight_block<kWKind>(a.w2_q, seg_row0 + j, a.K, b, w2);
+                    load_weight_block<kWKind>(a.w2_q, prow + 128, a.K, b, w2);
                     s2 = weight_scale<kWKind>(a.w2_s, seg_row0, j, a.K, b);
                 }
 #pragma unroll
@@ -184,7 +188,7 @@ cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     a.counts = L->counts;
     a.poff = L->poff;
     a.chunk_scan = L->chunk_scan;
-    a.w1_q = L->gate_q; a.w1_s = L->gate_s; a.w2_q = L->up_q; a.w2_s = L->up_s;
+    a.w1_q = L->gu_q; a.w1_s = L->gate_s; a.w2_q = L->gu_q; a.w2_s = L->up_s;
     a.aq = L->xq; a.as = L->xs;
     a.K = c.hidden; a.N = c.inter;
     a.hq = L->hq; a.hs = L->hs;
@@ -202,7 +206,7 @@ cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     CCArgs sg{};
     sg.n_seg = 1;
     sg.counts = L->sh_desc; sg.poff = L->sh_desc + 1; sg.chunk_scan = L->sh_desc + 5;
-    sg.w1_q = L->sh_gate_q; sg.w1_s = L->sh_gate_s; sg.w2_q = L->sh_up_q; sg.w2_s = L->sh_up_s;
+    sg.w1_q = L->sh_gu_q; sg.w1_s = L->sh_gate_s; sg.w2_q = L->sh_gu_q; sg.w2_s = L->sh_up_s;
     sg.aq = L->xq_tok; sg.as = L->xs_tok;
     sg.K = c.hidden; sg.N = c.inter;
     sg.hq = L->hq_sh; sg.hs = L->hs_sh;

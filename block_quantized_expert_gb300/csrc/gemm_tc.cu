@@ -35,10 +35,10 @@ namespace moe {
 
 using namespace tc;
 
-// Transaction bytes of one 128x128 e2m1 tile loaded with the 16-byte-aligned
-// 4-bit unpacking: the packed bytes read (8192), not the 16 KB footprint in
-// shared memory -- the copy leaves the 8-byte gaps untouched.
-constexpr uint32_t kFp4TileTx = 8192;
+// Transaction bytes of one 256-row weight copy: e2m1 codes unpacked by the
+// TMA into 16-byte slots count the packed bytes (256 x 64), e4m3 256 x 128.
+constexpr uint32_t kFp4BoxTx = 16384;
+constexpr uint32_t kFp8BoxTx = 32768;
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 struct TcArgs {
@@ -47,35 +47,35 @@ struct TcArgs {
     const int32_t* poff;       // [n_seg+1] padded row starts (multiples of 128)
     const int32_t* tile_scan;  // [n_seg+1] 128-row token tiles before segment e
     int K;                     // contraction length (multiple of 128)
-    int N_out;                 // output features (multiple of 128)
+    int N_out;                 // output features (multiple of 256 for down, 128 for gate/up)
+    int mt;                    // 256-row weight blocks per segment
     int seg_rows;              // weight rows per segment (0: one shared matrix)
-    const uint8_t* sfa0;       // weight scale atoms [rows/128][K/128][512]
-    const uint8_t* sfa1;
+    const uint8_t* sfa;        // weight scale atom pairs [blocks][K/128][2][512]
     const uint8_t* sfb;        // activation scale atoms [Rp/128][K/128][512]
     uint8_t* hq;               // gate/up: h codes [Rp][N_out] + atoms
     uint8_t* hs;
     float* y;                  // down: y[row][N_out]
     const int32_t* pos_row;    // down: padded position -> y row (null: identity)
     uint32_t* err;
-    uint32_t a_tx;             // TMA bytes of one weight tile
+    uint32_t a_tx;             // TMA bytes of one 256-row weight copy
     int32_t* sk_cnt;           // [gridDim] arrival counters of cut tiles, by first CTA (start at 0)
-    float* sk_part;            // [gridDim][2][kNumA][128][128] partial accumulators
+    float* sk_part;            // [gridDim][2][2][128][128] partial accumulators
 };
 
-template <bool kGateUp>
+// One pipeline stage: a 256-row weight tile (two 128-row MMA operands), up to
+// 128 token rows, a pair of weight scale atoms and one activation scale atom.
 struct TcCfg {
-    static constexpr int kNumA = kGateUp ? 2 : 1;
-    static constexpr int kStages = kGateUp ? 4 : 6;
-    static constexpr int kTileBytes = 16384;  // 128 rows x 128 B
-    static constexpr int kSfOff = (kNumA + 1) * kTileBytes;
-    static constexpr int kStageBytes = ((kSfOff + 512 * (kNumA + 1)) + 1023) / 1024 * 1024;
+    static constexpr int kStages = 4;
+    static constexpr int kABytes = 32768;  // 256 rows x 128 B (e2m1 in 16-byte slots, or e4m3)
+    static constexpr int kBBytes = 16384;  // 128 rows x 128 B
+    static constexpr int kSfOff = kABytes + kBBytes;
+    static constexpr int kStageBytes = ((kSfOff + 1024 + 512) + 1023) / 1024 * 1024;
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;  // + barriers + alignment slack
-    static constexpr uint32_t kTmemCols = kGateUp ? 512 : 256;
+    static constexpr uint32_t kTmemCols = 512;
     static constexpr uint32_t kAcc1Col = 128;
-    static constexpr uint32_t kSfBase = kGateUp ? 256 : 128;
-    static constexpr uint32_t kSfPerStage = 4 * (kNumA + 1);
-    static constexpr int kPrefetch = 8;  // weight tiles prefetched into L2 ahead of the loads
+    static constexpr uint32_t kSfBase = 256;
+    static constexpr uint32_t kSfPerStage = 12;  // A rows 0-127, A rows 128-255, B: 4 columns each
     static_assert(kSfBase + kStages * kSfPerStage <= kTmemCols, "tensor memory budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -83,11 +83,12 @@ struct TcCfg {
 constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
 
 struct Tile {
-    int e, m0, n0, nvalid, nt, arow, p0;
+    int e, n0, nvalid, nt, arow, f0, p0;
 };
 
-__device__ __forceinline__ Tile decode_tile(const TcArgs& a, int t, int MT) {
-    const int u = t / MT, m = t % MT;
+template <bool kGateUp>
+__device__ __forceinline__ Tile decode_tile(const TcArgs& a, int t) {
+    const int u = t / a.mt, m = t % a.mt;
     int lo = 0, hi = a.n_seg;  // segment with tile_scan[e] <= u < tile_scan[e+1]
     while (hi - lo > 1) {
         const int mid = (lo + hi) >> 1;
@@ -98,8 +99,8 @@ __device__ __forceinline__ Tile decode_tile(const TcArgs& a, int t, int MT) {
     T.n0 = (u - __ldg(a.tile_scan + lo)) * 128;
     T.nvalid = min(128, __ldg(a.counts + lo) - T.n0);
     T.nt = (T.nvalid + 31) & ~31;
-    T.m0 = m * 128;
-    T.arow = a.seg_rows * lo + T.m0;
+    T.arow = a.seg_rows * lo + m * 256;
+    T.f0 = m * (kGateUp ? 128 : 256);
     T.p0 = __ldg(a.poff + lo) + T.n0;
     return T;
 }
@@ -159,20 +160,26 @@ struct SegIter {
     }
 };
 
+// Token n of a tile from its two accumulator values: gate/up -> h = SiLU(g) * u
+// requantised to MXFP8 across the warp's 32 features; down -> two fp32 outputs.
 template <bool kGateUp>
 __device__ __forceinline__ void emit_token(const TcArgs& a, const Tile& T, int n, int q, int lane,
-                                           float g, float u) {
+                                           float v0, float v1) {
     const int p = T.p0 + n;
     const int fm = 32 * q + lane;
     if (kGateUp) {
-        const float h = silu_mul(g, u);
+        const float h = silu_mul(v0, v1);
         const int ex = mxfp8_exponent(warp_max(fabsf(h)));
         const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
-        a.hq[(size_t)p * a.N_out + T.m0 + fm] = (uint8_t)code;
-        if (lane == 0) a.hs[sf_atom_offset(p, (T.m0 + 32 * q) / 32, a.N_out)] = (uint8_t)(ex + 127);
+        a.hq[(size_t)p * a.N_out + T.f0 + fm] = (uint8_t)code;
+        if (lane == 0) a.hs[sf_atom_offset(p, (T.f0 + 32 * q) / 32, a.N_out)] = (uint8_t)(ex + 127);
     } else {
         const int row = a.pos_row ? __ldg(a.pos_row + p) : p;
-        if (row >= 0) a.y[(size_t)row * a.N_out + T.m0 + fm] = g;
+        if (row >= 0) {
+            float* yr = a.y + (size_t)row * a.N_out + T.f0;
+            yr[fm] = v0;
+            yr[128 + fm] = v1;
+        }
     }
 }
 
@@ -180,9 +187,10 @@ __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: 
 
 template <bool kGateUp, uint32_t kAFmt>
 __global__ void __launch_bounds__(kTcThreads, 1)
-k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUtensorMap tmA1,
-          const __grid_constant__ CUtensorMap tmB, const TcArgs a) {
-    using Cfg = TcCfg<kGateUp>;
+k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB32,
+          const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmB128,
+          const TcArgs a) {
+    using Cfg = TcCfg;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -197,9 +205,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int MT = a.N_out / 128;
     const int KB = a.K / 128;
-    const int tiles = __ldg(a.tile_scan + a.n_seg) * MT;
+    const int tiles = __ldg(a.tile_scan + a.n_seg) * a.mt;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
@@ -210,9 +217,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
         mbar_init(tmem_empty, 4);
         *abort_flag = 0;
         fence_mbar_init();
-        prefetch_tmap(&tmA0);
-        if (kGateUp) prefetch_tmap(&tmA1);
-        prefetch_tmap(&tmB);
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB32);
+        prefetch_tmap(&tmB64);
+        prefetch_tmap(&tmB128);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
     tc_fence_before();
@@ -234,36 +242,26 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
             uint32_t stage = 0, phase = 0;
             bool ok = true;
             while (ok && it.next(sg)) {
-                const Tile T = decode_tile(a, sg.tile, MT);
-                const uint32_t tx = Cfg::kNumA * a.a_tx + (uint32_t)T.nt * 128u + 512u * (Cfg::kNumA + 1);
-                const size_t atom_a = (size_t)(T.arow / 128) * KB;
+                const Tile T = decode_tile<kGateUp>(a, sg.tile);
+                // one copy for the token rows: a 32-, 64- or 128-row box
+                const CUtensorMap* tmB = T.nt == 32 ? &tmB32 : (T.nt == 64 ? &tmB64 : &tmB128);
+                const uint32_t b_rows = T.nt == 32 ? 32u : (T.nt == 64 ? 64u : 128u);
+                const uint32_t tx = a.a_tx + b_rows * 128u + 1024u + 512u;
+                const size_t atom_a = (size_t)(T.arow / 256) * KB;
                 const size_t atom_b = (size_t)(T.p0 / 128) * KB;
-                for (int kb = sg.kb0; kb < min(sg.kb1, sg.kb0 + Cfg::kPrefetch); ++kb) {
-                    prefetch_tile_l2(&tmA0, kb * 128, T.arow);
-                    if (kGateUp) prefetch_tile_l2(&tmA1, kb * 128, T.arow);
-                }
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (kb + Cfg::kPrefetch < sg.kb1) {
-                        prefetch_tile_l2(&tmA0, (kb + Cfg::kPrefetch) * 128, T.arow);
-                        if (kGateUp) prefetch_tile_l2(&tmA1, (kb + Cfg::kPrefetch) * 128, T.arow);
-                    }
                     if (!mbar_wait(empty_bar(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
                         give_up();
                         ok = false;
                         break;
                     }
                     uint8_t* st = smem + stage * Cfg::kStageBytes;
-                    uint8_t* bt = st + Cfg::kNumA * Cfg::kTileBytes;
-                    uint8_t* sf = st + Cfg::kSfOff;
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, tx);
-                    tma_load_2d(smem_u32(st), &tmA0, kb * 128, T.arow, fb);
-                    if (kGateUp) tma_load_2d(smem_u32(st + Cfg::kTileBytes), &tmA1, kb * 128, T.arow, fb);
-                    for (int i = 0; i < T.nt / 32; ++i)
-                        tma_load_2d(smem_u32(bt + i * 4096), &tmB, kb * 128, T.p0 + 32 * i, fb);
-                    bulk_load(smem_u32(sf), a.sfa0 + (atom_a + kb) * 512, 512, fb);
-                    if (kGateUp) bulk_load(smem_u32(sf + 512), a.sfa1 + (atom_a + kb) * 512, 512, fb);
-                    bulk_load(smem_u32(sf + 512 * Cfg::kNumA), a.sfb + (atom_b + kb) * 512, 512, fb);
+                    tma_load_2d(smem_u32(st), &tmA, kb * 128, T.arow, fb);
+                    tma_load_2d(smem_u32(st + Cfg::kABytes), tmB, kb * 128, T.p0, fb);
+                    bulk_load(smem_u32(st + Cfg::kSfOff), a.sfa + (atom_a + kb) * 1024, 1024, fb);
+                    bulk_load(smem_u32(st + Cfg::kSfOff + 1024), a.sfb + (atom_b + kb) * 512, 512, fb);
                     if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
@@ -274,7 +272,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             bool ok = true;
             while (ok && it.next(sg)) {
-                const Tile T = decode_tile(a, sg.tile, MT);
+                const Tile T = decode_tile<kGateUp>(a, sg.tile);
                 if (!mbar_wait(tmem_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
                     give_up();
                     break;
@@ -288,22 +286,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
                     }
                     tc_fence_after();
                     const uint32_t st = smem_u32(smem + stage * Cfg::kStageBytes);
-                    const uint32_t bt = st + Cfg::kNumA * Cfg::kTileBytes;
+                    const uint32_t bt = st + Cfg::kABytes;
                     const uint32_t sf = st + Cfg::kSfOff;
                     const uint32_t sf_col = tmem + Cfg::kSfBase + stage * Cfg::kSfPerStage;
-                    const uint32_t sfb_col = sf_col + 4 * Cfg::kNumA;
                     tmem_cp_32x128_x4(sf_col, desc_sf(sf));
-                    if (kGateUp) tmem_cp_32x128_x4(sf_col + 4, desc_sf(sf + 512));
-                    tmem_cp_32x128_x4(sfb_col, desc_sf(sf + 512 * Cfg::kNumA));
+                    tmem_cp_32x128_x4(sf_col + 4, desc_sf(sf + 512));
+                    tmem_cp_32x128_x4(sf_col + 8, desc_sf(sf + 1024));
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
                         const uint32_t id = idesc_mx(kAFmt, kFmtE4M3, 128, (uint32_t)T.nt, kk, kk);
                         const uint64_t bd = desc_sw128(bt + 32 * kk);
                         const uint32_t acc = (kb > sg.kb0 || kk) ? 1u : 0u;
-                        mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sfb_col, acc);
-                        if (kGateUp)
-                            mma_mx(tmem + Cfg::kAcc1Col, desc_sw128(st + Cfg::kTileBytes + 32 * kk), bd, id,
-                                   sf_col + 4, sfb_col, acc);
+                        mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sf_col + 8, acc);
+                        mma_mx(tmem + Cfg::kAcc1Col, desc_sw128(st + 16384 + 32 * kk), bd, id, sf_col + 4,
+                               sf_col + 8, acc);
                     }
                     mma_commit(empty_bar(stage));
                     if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
@@ -321,7 +317,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
         const bool leader = warp == 2 && lane == 0;
         uint32_t acc_phase = 0;
         while (it.next(sg)) {
-            const Tile T = decode_tile(a, sg.tile, MT);
+            const Tile T = decode_tile<kGateUp>(a, sg.tile);
             if (!mbar_wait(tmem_full, acc_phase, kWaitLimitNs, abort_flag)) {
                 if (lane == 0) give_up();
                 break;
@@ -333,13 +329,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
                 for (int c0 = 0; c0 < T.nt; c0 += 16) {
                     uint32_t g[16], u[16];
                     tmem_ld16(tq + (uint32_t)c0, g);
-                    if (kGateUp) tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
+                    tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
                     tmem_ld_wait();
 #pragma unroll
                     for (int i = 0; i < 16; ++i) {
                         if (c0 + i >= T.nvalid) break;  // warp-uniform
-                        emit_token<kGateUp>(a, T, c0 + i, q, lane, __uint_as_float(g[i]),
-                                            kGateUp ? __uint_as_float(u[i]) : 0.f);
+                        emit_token<kGateUp>(a, T, c0 + i, q, lane, __uint_as_float(g[i]), __uint_as_float(u[i]));
                     }
                 }
                 tc_fence_before();
@@ -348,17 +343,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
                 continue;
             }
             // a piece of a split tile: park the partial sums, count arrivals
-            float* part = a.sk_part +
-                          ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * Cfg::kNumA * 128 * 128;
+            float* part = a.sk_part + ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128;
             for (int c0 = 0; c0 < T.nt; c0 += 16) {
                 uint32_t g[16], u[16];
                 tmem_ld16(tq + (uint32_t)c0, g);
-                if (kGateUp) tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
+                tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
                 tmem_ld_wait();
 #pragma unroll
                 for (int i = 0; i < 16; ++i) {
                     part[(size_t)(c0 + i) * 128 + fm] = __uint_as_float(g[i]);
-                    if (kGateUp) part[(size_t)(128 + c0 + i) * 128 + fm] = __uint_as_float(u[i]);
+                    part[(size_t)(128 + c0 + i) * 128 + fm] = __uint_as_float(u[i]);
                 }
             }
             tc_fence_before();
@@ -375,13 +369,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
             __threadfence();
             // the last piece to arrive sums all pieces in K order and finishes the tile
             for (int n = 0; n < T.nvalid; ++n) {
-                float g = 0.f, u = 0.f;
+                float v0 = 0.f, v1 = 0.f;
                 for (int cc = sg.first_cta; cc <= sg.last_cta; ++cc) {
-                    const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * Cfg::kNumA * 128 * 128;
-                    g += __ldcg(pp + (size_t)n * 128 + fm);
-                    if (kGateUp) u += __ldcg(pp + (size_t)(128 + n) * 128 + fm);
+                    const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128;
+                    v0 += __ldcg(pp + (size_t)n * 128 + fm);
+                    v1 += __ldcg(pp + (size_t)(128 + n) * 128 + fm);
                 }
-                emit_token<kGateUp>(a, T, n, q, lane, g, u);
+                emit_token<kGateUp>(a, T, n, q, lane, v0, v1);
             }
             if (leader) a.sk_cnt[sg.first_cta] = 0;
         }
@@ -396,9 +390,13 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA0, const __grid_constant__ CUte
 }
 
 // ------------------------------------------------------------------- host --
+struct ActMaps {
+    CUtensorMap b32, b64, b128;
+};
+
 struct TcState {
-    CUtensorMap gate, up, down, sh_gate, sh_up, sh_down, xq, hq, xq_tok, hq_sh;
-    uint32_t fp4_tx;
+    CUtensorMap gu, down, sh_gu, sh_down;
+    ActMaps xq, hq, xq_tok, hq_sh;
 };
 
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
@@ -437,10 +435,14 @@ static bool make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t r
     return r == CUDA_SUCCESS;
 }
 
+static bool make_act_maps(ActMaps* m, const void* base, uint64_t cols, uint64_t rows) {
+    return make_map(&m->b32, base, cols, rows, 32, false) && make_map(&m->b64, base, cols, rows, 64, false) &&
+           make_map(&m->b128, base, cols, rows, 128, false);
+}
+
 template <bool G, uint32_t F>
 static cudaError_t set_smem_attr() {
-    return cudaFuncSetAttribute(k_gemm_tc<G, F>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                TcCfg<G>::kSmem);
+    return cudaFuncSetAttribute(k_gemm_tc<G, F>, cudaFuncAttributeMaxDynamicSharedMemorySize, TcCfg::kSmem);
 }
 
 cudaError_t tc_init(moe_layer* L) {
@@ -454,21 +456,17 @@ cudaError_t tc_init(moe_layer* L) {
     const uint64_t H = L->cfg.hidden, I = L->cfg.inter, E = L->cfg.n_experts;
     const uint64_t Rp = (uint64_t)L->Rp_max;
     const uint64_t Tpad = ((uint64_t)L->cfg.max_tokens + 127) / 128 * 128;
-    bool ok = make_map(&st->gate, L->gate_q, H, E * I, 128, true) &&
-              make_map(&st->up, L->up_q, H, E * I, 128, true) &&
-              make_map(&st->down, L->down_q, I, E * H, 128, true) &&
-              make_map(&st->xq, L->xq, H, Rp, 32, false) && make_map(&st->hq, L->hq, I, Rp, 32, false);
+    bool ok = make_map(&st->gu, L->gu_q, H, E * 2 * I, 256, true) &&
+              make_map(&st->down, L->down_q, I, E * H, 256, true) && make_act_maps(&st->xq, L->xq, H, Rp) &&
+              make_act_maps(&st->hq, L->hq, I, Rp);
     if (ok && L->cfg.has_shared)
-        ok = make_map(&st->sh_gate, L->sh_gate_q, H, I, 128, false) &&
-             make_map(&st->sh_up, L->sh_up_q, H, I, 128, false) &&
-             make_map(&st->sh_down, L->sh_down_q, I, H, 128, false) &&
-             make_map(&st->xq_tok, L->xq_tok, H, Tpad, 32, false) &&
-             make_map(&st->hq_sh, L->hq_sh, I, Tpad, 32, false);
+        ok = make_map(&st->sh_gu, L->sh_gu_q, H, 2 * I, 256, false) &&
+             make_map(&st->sh_down, L->sh_down_q, I, H, 256, false) &&
+             make_act_maps(&st->xq_tok, L->xq_tok, H, Tpad) && make_act_maps(&st->hq_sh, L->hq_sh, I, Tpad);
     if (!ok) {
         delete st;
         return cudaSuccess;  // no tensor-core path; the CUDA-core kernels run instead
     }
-    st->fp4_tx = kFp4TileTx;
     cudaError_t e = set_smem_attr<true, kFmtE2M1>();
     if (e == cudaSuccess) e = set_smem_attr<false, kFmtE2M1>();
     if (e == cudaSuccess) e = set_smem_attr<true, kFmtE4M3>();
@@ -487,9 +485,9 @@ void tc_free(moe_layer* L) {
 }
 
 template <bool G, uint32_t F>
-static cudaError_t tc_launch(moe_layer* L, const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                             const TcArgs& args, cudaStream_t s) {
-    k_gemm_tc<G, F><<<L->num_sms, kTcThreads, TcCfg<G>::kSmem, s>>>(a0, a1, b, args);
+static cudaError_t tc_launch(moe_layer* L, const CUtensorMap& a, const ActMaps& b, const TcArgs& args,
+                             cudaStream_t s) {
+    k_gemm_tc<G, F><<<L->num_sms, kTcThreads, TcCfg::kSmem, s>>>(a, b.b32, b.b64, b.b128, args);
     L->launches += 1;
     return cudaGetLastError();
 }
@@ -505,32 +503,32 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     g.tile_scan = L->tile_scan;
     g.K = c.hidden;
     g.N_out = c.inter;
-    g.seg_rows = c.inter;
-    g.sfa0 = L->gate_sf;
-    g.sfa1 = L->up_sf;
+    g.mt = c.inter / 128;
+    g.seg_rows = 2 * c.inter;
+    g.sfa = L->gu_sf;
     g.sfb = L->xs;
     g.hq = L->hq;
     g.hs = L->hs;
     g.err = L->d_err;
-    g.a_tx = st->fp4_tx;
+    g.a_tx = kFp4BoxTx;
     g.sk_part = L->sk_partials;
     g.sk_cnt = L->sk_counters;
-    cudaError_t e = tc_launch<true, kFmtE2M1>(L, st->gate, st->up, st->xq, g, s);
+    cudaError_t e = tc_launch<true, kFmtE2M1>(L, st->gu, st->xq, g, s);
     if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
     TcArgs d = g;
     d.K = c.inter;
     d.N_out = c.hidden;
+    d.mt = c.hidden / 256;
     d.seg_rows = c.hidden;
-    d.sfa0 = L->down_sf;
-    d.sfa1 = nullptr;
+    d.sfa = L->down_sf;
     d.sfb = L->hs;
     d.hq = nullptr;
     d.hs = nullptr;
     d.y = L->y;
     d.pos_row = L->pos_row;
     d.sk_cnt = L->sk_counters + L->num_sms;
-    e = tc_launch<false, kFmtE2M1>(L, st->down, st->down, st->hq, d, s);
+    e = tc_launch<false, kFmtE2M1>(L, st->down, st->hq, d, s);
     if (e != cudaSuccess || !c.has_shared) return e;
     TcArgs sg = g;
     sg.n_seg = 1;
@@ -538,27 +536,26 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     sg.poff = L->sh_desc + 1;
     sg.tile_scan = L->sh_desc + 3;
     sg.seg_rows = 0;
-    sg.sfa0 = L->sh_gate_sf;
-    sg.sfa1 = L->sh_up_sf;
+    sg.sfa = L->sh_gu_sf;
     sg.sfb = L->xs_tok;
     sg.hq = L->hq_sh;
     sg.hs = L->hs_sh;
-    sg.a_tx = 16384;
+    sg.a_tx = kFp8BoxTx;
     sg.sk_cnt = L->sk_counters + 2 * L->num_sms;
-    e = tc_launch<true, kFmtE4M3>(L, st->sh_gate, st->sh_up, st->xq_tok, sg, s);
+    e = tc_launch<true, kFmtE4M3>(L, st->sh_gu, st->xq_tok, sg, s);
     if (e != cudaSuccess) return e;
     TcArgs sd = sg;
     sd.K = c.inter;
     sd.N_out = c.hidden;
-    sd.sfa0 = L->sh_down_sf;
-    sd.sfa1 = nullptr;
+    sd.mt = c.hidden / 256;
+    sd.sfa = L->sh_down_sf;
     sd.sfb = L->hs_sh;
     sd.hq = nullptr;
     sd.hs = nullptr;
     sd.y = L->y_sh;
     sd.pos_row = nullptr;
     sd.sk_cnt = L->sk_counters + 3 * L->num_sms;
-    return tc_launch<false, kFmtE4M3>(L, st->sh_down, st->sh_down, st->hq_sh, sd, s);
+    return tc_launch<false, kFmtE4M3>(L, st->sh_down, st->hq_sh, sd, s);
 }
 
 }  // namespace moe

@@ -14,12 +14,15 @@ struct moe_layer {
     int num_sms;
     int gemm_path;  // 0 auto, 1 CUDA cores, 2 tcgen05
 
-    // -------- weights (library-owned copies, canonical layout) --------
-    uint8_t *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
-    uint8_t *sh_gate_q, *sh_gate_s, *sh_up_q, *sh_up_s, *sh_down_q, *sh_down_s;
-    // block scales repacked into 512-byte atoms for the tensor-core kernels
-    uint8_t *gate_sf, *up_sf, *down_sf;          // [E][rows/128][K/128][512]
-    uint8_t *sh_gate_sf, *sh_up_sf, *sh_down_sf;  // [rows/128][K/128][512]
+    // -------- weights (library-owned copies) --------
+    // gate/up codes interleaved per 128 features: [E][I/128][gate 128 rows, up 128 rows][H/2],
+    // so one 256-row copy brings the gate and up tiles of 128 features; down codes canonical
+    // [E][H][I/2]; scales canonical [E][rows][K/32] (read by the CUDA-core kernels).
+    uint8_t *gu_q, *gate_s, *up_s, *down_q, *down_s;
+    uint8_t *sh_gu_q, *sh_gate_s, *sh_up_s, *sh_down_q, *sh_down_s;  // shared: [I/128][256][H] e4m3
+    // scales as 512-byte atoms, two per 256-row block and 128-column step:
+    // [blocks][K/128][2][512] (gate/up: gate, up halves; down: rows 0-127, 128-255)
+    uint8_t *gu_sf, *down_sf, *sh_gu_sf, *sh_down_sf;
 
     // -------- workspace (sized by max_tokens) --------
     int R_max;        // max_tokens * k
@@ -93,8 +96,11 @@ cudaError_t cc_init();
 cudaError_t tc_init(moe_layer* L);
 void tc_free(moe_layer* L);
 cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid);
-cudaError_t repack_sf(const uint8_t* src, uint8_t* dst, int mats, int rows, int K,
-                      cudaStream_t s);
-cudaError_t expand_tile_sf(const uint8_t* src, uint8_t* dst, int rows, int K, cudaStream_t s);
+// Scale atoms of 256-row blocks (two 512-byte atoms per block and 128-column
+// step).  mode 0: halves from srcA / srcB (block g rows g*128..), canonical
+// [mats][rows][K/32] scales; 1: halves = rows (2g)*128.. and (2g+1)*128.. of srcA;
+// 2 and 3: the same from 128x128 tile scales [rows/128][K/128] (mats = 1).
+cudaError_t pack_sf_pairs(const uint8_t* srcA, const uint8_t* srcB, uint8_t* dst, int mats,
+                          int groups, int K, int mode, cudaStream_t s);
 
 }  // namespace moe

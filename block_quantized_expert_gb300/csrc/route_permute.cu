@@ -438,40 +438,41 @@ cudaError_t launch_hidden_gather(moe_layer* L, int T, uint8_t* hq, uint8_t* hs,
     return cudaGetLastError();
 }
 
-// Canonical block scales [mats][rows][K/32] -> 512-byte atoms
-// [mats][rows/128][K/128][512] (one thread per byte).
-__global__ void k_repack_sf(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst, int rows,
-                            int K, long long n) {
+// Scale atoms of 256-row blocks: dst [mats][groups][K/128][2][512], byte
+// (r % 32) * 16 + (r / 32) * 4 + kk of half h holds the scale of row r of that
+// half and 32-block kt*4 + kk (one thread per byte).
+__global__ void k_pack_sf_pairs(const uint8_t* __restrict__ srcA, const uint8_t* __restrict__ srcB,
+                                uint8_t* __restrict__ dst, int groups, int K, int mode, long long n) {
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= n) return;
-    const int KB = K / 32;
-    const long long per_mat = (long long)rows * KB;
-    const long long m = i / per_mat, rem = i % per_mat;
-    const int row = (int)(rem / KB), kb = (int)(rem % KB);
-    dst[m * per_mat + sf_atom_offset(row, kb, K)] = src[i];
+    const int KT = K / 128;
+    const int o = (int)(i % 512), h = (int)((i / 512) % 2);
+    const long long atom = i / 1024;  // (mat, group, kt)
+    const int kt = (int)(atom % KT);
+    const long long mg = atom / KT;
+    const int g = (int)(mg % groups);
+    const long long m = mg / groups;
+    const int r = (o / 16) + 32 * ((o % 16) / 4), kk = o % 4;
+    const int kb = kt * 4 + kk;
+    uint8_t v;
+    if (mode == 0) {
+        const long long row = m * (long long)groups * 128 + (long long)g * 128 + r;
+        v = (h ? srcB : srcA)[row * (K / 32) + kb];
+    } else if (mode == 1) {
+        const long long row = m * (long long)groups * 256 + (long long)(2 * g + h) * 128 + r;
+        v = srcA[row * (K / 32) + kb];
+    } else if (mode == 2) {
+        v = (h ? srcB : srcA)[(long long)g * KT + kt];
+    } else {
+        v = srcA[(long long)(2 * g + h) * KT + kt];
+    }
+    dst[i] = v;
 }
 
-cudaError_t repack_sf(const uint8_t* src, uint8_t* dst, int mats, int rows, int K,
-                      cudaStream_t s) {
-    const long long n = (long long)mats * rows * (K / 32);
-    k_repack_sf<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, dst, rows, K, n);
-    return cudaGetLastError();
-}
-
-// 128x128 tile scales [rows/128][K/128] -> atoms where every 32-block of the
-// tile carries the tile's scale.
-__global__ void k_expand_tile_sf(const uint8_t* __restrict__ src, uint8_t* __restrict__ dst,
-                                 int rows, int K, long long n) {
-    const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= n) return;
-    const int KB = K / 32;
-    const int row = (int)(i / KB), kb = (int)(i % KB);
-    dst[sf_atom_offset(row, kb, K)] = src[(size_t)(row / 128) * (K / 128) + kb / 4];
-}
-
-cudaError_t expand_tile_sf(const uint8_t* src, uint8_t* dst, int rows, int K, cudaStream_t s) {
-    const long long n = (long long)rows * (K / 32);
-    k_expand_tile_sf<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(src, dst, rows, K, n);
+cudaError_t pack_sf_pairs(const uint8_t* srcA, const uint8_t* srcB, uint8_t* dst, int mats,
+                          int groups, int K, int mode, cudaStream_t s) {
+    const long long n = (long long)mats * groups * (K / 128) * 1024;
+    k_pack_sf_pairs<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(srcA, srcB, dst, groups, K, mode, n);
     return cudaGetLastError();
 }
 

@@ -57,8 +57,8 @@ typedef enum {
     MOE_ERR_TIMEOUT = 5      /* a capped device-side wait ran out            */
 } moe_status;
 
-/* Shape of one layer.  hidden (H) and inter (I) must be multiples of 128
- * and at most 8192;
+/* Shape of one layer.  hidden (H) must be a multiple of 256 and inter (I) of
+ * 128, both at most 8192;
  * 1 <= top_k (k) <= min(n_experts, 8); 1 <= n_experts (E) <= 1024;
  * max_tokens bounds T of every later call and sizes the workspace.  The
  * guide's layer (section 1): H = 4096, I = 2048, E = 256, k = 6,

@@ -22,7 +22,7 @@ pytestmark = pytest.mark.gpu
 
 
 def _small_layer(E, k, max_tokens):
-    H = I = 128
+    H, I = 256, 128
     dev = "cuda:0"
     w = {"gate_q": torch.zeros((E, I, H // 2), dtype=torch.uint8, device=dev),
          "gate_s": torch.full((E, I, H // 32), 127, dtype=torch.uint8, device=dev),
