@@ -46,6 +46,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--trace", action="store_true",
+                    help="after timing, trace one more call of the GEMM kernels (stderr)")
     return ap.parse_args()
 
 
@@ -245,6 +247,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         ms = float(tm.item())
     bqe.moe_check(layer)
 
+    if args.trace:
+        trace_report(bqe, layer, step, K + W, dev)
+
     # per-stage device times from the sampled steps
     names = ["permute", "quantize", "gateup", "down", "combine"]
     st = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(5)] for evs in stage_events])
@@ -291,6 +296,31 @@ def run_ours(args, cfg, rank, world, local_rank):
     if world > 1:
         dist.destroy_process_group()
     return res
+
+
+def trace_report(bqe, layer, step, i, dev):
+    """Per GEMM launch of one more call: mean over CTAs of the wait counters."""
+    import torch
+    sms = torch.cuda.get_device_properties(dev).multi_processor_count
+    buf = torch.zeros(4 * sms * 8, dtype=torch.int64, device=dev)
+    bqe.moe_set_trace(layer, buf)
+    step(i)
+    torch.cuda.synchronize()
+    t = buf.view(4, sms, 8).cpu().numpy().astype(np.float64)
+    names = ["gateup", "down", "shared_gateup", "shared_down"]
+    for j in range(4):
+        if t[j, :, 0].max() == 0:
+            continue
+        dur = (t[j, :, 1] - t[j, :, 0]) / 1e3
+        span = (t[j, :, 1].max() - t[j, :, 0].min()) / 1e3
+        rep = {"launch": names[j], "span_us": round(span, 2), "cta_us_mean": round(dur.mean(), 2),
+               "producer_wait_free_us": round(t[j, :, 2].mean() / 1e3, 2),
+               "mma_wait_data_us": round(t[j, :, 3].mean() / 1e3, 2),
+               "mma_wait_acc_us": round(t[j, :, 4].mean() / 1e3, 2),
+               "epi_wait_acc_us": round(t[j, :, 5].mean() / 1e3, 2),
+               "epi_work_us": round(t[j, :, 6].mean() / 1e3, 2),
+               "stages_per_cta": round(t[j, :, 7].mean(), 1)}
+        print("TRACE", json.dumps(rep), file=sys.stderr, flush=True)
 
 
 def _ts_in(ts, a, b):

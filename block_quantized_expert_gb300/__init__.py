@@ -23,7 +23,7 @@ _STATUS = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
 EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_permute",
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
-           "moe_kernel_launches", "moe_permute_noalloc")
+           "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace")
 
 
 class MoeError(RuntimeError):
@@ -76,6 +76,7 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_set_stage_events": ([vp, C.POINTER(vp), i], i),
         "moe_kernel_launches": ([vp], C.c_ulonglong),
         "moe_permute_noalloc": ([vp, i, i, i, vp, vp, vp, vp], i),
+        "moe_set_trace": ([vp, vp, C.c_size_t], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -302,6 +303,16 @@ def moe_check(layer: Layer, stream=None) -> int:
     st = load_library().moe_check(layer.ptr, _stream(stream))
     _check(st, layer.ptr)
     return st
+
+
+def moe_set_trace(layer: Layer, buf):
+    """buf: CUDA int64 tensor of >= 4 * num_sms * 8 entries, or None."""
+    import torch
+    if buf is None:
+        _check(load_library().moe_set_trace(layer.ptr, None, 0), layer.ptr)
+        return
+    _check(load_library().moe_set_trace(layer.ptr, _ptr(buf, torch.int64, None, "buf"), buf.numel()),
+           layer.ptr)
 
 
 def moe_kernel_launches(layer: Layer) -> int:

@@ -272,6 +272,14 @@ moe_status moe_set_stage_events(moe_layer* L, void* const* events, int n) {
 
 unsigned long long moe_kernel_launches(const moe_layer* L) { return L ? L->launches : 0ull; }
 
+moe_status moe_set_trace(moe_layer* L, unsigned long long* buf, size_t entries) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (buf && entries < (size_t)4 * L->num_sms * 8)
+        return fail(L, MOE_ERR_INVALID_ARG, "trace buffer needs 4 * num_sms * 8 entries");
+    L->trace = buf;
+    return MOE_OK;
+}
+
 moe_status moe_set_gemm_path(moe_layer* L, int path) {
     if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
     if (path < 0 || path > 2) return fail(L, MOE_ERR_INVALID_ARG, "path must be 0, 1 or 2");
@@ -342,6 +350,7 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, int T, const int32_t* id
     if (e == cudaSuccess) e = run_gemms(L, T, s, ev ? L->stage_ev[3] : nullptr);
     if (e == cudaSuccess) e = mark(4, cudaSuccess);
     if (e == cudaSuccess) e = mark(5, moe::launch_combine(L, ids, w, T, out, s));
+    L->trace = nullptr;
     return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward");
 }
 

@@ -60,6 +60,7 @@ struct TcArgs {
     uint32_t a_tx;             // TMA bytes of one 256-row weight copy
     int32_t* sk_cnt;           // [gridDim] arrival counters of cut tiles, by first CTA (start at 0)
     float* sk_part;            // [gridDim][2][2][128][128] partial accumulators
+    unsigned long long* trace; // [gridDim][8] wait-time counters, or null
 };
 
 // One pipeline stage: a 256-row weight tile (two 128-row MMA operands), up to
@@ -80,7 +81,8 @@ struct TcCfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-constexpr int kTcThreads = 192;  // warp 0: TMA, warp 1: MMA, warps 2-5: epilogue
+constexpr int kTcThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2-9: epilogue
+constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, each half of the token columns
 
 struct Tile {
     int e, n0, nvalid, nt, arow, f0, p0;
@@ -183,10 +185,20 @@ __device__ __forceinline__ void emit_token(const TcArgs& a, const Tile& T, int n
     }
 }
 
-__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// mbar_wait that adds the waited wall time to *acc when tracing.
+__device__ __forceinline__ bool timed_wait(uint32_t bar, uint32_t parity, volatile int* abort,
+                                           bool tr, unsigned long long& acc) {
+    if (!tr) return mbar_wait(bar, parity, kWaitLimitNs, abort);
+    const uint64_t t0 = globaltimer();
+    const bool ok = mbar_wait(bar, parity, kWaitLimitNs, abort);
+    acc += globaltimer() - t0;
+    return ok;
+}
 
 template <bool kGateUp, uint32_t kAFmt>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __maxnreg__(200)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB32,
           const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmB128,
           const TcArgs a) {
@@ -207,6 +219,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = a.K / 128;
     const int tiles = __ldg(a.tile_scan + a.n_seg) * a.mt;
+    const bool tr = a.trace != nullptr;
+    unsigned long long* trc = tr ? a.trace + (size_t)blockIdx.x * 8 : nullptr;
+    if (tr && threadIdx.x == 0) trc[0] = globaltimer();
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < Cfg::kStages; ++s) {
@@ -214,7 +229,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             mbar_init(empty_bar(s), 1);
         }
         mbar_init(tmem_full, 1);
-        mbar_init(tmem_empty, 4);
+        mbar_init(tmem_empty, kEpiWarps);
         *abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmA);
@@ -241,6 +256,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (lane == 0) {
             uint32_t stage = 0, phase = 0;
             bool ok = true;
+            unsigned long long w_empty = 0;
             while (ok && it.next(sg)) {
                 const Tile T = decode_tile<kGateUp>(a, sg.tile);
                 // one copy for the token rows: a 32-, 64- or 128-row box
@@ -250,7 +266,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 const size_t atom_a = (size_t)(T.arow / 256) * KB;
                 const size_t atom_b = (size_t)(T.p0 / 128) * KB;
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                    if (!timed_wait(empty_bar(stage), phase ^ 1u, abort_flag, tr, w_empty)) {
                         give_up();
                         ok = false;
                         break;
@@ -265,25 +281,28 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
                 }
             }
+            if (tr) trc[2] = w_empty;
         }
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
         if (lane == 0) {
             uint32_t stage = 0, phase = 0, acc_phase = 0;
             bool ok = true;
+            unsigned long long w_full = 0, w_acc = 0, n_stages = 0;
             while (ok && it.next(sg)) {
                 const Tile T = decode_tile<kGateUp>(a, sg.tile);
-                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                if (!timed_wait(tmem_empty, acc_phase ^ 1u, abort_flag, tr, w_acc)) {
                     give_up();
                     break;
                 }
                 tc_fence_after();
                 for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, kWaitLimitNs, abort_flag)) {
+                    if (!timed_wait(full_bar(stage), phase, abort_flag, tr, w_full)) {
                         give_up();
                         ok = false;
                         break;
                     }
+                    ++n_stages;
                     tc_fence_after();
                     const uint32_t st = smem_u32(smem + stage * Cfg::kStageBytes);
                     const uint32_t bt = st + Cfg::kABytes;
@@ -308,56 +327,66 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 mma_commit(tmem_full);
                 acc_phase ^= 1u;
             }
+            if (tr) { trc[3] = w_full; trc[4] = w_acc; trc[7] = n_stages; }
         }
     } else {
         // ---------------------------------------------------- epilogue --
-        const int q = warp & 3;  // the TMEM lane quarter this warp may access
+        // Warp w (2..9) reads TMEM lanes of quarter w % 4 and token columns
+        // [64 * h, 64 * h + 64), h = (w - 2) / 4: it copies both accumulators'
+        // columns to registers, frees the accumulator for the next tile, and
+        // only then does the SwiGLU / requantisation or the stores.
+        const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
         const int fm = 32 * q + lane;
-        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        const int cb = 64 * hf;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)cb;
         const bool leader = warp == 2 && lane == 0;
         uint32_t acc_phase = 0;
+        unsigned long long w_tf = 0, t_work = 0;
         while (it.next(sg)) {
             const Tile T = decode_tile<kGateUp>(a, sg.tile);
-            if (!mbar_wait(tmem_full, acc_phase, kWaitLimitNs, abort_flag)) {
+            if (!timed_wait(tmem_full, acc_phase, abort_flag, tr, w_tf)) {
                 if (lane == 0) give_up();
                 break;
             }
+            const uint64_t tw0 = tr ? globaltimer() : 0;
             tc_fence_after();
             acc_phase ^= 1u;
-            if (sg.first_cta == sg.last_cta) {
-                // whole tile: straight from tensor memory
-                for (int c0 = 0; c0 < T.nt; c0 += 16) {
-                    uint32_t g[16], u[16];
-                    tmem_ld16(tq + (uint32_t)c0, g);
-                    tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
-                    tmem_ld_wait();
+            uint32_t v0[4][16], v1[4][16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        if (c0 + i >= T.nvalid) break;  // warp-uniform
-                        emit_token<kGateUp>(a, T, c0 + i, q, lane, __uint_as_float(g[i]), __uint_as_float(u[i]));
-                    }
+            for (int j = 0; j < 4; ++j) {
+                if (cb + 16 * j < T.nt) {  // warp-uniform
+                    tmem_ld16(tq + 16 * j, v0[j]);
+                    tmem_ld16(tq + Cfg::kAcc1Col + 16 * j, v1[j]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(tmem_empty);
+            }
+            tmem_ld_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            const int nv = min(64, T.nvalid - cb);  // valid columns of this warp (may be <= 0)
+            if (sg.first_cta == sg.last_cta) {
+#pragma unroll
+                for (int i = 0; i < 64; i += 4) {
+                    if (i >= nv) break;  // warp-uniform
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        if (i + k < nv)
+                            emit_token<kGateUp>(a, T, cb + i + k, q, lane, __uint_as_float(v0[(i + k) >> 4][(i + k) & 15]),
+                                                __uint_as_float(v1[(i + k) >> 4][(i + k) & 15]));
+                }
+                if (tr) t_work += globaltimer() - tw0;
                 continue;
             }
             // a piece of a split tile: park the partial sums, count arrivals
             float* part = a.sk_part + ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128;
-            for (int c0 = 0; c0 < T.nt; c0 += 16) {
-                uint32_t g[16], u[16];
-                tmem_ld16(tq + (uint32_t)c0, g);
-                tmem_ld16(tq + Cfg::kAcc1Col + (uint32_t)c0, u);
-                tmem_ld_wait();
 #pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    part[(size_t)(c0 + i) * 128 + fm] = __uint_as_float(g[i]);
-                    part[(size_t)(128 + c0 + i) * 128 + fm] = __uint_as_float(u[i]);
+            for (int i = 0; i < 64; ++i) {
+                if (cb + i < T.nt) {
+                    part[(size_t)(cb + i) * 128 + fm] = __uint_as_float(v0[i >> 4][i & 15]);
+                    part[(size_t)(128 + cb + i) * 128 + fm] = __uint_as_float(v1[i >> 4][i & 15]);
                 }
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty);
             __threadfence();
             epi_bar();
             if (leader) {
@@ -368,20 +397,24 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             if (!*last_flag) continue;
             __threadfence();
             // the last piece to arrive sums all pieces in K order and finishes the tile
-            for (int n = 0; n < T.nvalid; ++n) {
-                float v0 = 0.f, v1 = 0.f;
+            for (int n = cb; n < min(T.nvalid, cb + 64); ++n) {
+                float s0 = 0.f, s1 = 0.f;
                 for (int cc = sg.first_cta; cc <= sg.last_cta; ++cc) {
                     const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128;
-                    v0 += __ldcg(pp + (size_t)n * 128 + fm);
-                    v1 += __ldcg(pp + (size_t)(128 + n) * 128 + fm);
+                    s0 += __ldcg(pp + (size_t)n * 128 + fm);
+                    s1 += __ldcg(pp + (size_t)(128 + n) * 128 + fm);
                 }
-                emit_token<kGateUp>(a, T, n, q, lane, v0, v1);
+                emit_token<kGateUp>(a, T, n, q, lane, s0, s1);
             }
+            epi_bar();  // everyone has read the slots before the counter is reused
             if (leader) a.sk_cnt[sg.first_cta] = 0;
+            if (tr) t_work += globaltimer() - tw0;
         }
+        if (tr && leader) { trc[5] = w_tf; trc[6] = t_work; }
     }
 
     __syncthreads();
+    if (tr && threadIdx.x == 0) trc[1] = globaltimer();
     if (*abort_flag) spin_ns(200000);  // copies / MMAs still in flight land first
     if (warp == 1) {
         tc_fence_after();
@@ -513,6 +546,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     g.a_tx = kFp4BoxTx;
     g.sk_part = L->sk_partials;
     g.sk_cnt = L->sk_counters;
+    g.trace = L->trace;
     cudaError_t e = tc_launch<true, kFmtE2M1>(L, st->gu, st->xq, g, s);
     if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
     if (e != cudaSuccess) return e;
@@ -528,6 +562,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     d.y = L->y;
     d.pos_row = L->pos_row;
     d.sk_cnt = L->sk_counters + L->num_sms;
+    d.trace = L->trace ? L->trace + (size_t)L->num_sms * 8 : nullptr;
     e = tc_launch<false, kFmtE2M1>(L, st->down, st->hq, d, s);
     if (e != cudaSuccess || !c.has_shared) return e;
     TcArgs sg = g;
@@ -542,6 +577,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     sg.hs = L->hs_sh;
     sg.a_tx = kFp8BoxTx;
     sg.sk_cnt = L->sk_counters + 2 * L->num_sms;
+    sg.trace = L->trace ? L->trace + (size_t)2 * L->num_sms * 8 : nullptr;
     e = tc_launch<true, kFmtE4M3>(L, st->sh_gu, st->xq_tok, sg, s);
     if (e != cudaSuccess) return e;
     TcArgs sd = sg;
@@ -555,6 +591,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     sd.y = L->y_sh;
     sd.pos_row = nullptr;
     sd.sk_cnt = L->sk_counters + 3 * L->num_sms;
+    sd.trace = L->trace ? L->trace + (size_t)3 * L->num_sms * 8 : nullptr;
     return tc_launch<false, kFmtE4M3>(L, st->sh_down, st->hq_sh, sd, s);
 }
 

@@ -58,6 +58,7 @@ struct moe_layer {
 
     void* tc;             // tensor-core kernel state (tensor maps), or null
     unsigned long long launches;  // kernels enqueued so far
+    unsigned long long* trace;    // one-shot kernel trace buffer (diagnostics), or null
     cudaEvent_t stage_ev[6];  // one-shot stage events for the next forward
     int stage_ev_set;
 

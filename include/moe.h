@@ -178,6 +178,15 @@ const char* moe_last_error(const moe_layer* layer);
  * ordered, so it may be captured in a CUDA graph.                         */
 moe_status moe_set_stage_events(moe_layer* layer, void* const* events, int n);
 
+/* Kernel trace (diagnostics): when `buf` is non-NULL, the tensor-core GEMM
+ * launches of the next moe_forward on `layer` write, per CTA, 8 counters
+ * [start ns, end ns, producer ns waiting for free stages, MMA ns waiting for
+ * data, MMA ns waiting for the accumulator, epilogue ns waiting for the
+ * accumulator, epilogue ns working, K-stages issued] to buf (device u64),
+ * launch j of that forward at buf + j * num_sms * 8; `entries` must be at
+ * least 4 * num_sms * 8.  One-shot, like moe_set_stage_events.             */
+moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entries);
+
 /* Number of CUDA kernels this layer has enqueued since moe_create (a launch
  * made while a stream is being captured counts once, although every replay
  * of the graph runs it again).                                             */
