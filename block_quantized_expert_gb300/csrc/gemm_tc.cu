@@ -81,7 +81,9 @@ struct TcCfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-constexpr int kTcThreads = 320;  // warp 0: TMA, warp 1: MMA, warps 2-9: epilogue
+// warp 0: TMA, warp 1: MMA, warps 2-9: epilogue.  Ten warps put three on two
+// of the four SM sub-partitions, whose 16K registers cap a thread at 168.
+constexpr int kTcThreads = 320;
 constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, each half of the token columns
 
 struct Tile {
@@ -198,7 +200,7 @@ __device__ __forceinline__ bool timed_wait(uint32_t bar, uint32_t parity, volati
 }
 
 template <bool kGateUp, uint32_t kAFmt>
-__global__ void __maxnreg__(200)
+__global__ void __launch_bounds__(kTcThreads, 1)
 k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB32,
           const __grid_constant__ CUtensorMap tmB64, const __grid_constant__ CUtensorMap tmB128,
           const TcArgs a) {
