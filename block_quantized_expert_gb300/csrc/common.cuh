@@ -89,4 +89,13 @@ __device__ __forceinline__ void raise_flag(uint32_t* err, uint32_t bit) {
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return g / (1.0f + expf(-g)) * u; }
 
+// Programmatic dependent launch: allow the next kernel of the stream to be
+// scheduled now (its prologue overlaps this kernel), and wait until the
+// previous kernel has completed and its writes are visible.  Every kernel
+// waits before its first global access, so stream order is kept.
+__device__ __forceinline__ void pdl_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 }  // namespace moe

@@ -63,6 +63,8 @@ __device__ __forceinline__ float weight_scale(const uint8_t* __restrict__ s, siz
 template <int kWKind, bool kGateUp>
 __global__ void __launch_bounds__(kCCThreads) k_gemm_cc(CCArgs a) {
     extern __shared__ float smem[];
+    pdl_launch_dependents();
+    pdl_wait();
     float* xf = smem;                          // [kChunk][K]
     float* hb = smem + kChunk * a.K;           // [kChunk][32]
     __shared__ float lut8[256];
@@ -174,9 +176,8 @@ template <int kWKind, bool kGateUp>
 static cudaError_t cc_launch(moe_layer* L, const CCArgs& a, cudaStream_t s) {
     const size_t smem = sizeof(float) * (size_t)kChunk * (a.K + 32);
     const int grid = L->num_sms * 2;
-    k_gemm_cc<kWKind, kGateUp><<<grid, kCCThreads, smem, s>>>(a);
     L->launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_cc<kWKind, kGateUp>, dim3(grid), dim3(kCCThreads), smem, s, a);
 }
 
 cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {

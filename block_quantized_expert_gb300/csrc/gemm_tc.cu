@@ -220,7 +220,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = a.K / 128;
-    const int tiles = __ldg(a.tile_scan + a.n_seg) * a.mt;
     const bool tr = a.trace != nullptr;
     unsigned long long* trc = tr ? a.trace + (size_t)blockIdx.x * 8 : nullptr;
     if (tr && threadIdx.x == 0) trc[0] = globaltimer();
@@ -244,6 +243,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
+    // the prologue above overlaps the previous kernel; its outputs are read below
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tiles = __ldg(a.tile_scan + a.n_seg) * a.mt;
 
     auto give_up = [&]() {
         *abort_flag = 1;
@@ -522,9 +525,9 @@ void tc_free(moe_layer* L) {
 template <bool G, uint32_t F>
 static cudaError_t tc_launch(moe_layer* L, const CUtensorMap& a, const ActMaps& b, const TcArgs& args,
                              cudaStream_t s) {
-    k_gemm_tc<G, F><<<L->num_sms, kTcThreads, TcCfg::kSmem, s>>>(a, b.b32, b.b64, b.b128, args);
     L->launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(k_gemm_tc<G, F>, dim3(L->num_sms), dim3(kTcThreads), TcCfg::kSmem, s, a, b.b32, b.b64,
+                      b.b128, args);
 }
 
 cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/moe.h"
 
@@ -68,6 +69,24 @@ struct moe_layer {
 namespace moe {
 
 constexpr int kChunk = 4;  // tokens per CUDA-core GEMM work item
+
+// Launch with a programmatic (early-launch) edge to the previous kernel of the
+// stream; the kernels synchronise on it with pdl_wait().
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Launchers; each returns the launch error (cudaSuccess on success).
 cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,

@@ -20,6 +20,8 @@ namespace moe {
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
                                                int k, float w_scale, int32_t* __restrict__ ids,
                                                float* __restrict__ w, uint32_t* err) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
@@ -62,10 +64,9 @@ cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids,
                          cudaStream_t s) {
     const int warps_per_block = 8;
     dim3 grid((T + warps_per_block - 1) / warps_per_block);
-    k_route<<<grid, 32 * warps_per_block, 0, s>>>(logits, T, L->cfg.n_experts, L->cfg.top_k,
-                                                  L->cfg.w_scale, ids, w, L->d_err);
     L->launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(k_route, grid, dim3(32 * warps_per_block), 0, s, logits, T, L->cfg.n_experts,
+                      L->cfg.top_k, L->cfg.w_scale, ids, w, L->d_err);
 }
 
 // Hash-routed layers (guide, section 1: tid2eid maps a token id to its k
@@ -73,6 +74,8 @@ cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids,
 __global__ void k_route_hash(const int32_t* __restrict__ tok, const int32_t* __restrict__ tab,
                              int V, int T, int k, int E, float w_each, int32_t* __restrict__ ids,
                              float* __restrict__ w, uint32_t* err) {
+    pdl_launch_dependents();
+    pdl_wait();
     int t = blockIdx.x * blockDim.x + threadIdx.x;
     if (t >= T) return;
     int id = tok[t];
@@ -89,10 +92,9 @@ __global__ void k_route_hash(const int32_t* __restrict__ tok, const int32_t* __r
 cudaError_t launch_route_hash(moe_layer* L, const int32_t* tok, const int32_t* tab, int V,
                               int T, int32_t* ids, float* w, cudaStream_t s) {
     float w_each = L->cfg.w_scale / (float)L->cfg.top_k;
-    k_route_hash<<<(T + 127) / 128, 128, 0, s>>>(tok, tab, V, T, L->cfg.top_k, L->cfg.n_experts,
-                                                 w_each, ids, w, L->d_err);
     L->launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(k_route_hash, dim3((T + 127) / 128), dim3(128), 0, s, tok, tab, V, T, L->cfg.top_k,
+                      L->cfg.n_experts, w_each, ids, w, L->d_err);
 }
 
 // ---------------------------------------------------------------- permute --
@@ -139,6 +141,8 @@ __global__ void __launch_bounds__(1024) k_permute(
     int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
     int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
     int T, uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
+    pdl_launch_dependents();
+    pdl_wait();
     extern __shared__ int dyn[];  // cnt, cursor, s_off, s_poff [E] each; then wc [32][E] bytes
     int* cnt = dyn;
     int* cursor = dyn + E;
@@ -233,12 +237,11 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
                            int32_t* row_src, int32_t* row_dst, cudaStream_t s) {
     const int R = T * L->cfg.top_k;
     const size_t smem = (size_t)48 * L->cfg.n_experts;
-    k_permute<<<1, 1024, smem, s>>>(ids, R, L->cfg.n_experts, offsets, row_src, row_dst, L->counts,
-                                 L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
-                                 L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err,
-                                 L->sk_counters, L->sk_counters ? 4 * L->num_sms : 0);
     L->launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(k_permute, dim3(1), dim3(1024), smem, s, ids, R, L->cfg.n_experts, offsets, row_src,
+                      row_dst, L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
+                      L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err, L->sk_counters,
+                      L->sk_counters ? 4 * L->num_sms : 0);
 }
 
 // The same counting sort with caller-chosen bookkeeping buffers (no layer):
@@ -277,6 +280,8 @@ struct QuantDst {
 template <int kMode>
 __global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x, int T, int H,
                                                   QuantDst d) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int lane = threadIdx.x & 31;
     const int tasks_per_row = (H + 255) / 256;
     const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
@@ -333,9 +338,8 @@ static cudaError_t quantize_launch(int mode, const uint16_t* x, int T, int H, Qu
     const long long tasks = (long long)T * ((H + 255) / 256);
     const int threads = 256;
     const long long blocks = (tasks * 32 + threads - 1) / threads;
-    if (mode == 0) k_quantize<0><<<(unsigned)blocks, threads, 0, s>>>(x, T, H, d);
-    else k_quantize<1><<<(unsigned)blocks, threads, 0, s>>>(x, T, H, d);
-    return cudaGetLastError();
+    if (mode == 0) return launch_pdl(k_quantize<0>, dim3((unsigned)blocks), dim3(threads), 0, s, x, T, H, d);
+    return launch_pdl(k_quantize<1>, dim3((unsigned)blocks), dim3(threads), 0, s, x, T, H, d);
 }
 
 cudaError_t launch_quantize_canonical(moe_layer* L, const uint16_t* x, int T, uint8_t* q,
@@ -371,6 +375,8 @@ __global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids
                                                  const float* __restrict__ y,
                                                  const float* __restrict__ y_sh, int T, int H,
                                                  int k, float* __restrict__ out) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int H4 = H / 4;
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
     if (i >= (long long)T * H4) return;
@@ -410,17 +416,19 @@ __global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids
 cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int T,
                            float* out, cudaStream_t s) {
     const long long n = (long long)T * (L->cfg.hidden / 4);
-    k_combine<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(
-        ids, w, L->row_pos, L->y, L->cfg.has_shared ? L->y_sh : nullptr, T, L->cfg.hidden,
-        L->cfg.top_k, out);
     L->launches += 1;
-    return cudaGetLastError();
+    return launch_pdl(k_combine, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, ids, w,
+                      (const int32_t*)L->row_pos, (const float*)L->y,
+                      (const float*)(L->cfg.has_shared ? L->y_sh : nullptr), T, L->cfg.hidden,
+                      L->cfg.top_k, out);
 }
 
 // ----------------------------------------------------------- test helpers --
 __global__ void k_hidden_gather(const int32_t* __restrict__ row_pos, const uint8_t* __restrict__ hq,
                                 const uint8_t* __restrict__ hs, int R, int I, uint8_t* __restrict__ oq,
                                 uint8_t* __restrict__ os) {
+    pdl_launch_dependents();
+    pdl_wait();
     const int r = blockIdx.x;
     if (r >= R) return;
     const int p = row_pos[r];
