@@ -176,9 +176,9 @@ def run_ours(args, cfg, rank, world, local_rank):
         j = i % S
         if hashed:
             bqe.moe_route_hash(layer, tok_all[j], tab, ids, wt)
+            bqe.moe_forward(layer, x_all[j], ids, wt, out)
         else:
-            bqe.moe_route(layer, lg_all[j], ids, wt)
-        bqe.moe_forward(layer, x_all[j], ids, wt, out)
+            bqe.moe_route_forward(layer, lg_all[j], x_all[j], ids, wt, out)
 
     # experts touched per input batch (for the algorithmic byte count)
     touched, rows = [], cfg.T * cfg.k

@@ -23,7 +23,7 @@ _STATUS = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
 EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_permute",
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
-           "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace")
+           "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace", "moe_route_forward")
 
 
 class MoeError(RuntimeError):
@@ -77,6 +77,7 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_kernel_launches": ([vp], C.c_ulonglong),
         "moe_permute_noalloc": ([vp, i, i, i, vp, vp, vp, vp], i),
         "moe_set_trace": ([vp, vp, C.c_size_t], i),
+        "moe_route_forward": ([vp, vp, vp, i, vp, vp, vp, vp], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -274,6 +275,21 @@ def moe_forward(layer: Layer, x, ids, w, out, stream=None):
                                     _ptr(ids, torch.int32, (T, c.top_k), "ids"),
                                     _ptr(w, torch.float32, (T, c.top_k), "w"),
                                     _ptr(out, torch.float32, (T, c.hidden), "out"), _stream(stream))
+    _check(st, layer.ptr)
+
+
+def moe_route_forward(layer: Layer, logits, x, ids, w, out, stream=None):
+    """Routing and layer in one call (ids, w and out are written)."""
+    import torch
+    T = x.shape[0]
+    c = layer.cfg
+    if x.dtype == torch.bfloat16:
+        x = x.view(torch.int16)
+    st = load_library().moe_route_forward(
+        layer.ptr, _ptr(logits, torch.float32, (T, c.n_experts), "logits"),
+        _ptr(x, torch.int16, (T, c.hidden), "x"), T, _ptr(ids, torch.int32, (T, c.top_k), "ids"),
+        _ptr(w, torch.float32, (T, c.top_k), "w"), _ptr(out, torch.float32, (T, c.hidden), "out"),
+        _stream(stream))
     _check(st, layer.ptr)
 
 

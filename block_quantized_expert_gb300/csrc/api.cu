@@ -4,6 +4,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <functional>
 #include <new>
 
 #include "common.cuh"
@@ -75,7 +76,7 @@ size_t workspace_bytes(const moe_config& c) {
     b += T * H * 2 + T * E * 4 + T * H * 4 + 2 * T * k * 4;  // staging
     b += 256;                                    // error word
     // split-tile counters and partial accumulators (sized for up to 256 SMs)
-    b += (size_t)4 * 256 * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
+    b += (size_t)(4 * 256 + 32) * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
     return b;
 }
 
@@ -105,18 +106,46 @@ moe_status check_T(moe_layer* L, int T) {
     return MOE_OK;
 }
 
-// The GEMM steps (gate/up + SwiGLU + requant, down; routed and shared);
-// `mid` (if set) is recorded after the routed gate/up launch.
-cudaError_t run_gemms(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {
-    if (L->gemm_path != 2 || L->tc == nullptr) return moe::launch_gemm_cc(L, T, s, mid);
-    return moe::launch_gemm_tc(L, T, s, mid);
-}
 
 }  // namespace
 
 namespace moe {
 void set_thread_error(const char* msg) { snprintf(g_tls_error, sizeof(g_tls_error), "%s", msg); }
 }  // namespace moe
+
+namespace {
+
+// The kernels of one layer call.  Small batches (T <= kFrontMaxT) run the
+// routing (when logits are given), the counting sort and the quantisation in
+// one CTA; on the tensor-core path without a shared expert the combine is
+// fused into the down GEMM.  `mark(i, e)` records stage event i (optional).
+cudaError_t forward_kernels(moe_layer* L, const float* logits, const uint16_t* x, int T, int32_t* ids,
+                            float* w, float* out, cudaStream_t s,
+                            const std::function<cudaError_t(int, cudaError_t)>& mark) {
+    auto M = [&](int i, cudaError_t e) { return mark ? mark(i, e) : e; };
+    const bool small = T <= moe::kFrontMaxT;
+    const bool tc = L->gemm_path != 1 && L->tc != nullptr;  // automatic: tensor cores
+    const bool fuse_combine = tc && small && !L->cfg.has_shared && T <= moe::kFusedCombineMaxT;
+    cudaError_t e = M(0, cudaSuccess);
+    if (e == cudaSuccess && small) {
+        e = M(1, moe::launch_front(L, logits, ids, w, x, T, s));
+        if (e == cudaSuccess) e = M(2, cudaSuccess);
+    } else {
+        if (e == cudaSuccess && logits) e = moe::launch_route(L, logits, T, ids, w, s);
+        if (e == cudaSuccess) e = M(1, moe::launch_permute(L, ids, T, L->offsets, L->row_src, L->row_dst, s));
+        if (e == cudaSuccess) e = M(2, moe::launch_quantize_scatter(L, x, T, s));
+    }
+    cudaEvent_t mid = mark ? L->stage_ev[3] : nullptr;
+    if (e == cudaSuccess) {
+        if (tc) e = moe::launch_gemm_tc(L, T, s, mid, fuse_combine ? ids : nullptr, w, out);
+        else e = moe::launch_gemm_cc(L, T, s, mid);
+    }
+    if (e == cudaSuccess) e = M(4, cudaSuccess);
+    if (e == cudaSuccess) e = M(5, fuse_combine ? cudaSuccess : moe::launch_combine(L, ids, w, T, out, s));
+    return e;
+}
+
+}  // namespace
 
 extern "C" {
 
@@ -187,7 +216,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     A(&L->x_stage, T * H * 2); A(&L->logits_stage, T * E * 4); A(&L->out_stage, T * H * 4);
     A(&L->ids_stage, T * k * 4); A(&L->w_stage, T * k * 4);
     A(&L->d_err, 256);
-    A(&L->sk_counters, (size_t)4 * L->num_sms * 4);
+    A(&L->sk_counters, (size_t)moe::kSkCounters(L) * 4);
     A(&L->sk_partials, (size_t)L->num_sms * 2 * 2 * 128 * 128 * 4);
     if (a != cudaSuccess) {
         cudaGetLastError();
@@ -228,7 +257,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     // a defined workspace: padding rows of the activation buffers read as zero
     void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters};
     size_t zn[] = {z.Rp * H, z.Rp * H / 32, z.Rp * I, z.Rp * I / 32, 256, z.Rp * 4,
-                   (size_t)4 * L->num_sms * 4};
+                   (size_t)moe::kSkCounters(L) * 4};
     for (int i = 0; i < 7 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
     if (c.has_shared) {
         void* zs[] = {L->xq_tok, L->xs_tok, L->hq_sh, L->hs_sh};
@@ -339,19 +368,36 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, int T, const int32_t* id
     L->stage_ev_set = 0;
     // external records: inside a stream capture they become timestamped
     // event nodes of the graph (not capture-internal dependencies)
-    auto mark = [&](int i, cudaError_t e) {
+    std::function<cudaError_t(int, cudaError_t)> mark = [&](int i, cudaError_t e) {
         return (ev && e == cudaSuccess)
                    ? cudaEventRecordWithFlags(L->stage_ev[i], s, cudaEventRecordExternal)
                    : e;
     };
-    cudaError_t e = mark(0, cudaSuccess);
-    if (e == cudaSuccess) e = mark(1, moe::launch_permute(L, ids, T, L->offsets, L->row_src, L->row_dst, s));
-    if (e == cudaSuccess) e = mark(2, moe::launch_quantize_scatter(L, x, T, s));
-    if (e == cudaSuccess) e = run_gemms(L, T, s, ev ? L->stage_ev[3] : nullptr);
-    if (e == cudaSuccess) e = mark(4, cudaSuccess);
-    if (e == cudaSuccess) e = mark(5, moe::launch_combine(L, ids, w, T, out, s));
+    cudaError_t e = forward_kernels(L, nullptr, x, T, const_cast<int32_t*>(ids), const_cast<float*>(w),
+                                    out, s, ev ? mark : std::function<cudaError_t(int, cudaError_t)>());
     L->trace = nullptr;
     return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward");
+}
+
+moe_status moe_route_forward(moe_layer* L, const float* logits, const uint16_t* x, int T, int32_t* ids,
+                             float* w, float* out, moe_stream_t stream) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!logits || !x || !ids || !w || !out) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
+    if (!aligned(x, 16) || !aligned(out, 16))
+        return fail(L, MOE_ERR_INVALID_ARG, "x and out must be 16-byte aligned");
+    if (moe_status st = check_T(L, T)) return st;
+    const bool ev = L->stage_ev_set != 0;
+    L->stage_ev_set = 0;
+    cudaStream_t s = (cudaStream_t)stream;
+    std::function<cudaError_t(int, cudaError_t)> mark = [&](int i, cudaError_t e) {
+        return (ev && e == cudaSuccess)
+                   ? cudaEventRecordWithFlags(L->stage_ev[i], s, cudaEventRecordExternal)
+                   : e;
+    };
+    cudaError_t e = forward_kernels(L, logits, x, T, ids, w, out, s,
+                                    ev ? mark : std::function<cudaError_t(int, cudaError_t)>());
+    L->trace = nullptr;
+    return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_route_forward");
 }
 
 moe_status moe_forward_host(moe_layer* L, const uint16_t* x, const float* logits, int T,
@@ -365,8 +411,8 @@ moe_status moe_forward_host(moe_layer* L, const uint16_t* x, const float* logits
     if (e == cudaSuccess)
         e = cudaMemcpyAsync(L->logits_stage, logits, (size_t)T * E * 4, cudaMemcpyHostToDevice, s);
     if (e != cudaSuccess) return cuda_fail(L, e, "moe_forward_host: input copy");
-    moe_status st = moe_route(L, L->logits_stage, T, L->ids_stage, L->w_stage, stream);
-    if (st == MOE_OK) st = moe_forward(L, L->x_stage, T, L->ids_stage, L->w_stage, L->out_stage, stream);
+    moe_status st = moe_route_forward(L, L->logits_stage, L->x_stage, T, L->ids_stage, L->w_stage,
+                                      L->out_stage, stream);
     if (st != MOE_OK) return st;
     e = cudaMemcpyAsync(out, L->out_stage, (size_t)T * H * 4, cudaMemcpyDeviceToHost, s);
     return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward_host: output copy");

@@ -169,7 +169,7 @@ cudaError_t cc_init() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    return e;
+    return e;  // the dynamic smem request already selects the largest carveout
 }
 
 template <int kWKind, bool kGateUp>

@@ -25,6 +25,7 @@
 // tensor memory and exits.
 #include <cuda.h>
 
+#include <climits>
 #include <new>
 
 #include "common.cuh"
@@ -61,6 +62,15 @@ struct TcArgs {
     int32_t* sk_cnt;           // [gridDim] arrival counters of cut tiles, by first CTA (start at 0)
     float* sk_part;            // [gridDim][2][2][128][128] partial accumulators
     unsigned long long* trace; // [gridDim][8] wait-time counters, or null
+    // fused combine (down GEMM of small batches): after the last tile of a
+    // 256-feature block, out[t][f] = sum over the token's experts in ascending
+    // id order of w * y[t*k + j][f]
+    const int32_t* cmb_ids;    // [T][k], or null (separate combine kernel)
+    const float* cmb_w;        // [T][k]
+    float* cmb_out;            // [T][N_out]
+    const int32_t* cmb_row_pos;  // [T*k] padded position of row r (-1: dropped)
+    int cmb_T, cmb_k;
+    int32_t* cmb_cnt;          // [N_out / 256] tiles finished per block (start at 0)
 };
 
 // One pipeline stage: a 256-row weight tile (two 128-row MMA operands), up to
@@ -188,6 +198,56 @@ __device__ __forceinline__ void emit_token(const TcArgs& a, const Tile& T, int n
 }
 
 __device__ __forceinline__ void epi_bar() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+// Fused combine of features [f0, f0 + 256): epilogue thread i owns feature
+// f0 + i; each token's experts are summed in ascending id order (equal ids in
+// j order), the routing weight applied in fp32 -- the order of k_combine.
+__device__ void combine_block(const TcArgs& a, int f0, int i) {
+    const int k = a.cmb_k;
+    for (int t = 0; t < a.cmb_T; ++t) {
+        int order[kMaxTopK];
+        int idv[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            order[j] = j;
+            idv[j] = (j < k) ? __ldg(a.cmb_ids + (size_t)t * k + j) : INT_MAX;
+        }
+#pragma unroll
+        for (int x = 1; x < kMaxTopK; ++x)
+#pragma unroll
+            for (int b = x; b > 0; --b)
+                if (idv[order[b - 1]] > idv[order[b]]) {
+                    const int tmp = order[b]; order[b] = order[b - 1]; order[b - 1] = tmp;
+                }
+        float acc = 0.f;
+#pragma unroll
+        for (int x = 0; x < kMaxTopK; ++x) {
+            if (x < k) {
+                const int r = t * k + order[x];
+                if (__ldg(a.cmb_row_pos + r) < 0) continue;  // dropped row (bad id)
+                acc += __ldg(a.cmb_w + r) * __ldcg(a.y + (size_t)r * a.N_out + f0 + i);
+            }
+        }
+        a.cmb_out[(size_t)t * a.N_out + f0 + i] = acc;
+    }
+}
+
+// Called by the 8 epilogue warps after they wrote the y rows of a finished
+// tile of features [f0, f0 + 256): count the tile; the block's last tile
+// combines the block.
+__device__ __forceinline__ void tile_done_combine(const TcArgs& a, int f0, bool leader, volatile int* flag,
+                                                  int warp, int lane) {
+    __threadfence();
+    epi_bar();
+    if (leader) {
+        const int ntiles = __ldg(a.tile_scan + a.n_seg);
+        *flag = (atomicAdd(a.cmb_cnt + f0 / 256, 1) == ntiles - 1);
+    }
+    epi_bar();
+    if (!*flag) return;
+    __threadfence();
+    combine_block(a, f0, (warp - 2) * 32 + lane);
+}
 
 // mbar_wait that adds the waited wall time to *acc when tracing.
 __device__ __forceinline__ bool timed_wait(uint32_t bar, uint32_t parity, volatile int* abort,
@@ -380,6 +440,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                             emit_token<kGateUp>(a, T, cb + i + k, q, lane, __uint_as_float(v0[(i + k) >> 4][(i + k) & 15]),
                                                 __uint_as_float(v1[(i + k) >> 4][(i + k) & 15]));
                 }
+                if (!kGateUp && a.cmb_out) tile_done_combine(a, T.f0, leader, last_flag, warp, lane);
                 if (tr) t_work += globaltimer() - tw0;
                 continue;
             }
@@ -413,6 +474,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             }
             epi_bar();  // everyone has read the slots before the counter is reused
             if (leader) a.sk_cnt[sg.first_cta] = 0;
+            if (!kGateUp && a.cmb_out) tile_done_combine(a, T.f0, leader, last_flag, warp, lane);
             if (tr) t_work += globaltimer() - tw0;
         }
         if (tr && leader) { trc[5] = w_tf; trc[6] = t_work; }
@@ -530,8 +592,8 @@ static cudaError_t tc_launch(moe_layer* L, const CUtensorMap& a, const ActMaps& 
                       b.b128, args);
 }
 
-cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid) {
-    (void)T;
+cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid, const int32_t* cmb_ids,
+                           const float* cmb_w, float* cmb_out) {
     const TcState* st = static_cast<const TcState*>(L->tc);
     const moe_config& c = L->cfg;
     TcArgs g{};
@@ -567,6 +629,15 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     d.y = L->y;
     d.pos_row = L->pos_row;
     d.sk_cnt = L->sk_counters + L->num_sms;
+    if (cmb_ids) {
+        d.cmb_ids = cmb_ids;
+        d.cmb_w = cmb_w;
+        d.cmb_out = cmb_out;
+        d.cmb_row_pos = L->row_pos;
+        d.cmb_T = T;
+        d.cmb_k = c.top_k;
+        d.cmb_cnt = L->sk_counters + 4 * L->num_sms;
+    }
     d.trace = L->trace ? L->trace + (size_t)L->num_sms * 8 : nullptr;
     e = tc_launch<false, kFmtE2M1>(L, st->down, st->hq, d, s);
     if (e != cudaSuccess || !c.has_shared) return e;

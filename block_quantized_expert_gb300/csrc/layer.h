@@ -68,7 +68,13 @@ struct moe_layer {
 
 namespace moe {
 
-constexpr int kChunk = 4;  // tokens per CUDA-core GEMM work item
+constexpr int kChunk = 4;      // tokens per CUDA-core GEMM work item
+constexpr int kFrontMaxT = 32; // batches up to this size use the one-CTA front kernel
+constexpr int kFusedCombineMaxT = 32;  // and the combine fused into the down GEMM
+
+// split-tile counters: 4 GEMM launches x num_sms, then one per 256-feature
+// block of the fused combine (H / 256 <= 32)
+inline int kSkCounters(const moe_layer* L) { return 4 * L->num_sms + 32; }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
 // stream; the kernels synchronise on it with pdl_wait().
@@ -99,6 +105,9 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
 cudaError_t launch_quantize_canonical(moe_layer* L, const uint16_t* x, int T, uint8_t* q,
                                       uint8_t* sc, cudaStream_t s);
 cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cudaStream_t s);
+// route (if logits) + permute + quantise in one CTA, for T <= kFrontMaxT
+cudaError_t launch_front(moe_layer* L, const float* logits, int32_t* ids, float* w, const uint16_t* x,
+                         int T, cudaStream_t s);
 cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int T,
                            float* out, cudaStream_t s);
 cudaError_t launch_hidden_gather(moe_layer* L, int T, uint8_t* hq, uint8_t* hs,
@@ -115,7 +124,10 @@ cudaError_t cc_init();
 // Tensor-core path.
 cudaError_t tc_init(moe_layer* L);
 void tc_free(moe_layer* L);
-cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid);
+// cmb_ids != null: fuse the combine into the down GEMM (out = sum over the
+// token's experts in ascending order of w * y); requires no shared expert.
+cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid, const int32_t* cmb_ids,
+                           const float* cmb_w, float* cmb_out);
 // Scale atoms of 256-row blocks (two 512-byte atoms per block and 128-column
 // step).  mode 0: halves from srcA / srcB (block g rows g*128..), canonical
 // [mats][rows][K/32] scales; 1: halves = rows (2g)*128.. and (2g+1)*128.. of srcA;

@@ -17,15 +17,10 @@ namespace moe {
 // expert index (guide, section 1: SQRT_SOFTPLUS gating, top-k).  Lane j < k
 // then evaluates s_j in fp32 and every lane sums s_0..s_{k-1} in that order;
 // w_j = w_scale * s_j / sum (guide, section 3.2).
-__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
-                                               int k, float w_scale, int32_t* __restrict__ ids,
-                                               float* __restrict__ w, uint32_t* err) {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (t >= T) return;
-    const float* row = logits + (size_t)t * E;
+// Routing of one token by one warp: writes ids_t[0..k) and w_t[0..k).
+__device__ void route_token(const float* __restrict__ row, int E, int k, float w_scale,
+                            int32_t* __restrict__ ids_t, float* __restrict__ w_t, uint32_t* err,
+                            int lane) {
     uint32_t taken = 0;  // bit i <-> expert lane + 32 i
     int my_sel = -1;     // lane j keeps the j-th selection
     float my_logit = 0.f;
@@ -54,10 +49,21 @@ __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits,
     float sum = 0.f;
     for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, s, j);
     if (lane < k) {
-        ids[(size_t)t * k + lane] = ok ? my_sel : -1;
-        w[(size_t)t * k + lane] = ok ? w_scale * s / sum : 0.0f;
+        ids_t[lane] = ok ? my_sel : -1;
+        w_t[lane] = ok ? w_scale * s / sum : 0.0f;
     }
     if (!ok && lane == 0) raise_flag(err, ERR_BAD_ID);
+}
+
+__global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
+                                               int k, float w_scale, int32_t* __restrict__ ids,
+                                               float* __restrict__ w, uint32_t* err) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int lane = threadIdx.x & 31;
+    if (t >= T) return;
+    route_token(logits + (size_t)t * E, E, k, w_scale, ids + (size_t)t * k, w + (size_t)t * k, err, lane);
 }
 
 cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,
@@ -135,15 +141,13 @@ __device__ Int4Scan block_exclusive_scan4(Int4Scan v, Int4Scan* warp_tot, Int4Sc
 // (match_any).  Integer atomics only count, so the result is deterministic.
 // Besides the ABI outputs it fills the padded bookkeeping of the GEMMs:
 // every expert segment starts at a multiple of 128 rows.
-__global__ void __launch_bounds__(1024) k_permute(
+__device__ void permute_body(
     const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
     int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
     int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
-    int T, uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
-    pdl_launch_dependents();
-    pdl_wait();
-    extern __shared__ int dyn[];  // cnt, cursor, s_off, s_poff [E] each; then wc [32][E] bytes
+    int T, uint32_t* err, int32_t* __restrict__ zero, int n_zero, int* dyn) {
+    // dyn (shared): cnt, cursor, s_off, s_poff [E] each; then wc [32][E] bytes
     int* cnt = dyn;
     int* cursor = dyn + E;
     int* s_off = dyn + 2 * E;
@@ -233,6 +237,19 @@ __global__ void __launch_bounds__(1024) k_permute(
     }
 }
 
+__global__ void __launch_bounds__(1024) k_permute(
+    const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
+    int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
+    int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
+    int T, uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
+    extern __shared__ int dyn[];
+    pdl_launch_dependents();
+    pdl_wait();
+    permute_body(ids, R, E, offsets, row_src, row_dst, counts, poff, tile_scan, chunk_scan, row_pos,
+                 pos_row, sh_desc, T, err, zero, n_zero, dyn);
+}
+
 cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* offsets,
                            int32_t* row_src, int32_t* row_dst, cudaStream_t s) {
     const int R = T * L->cfg.top_k;
@@ -241,7 +258,7 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
     return launch_pdl(k_permute, dim3(1), dim3(1024), smem, s, ids, R, L->cfg.n_experts, offsets, row_src,
                       row_dst, L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
                       L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err, L->sk_counters,
-                      L->sk_counters ? 4 * L->num_sms : 0);
+                      L->sk_counters ? kSkCounters(L) : 0);
 }
 
 // The same counting sort with caller-chosen bookkeeping buffers (no layer):
@@ -256,10 +273,7 @@ cudaError_t launch_permute_raw(const int32_t* ids, int T, int k, int E, int32_t*
     return cudaGetLastError();
 }
 
-cudaError_t kernels_init() {
-    return cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                48 * kMaxExperts);
-}
+
 
 // --------------------------------------------------------------- quantise --
 // MXFP8 of bf16 rows.  A group of 4 lanes owns one 32-block (8 elements per
@@ -277,15 +291,11 @@ struct QuantDst {
     uint8_t* xs_tok;
 };
 
+// One warp-task: 256 elements (8 blocks) of token row t.
 template <int kMode>
-__global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x, int T, int H,
-                                                  QuantDst d) {
-    pdl_launch_dependents();
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
+__device__ __forceinline__ void quantize_task(const uint16_t* __restrict__ x, int H, const QuantDst& d,
+                                              int task, int lane) {
     const int tasks_per_row = (H + 255) / 256;
-    const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-    if (task >= T * tasks_per_row) return;
     const int t = task / tasks_per_row;
     const int b = (task % tasks_per_row) * 8 + (lane >> 2);  // 32-block index
     const int part = lane & 3;
@@ -333,6 +343,43 @@ __global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x
     }
 }
 
+template <int kMode>
+__global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x, int T, int H,
+                                                  QuantDst d) {
+    pdl_launch_dependents();
+    pdl_wait();
+    const int task = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    if (task >= T * ((H + 255) / 256)) return;
+    quantize_task<kMode>(x, H, d, task, threadIdx.x & 31);
+}
+
+// Small batches in one CTA (T <= kFrontMaxT): optional routing (one warp per
+// token), the counting sort and the quantisation, each phase after a barrier.
+// Saves two kernel boundaries on the decode path.
+__global__ void __launch_bounds__(1024) k_front(
+    const float* __restrict__ logits, float w_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
+    const uint16_t* __restrict__ x, int T, int k, int E, int H, QuantDst qd, int32_t* __restrict__ offsets,
+    int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
+    int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
+    int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
+    uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
+    extern __shared__ int dyn[];
+    pdl_launch_dependents();
+    pdl_wait();
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (logits) {
+        if (warp < T)
+            route_token(logits + (size_t)warp * E, E, k, w_scale, ids + (size_t)warp * k,
+                        wts + (size_t)warp * k, err, lane);
+        __syncthreads();
+    }
+    permute_body(ids, T * k, E, offsets, row_src, row_dst, counts, poff, tile_scan, chunk_scan, row_pos,
+                 pos_row, sh_desc, T, err, zero, n_zero, dyn);
+    __syncthreads();
+    const int tasks = T * ((H + 255) / 256);
+    for (int task = warp; task < tasks; task += 32) quantize_task<1>(x, H, qd, task, lane);
+}
+
 static cudaError_t quantize_launch(int mode, const uint16_t* x, int T, int H, QuantDst d,
                                    cudaStream_t s) {
     const long long tasks = (long long)T * ((H + 255) / 256);
@@ -349,6 +396,26 @@ cudaError_t launch_quantize_canonical(moe_layer* L, const uint16_t* x, int T, ui
     d.q = q;
     d.s = sc;
     return quantize_launch(0, x, T, L->cfg.hidden, d, s);
+}
+
+cudaError_t launch_front(moe_layer* L, const float* logits, int32_t* ids, float* w, const uint16_t* x,
+                         int T, cudaStream_t s) {
+    QuantDst d{};
+    d.xq = L->xq;
+    d.xs = L->xs;
+    d.row_pos = L->row_pos;
+    d.k = L->cfg.top_k;
+    if (L->cfg.has_shared) {
+        d.xq_tok = L->xq_tok;
+        d.xs_tok = L->xs_tok;
+    }
+    const size_t smem = (size_t)48 * L->cfg.n_experts;
+    L->launches += 1;
+    return launch_pdl(k_front, dim3(1), dim3(1024), smem, s, logits, L->cfg.w_scale, ids, w, x, T,
+                      L->cfg.top_k, L->cfg.n_experts, L->cfg.hidden, d, L->offsets, L->row_src, L->row_dst,
+                      L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
+                      L->cfg.has_shared ? L->sh_desc : nullptr, L->d_err, L->sk_counters,
+                      L->sk_counters ? kSkCounters(L) : 0);
 }
 
 cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cudaStream_t s) {
@@ -482,6 +549,30 @@ cudaError_t pack_sf_pairs(const uint8_t* srcA, const uint8_t* srcB, uint8_t* dst
     const long long n = (long long)mats * groups * (K / 128) * 1024;
     k_pack_sf_pairs<<<(unsigned)((n + 255) / 256), 256, 0, s>>>(srcA, srcB, dst, groups, K, mode, n);
     return cudaGetLastError();
+}
+
+// One shared-memory carveout for every kernel of the forward: the GEMMs need
+// the maximum, and an SM whose carveout changes between two kernels must
+// drain and reconfigure.
+template <typename K>
+static cudaError_t max_carveout(K kernel) {
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                cudaSharedmemCarveoutMaxShared);
+}
+
+cudaError_t kernels_init() {
+    cudaError_t e = cudaFuncSetAttribute(k_permute, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         48 * kMaxExperts);
+    if (e == cudaSuccess) e = max_carveout(k_permute);
+    if (e == cudaSuccess) e = max_carveout(k_route);
+    if (e == cudaSuccess) e = max_carveout(k_route_hash);
+    if (e == cudaSuccess) e = max_carveout(k_quantize<0>);
+    if (e == cudaSuccess) e = max_carveout(k_quantize<1>);
+    if (e == cudaSuccess) e = max_carveout(k_combine);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_front, cudaFuncAttributeMaxDynamicSharedMemorySize, 48 * kMaxExperts);
+    if (e == cudaSuccess) e = max_carveout(k_front);
+    return e;
 }
 
 }  // namespace moe

@@ -145,6 +145,13 @@ moe_status moe_quantize(moe_layer* layer, const uint16_t* x, int T, uint8_t* q, 
 moe_status moe_forward(moe_layer* layer, const uint16_t* x, int T, const int32_t* ids,
                        const float* w, float* out, moe_stream_t stream);
 
+/* Routing and layer in one call: moe_route followed by moe_forward, with
+ * ids [T][k] and w [T][k] (device) written as moe_route writes them and out
+ * [T][H] as moe_forward.  Small batches (T <= 32) run the routing, the
+ * counting sort and the quantisation in one kernel.                        */
+moe_status moe_route_forward(moe_layer* layer, const float* logits, const uint16_t* x, int T,
+                             int32_t* ids, float* w, float* out, moe_stream_t stream);
+
 /* Whole layer from host memory: copies x (host u16 [T][H]) and logits (host
  * f32 [T][E]) into the layer's staging buffers, runs moe_route and
  * moe_forward, and copies the result to out (host f32 [T][H]).  Asynchronous
@@ -192,8 +199,8 @@ moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entri
  * of the graph runs it again).                                             */
 unsigned long long moe_kernel_launches(const moe_layer* layer);
 
-/* Kernel path of the GEMM steps: 0 = automatic, 1 = CUDA-core kernels,
- * 2 = tcgen05 block-scaled tensor-core kernels.  Both compute the same
+/* Kernel path of the GEMM steps: 0 = automatic (tcgen05 when the device is
+ * sm_103), 1 = CUDA-core kernels, 2 = tcgen05 block-scaled tensor-core kernels.  Both compute the same
  * layer; the choice only affects speed and the order of fp32 additions.    */
 moe_status moe_set_gemm_path(moe_layer* layer, int path);
 

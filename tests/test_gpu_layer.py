@@ -194,6 +194,25 @@ def test_forward_is_deterministic_and_host_entry_matches(tiny):
     assert oh.numpy().tobytes() == a.tobytes()
 
 
+@pytest.mark.parametrize("path", PATHS)
+@pytest.mark.parametrize("T", [1, 4, 32, 64])
+def test_route_forward_equals_route_then_forward(tiny, path, T):
+    """The one-call entry point (fused routing/sort/quantisation for small
+    batches) gives the same bytes as the two calls."""
+    cfg, w, layer = tiny
+    bqe.moe_set_gemm_path(layer, path)
+    tk = G.tokens(0, n=T)
+    ids, wd = G.route_dev(layer, tk.logits, cfg.k)
+    a = G.forward_dev(layer, tk.x_bits, ids, wd).cpu().numpy()
+    ids2 = torch.empty_like(ids)
+    w2 = torch.empty_like(wd)
+    out2 = torch.empty((T, cfg.H), dtype=torch.float32, device=G.DEV)
+    bqe.moe_route_forward(layer, G.to_dev(tk.logits), G.to_dev(tk.x_bits, torch.int16), ids2, w2, out2)
+    bqe.moe_check(layer)
+    assert torch.equal(ids, ids2) and torch.equal(wd, w2)
+    assert out2.cpu().numpy().tobytes() == a.tobytes()
+
+
 def test_argument_errors(tiny):
     cfg, w, layer = tiny
     lib = bqe.load_library()
