@@ -255,7 +255,18 @@ def run_ours(args, cfg, rank, world, local_rank):
     st = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(5)] for evs in stage_events])
     stage_ms = dict(zip(names, st.mean(0).tolist()))
     byts = algorithmic_bytes(cfg, avg_touched, rows)
-    dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
+    step_bytes = byts["gateup"] + byts["down"]
+    if stage_ms["down"] < 1e-3 * stage_ms["gateup"]:
+        # one token on the automatic path: the whole layer is one kernel
+        # (timed as the gate/up stage), so it moves both GEMMs' bytes
+        dom = "layer"
+        byts["layer"] = byts["gateup"] + byts["down"]
+        stage_ms["layer"] = stage_ms.pop("gateup")
+        stage_ms.pop("down")
+        kernel = "whole-layer decode kernel"
+    else:
+        dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
+        kernel = f"{dom} GEMM"
     achieved = byts[dom] / (stage_ms[dom] * 1e-3) / 1e9
     peaks = {}
     try:
@@ -280,12 +291,12 @@ def run_ours(args, cfg, rank, world, local_rank):
            "gpu_launches": int(launches),
            "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
            "experts_touched_per_step": avg_touched,
-           "roofline": {"bound": "hbm", "kernel": f"{dom} GEMM", "achieved": round(achieved, 1),
+           "roofline": {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
                         "peak": peak, "unit": "GB/s", "frac": round(achieved / peak, 4),
                         "traffic": None, "algorithmic_bytes_per_launch": int(byts[dom]),
                         "peak_source": peak_src,
                         "hbm_frac_whole_step": round(
-                            (byts["gateup"] + byts["down"]) / (ms / K * 1e-3) / 1e9 / peak, 4)},
+                            step_bytes / (ms / K * 1e-3) / 1e9 / peak, 4)},
            "clocks": clocks}
 
     if not args.no_e2e:
@@ -299,21 +310,49 @@ def run_ours(args, cfg, rank, world, local_rank):
 
 
 def trace_report(bqe, layer, step, i, dev):
-    """Per GEMM launch of one more call: mean over CTAs of the wait counters."""
+    """Timeline of one more call: front kernel and GEMM launches (stderr)."""
     import torch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
-    buf = torch.zeros(4 * sms * 8, dtype=torch.int64, device=dev)
-    bqe.moe_set_trace(layer, buf)
-    step(i)
-    torch.cuda.synchronize()
-    t = buf.view(4, sms, 8).cpu().numpy().astype(np.float64)
+    buf = torch.zeros(4 * sms * 12 + 4, dtype=torch.int64, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for k in range(4):
+            step(i + k)
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):  # as in the timed region: graph replay
+            for k in range(8):
+                if k == 7:
+                    bqe.moe_set_trace(layer, buf)
+                step(i + k)
+        g.replay()
+        stream.synchronize()
+    raw = buf.cpu().numpy().astype(np.float64)
+    t = raw[: 4 * sms * 12].reshape(4, sms, 12)
+    fr = raw[4 * sms * 12:]
+    t0 = fr[0] if fr[0] > 0 else t[0, :, 0].min()
+    if fr[0] > 0:
+        print("TRACE", json.dumps({"launch": "front", "entry_us": 0.0, "wait_end_us": round((fr[1] - t0) / 1e3, 2),
+                                   "exit_us": round((fr[2] - t0) / 1e3, 2)}), file=sys.stderr, flush=True)
+    if t[0, :, 9].max() > 0:  # the whole-layer decode kernel
+        e0 = t[0, :, 0].min()
+        rep = {"launch": "decode"}
+        for key, c, f in (("first_entry_us", 0, np.min), ("wait_end_us", 8, np.min),
+                          ("routed_quantised_us", 9, np.max), ("gateup_done_first_us", 10, np.min),
+                          ("gateup_done_last_us", 10, np.max), ("barrier_passed_us", 11, np.max),
+                          ("down_operands_us", 2, np.max), ("last_exit_us", 1, np.max)):
+            rep[key] = round((f(t[0, :, c]) - e0) / 1e3, 2)
+        print("TRACE", json.dumps(rep), file=sys.stderr, flush=True)
+        return
     names = ["gateup", "down", "shared_gateup", "shared_down"]
     for j in range(4):
         if t[j, :, 0].max() == 0:
             continue
         dur = (t[j, :, 1] - t[j, :, 0]) / 1e3
-        span = (t[j, :, 1].max() - t[j, :, 0].min()) / 1e3
-        rep = {"launch": names[j], "span_us": round(span, 2), "cta_us_mean": round(dur.mean(), 2),
+        rep = {"launch": names[j], "first_entry_us": round((t[j, :, 0].min() - t0) / 1e3, 2),
+               "wait_end_us": round((t[j, :, 8].min() - t0) / 1e3, 2),
+               "last_exit_us": round((t[j, :, 1].max() - t0) / 1e3, 2),
+               "cta_us_mean": round(dur.mean(), 2),
                "producer_wait_free_us": round(t[j, :, 2].mean() / 1e3, 2),
                "mma_wait_data_us": round(t[j, :, 3].mean() / 1e3, 2),
                "mma_wait_acc_us": round(t[j, :, 4].mean() / 1e3, 2),

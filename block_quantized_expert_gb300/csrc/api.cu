@@ -127,6 +127,17 @@ cudaError_t forward_kernels(moe_layer* L, const float* logits, const uint16_t* x
     const bool tc = L->gemm_path != 1 && L->tc != nullptr;  // automatic: tensor cores
     const bool fuse_combine = tc && small && !L->cfg.has_shared && T <= moe::kFusedCombineMaxT;
     cudaError_t e = M(0, cudaSuccess);
+    if (tc && L->gemm_path == 0 && logits && T == 1 && moe::decode_supported(L)) {
+        // one token: the whole layer in one cooperative kernel (the stage
+        // marks before it are empty and its time shows as the gate/up stage)
+        if (e == cudaSuccess) e = M(1, cudaSuccess);
+        if (e == cudaSuccess) e = M(2, cudaSuccess);
+        if (e == cudaSuccess) e = moe::launch_decode(L, logits, x, ids, w, out, s);
+        if (e == cudaSuccess) e = M(3, cudaSuccess);
+        if (e == cudaSuccess) e = M(4, cudaSuccess);
+        if (e == cudaSuccess) e = M(5, cudaSuccess);
+        return e;
+    }
     if (e == cudaSuccess && small) {
         e = M(1, moe::launch_front(L, logits, ids, w, x, T, s));
         if (e == cudaSuccess) e = M(2, cudaSuccess);
@@ -303,8 +314,8 @@ unsigned long long moe_kernel_launches(const moe_layer* L) { return L ? L->launc
 
 moe_status moe_set_trace(moe_layer* L, unsigned long long* buf, size_t entries) {
     if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
-    if (buf && entries < (size_t)4 * L->num_sms * 8)
-        return fail(L, MOE_ERR_INVALID_ARG, "trace buffer needs 4 * num_sms * 8 entries");
+    if (buf && entries < (size_t)4 * L->num_sms * 12 + 4)
+        return fail(L, MOE_ERR_INVALID_ARG, "trace buffer needs 4 * num_sms * 12 + 4 entries");
     L->trace = buf;
     return MOE_OK;
 }

@@ -30,6 +30,7 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "route.cuh"
 #include "tc_ptx.cuh"
 
 namespace moe {
@@ -61,7 +62,7 @@ struct TcArgs {
     uint32_t a_tx;             // TMA bytes of one 256-row weight copy
     int32_t* sk_cnt;           // [gridDim] arrival counters of cut tiles, by first CTA (start at 0)
     float* sk_part;            // [gridDim][2][2][128][128] partial accumulators
-    unsigned long long* trace; // [gridDim][8] wait-time counters, or null
+    unsigned long long* trace; // [gridDim][12] timing counters, or null
     // fused combine (down GEMM of small batches): after the last tile of a
     // 256-feature block, out[t][f] = sum over the token's experts in ascending
     // id order of w * y[t*k + j][f]
@@ -277,11 +278,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::kStages + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    volatile int* routed_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = a.K / 128;
     const bool tr = a.trace != nullptr;
-    unsigned long long* trc = tr ? a.trace + (size_t)blockIdx.x * 8 : nullptr;
+    unsigned long long* trc = tr ? a.trace + (size_t)blockIdx.x * 12 : nullptr;
     if (tr && threadIdx.x == 0) trc[0] = globaltimer();
 
     if (threadIdx.x == 0) {
@@ -306,6 +308,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     // the prologue above overlaps the previous kernel; its outputs are read below
     pdl_launch_dependents();
     pdl_wait();
+    if (tr && threadIdx.x == 0) trc[8] = globaltimer();
     const int tiles = __ldg(a.tile_scan + a.n_seg) * a.mt;
 
     auto give_up = [&]() {
@@ -410,10 +413,10 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         unsigned long long w_tf = 0, t_work = 0;
         while (it.next(sg)) {
             const Tile T = decode_tile<kGateUp>(a, sg.tile);
-            if (!timed_wait(tmem_full, acc_phase, abort_flag, tr, w_tf)) {
-                if (lane == 0) give_up();
-                break;
-            }
+            // on a timeout the epilogue goes on with whatever the accumulator
+            // holds (the error is raised), so all eight warps keep meeting at
+            // the same named barriers
+            if (!timed_wait(tmem_full, acc_phase, abort_flag, tr, w_tf) && lane == 0) give_up();
             const uint64_t tw0 = tr ? globaltimer() : 0;
             tc_fence_after();
             acc_phase ^= 1u;
@@ -486,6 +489,422 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem, Cfg::kTmemCols);
+    }
+}
+
+// ------------------------------------------------------------- decode --
+// The whole layer for one token (T = 1, learned router, no shared expert) in
+// one cooperative kernel of one CTA per SM -- route, quantise, gate/up,
+// down, combine -- so nothing of the token goes through a kernel boundary.
+// Every CTA routes the token itself (the same warp-argmax as k_route, hence
+// the same experts and weights everywhere) and quantises x straight into
+// resident shared-memory B tiles of N = 16 rows (row 0 is the token, rows
+// 1-15 stay zero); the weights stream through the same TMA / tcgen05 pipeline
+// as k_gemm_tc, split stream-K over all SMs.  A grid barrier separates the
+// gate/up phase from the down phase; h crosses it through global memory.
+
+constexpr int kDecN = 16;                 // MMA N: the single token and 15 zero rows
+constexpr int kDecBTile = kDecN * 128;    // 2 KB of B per 128-wide K step
+constexpr int kDecStageBytes = 32768 + 1024;  // 256 weight rows + their scale atoms
+constexpr int kDecStages = 4;
+constexpr int kDecResOff = kDecStages * kDecStageBytes;  // resident B tiles (64 KB)
+constexpr int kDecSfbSlot = 64 * 16 + 512;               // scale bytes of 64 K steps + one copy's reach
+constexpr int kDecSfbOff = kDecResOff + 65536;           // resident B scales (2 slots)
+constexpr int kDecBarOff = kDecSfbOff + 2 * kDecSfbSlot;
+constexpr int kDecSmem = kDecBarOff + 512 + 1024;
+static_assert(kDecSmem <= 232448, "shared memory budget");
+
+struct DecArgs {
+    const float* logits;  // [E]
+    const uint16_t* x;    // [H] bf16
+    int E, k, H, I;
+    float w_scale;
+    int32_t* ids_out;     // [k]
+    float* w_out;         // [k]
+    float* out;           // [H]
+    const uint8_t* gu_sf;
+    const uint8_t* down_sf;
+    uint8_t* hq;          // [k][I] e4m3 (scratch)
+    uint8_t* hs;          // [k][I/32] UE8M0 (scratch)
+    float* y;             // [k][H] down outputs (scratch)
+    float* sk_part;       // [G][2][2][128][128]
+    int32_t* sk_cnt_gu;   // [G]
+    int32_t* sk_cnt_dn;   // [G]
+    int32_t* cmb_cnt;     // [H/256]
+    unsigned* gbar;       // [2]: arrival count, generation
+    uint32_t* err;
+    unsigned long long* trace;  // [gridDim][12] ns timestamps, or null
+};
+
+// Bounded grid-wide barrier (all CTAs are co-resident: cooperative launch).
+__device__ bool grid_barrier(unsigned* gbar, unsigned G, volatile int* abort) {
+    __syncthreads();
+    __shared__ int ok_s;
+    if (threadIdx.x == 0) {
+        volatile unsigned* gen = gbar + 1;
+        const unsigned g0 = *gen;
+        __threadfence();
+        bool ok = true;
+        if (atomicAdd(gbar, 1u) == G - 1) {
+            atomicExch(gbar, 0u);
+            __threadfence();
+            atomicAdd(gbar + 1, 1u);
+        } else {
+            const uint64_t t0 = globaltimer();
+            while (*gen == g0) {
+                if (globaltimer() - t0 > kWaitLimitNs || *abort) { ok = false; break; }
+            }
+        }
+        __threadfence();
+        ok_s = ok;
+    }
+    __syncthreads();
+    return ok_s != 0;
+}
+
+// The stream-K gate/up or down phase of the decode kernel (one token).
+template <bool kGateUp>
+__device__ void decode_phase(const DecArgs& a, const CUtensorMap* tmA, const uint8_t* sfa, uint8_t* smem,
+                             uint32_t bar0, uint32_t tmem, const int* seg_e, const int* seg_j,
+                             const float* seg_w, const int* slot_s, uint32_t& stage, uint32_t& phase,
+                             uint32_t& acc_phase, volatile int* abort_flag, volatile int* last_flag,
+                             int32_t* sk_cnt) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int MT = kGateUp ? a.I / 128 : a.H / 256;
+    const int K = kGateUp ? a.H : a.I;
+    const int KB = K / 128;
+    const int seg_rows = kGateUp ? 2 * a.I : a.H;
+    const int tiles = a.k * MT;
+    auto full_bar = [&](int st) { return bar0 + 8u * st; };
+    auto empty_bar = [&](int st) { return bar0 + 8u * (kDecStages + st); };
+    const uint32_t tmem_full = bar0 + 8u * (2 * kDecStages);
+    const uint32_t tmem_empty = tmem_full + 8u;
+    const uint32_t res_base = smem_u32(smem + kDecResOff);
+    const uint32_t sfb_base = smem_u32(smem + kDecSfbOff);
+    auto give_up = [&]() {
+        *abort_flag = 1;
+        raise_flag(a.err, ERR_TIMEOUT);
+    };
+    auto slot_of = [&](int s) { return kGateUp ? 0 : (slot_s[1] == s ? 1 : 0); };
+    SegIter it;
+    it.init(tiles, KB, (int)gridDim.x, (int)blockIdx.x);
+    Seg sg;
+    if (warp == 0) {
+        if (lane == 0) {
+            bool ok = true;
+            while (ok && it.next(sg)) {
+                const int s = sg.tile / MT, m = sg.tile % MT;
+                const int arow = seg_e[s] * seg_rows + m * 256;
+                const size_t atom_a = (size_t)(arow / 256) * KB;
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* st = smem + stage * kDecStageBytes;
+                    const uint32_t fb = full_bar(stage);
+                    mbar_arrive_expect_tx(fb, kFp4BoxTx + 1024u);
+                    tma_load_2d(smem_u32(st), tmA, kb * 128, arow, fb);
+                    bulk_load(smem_u32(st + 32768), sfa + (atom_a + kb) * 1024, 1024, fb);
+                    if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
+                }
+            }
+        }
+    } else if (warp == 1) {
+        if (lane == 0) {
+            bool ok = true;
+            while (ok && it.next(sg)) {
+                const int s = sg.tile / MT;
+                const int sl = slot_of(s);
+                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
+                    give_up();
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                    if (!mbar_wait(full_bar(stage), phase, kWaitLimitNs, abort_flag)) {
+                        give_up();
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t st = smem_u32(smem + stage * kDecStageBytes);
+                    const uint32_t sf_col = tmem + 256 + stage * 12;
+                    const uint32_t bt = res_base + sl * 32768 + kb * kDecBTile;
+                    tmem_cp_32x128_x4(sf_col, desc_sf(st + 32768));
+                    tmem_cp_32x128_x4(sf_col + 4, desc_sf(st + 32768 + 512));
+                    tmem_cp_32x128_x4(sf_col + 8, desc_sf(sfb_base + sl * kDecSfbSlot + kb * 16));
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk) {
+                        const uint32_t id = idesc_mx(kFmtE2M1, kFmtE4M3, 128, kDecN, kk, kk);
+                        const uint64_t bd = desc_sw128(bt + 32 * kk);
+                        const uint32_t acc = (kb > sg.kb0 || kk) ? 1u : 0u;
+                        mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sf_col + 8, acc);
+                        mma_mx(tmem + 128, desc_sw128(st + 16384 + 32 * kk), bd, id, sf_col + 4, sf_col + 8, acc);
+                    }
+                    mma_commit(empty_bar(stage));
+                    if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
+                }
+                if (!ok) break;
+                mma_commit(tmem_full);
+                acc_phase ^= 1u;
+            }
+        }
+    } else {
+        // epilogue: only token column 0 is real; warps of the second column
+        // half take part in the barriers only
+        const int q = warp & 3;
+        const int hf = (warp - 2) >> 2;
+        const int fm = 32 * q + lane;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
+        const bool leader = warp == 2 && lane == 0;
+        while (it.next(sg)) {
+            const int s = sg.tile / MT, m = sg.tile % MT;
+            const int f0 = m * (kGateUp ? 128 : 256);
+            // on a timeout the epilogue goes on with whatever the accumulator
+            // holds (the error is raised), so all eight warps keep meeting at
+            // the same named barriers
+            if (!mbar_wait(tmem_full, acc_phase, kWaitLimitNs, abort_flag) && lane == 0) give_up();
+            tc_fence_after();
+            acc_phase ^= 1u;
+            float v0 = 0.f, v1 = 0.f;
+            if (hf == 0) {
+                uint32_t r0[16], r1[16];
+                tmem_ld16(tq, r0);
+                tmem_ld16(tq + 128, r1);
+                tmem_ld_wait();
+                v0 = __uint_as_float(r0[0]);
+                v1 = __uint_as_float(r1[0]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(tmem_empty);
+            bool emit = true;
+            if (sg.first_cta != sg.last_cta) {
+                float* part = a.sk_part + ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128;
+                if (hf == 0) {
+                    part[fm] = v0;
+                    part[(size_t)128 * 128 + fm] = v1;
+                }
+                __threadfence();
+                epi_bar();
+                if (leader) {
+                    const int nparts = sg.last_cta - sg.first_cta + 1;
+                    *last_flag = (atomicAdd(sk_cnt + sg.first_cta, 1) == nparts - 1);
+                }
+                epi_bar();
+                emit = *last_flag != 0;
+                if (emit) {
+                    __threadfence();
+                    v0 = 0.f;
+                    v1 = 0.f;
+                    for (int cc = sg.first_cta; cc <= sg.last_cta; ++cc) {
+                        const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128;
+                        v0 += __ldcg(pp + fm);
+                        v1 += __ldcg(pp + (size_t)128 * 128 + fm);
+                    }
+                }
+                epi_bar();
+                if (emit && leader) sk_cnt[sg.first_cta] = 0;
+            }
+            if (!emit) continue;
+            if (kGateUp) {
+                if (hf == 0) {
+                    const float h = silu_mul(v0, v1);
+                    const int ex = mxfp8_exponent(warp_max(fabsf(h)));
+                    const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
+                    a.hq[(size_t)s * a.I + f0 + fm] = (uint8_t)code;
+                    if (lane == 0) a.hs[(size_t)s * (a.I / 32) + (f0 + 32 * q) / 32] = (uint8_t)(ex + 127);
+                }
+            } else {
+                if (hf == 0) {
+                    float* yr = a.y + (size_t)seg_j[s] * a.H + f0;
+                    yr[fm] = v0;
+                    yr[128 + fm] = v1;
+                }
+                // the block's last expert tile combines it (ascending expert order)
+                __threadfence();
+                epi_bar();
+                if (leader) *last_flag = (atomicAdd(a.cmb_cnt + m, 1) == a.k - 1);
+                epi_bar();
+                if (*last_flag) {
+                    __threadfence();
+                    const int i = (warp - 2) * 32 + lane;
+                    float acc = 0.f;
+                    for (int ss = 0; ss < a.k; ++ss)
+                        acc += seg_w[ss] * __ldcg(a.y + (size_t)seg_j[ss] * a.H + f0 + i);
+                    a.out[f0 + i] = acc;
+                    epi_bar();
+                    if (leader) a.cmb_cnt[m] = 0;
+                }
+            }
+        }
+    }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1)
+k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUtensorMap tmDN, const DecArgs a) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);
+    const uint32_t bar0 = smem_u32(bars);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDecStages + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
+    volatile int* routed_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
+    int* seg_e = reinterpret_cast<int*>(tmem_slot + 4);        // [8] experts, ascending
+    int* seg_j = seg_e + 8;                                     // [8] their j
+    float* seg_w = reinterpret_cast<float*>(seg_j + 8);         // [8] their weights
+    int* ids_s = reinterpret_cast<int*>(seg_w + 8);             // [8] router output, j order
+    float* w_s = reinterpret_cast<float*>(ids_s + 8);           // [8]
+    int* slot_s = reinterpret_cast<int*>(w_s + 8);              // [2] down-phase expert slots
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int k = a.k;
+
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kDecStages; ++st) {
+            mbar_init(bar0 + 8u * st, 1);
+            mbar_init(bar0 + 8u * (kDecStages + st), 1);
+        }
+        mbar_init(bar0 + 8u * (2 * kDecStages), 1);
+        mbar_init(bar0 + 8u * (2 * kDecStages) + 8u, kEpiWarps);
+        *abort_flag = 0;
+        fence_mbar_init();
+        prefetch_tmap(&tmGU);
+        prefetch_tmap(&tmDN);
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
+    // zero the resident B tiles and scales (rows 1-15 stay zero)
+    for (int i = threadIdx.x; i < (65536 + 2 * kDecSfbSlot) / 16; i += kTcThreads)
+        reinterpret_cast<uint4*>(smem + kDecResOff)[i] = make_uint4(0, 0, 0, 0);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    // trace: [0] entry, [8] wait end, [9] routed and quantised, [10] gate/up
+    // done, [11] grid barrier passed, [2] down operands built, [1] exit
+    unsigned long long* trc = a.trace ? a.trace + (size_t)blockIdx.x * 12 : nullptr;
+    const bool tr0 = trc && threadIdx.x == 0;
+    if (tr0) trc[0] = globaltimer();
+    pdl_launch_dependents();
+    pdl_wait();
+    if (tr0) trc[8] = globaltimer();
+
+    // ---- route (every CTA the same) and quantise x into the resident B tiles
+    if (warp == 2) route_token(a.logits, a.E, k, a.w_scale, ids_s, w_s, a.err, lane);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        int order[kMaxTopK];
+        for (int j = 0; j < k; ++j) order[j] = j;
+        for (int x = 1; x < k; ++x)
+            for (int b = x; b > 0 && ids_s[order[b - 1]] > ids_s[order[b]]; --b) {
+                const int tmp = order[b]; order[b] = order[b - 1]; order[b - 1] = tmp;
+            }
+        bool ok = true;
+        for (int x = 0; x < k; ++x) {
+            seg_e[x] = ids_s[order[x]];
+            seg_j[x] = order[x];
+            seg_w[x] = w_s[order[x]];
+            ok = ok && seg_e[x] >= 0 && seg_e[x] < a.E;
+        }
+        *routed_flag = ok;
+        if (blockIdx.x == 0)
+            for (int j = 0; j < k; ++j) { a.ids_out[j] = ids_s[j]; a.w_out[j] = w_s[j]; }
+    }
+    {
+        const int tasks = a.H / 256;  // 8 blocks of 32 per warp-task, 4 lanes per block
+        for (int task = warp; task < tasks; task += kTcThreads / 32) {
+            const int b = task * 8 + (lane >> 2), part = lane & 3, h = b * 32 + part * 8;
+            const uint4 raw = *reinterpret_cast<const uint4*>(a.x + h);
+            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
+            float v[8];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(wv[i] << 16);
+                v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            const int ex = mxfp8_exponent(amax);
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                lo |= f32x2_to_e4m3x2(scale_pow2(v[2 * i], ex), scale_pow2(v[2 * i + 1], ex)) << (16 * i);
+                hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
+            }
+            // row 0 of the 16-row tile of K step h / 128 (the 128-byte swizzle
+            // leaves row 0 in order)
+            *reinterpret_cast<uint2*>(smem + kDecResOff + (h / 128) * kDecBTile + (h % 128)) = make_uint2(lo, hi);
+            if (part == 0) smem[kDecSfbOff + (b / 4) * 16 + (b % 4)] = (uint8_t)(ex + 127);
+        }
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncthreads();
+    if (tr0) trc[9] = globaltimer();
+    const bool routed = *routed_flag != 0;
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    if (routed) {
+        slot_s[0] = slot_s[1] = -1;
+        decode_phase<true>(a, &tmGU, a.gu_sf, smem, bar0, tmem, seg_e, seg_j, seg_w, slot_s, stage, phase,
+                           acc_phase, abort_flag, last_flag, a.sk_cnt_gu);
+        if (tr0) trc[10] = globaltimer();
+        if (grid_barrier(a.gbar, gridDim.x, abort_flag)) {
+            if (tr0) trc[11] = globaltimer();
+            // the down phase's B tiles: h of (at most two) experts of this CTA's range
+            if (threadIdx.x == 0) {
+                SegIter it;
+                it.init(k * (a.H / 256), a.I / 128, (int)gridDim.x, (int)blockIdx.x);
+                Seg sg;
+                int n = 0;
+                slot_s[0] = slot_s[1] = -1;
+                while (it.next(sg)) {  // ranges are contiguous: expert indices ascend
+                    const int s = sg.tile / (a.H / 256);
+                    if (n > 0 && slot_s[n - 1] == s) continue;
+                    if (n == 2) {  // more than two experts in one CTA's range: not supported
+                        raise_flag(a.err, ERR_TIMEOUT);
+                        *abort_flag = 1;
+                        break;
+                    }
+                    slot_s[n++] = s;
+                }
+            }
+            __syncthreads();
+            for (int sl = 0; sl < 2; ++sl) {
+                const int s = slot_s[sl];
+                if (s < 0) continue;
+                for (int i = threadIdx.x; i < a.I / 16; i += kTcThreads) {  // 16 codes per thread
+                    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.hq + (size_t)s * a.I) + i);
+                    const int c = i * 16;
+                    *reinterpret_cast<uint4*>(smem + kDecResOff + sl * 32768 + (c / 128) * kDecBTile + (c % 128)) = v;
+                }
+                for (int b = threadIdx.x; b < a.I / 32; b += kTcThreads)
+                    smem[kDecSfbOff + sl * kDecSfbSlot + (b / 4) * 16 + (b % 4)] = a.hs[(size_t)s * (a.I / 32) + b];
+            }
+            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+            __syncthreads();
+            if (tr0) trc[2] = globaltimer();
+            decode_phase<false>(a, &tmDN, a.down_sf, smem, bar0, tmem, seg_e, seg_j, seg_w, slot_s, stage,
+                                phase, acc_phase, abort_flag, last_flag, a.sk_cnt_dn);
+        } else {
+            raise_flag(a.err, ERR_TIMEOUT);
+        }
+    } else {
+        // no valid routing (ERR_BAD_ID is raised): every row is dropped, as
+        // in the grouped path, and the output is zero
+        for (int i = blockIdx.x * kTcThreads + threadIdx.x; i < a.H; i += gridDim.x * kTcThreads)
+            a.out[i] = 0.f;
+    }
+    __syncthreads();
+    if (tr0) trc[1] = globaltimer();
+    if (*abort_flag) spin_ns(200000);
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
     }
 }
 
@@ -567,7 +986,8 @@ cudaError_t tc_init(moe_layer* L) {
         delete st;
         return cudaSuccess;  // no tensor-core path; the CUDA-core kernels run instead
     }
-    cudaError_t e = set_smem_attr<true, kFmtE2M1>();
+    cudaError_t e = cudaFuncSetAttribute(k_decode, cudaFuncAttributeMaxDynamicSharedMemorySize, kDecSmem);
+    if (e == cudaSuccess) e = set_smem_attr<true, kFmtE2M1>();
     if (e == cudaSuccess) e = set_smem_attr<false, kFmtE2M1>();
     if (e == cudaSuccess) e = set_smem_attr<true, kFmtE4M3>();
     if (e == cudaSuccess) e = set_smem_attr<false, kFmtE4M3>();
@@ -638,7 +1058,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid,
         d.cmb_k = c.top_k;
         d.cmb_cnt = L->sk_counters + 4 * L->num_sms;
     }
-    d.trace = L->trace ? L->trace + (size_t)L->num_sms * 8 : nullptr;
+    d.trace = L->trace ? L->trace + (size_t)L->num_sms * 12 : nullptr;
     e = tc_launch<false, kFmtE2M1>(L, st->down, st->hq, d, s);
     if (e != cudaSuccess || !c.has_shared) return e;
     TcArgs sg = g;
@@ -653,7 +1073,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid,
     sg.hs = L->hs_sh;
     sg.a_tx = kFp8BoxTx;
     sg.sk_cnt = L->sk_counters + 2 * L->num_sms;
-    sg.trace = L->trace ? L->trace + (size_t)2 * L->num_sms * 8 : nullptr;
+    sg.trace = L->trace ? L->trace + (size_t)2 * L->num_sms * 12 : nullptr;
     e = tc_launch<true, kFmtE4M3>(L, st->sh_gu, st->xq_tok, sg, s);
     if (e != cudaSuccess) return e;
     TcArgs sd = sg;
@@ -667,8 +1087,62 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid,
     sd.y = L->y_sh;
     sd.pos_row = nullptr;
     sd.sk_cnt = L->sk_counters + 3 * L->num_sms;
-    sd.trace = L->trace ? L->trace + (size_t)3 * L->num_sms * 8 : nullptr;
+    sd.trace = L->trace ? L->trace + (size_t)3 * L->num_sms * 12 : nullptr;
     return tc_launch<false, kFmtE4M3>(L, st->sh_down, st->hq_sh, sd, s);
+}
+
+}  // namespace moe
+
+namespace moe {
+
+bool decode_supported(const moe_layer* L) {
+    // x resident as H / 128 B tiles of 2 KB (64 KB), h of two experts as
+    // I / 128 tiles each (2 x 32 KB); a CTA range spans at most two experts
+    // when k * (H / 256) <= 2 * SMs (always so when split)
+    const moe_config& c = L->cfg;
+    return L->tc != nullptr && !c.has_shared && c.hidden % 256 == 0 && c.hidden <= 4096 &&
+           c.inter <= 2048 && c.top_k <= kMaxTopK && c.top_k * (c.hidden / 256) <= 2 * L->num_sms;
+}
+
+// One token: route + layer in the cooperative decode kernel.
+cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w,
+                          float* out, cudaStream_t s) {
+    const TcState* st = static_cast<const TcState*>(L->tc);
+    DecArgs a{};
+    a.logits = logits;
+    a.x = x;
+    a.E = L->cfg.n_experts;
+    a.k = L->cfg.top_k;
+    a.H = L->cfg.hidden;
+    a.I = L->cfg.inter;
+    a.w_scale = L->cfg.w_scale;
+    a.ids_out = ids;
+    a.w_out = w;
+    a.out = out;
+    a.gu_sf = L->gu_sf;
+    a.down_sf = L->down_sf;
+    a.hq = L->hq;
+    a.hs = L->hs;
+    a.y = L->y;
+    a.sk_part = L->sk_partials;
+    a.sk_cnt_gu = L->sk_counters;
+    a.sk_cnt_dn = L->sk_counters + L->num_sms;
+    a.cmb_cnt = L->sk_counters + 4 * L->num_sms;
+    a.gbar = reinterpret_cast<unsigned*>(L->sk_counters + 4 * L->num_sms + 32);
+    a.err = L->d_err;
+    a.trace = L->trace;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(L->num_sms);
+    cfg.blockDim = dim3(kTcThreads);
+    cfg.dynamicSmemBytes = kDecSmem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    L->launches += 1;
+    return cudaLaunchKernelEx(&cfg, k_decode, st->gu, st->down, a);
 }
 
 }  // namespace moe

@@ -74,7 +74,9 @@ constexpr int kFusedCombineMaxT = 32;  // and the combine fused into the down GE
 
 // split-tile counters: 4 GEMM launches x num_sms, then one per 256-feature
 // block of the fused combine (H / 256 <= 32)
-inline int kSkCounters(const moe_layer* L) { return 4 * L->num_sms + 32; }
+// block of the fused combine (H / 256 <= 32), then the decode kernel's grid
+// barrier words (arrival count, generation)
+inline int kSkCounters(const moe_layer* L) { return 4 * L->num_sms + 32 + 8; }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
 // stream; the kernels synchronise on it with pdl_wait().
@@ -123,6 +125,9 @@ cudaError_t cc_init();
 
 // Tensor-core path.
 cudaError_t tc_init(moe_layer* L);
+bool decode_supported(const moe_layer* L);
+cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w,
+                          float* out, cudaStream_t s);
 void tc_free(moe_layer* L);
 // cmb_ids != null: fuse the combine into the down GEMM (out = sum over the
 // token's experts in ascending order of w * y); requires no shared expert.

@@ -7,53 +7,9 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "route.cuh"
 
 namespace moe {
-
-// ------------------------------------------------------------------ route --
-// One warp per token.  The top-k by score s = sqrt(softplus(logit)) is the
-// top-k by logit (s is strictly increasing), so the selection compares the
-// fp32 logits exactly: k warp-wide argmax passes, equal values to the lower
-// expert index (guide, section 1: SQRT_SOFTPLUS gating, top-k).  Lane j < k
-// then evaluates s_j in fp32 and every lane sums s_0..s_{k-1} in that order;
-// w_j = w_scale * s_j / sum (guide, section 3.2).
-// Routing of one token by one warp: writes ids_t[0..k) and w_t[0..k).
-__device__ void route_token(const float* __restrict__ row, int E, int k, float w_scale,
-                            int32_t* __restrict__ ids_t, float* __restrict__ w_t, uint32_t* err,
-                            int lane) {
-    uint32_t taken = 0;  // bit i <-> expert lane + 32 i
-    int my_sel = -1;     // lane j keeps the j-th selection
-    float my_logit = 0.f;
-    bool ok = true;
-    for (int j = 0; j < k; ++j) {
-        float best = -INFINITY;
-        int bi = INT_MAX;
-        for (int i = 0, e = lane; e < E; ++i, e += 32) {
-            if ((taken >> i) & 1u) continue;
-            float v = __ldg(row + e);
-            if (v > best || (v == best && e < bi)) { best = v; bi = e; }
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) {
-            float ob = __shfl_xor_sync(0xFFFFFFFFu, best, o);
-            int oi = __shfl_xor_sync(0xFFFFFFFFu, bi, o);
-            if (ob > best || (ob == best && oi < bi)) { best = ob; bi = oi; }
-        }
-        if (bi >= E) { ok = false; bi = -1; }
-        if (lane == j) { my_sel = bi; my_logit = best; }
-        if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
-    }
-    float s = 0.f;
-    if (lane < k && my_sel >= 0)
-        s = sqrtf(fmaxf(my_logit, 0.f) + log1pf(expf(-fabsf(my_logit))));
-    float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, s, j);
-    if (lane < k) {
-        ids_t[lane] = ok ? my_sel : -1;
-        w_t[lane] = ok ? w_scale * s / sum : 0.0f;
-    }
-    if (!ok && lane == 0) raise_flag(err, ERR_BAD_ID);
-}
 
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
                                                int k, float w_scale, int32_t* __restrict__ ids,
@@ -362,10 +318,13 @@ __global__ void __launch_bounds__(1024) k_front(
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
     int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
     int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc,
-    uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
+    uint32_t* err, int32_t* __restrict__ zero, int n_zero, unsigned long long* trace) {
     extern __shared__ int dyn[];
+    unsigned long long t_in = 0;
+    if (trace && threadIdx.x == 0) t_in = tc_globaltimer();
     pdl_launch_dependents();
     pdl_wait();
+    if (trace && threadIdx.x == 0) { trace[0] = t_in; trace[1] = tc_globaltimer(); }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (logits) {
         if (warp < T)
@@ -378,6 +337,10 @@ __global__ void __launch_bounds__(1024) k_front(
     __syncthreads();
     const int tasks = T * ((H + 255) / 256);
     for (int task = warp; task < tasks; task += 32) quantize_task<1>(x, H, qd, task, lane);
+    if (trace) {
+        __syncthreads();
+        if (threadIdx.x == 0) trace[2] = tc_globaltimer();
+    }
 }
 
 static cudaError_t quantize_launch(int mode, const uint16_t* x, int T, int H, QuantDst d,
@@ -415,7 +378,8 @@ cudaError_t launch_front(moe_layer* L, const float* logits, int32_t* ids, float*
                       L->cfg.top_k, L->cfg.n_experts, L->cfg.hidden, d, L->offsets, L->row_src, L->row_dst,
                       L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
                       L->cfg.has_shared ? L->sh_desc : nullptr, L->d_err, L->sk_counters,
-                      L->sk_counters ? kSkCounters(L) : 0);
+                      L->sk_counters ? kSkCounters(L) : 0,
+                      L->trace ? L->trace + (size_t)4 * L->num_sms * 12 : nullptr);
 }
 
 cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cudaStream_t s) {

@@ -148,7 +148,10 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, int T, const int32_t
 /* Routing and layer in one call: moe_route followed by moe_forward, with
  * ids [T][k] and w [T][k] (device) written as moe_route writes them and out
  * [T][H] as moe_forward.  Small batches (T <= 32) run the routing, the
- * counting sort and the quantisation in one kernel.                        */
+ * counting sort and the quantisation in one kernel.  One token on the
+ * automatic path runs as one cooperative kernel of one CTA per SM (route,
+ * quantise, gate/up, down, combine; a bounded grid barrier between gate/up
+ * and down); moe_hidden does not report h after such a call.              */
 moe_status moe_route_forward(moe_layer* layer, const float* logits, const uint16_t* x, int T,
                              int32_t* ids, float* w, float* out, moe_stream_t stream);
 
@@ -185,13 +188,16 @@ const char* moe_last_error(const moe_layer* layer);
  * ordered, so it may be captured in a CUDA graph.                         */
 moe_status moe_set_stage_events(moe_layer* layer, void* const* events, int n);
 
-/* Kernel trace (diagnostics): when `buf` is non-NULL, the tensor-core GEMM
- * launches of the next moe_forward on `layer` write, per CTA, 8 counters
- * [start ns, end ns, producer ns waiting for free stages, MMA ns waiting for
+/* Kernel trace (diagnostics): when `buf` is non-NULL, the next moe_forward /
+ * moe_route_forward on `layer` records global-timer values and wait times in
+ * buf (device u64): tensor-core GEMM launch j (0 gate/up, 1 down, 2 and 3 the
+ * shared expert) writes 12 counters per CTA at buf + (j * num_sms + cta) * 12:
+ * [entry ns, exit ns, producer ns waiting for free stages, MMA ns waiting for
  * data, MMA ns waiting for the accumulator, epilogue ns waiting for the
- * accumulator, epilogue ns working, K-stages issued] to buf (device u64),
- * launch j of that forward at buf + j * num_sms * 8; `entries` must be at
- * least 4 * num_sms * 8.  One-shot, like moe_set_stage_events.             */
+ * accumulator, epilogue ns working, K-stages issued, ns when the wait for the
+ * previous kernel ended]; the one-CTA front kernel of small batches writes
+ * [entry, wait end, exit] at buf + 4 * num_sms * 12.  entries >= 4 * num_sms
+ * * 12 + 4.  One-shot, like moe_set_stage_events.                        */
 moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entries);
 
 /* Number of CUDA kernels this layer has enqueued since moe_create (a launch
@@ -200,8 +206,11 @@ moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entri
 unsigned long long moe_kernel_launches(const moe_layer* layer);
 
 /* Kernel path of the GEMM steps: 0 = automatic (tcgen05 when the device is
- * sm_103), 1 = CUDA-core kernels, 2 = tcgen05 block-scaled tensor-core kernels.  Both compute the same
- * layer; the choice only affects speed and the order of fp32 additions.    */
+ * sm_103, and moe_route_forward of one token as the single whole-layer
+ * decode kernel when the shape allows: H <= 4096, I <= 2048, no shared
+ * expert), 1 = CUDA-core kernels, 2 = tcgen05 block-scaled tensor-core
+ * kernels only (never the decode kernel).  All compute the same layer; the
+ * choice only affects speed and the order of fp32 additions.               */
 moe_status moe_set_gemm_path(moe_layer* layer, int path);
 
 /* Token -> expert grouping without a layer and without any allocation.

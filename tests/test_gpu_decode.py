@@ -1,0 +1,123 @@
+"""The whole-layer decode kernel (one token through moe_route_forward on the
+automatic path: route, quantise, gate/up, down and combine in one
+cooperative launch) against the fp64 oracle and against the grouped
+tensor-core kernels, eagerly and replayed from a CUDA graph."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_expert_gb300 as bqe
+from oracle import oracle as orc
+from tests import _gpu as G
+from workloads import CONFIGS
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    cfg = CONFIGS[1]
+    w = G.weights_np(1)
+    return cfg, w, G.make_layer(cfg, w, max_tokens=64)
+
+
+@pytest.fixture(scope="module")
+def tiny_layer():
+    cfg = CONFIGS[0]
+    w = G.weights_np(0)
+    return cfg, w, G.make_layer(cfg, w, max_tokens=64)
+
+
+def _route_forward(layer, logits_np, x_bits_np, path):
+    bqe.moe_set_gemm_path(layer, path)
+    H, k = layer.cfg.hidden, layer.cfg.top_k
+    ids = torch.empty((1, k), dtype=torch.int32, device=G.DEV)
+    w = torch.empty((1, k), dtype=torch.float32, device=G.DEV)
+    out = torch.full((1, H), 7.0, dtype=torch.float32, device=G.DEV)
+    n0 = bqe.moe_kernel_launches(layer)
+    bqe.moe_route_forward(layer, G.to_dev(logits_np.astype(np.float32)),
+                          G.to_dev(x_bits_np.astype(np.uint16), torch.int16), ids, w, out)
+    bqe.moe_check(layer)
+    return ids, w, out, bqe.moe_kernel_launches(layer) - n0
+
+
+def _check_token(cfg, wts, layer, tk, t):
+    lg, xb = tk.logits[t:t + 1], tk.x_bits[t:t + 1]
+    ids, w, out, n = _route_forward(layer, lg, xb, 0)
+    assert n == 1  # one kernel for the whole layer
+    rid, rw = orc.route_learned(lg, cfg.k, cfg.w_scale)
+    assert np.array_equal(ids.cpu().numpy(), rid)
+    assert np.abs(w.cpu().numpy() - rw).max() <= 8 * 2.0 ** -24 * cfg.w_scale
+    ref = orc.layer_forward(wts, xb, rid, w.cpu().numpy().astype(np.float64))
+    norm, elem = G.compare_out(out.cpu().numpy(), ref)
+    assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (norm, elem)
+    # the grouped tcgen05 kernels split the same tiles over the same CTAs and
+    # add the same partial sums in the same order: identical bytes
+    ids2, w2, out2, n2 = _route_forward(layer, lg, xb, 2)
+    assert n2 > 1
+    assert torch.equal(ids, ids2) and torch.equal(w, w2)
+    assert out.cpu().numpy().tobytes() == out2.cpu().numpy().tobytes()
+
+
+def test_decode_kernel_decode_shape(decode_layer):
+    cfg, wts, layer = decode_layer
+    tk = G.tokens(1, n=10)
+    for t in range(10):
+        _check_token(cfg, wts, layer, tk, t)
+
+
+def test_decode_kernel_tiny_shape(tiny_layer):
+    """H = 256, I = 128: two gate/up tiles of two K-steps, no stream-K split,
+    most CTAs idle until the grid barrier."""
+    cfg, wts, layer = tiny_layer
+    tk = G.tokens(0, n=6)
+    for t in range(6):
+        _check_token(cfg, wts, layer, tk, t)
+
+
+def test_decode_kernel_graph_replay(decode_layer):
+    cfg, wts, layer = decode_layer
+    bqe.moe_set_gemm_path(layer, 0)
+    tk = G.tokens(1, n=4)
+    lg = torch.zeros((1, cfg.E), dtype=torch.float32, device=G.DEV)
+    xb = torch.zeros((1, cfg.H), dtype=torch.int16, device=G.DEV)
+    ids = torch.empty((1, cfg.k), dtype=torch.int32, device=G.DEV)
+    w = torch.empty((1, cfg.k), dtype=torch.float32, device=G.DEV)
+    out = torch.empty((1, cfg.H), dtype=torch.float32, device=G.DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        bqe.moe_route_forward(layer, lg, xb, ids, w, out)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            bqe.moe_route_forward(layer, lg, xb, ids, w, out)
+    for t in range(4):
+        lg.copy_(G.to_dev(tk.logits[t:t + 1].astype(np.float32)))
+        xb.copy_(G.to_dev(tk.x_bits[t:t + 1].astype(np.uint16), torch.int16))
+        g.replay()
+        torch.cuda.synchronize()
+        bqe.moe_check(layer)
+        ids_e, w_e, out_e, _ = _route_forward(layer, tk.logits[t:t + 1], tk.x_bits[t:t + 1], 0)
+        assert torch.equal(ids, ids_e) and torch.equal(w, w_e)
+        assert out.cpu().numpy().tobytes() == out_e.cpu().numpy().tobytes()
+
+
+def test_decode_kernel_unroutable_token(tiny_layer):
+    """All logits NaN: no expert can be selected; the ids are -1, the output
+    is zero (every row dropped) and moe_check reports the bad routing."""
+    cfg, wts, layer = tiny_layer
+    bqe.moe_set_gemm_path(layer, 0)
+    lg = torch.full((1, cfg.E), float("nan"), dtype=torch.float32, device=G.DEV)
+    xb = G.to_dev(G.tokens(0, n=1).x_bits.astype(np.uint16), torch.int16)
+    ids = torch.empty((1, cfg.k), dtype=torch.int32, device=G.DEV)
+    w = torch.empty((1, cfg.k), dtype=torch.float32, device=G.DEV)
+    out = torch.full((1, cfg.H), 7.0, dtype=torch.float32, device=G.DEV)
+    bqe.moe_route_forward(layer, lg, xb, ids, w, out)
+    with pytest.raises(bqe.MoeError) as ei:
+        bqe.moe_check(layer)
+    assert ei.value.status == bqe.MOE_ERR_INVALID_ARG
+    assert (ids.cpu().numpy() == -1).all()
+    assert (out.cpu().numpy() == 0).all()
+    # the layer stays usable
+    tk = G.tokens(0, n=1)
+    _check_token(cfg, wts, layer, tk, 0)
