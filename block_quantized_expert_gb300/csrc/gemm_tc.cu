@@ -248,6 +248,8 @@ __device__ __forceinline__ void tile_done_combine(const TcArgs& a, int f0, bool 
     if (!*flag) return;
     __threadfence();
     combine_block(a, f0, (warp - 2) * 32 + lane);
+    epi_bar();
+    if (leader) a.cmb_cnt[f0 / 256] = 0;  // counters are left at zero
 }
 
 // mbar_wait that adds the waited wall time to *acc when tracing.
@@ -258,6 +260,16 @@ __device__ __forceinline__ bool timed_wait(uint32_t bar, uint32_t parity, volati
     const bool ok = mbar_wait(bar, parity, kWaitLimitNs, abort);
     acc += globaltimer() - t0;
     return ok;
+}
+
+// The producer and MMA roles run as whole warps (so every warp reaches the
+// CTA-wide barriers converged): lane 0 waits and issues, the warp learns the
+// outcome of each wait from it.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, bool tr,
+                                          unsigned long long& acc, int lane) {
+    int ok = 1;
+    if (lane == 0) ok = timed_wait(bar, parity, abort, tr, acc) ? 1 : 0;
+    return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
 template <bool kGateUp, uint32_t kAFmt>
@@ -278,7 +290,6 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * Cfg::kStages + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
     volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    volatile int* routed_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int KB = a.K / 128;
@@ -301,6 +312,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         prefetch_tmap(&tmB128);
     }
     if (warp == 1) tmem_alloc(smem_u32(tmem_slot), Cfg::kTmemCols);
+    __syncwarp();  // warps reach CTA barriers converged (lane 0 may have run a role)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -321,24 +333,24 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 
     if (warp == 0) {
         // ------------------------------------------------ TMA producer --
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0;
-            bool ok = true;
-            unsigned long long w_empty = 0;
-            while (ok && it.next(sg)) {
-                const Tile T = decode_tile<kGateUp>(a, sg.tile);
-                // one copy for the token rows: a 32-, 64- or 128-row box
-                const CUtensorMap* tmB = T.nt == 32 ? &tmB32 : (T.nt == 64 ? &tmB64 : &tmB128);
-                const uint32_t b_rows = T.nt == 32 ? 32u : (T.nt == 64 ? 64u : 128u);
-                const uint32_t tx = a.a_tx + b_rows * 128u + 1024u + 512u;
-                const size_t atom_a = (size_t)(T.arow / 256) * KB;
-                const size_t atom_b = (size_t)(T.p0 / 128) * KB;
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!timed_wait(empty_bar(stage), phase ^ 1u, abort_flag, tr, w_empty)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
+        uint32_t stage = 0, phase = 0;
+        bool ok = true;
+        unsigned long long w_empty = 0;
+        while (ok && it.next(sg)) {
+            const Tile T = decode_tile<kGateUp>(a, sg.tile);
+            // one copy for the token rows: a 32-, 64- or 128-row box
+            const CUtensorMap* tmB = T.nt == 32 ? &tmB32 : (T.nt == 64 ? &tmB64 : &tmB128);
+            const uint32_t b_rows = T.nt == 32 ? 32u : (T.nt == 64 ? 64u : 128u);
+            const uint32_t tx = a.a_tx + b_rows * 128u + 1024u + 512u;
+            const size_t atom_a = (size_t)(T.arow / 256) * KB;
+            const size_t atom_b = (size_t)(T.p0 / 128) * KB;
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag, tr, w_empty, lane)) {
+                    if (lane == 0) give_up();
+                    ok = false;
+                    break;
+                }
+                if (lane == 0) {
                     uint8_t* st = smem + stage * Cfg::kStageBytes;
                     const uint32_t fb = full_bar(stage);
                     mbar_arrive_expect_tx(fb, tx);
@@ -346,31 +358,30 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                     tma_load_2d(smem_u32(st + Cfg::kABytes), tmB, kb * 128, T.p0, fb);
                     bulk_load(smem_u32(st + Cfg::kSfOff), a.sfa + (atom_a + kb) * 1024, 1024, fb);
                     bulk_load(smem_u32(st + Cfg::kSfOff + 1024), a.sfb + (atom_b + kb) * 512, 512, fb);
-                    if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
                 }
+                if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
             }
-            if (tr) trc[2] = w_empty;
         }
+        if (tr && lane == 0) trc[2] = w_empty;
     } else if (warp == 1) {
         // ------------------------------------------------- MMA issuer --
-        if (lane == 0) {
-            uint32_t stage = 0, phase = 0, acc_phase = 0;
-            bool ok = true;
-            unsigned long long w_full = 0, w_acc = 0, n_stages = 0;
-            while (ok && it.next(sg)) {
-                const Tile T = decode_tile<kGateUp>(a, sg.tile);
-                if (!timed_wait(tmem_empty, acc_phase ^ 1u, abort_flag, tr, w_acc)) {
-                    give_up();
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        bool ok = true;
+        unsigned long long w_full = 0, w_acc = 0, n_stages = 0;
+        while (ok && it.next(sg)) {
+            const Tile T = decode_tile<kGateUp>(a, sg.tile);
+            if (!warp_wait(tmem_empty, acc_phase ^ 1u, abort_flag, tr, w_acc, lane)) {
+                if (lane == 0) give_up();
+                break;
+            }
+            for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+                if (!warp_wait(full_bar(stage), phase, abort_flag, tr, w_full, lane)) {
+                    if (lane == 0) give_up();
+                    ok = false;
                     break;
                 }
-                tc_fence_after();
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!timed_wait(full_bar(stage), phase, abort_flag, tr, w_full)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
-                    ++n_stages;
+                ++n_stages;
+                if (lane == 0) {
                     tc_fence_after();
                     const uint32_t st = smem_u32(smem + stage * Cfg::kStageBytes);
                     const uint32_t bt = st + Cfg::kABytes;
@@ -389,14 +400,16 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                                sf_col + 8, acc);
                     }
                     mma_commit(empty_bar(stage));
-                    if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
                 }
-                if (!ok) break;
-                mma_commit(tmem_full);
-                acc_phase ^= 1u;
+                __syncwarp();
+                if (++stage == Cfg::kStages) { stage = 0; phase ^= 1u; }
             }
-            if (tr) { trc[3] = w_full; trc[4] = w_acc; trc[7] = n_stages; }
+            if (!ok) break;
+            if (lane == 0) mma_commit(tmem_full);
+            __syncwarp();
+            acc_phase ^= 1u;
         }
+        if (tr && lane == 0) { trc[3] = w_full; trc[4] = w_acc; trc[7] = n_stages; }
     } else {
         // ---------------------------------------------------- epilogue --
         // Warp w (2..9) reads TMEM lanes of quarter w % 4 and token columns
@@ -483,6 +496,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (tr && leader) { trc[5] = w_tf; trc[6] = t_work; }
     }
 
+    __syncwarp();  // the producer / MMA lane rejoins its warp before the CTA barrier
     __syncthreads();
     if (tr && threadIdx.x == 0) trc[1] = globaltimer();
     if (*abort_flag) spin_ns(200000);  // copies / MMAs still in flight land first
@@ -496,23 +510,56 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 // The whole layer for one token (T = 1, learned router, no shared expert) in
 // one cooperative kernel of one CTA per SM -- route, quantise, gate/up,
 // down, combine -- so nothing of the token goes through a kernel boundary.
-// Every CTA routes the token itself (the same warp-argmax as k_route, hence
-// the same experts and weights everywhere) and quantises x straight into
-// resident shared-memory B tiles of N = 16 rows (row 0 is the token, rows
-// 1-15 stay zero); the weights stream through the same TMA / tcgen05 pipeline
-// as k_gemm_tc, split stream-K over all SMs.  A grid barrier separates the
-// gate/up phase from the down phase; h crosses it through global memory.
+// Every CTA routes the token itself (ranks of the fp32 logits, the selection
+// k_route makes, hence the same experts and weights everywhere) and
+// quantises x straight into a resident shared-memory B row.  The weights
+// stream through the TMA / tcgen05 pipeline of k_gemm_tc, split stream-K
+// over all SMs; the producer runs on from the gate/up weights into the down
+// weights (they do not depend on h).
+//
+// Cross-CTA hand-offs go through flags that hold the launch's epoch (a
+// 64-bit launch counter that only grows), so nothing is ever reset: a tile
+// cut between CTAs is finished by the CTA holding its first K-steps (it
+// reaches that piece last), which waits for the other pieces' flags and adds
+// the pieces in K order; a gate/up tile's owner publishes h and an h flag;
+// a CTA starts its down phase once the h flags of its experts are set; the
+// owner of the last expert's tile of each 256-feature block waits for the
+// other experts' y flags and writes the combined output.
 
-constexpr int kDecN = 16;                 // MMA N: the single token and 15 zero rows
-constexpr int kDecBTile = kDecN * 128;    // 2 KB of B per 128-wide K step
+// Orientation: with a single token the MMA cost is per instruction, not
+// per column, so the weights are the B operand (N = 256: one MMA per K=32
+// step covers a whole 256-row tile) and the token is the A operand (M =
+// 128).  The token's codes are one contiguous row read through a no-swizzle
+// K-major descriptor whose 16-byte K chunks are 16 bytes apart and whose
+// 8-row groups all alias (stride 0): A rows 0, 8, ..., 120 are the token and
+// the others are shifted copies, so TMEM lanes 0, 32, 64 and 96 each hold the
+// token's outputs (one per lane quarter) and the other lanes are not read.
+// D[lane][n] is weight row n of the tile: gate/up columns 0-127 are gate
+// features, 128-255 the matching up features; down columns are 256 outputs.
 constexpr int kDecStageBytes = 32768 + 1024;  // 256 weight rows + their scale atoms
-constexpr int kDecStages = 4;
-constexpr int kDecResOff = kDecStages * kDecStageBytes;  // resident B tiles (64 KB)
-constexpr int kDecSfbSlot = 64 * 16 + 512;               // scale bytes of 64 K steps + one copy's reach
-constexpr int kDecSfbOff = kDecResOff + 65536;           // resident B scales (2 slots)
-constexpr int kDecBarOff = kDecSfbOff + 2 * kDecSfbSlot;
-constexpr int kDecSmem = kDecBarOff + 512 + 1024;
+constexpr int kDecStages = 6;
+constexpr int kDecResOff = kDecStages * kDecStageBytes;  // A rows: x (H <= 4096) or h of two experts
+constexpr int kDecSlotBytes = 2048 + 256;                // one h row (I <= 2048) + what the aliased rows reach
+constexpr int kDecResBytes = 2 * kDecSlotBytes;          // also covers x: 4096 + 512
+// Token scales: the source rows of the A scale copies, one 16-byte row per K
+// step holding the step's four block scales once per lane quarter (the token
+// rows 0, 32, 64, 96); a copy reads 512 bytes from its row.
+constexpr int kDecTokScaleSlot = 64 * 16 + 512;
+constexpr int kDecTokScaleOff = kDecResOff + kDecResBytes;  // token scale rows (2 slots)
+constexpr int kDecBarOff = kDecTokScaleOff + 2 * kDecTokScaleSlot;
+constexpr int kDecUpOff = kDecBarOff + 512;              // gate/up epilogue: the 128 up values of a tile
+constexpr int kDecSmem = kDecUpOff + 512 + 1024;
+// tensor memory: D in columns 0-255; weight scales, 8 per stage; the
+// token's scales of the down phase, 4 per stage; those of the gate/up
+// phase, 4 per K step for every step (copied at the phase start, while the
+// first weights are still in flight)
+constexpr uint32_t kDecSfbCol = 256;
+constexpr uint32_t kDecSfaStageCol = kDecSfbCol + 8 * kDecStages;
+constexpr uint32_t kDecSfaResCol = kDecSfaStageCol + 4 * kDecStages;
+static_assert(kDecSfaResCol + 4 * 32 <= 512, "tensor memory budget");
+constexpr int kDecMaxTiles = 128;             // k * (I / 128) and k * (H / 256) for k <= 8, H <= 4096, I <= 2048
 static_assert(kDecSmem <= 232448, "shared memory budget");
+static_assert(kDecStageBytes % 1024 == 0, "128-byte swizzled A tiles need 1024-byte alignment");
 
 struct DecArgs {
     const float* logits;  // [E]
@@ -527,218 +574,269 @@ struct DecArgs {
     uint8_t* hq;          // [k][I] e4m3 (scratch)
     uint8_t* hs;          // [k][I/32] UE8M0 (scratch)
     float* y;             // [k][H] down outputs (scratch)
-    float* sk_part;       // [G][2][2][128][128]
-    int32_t* sk_cnt_gu;   // [G]
-    int32_t* sk_cnt_dn;   // [G]
-    int32_t* cmb_cnt;     // [H/256]
-    unsigned* gbar;       // [2]: arrival count, generation
+    float* sk_part;       // [G][2][2][128][128] partial accumulators of cut tiles
+    unsigned long long* launches;  // launch counter (epoch = value / gridDim.x)
+    uint32_t* piece_flag;  // [2 phases][G][2]: a cut tile's piece parked by CTA c in slot s
+    uint32_t* h_flag;      // [kDecMaxTiles]: h of gate/up tile t written
+    uint32_t* y_flag;      // [kDecMaxTiles]: y of down tile t written
     uint32_t* err;
     unsigned long long* trace;  // [gridDim][12] ns timestamps, or null
 };
 
-// Bounded grid-wide barrier (all CTAs are co-resident: cooperative launch).
-__device__ bool grid_barrier(unsigned* gbar, unsigned G, volatile int* abort) {
-    __syncthreads();
-    __shared__ int ok_s;
-    if (threadIdx.x == 0) {
-        volatile unsigned* gen = gbar + 1;
-        const unsigned g0 = *gen;
-        __threadfence();
-        bool ok = true;
-        if (atomicAdd(gbar, 1u) == G - 1) {
-            atomicExch(gbar, 0u);
-            __threadfence();
-            atomicAdd(gbar + 1, 1u);
-        } else {
-            const uint64_t t0 = globaltimer();
-            while (*gen == g0) {
-                if (globaltimer() - t0 > kWaitLimitNs || *abort) { ok = false; break; }
-            }
-        }
-        __threadfence();
-        ok_s = ok;
-    }
-    __syncthreads();
-    return ok_s != 0;
-}
-
-// The stream-K gate/up or down phase of the decode kernel (one token).
-template <bool kGateUp>
-__device__ void decode_phase(const DecArgs& a, const CUtensorMap* tmA, const uint8_t* sfa, uint8_t* smem,
-                             uint32_t bar0, uint32_t tmem, const int* seg_e, const int* seg_j,
-                             const float* seg_w, const int* slot_s, uint32_t& stage, uint32_t& phase,
-                             uint32_t& acc_phase, volatile int* abort_flag, volatile int* last_flag,
-                             int32_t* sk_cnt) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int MT = kGateUp ? a.I / 128 : a.H / 256;
-    const int K = kGateUp ? a.H : a.I;
-    const int KB = K / 128;
-    const int seg_rows = kGateUp ? 2 * a.I : a.H;
-    const int tiles = a.k * MT;
-    auto full_bar = [&](int st) { return bar0 + 8u * st; };
-    auto empty_bar = [&](int st) { return bar0 + 8u * (kDecStages + st); };
-    const uint32_t tmem_full = bar0 + 8u * (2 * kDecStages);
-    const uint32_t tmem_empty = tmem_full + 8u;
-    const uint32_t res_base = smem_u32(smem + kDecResOff);
-    const uint32_t sfb_base = smem_u32(smem + kDecSfbOff);
-    auto give_up = [&]() {
+// Shared state of one decode CTA.
+struct DecCtx {
+    uint8_t* smem;
+    uint32_t bar0, tmem;
+    uint32_t epoch;      // this launch's flag value
+    volatile int* abort_flag;
+    const int* seg_e;    // [k] experts, ascending
+    const int* seg_j;    // [k] their position in the router output
+    const float* seg_w;  // [k] their weights
+    const int* slot_s;   // [2] down phase: the experts whose h sits in B slots 0 / 1
+    __device__ uint32_t full_bar(int st) const { return bar0 + 8u * st; }
+    __device__ uint32_t empty_bar(int st) const { return bar0 + 8u * (kDecStages + st); }
+    __device__ uint32_t tmem_full() const { return bar0 + 8u * (2 * kDecStages); }
+    __device__ uint32_t tmem_empty() const { return bar0 + 8u * (2 * kDecStages) + 8u; }
+    __device__ uint32_t h_bar() const { return bar0 + 8u * (2 * kDecStages) + 16u; }  // down-phase A rows landed
+    __device__ void give_up(const DecArgs& a) const {
         *abort_flag = 1;
         raise_flag(a.err, ERR_TIMEOUT);
-    };
-    auto slot_of = [&](int s) { return kGateUp ? 0 : (slot_s[1] == s ? 1 : 0); };
+    }
+};
+
+template <bool kGateUp>
+__device__ __forceinline__ void dec_shape(const DecArgs& a, int& MT, int& KB, int& seg_rows) {
+    MT = kGateUp ? a.I / 128 : a.H / 256;
+    KB = (kGateUp ? a.H : a.I) / 128;
+    seg_rows = kGateUp ? 2 * a.I : a.H;
+}
+
+// Warps 1-9 (all but the TMA producer).
+__device__ __forceinline__ void work_bar() { asm volatile("bar.sync 2, 288;" ::: "memory"); }
+
+// Publish / await a flag value.  A CTA publishes with a named barrier over
+// its writers followed by one gpu-scope release store (cumulative over the
+// writes the barrier ordered before it); a waiter's acquire load followed by
+// a named barrier makes them visible to its whole CTA.  The wait gives up
+// after kWaitLimitNs or when the CTA aborts.
+__device__ __forceinline__ void flag_set(uint32_t* f, uint32_t v) {
+    asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t flag_get(const uint32_t* f) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
+    return v;
+}
+__device__ bool flag_wait(const uint32_t* f, uint32_t v, volatile int* abort) {
+    if (flag_get(f) == v) return true;
+    const uint64_t t0 = globaltimer();
+    while (flag_get(f) != v) {
+        if (globaltimer() - t0 > kWaitLimitNs || *abort) return false;
+        __nanosleep(32);
+    }
+    return true;
+}
+
+// TMA producer (warp 0; lane 0 waits and issues): the weight tiles and
+// scale atoms of this CTA's stream-K range, into the stage ring.
+template <bool kGateUp>
+__device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap* tmA, uint32_t& stage,
+                            uint32_t& phase, int lane) {
+    int MT, KB, seg_rows;
+    dec_shape<kGateUp>(a, MT, KB, seg_rows);
+    const uint8_t* sfa = kGateUp ? a.gu_sf : a.down_sf;
     SegIter it;
-    it.init(tiles, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(a.k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
     Seg sg;
-    if (warp == 0) {
-        if (lane == 0) {
-            bool ok = true;
-            while (ok && it.next(sg)) {
-                const int s = sg.tile / MT, m = sg.tile % MT;
-                const int arow = seg_e[s] * seg_rows + m * 256;
-                const size_t atom_a = (size_t)(arow / 256) * KB;
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!mbar_wait(empty_bar(stage), phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
-                    uint8_t* st = smem + stage * kDecStageBytes;
-                    const uint32_t fb = full_bar(stage);
-                    mbar_arrive_expect_tx(fb, kFp4BoxTx + 1024u);
-                    tma_load_2d(smem_u32(st), tmA, kb * 128, arow, fb);
-                    bulk_load(smem_u32(st + 32768), sfa + (atom_a + kb) * 1024, 1024, fb);
-                    if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
-                }
+    while (it.next(sg)) {
+        const int s = sg.tile / MT, m = sg.tile % MT;
+        const int arow = c.seg_e[s] * seg_rows + m * 256;
+        const size_t atom_a = (size_t)(arow / 256) * KB;
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+            unsigned long long none = 0;
+            if (!warp_wait(c.empty_bar(stage), phase ^ 1u, c.abort_flag, false, none, lane)) {
+                if (lane == 0) c.give_up(a);
+                return false;
             }
-        }
-    } else if (warp == 1) {
-        if (lane == 0) {
-            bool ok = true;
-            while (ok && it.next(sg)) {
-                const int s = sg.tile / MT;
-                const int sl = slot_of(s);
-                if (!mbar_wait(tmem_empty, acc_phase ^ 1u, kWaitLimitNs, abort_flag)) {
-                    give_up();
-                    break;
-                }
-                tc_fence_after();
-                for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                    if (!mbar_wait(full_bar(stage), phase, kWaitLimitNs, abort_flag)) {
-                        give_up();
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t st = smem_u32(smem + stage * kDecStageBytes);
-                    const uint32_t sf_col = tmem + 256 + stage * 12;
-                    const uint32_t bt = res_base + sl * 32768 + kb * kDecBTile;
-                    tmem_cp_32x128_x4(sf_col, desc_sf(st + 32768));
-                    tmem_cp_32x128_x4(sf_col + 4, desc_sf(st + 32768 + 512));
-                    tmem_cp_32x128_x4(sf_col + 8, desc_sf(sfb_base + sl * kDecSfbSlot + kb * 16));
-#pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t id = idesc_mx(kFmtE2M1, kFmtE4M3, 128, kDecN, kk, kk);
-                        const uint64_t bd = desc_sw128(bt + 32 * kk);
-                        const uint32_t acc = (kb > sg.kb0 || kk) ? 1u : 0u;
-                        mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sf_col + 8, acc);
-                        mma_mx(tmem + 128, desc_sw128(st + 16384 + 32 * kk), bd, id, sf_col + 4, sf_col + 8, acc);
-                    }
-                    mma_commit(empty_bar(stage));
-                    if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
-                }
-                if (!ok) break;
-                mma_commit(tmem_full);
-                acc_phase ^= 1u;
+            if (lane == 0) {
+                uint8_t* st = c.smem + stage * kDecStageBytes;
+                const uint32_t fb = c.full_bar(stage);
+                mbar_arrive_expect_tx(fb, kFp4BoxTx + 1024u);
+                tma_load_2d(smem_u32(st), tmA, kb * 128, arow, fb);
+                bulk_load(smem_u32(st + 32768), sfa + (atom_a + kb) * 1024, 1024, fb);
             }
+            if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
         }
-    } else {
-        // epilogue: only token column 0 is real; warps of the second column
-        // half take part in the barriers only
-        const int q = warp & 3;
-        const int hf = (warp - 2) >> 2;
-        const int fm = 32 * q + lane;
-        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
-        const bool leader = warp == 2 && lane == 0;
-        while (it.next(sg)) {
-            const int s = sg.tile / MT, m = sg.tile % MT;
-            const int f0 = m * (kGateUp ? 128 : 256);
-            // on a timeout the epilogue goes on with whatever the accumulator
-            // holds (the error is raised), so all eight warps keep meeting at
-            // the same named barriers
-            if (!mbar_wait(tmem_full, acc_phase, kWaitLimitNs, abort_flag) && lane == 0) give_up();
+    }
+    return true;
+}
+
+// MMA issuer (warp 1; lane 0 waits and issues): per K=32 step one M = 128,
+// N = 256 MMA of the resident token row against the streamed weight tile.
+template <bool kGateUp>
+__device__ bool dec_mma(const DecArgs& a, const DecCtx& c, uint32_t& stage, uint32_t& phase,
+                        uint32_t& acc_phase, unsigned long long* wait_ns, int lane) {
+    int MT, KB, seg_rows;
+    dec_shape<kGateUp>(a, MT, KB, seg_rows);
+    const uint32_t res_base = smem_u32(c.smem + kDecResOff);
+    const uint32_t tok_base = smem_u32(c.smem + kDecTokScaleOff);
+    unsigned long long none = 0;
+    if (kGateUp) {
+        if (lane == 0) {
             tc_fence_after();
-            acc_phase ^= 1u;
-            float v0 = 0.f, v1 = 0.f;
-            if (hf == 0) {
-                uint32_t r0[16], r1[16];
-                tmem_ld16(tq, r0);
-                tmem_ld16(tq + 128, r1);
-                tmem_ld_wait();
-                v0 = __uint_as_float(r0[0]);
-                v1 = __uint_as_float(r1[0]);
+            for (int kb = 0; kb < KB; ++kb)
+                tmem_cp_32x128_x4(c.tmem + kDecSfaResCol + kb * 4, desc_sf(tok_base + kb * 16));
+        }
+        __syncwarp();
+    } else if (!warp_wait(c.h_bar(), 0, c.abort_flag, false, none, lane)) {  // h rows and scales
+        if (lane == 0) c.give_up(a);
+        return false;
+    }
+    SegIter it;
+    it.init(a.k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    Seg sg;
+    while (it.next(sg)) {
+        const int s = sg.tile / MT;
+        const int sl = (!kGateUp && c.slot_s[1] == s) ? 1 : 0;
+        if (!warp_wait(c.tmem_empty(), acc_phase ^ 1u, c.abort_flag, false, none, lane)) {
+            if (lane == 0) c.give_up(a);
+            return false;
+        }
+        for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+            if (!warp_wait(c.full_bar(stage), phase, c.abort_flag, wait_ns != nullptr,
+                           wait_ns ? *wait_ns : none, lane)) {
+                if (lane == 0) c.give_up(a);
+                return false;
             }
-            tc_fence_before();
+            if (lane == 0) {
+                tc_fence_after();
+                const uint32_t st = smem_u32(c.smem + stage * kDecStageBytes);
+                const uint32_t sfb_col = c.tmem + kDecSfbCol + stage * 8;  // weight rows 0-127, 128-255
+                const uint32_t at = res_base + sl * kDecSlotBytes + kb * 128;
+                uint32_t sfa_col = c.tmem + kDecSfaResCol + kb * 4;
+                if (!kGateUp) {
+                    sfa_col = c.tmem + kDecSfaStageCol + stage * 4;
+                    tmem_cp_32x128_x4(sfa_col, desc_sf(tok_base + sl * kDecTokScaleSlot + kb * 16));
+                }
+                tmem_cp_32x128_x4(sfb_col, desc_sf(st + 32768));
+                tmem_cp_32x128_x4(sfb_col + 4, desc_sf(st + 32768 + 512));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint32_t id = idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk);
+                    const uint32_t acc = (kb > sg.kb0 || kk) ? 1u : 0u;
+                    mma_mx(c.tmem, smem_desc(at + 32 * kk, 16, 0, 0), desc_sw128(st + 32 * kk), id, sfa_col,
+                           sfb_col, acc);
+                }
+                mma_commit(c.empty_bar(stage));
+            }
             __syncwarp();
-            if (lane == 0) mbar_arrive(tmem_empty);
-            bool emit = true;
-            if (sg.first_cta != sg.last_cta) {
-                float* part = a.sk_part + ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128;
-                if (hf == 0) {
-                    part[fm] = v0;
-                    part[(size_t)128 * 128 + fm] = v1;
-                }
-                __threadfence();
-                epi_bar();
-                if (leader) {
-                    const int nparts = sg.last_cta - sg.first_cta + 1;
-                    *last_flag = (atomicAdd(sk_cnt + sg.first_cta, 1) == nparts - 1);
-                }
-                epi_bar();
-                emit = *last_flag != 0;
-                if (emit) {
-                    __threadfence();
-                    v0 = 0.f;
-                    v1 = 0.f;
-                    for (int cc = sg.first_cta; cc <= sg.last_cta; ++cc) {
-                        const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128;
-                        v0 += __ldcg(pp + fm);
-                        v1 += __ldcg(pp + (size_t)128 * 128 + fm);
-                    }
-                }
-                epi_bar();
-                if (emit && leader) sk_cnt[sg.first_cta] = 0;
+            if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
+        }
+        if (lane == 0) mma_commit(c.tmem_full());
+        __syncwarp();
+        acc_phase ^= 1u;
+    }
+    return true;
+}
+
+// Epilogue (warps 2-9): warp w takes D columns 32 (w - 2) .. + 31 from the
+// token lane of its lane quarter (lane 0 of the warp reads them, the warp
+// shares them out: thread t gets column 32 (w - 2) + t).  Gate/up: warps 6-9
+// hand their up values to warps 2-5 through shared memory, which form h =
+// SiLU(g) * u and requantise it to MXFP8 (32 features = one warp).  Down: y,
+// or for the last expert's tile of a feature block the combined output.
+template <bool kGateUp>
+__device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_phase) {
+    int MT, KB, seg_rows;
+    dec_shape<kGateUp>(a, MT, KB, seg_rows);
+    uint32_t* pflag = a.piece_flag + (kGateUp ? 0 : 2 * gridDim.x);
+    const int pcol = kGateUp ? 0 : 256;  // the two phases park pieces in different columns
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;
+    const int col = 32 * (warp - 2) + lane;  // this thread's D column (0-255)
+    const uint32_t taddr = c.tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(32 * (warp - 2));
+    float* up_s = reinterpret_cast<float*>(c.smem + kDecUpOff);
+    const bool lead_warp = warp == 2;
+    SegIter it;
+    it.init(a.k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    Seg sg;
+    while (it.next(sg)) {
+        const int s = sg.tile / MT, m = sg.tile % MT;
+        const int f0 = m * (kGateUp ? 128 : 256);
+        // on a timeout the epilogue goes on with whatever the accumulator
+        // holds (the error is raised), so all eight warps keep meeting at
+        // the same named barriers
+        if (!mbar_wait(c.tmem_full(), acc_phase, kWaitLimitNs, c.abort_flag) && lane == 0) c.give_up(a);
+        tc_fence_after();
+        acc_phase ^= 1u;
+        uint32_t r[32];
+        tmem_ld32(taddr, r);
+        tmem_ld_wait();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(c.tmem_empty());
+        float v = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+            const float x = __shfl_sync(0xFFFFFFFFu, __uint_as_float(r[i]), 0);
+            if (lane == i) v = x;
+        }
+        if (sg.first_cta != sg.last_cta) {
+            const int slot = it.slot(blockIdx.x, sg.tile);
+            if ((int)blockIdx.x != sg.first_cta) {
+                // a later piece: park it and go on
+                a.sk_part[((size_t)blockIdx.x * 2 + slot) * 2 * 128 * 128 + pcol + col] = v;
+                epi_bar();  // the release store below publishes the whole CTA's writes
+                if (lead_warp && lane == 0) flag_set(pflag + blockIdx.x * 2 + slot, c.epoch);
+                continue;
             }
-            if (!emit) continue;
-            if (kGateUp) {
-                if (hf == 0) {
-                    const float h = silu_mul(v0, v1);
-                    const int ex = mxfp8_exponent(warp_max(fabsf(h)));
-                    const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
-                    a.hq[(size_t)s * a.I + f0 + fm] = (uint8_t)code;
-                    if (lane == 0) a.hs[(size_t)s * (a.I / 32) + (f0 + 32 * q) / 32] = (uint8_t)(ex + 127);
-                }
-            } else {
-                if (hf == 0) {
-                    float* yr = a.y + (size_t)seg_j[s] * a.H + f0;
-                    yr[fm] = v0;
-                    yr[128 + fm] = v1;
-                }
-                // the block's last expert tile combines it (ascending expert order)
-                __threadfence();
-                epi_bar();
-                if (leader) *last_flag = (atomicAdd(a.cmb_cnt + m, 1) == a.k - 1);
-                epi_bar();
-                if (*last_flag) {
-                    __threadfence();
-                    const int i = (warp - 2) * 32 + lane;
-                    float acc = 0.f;
-                    for (int ss = 0; ss < a.k; ++ss)
-                        acc += seg_w[ss] * __ldcg(a.y + (size_t)seg_j[ss] * a.H + f0 + i);
-                    a.out[f0 + i] = acc;
-                    epi_bar();
-                    if (leader) a.cmb_cnt[m] = 0;
-                }
+            // the first piece (this CTA's last segment): the later pieces are
+            // parked by the following CTAs, which met them first
+            if (lead_warp) {
+                bool ok = true;
+                const int cc = sg.first_cta + 1 + lane;
+                if (cc <= sg.last_cta) ok = flag_wait(pflag + cc * 2 + it.slot(cc, sg.tile), c.epoch, c.abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
             }
+            epi_bar();  // the acquire loads above make the pieces visible to the CTA
+            float sum = 0.f + v;
+            for (int cc = sg.first_cta + 1; cc <= sg.last_cta; ++cc)
+                sum += __ldcg(a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128 + pcol + col);
+            v = sum;
+        }
+        if (kGateUp) {
+            if (warp >= 6) up_s[col - 128] = v;
+            epi_bar();
+            if (warp < 6) {
+                const float h = silu_mul(v, up_s[col]);
+                const int ex = mxfp8_exponent(warp_max(fabsf(h)));
+                const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
+                a.hq[(size_t)s * a.I + f0 + col] = (uint8_t)code;
+                // h's scale rows in the layout of the A scale copies: per K
+                // step of the down GEMM 16 bytes, block kk once per lane quarter
+                const int blk = (f0 + col - lane) / 32;
+                if (lane < 4) a.hs[((size_t)s * (a.I / 128) + blk / 4) * 16 + 4 * lane + blk % 4] = (uint8_t)(ex + 127);
+            }
+            epi_bar();
+            if (lead_warp && lane == 0) flag_set(a.h_flag + sg.tile, c.epoch);
+        } else if (s < a.k - 1) {
+            a.y[(size_t)c.seg_j[s] * a.H + f0 + col] = v;
+            epi_bar();
+            if (lead_warp && lane == 0) flag_set(a.y_flag + sg.tile, c.epoch);
+        } else {
+            // the last expert's tile of block m: combine the block in
+            // ascending expert order, this tile's y from registers
+            if (lead_warp) {
+                bool ok = true;
+                if (lane < a.k - 1) ok = flag_wait(a.y_flag + lane * MT + m, c.epoch, c.abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
+            }
+            epi_bar();  // the acquire loads above make the pieces visible to the CTA
+            float o = 0.f;
+            for (int ss = 0; ss < a.k - 1; ++ss)
+                o += c.seg_w[ss] * __ldcg(a.y + (size_t)c.seg_j[ss] * a.H + f0 + col);
+            o += c.seg_w[a.k - 1] * v;
+            a.out[f0 + col] = o;
         }
     }
 }
@@ -749,149 +847,238 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);
-    const uint32_t bar0 = smem_u32(bars);
-    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * kDecStages + 2);
-    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-    volatile int* last_flag = reinterpret_cast<volatile int*>(tmem_slot + 2);
-    volatile int* routed_flag = reinterpret_cast<volatile int*>(tmem_slot + 3);
-    int* seg_e = reinterpret_cast<int*>(tmem_slot + 4);        // [8] experts, ascending
-    int* seg_j = seg_e + 8;                                     // [8] their j
-    float* seg_w = reinterpret_cast<float*>(seg_j + 8);         // [8] their weights
-    int* ids_s = reinterpret_cast<int*>(seg_w + 8);             // [8] router output, j order
-    float* w_s = reinterpret_cast<float*>(ids_s + 8);           // [8]
-    int* slot_s = reinterpret_cast<int*>(w_s + 8);              // [2] down-phase expert slots
+    uint32_t* words = reinterpret_cast<uint32_t*>(bars + 2 * kDecStages + 3);
+    // words: [0] tmem base, [1] abort, [2] epoch, [3] routed, [4..7] spare,
+    // then seg_e, seg_j, seg_w, sel (8 each), slot_s (2)
+    int* seg_e = reinterpret_cast<int*>(words + 8);
+    int* seg_j = seg_e + 8;
+    float* seg_w = reinterpret_cast<float*>(seg_j + 8);
+    int* sel = reinterpret_cast<int*>(seg_w + 8);
+    int* slot_s = sel + 8;
+    float* lg = reinterpret_cast<float*>(smem);  // logits, in stage 0 before the ring starts
+    DecCtx c;
+    c.smem = smem;
+    c.bar0 = smem_u32(bars);
+    c.abort_flag = reinterpret_cast<volatile int*>(words + 1);
+    c.seg_e = seg_e;
+    c.seg_j = seg_j;
+    c.seg_w = seg_w;
+    c.slot_s = slot_s;
+    volatile int* routed_flag = reinterpret_cast<volatile int*>(words + 3);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int k = a.k;
+    const int k = a.k, E = a.E;
 
     if (threadIdx.x == 0) {
         for (int st = 0; st < kDecStages; ++st) {
-            mbar_init(bar0 + 8u * st, 1);
-            mbar_init(bar0 + 8u * (kDecStages + st), 1);
+            mbar_init(c.full_bar(st), 1);
+            mbar_init(c.empty_bar(st), 1);
         }
-        mbar_init(bar0 + 8u * (2 * kDecStages), 1);
-        mbar_init(bar0 + 8u * (2 * kDecStages) + 8u, kEpiWarps);
-        *abort_flag = 0;
+        mbar_init(c.tmem_full(), 1);
+        mbar_init(c.tmem_empty(), kEpiWarps);
+        mbar_init(c.h_bar(), 1);
+        *c.abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmGU);
         prefetch_tmap(&tmDN);
     }
-    if (warp == 1) tmem_alloc(smem_u32(tmem_slot), 512);
-    // zero the resident B tiles and scales (rows 1-15 stay zero)
-    for (int i = threadIdx.x; i < (65536 + 2 * kDecSfbSlot) / 16; i += kTcThreads)
+    if (threadIdx.x < 8) sel[threadIdx.x] = -1;
+    if (threadIdx.x < 2) slot_s[threadIdx.x] = -1;
+    if (warp == 1) tmem_alloc(smem_u32(words), 512);
+    // zero the resident token rows and scale rows
+    for (int i = threadIdx.x; i < (kDecResBytes + 2 * kDecTokScaleSlot) / 16; i += kTcThreads)
         reinterpret_cast<uint4*>(smem + kDecResOff)[i] = make_uint4(0, 0, 0, 0);
+    __syncwarp();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    const uint32_t tmem = *tmem_slot;
-    // trace: [0] entry, [8] wait end, [9] routed and quantised, [10] gate/up
-    // done, [11] grid barrier passed, [2] down operands built, [1] exit
+    c.tmem = words[0];
+    // trace: [0] entry, [8] wait end, [9] routed, [1] exit (thread 0)
     unsigned long long* trc = a.trace ? a.trace + (size_t)blockIdx.x * 12 : nullptr;
-    const bool tr0 = trc && threadIdx.x == 0;
-    if (tr0) trc[0] = globaltimer();
+    if (trc && threadIdx.x == 0) trc[0] = globaltimer();
     pdl_launch_dependents();
     pdl_wait();
-    if (tr0) trc[8] = globaltimer();
+    if (trc && threadIdx.x == 0) trc[8] = globaltimer();
 
-    // ---- route (every CTA the same) and quantise x into the resident B tiles
-    if (warp == 2) route_token(a.logits, a.E, k, a.w_scale, ids_s, w_s, a.err, lane);
-    __syncthreads();
+    // ---- this launch's epoch; x loads in flight while the logits are ranked
     if (threadIdx.x == 0) {
-        int order[kMaxTopK];
-        for (int j = 0; j < k; ++j) order[j] = j;
-        for (int x = 1; x < k; ++x)
-            for (int b = x; b > 0 && ids_s[order[b - 1]] > ids_s[order[b]]; --b) {
-                const int tmp = order[b]; order[b] = order[b - 1]; order[b - 1] = tmp;
-            }
-        bool ok = true;
-        for (int x = 0; x < k; ++x) {
-            seg_e[x] = ids_s[order[x]];
-            seg_j[x] = order[x];
-            seg_w[x] = w_s[order[x]];
-            ok = ok && seg_e[x] >= 0 && seg_e[x] < a.E;
-        }
-        *routed_flag = ok;
-        if (blockIdx.x == 0)
-            for (int j = 0; j < k; ++j) { a.ids_out[j] = ids_s[j]; a.w_out[j] = w_s[j]; }
+        // every CTA adds one per launch: the count is a multiple of gridDim
+        // between launches, so all CTAs of a launch read the same quotient
+        const unsigned long long n = atomicAdd(a.launches, 1ull);
+        words[2] = (uint32_t)(n / gridDim.x) + 1u;
     }
-    {
-        const int tasks = a.H / 256;  // 8 blocks of 32 per warp-task, 4 lanes per block
-        for (int task = warp; task < tasks; task += kTcThreads / 32) {
-            const int b = task * 8 + (lane >> 2), part = lane & 3, h = b * 32 + part * 8;
-            const uint4 raw = *reinterpret_cast<const uint4*>(a.x + h);
-            const uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
-            float v[8];
-            float amax = 0.f;
+    const int nch = a.H / 8;  // 8-element chunks; a 32-block is 4 chunks of 4 aligned lanes
+    uint4 xr[2];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[2 * i] = __uint_as_float(wv[i] << 16);
-                v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-            const int ex = mxfp8_exponent(amax);
-            uint32_t lo = 0, hi = 0;
-#pragma unroll
-            for (int i = 0; i < 2; ++i) {
-                lo |= f32x2_to_e4m3x2(scale_pow2(v[2 * i], ex), scale_pow2(v[2 * i + 1], ex)) << (16 * i);
-                hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
-            }
-            // row 0 of the 16-row tile of K step h / 128 (the 128-byte swizzle
-            // leaves row 0 in order)
-            *reinterpret_cast<uint2*>(smem + kDecResOff + (h / 128) * kDecBTile + (h % 128)) = make_uint2(lo, hi);
-            if (part == 0) smem[kDecSfbOff + (b / 4) * 16 + (b % 4)] = (uint8_t)(ex + 127);
-        }
+    for (int r = 0; r < 2; ++r) {
+        const int ch = threadIdx.x + r * kTcThreads;
+        if (ch < nch) xr[r] = *reinterpret_cast<const uint4*>(a.x + (size_t)ch * 8);
     }
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    // top-k by rank (larger logit first, equal logits by lower index; NaN
+    // never selected), in two rounds: each warp ranks a 32-logit chunk among
+    // itself and keeps its local top k as candidates -- every global top-k
+    // logit is one -- then warp 0 ranks each candidate among all candidates.
+    const int nchunk = (E + 31) / 32;
+    int* cand = reinterpret_cast<int*>(smem + 4096);  // [nchunk][k], after the logits
+    for (int chk = warp; chk < nchunk; chk += kTcThreads / 32) {
+        const int e = chk * 32 + lane;
+        const float v = e < E ? __ldg(a.logits + e) : __int_as_float(0x7FC00000);
+        if (e < E) lg[e] = v;
+        int r = 0;
+#pragma unroll
+        for (int l2 = 0; l2 < 32; ++l2) {
+            const float u = __shfl_sync(0xFFFFFFFFu, v, l2);
+            r += (u > v || (u == v && l2 < lane)) ? 1 : 0;
+        }
+        if (lane < k) cand[chk * k + lane] = -1;
+        __syncwarp();
+        if (v == v && r < k) cand[chk * k + r] = e;
+    }
     __syncthreads();
-    if (tr0) trc[9] = globaltimer();
-    const bool routed = *routed_flag != 0;
-    uint32_t stage = 0, phase = 0, acc_phase = 0;
-    if (routed) {
-        slot_s[0] = slot_s[1] = -1;
-        decode_phase<true>(a, &tmGU, a.gu_sf, smem, bar0, tmem, seg_e, seg_j, seg_w, slot_s, stage, phase,
-                           acc_phase, abort_flag, last_flag, a.sk_cnt_gu);
-        if (tr0) trc[10] = globaltimer();
-        if (grid_barrier(a.gbar, gridDim.x, abort_flag)) {
-            if (tr0) trc[11] = globaltimer();
-            // the down phase's B tiles: h of (at most two) experts of this CTA's range
-            if (threadIdx.x == 0) {
+    if (warp == 0) {
+        const int nc = nchunk * k;
+        for (int t = lane; t < nc; t += 32) {
+            const int e = cand[t];
+            if (e < 0) continue;
+            const float v = lg[e];
+            int r = 0;
+            for (int t2 = 0; t2 < nc; ++t2) {
+                const int e2 = cand[t2];
+                if (e2 < 0) continue;
+                const float u = lg[e2];
+                r += (u > v || (u == v && e2 < e)) ? 1 : 0;
+            }
+            if (r < k) sel[r] = e;
+        }
+        __syncwarp();
+        // routing weights: lane j < k takes the j-th selection; w_j =
+        // w_scale * s_j / (s_0 + ... + s_{k-1}), s = sqrt(softplus(logit)), in fp32
+        const int e = lane < k ? sel[lane] : 0;
+        const bool ok = __all_sync(0xFFFFFFFFu, e >= 0);
+        float sv = 0.f;
+        if (lane < k && ok) {
+            const float l = lg[e];
+            sv = sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))));
+        }
+        float sum = 0.f;
+        for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, sv, j);
+        const float wj = ok ? a.w_scale * sv / sum : 0.0f;
+        if (lane < k && blockIdx.x == 0) {
+            a.ids_out[lane] = ok ? e : -1;
+            a.w_out[lane] = wj;
+        }
+        // position in ascending expert order (the combine order; ids are distinct)
+        int pos = 0;
+        for (int j = 0; j < k; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
+        if (lane < k) {
+            seg_e[pos] = e;
+            seg_w[pos] = wj;
+            seg_j[pos] = lane;
+        }
+        if (lane == 0) {
+            if (!ok && blockIdx.x == 0) raise_flag(a.err, ERR_BAD_ID);
+            *routed_flag = ok;
+        }
+    }
+    // ---- quantise x into the resident B row (MXFP8, 32-blocks)
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+        const int ch = threadIdx.x + r * kTcThreads;
+        if (ch - lane >= nch) continue;  // warp-uniform (nch is a multiple of 32)
+        const uint32_t wv[4] = {xr[r].x, xr[r].y, xr[r].z, xr[r].w};
+        float v[8];
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            v[2 * i] = __uint_as_float(wv[i] << 16);
+            v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+        const int ex = mxfp8_exponent(amax);
+        uint32_t lo = 0, hi = 0;
+#pragma unroll
+        for (int i = 0; i < 2; ++i) {
+            lo |= f32x2_to_e4m3x2(scale_pow2(v[2 * i], ex), scale_pow2(v[2 * i + 1], ex)) << (16 * i);
+            hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
+        }
+        const int h = ch * 8, b = ch >> 2;
+        *reinterpret_cast<uint2*>(smem + kDecResOff + h) = make_uint2(lo, hi);
+        // the scale row of K step b / 4: block b % 4, once per lane quarter
+        smem[kDecTokScaleOff + (b / 4) * 16 + 4 * (ch & 3) + (b % 4)] = (uint8_t)(ex + 127);
+    }
+    // generic-proxy writes (B row, scales; the logits' stage-0 bytes TMA
+    // overwrites next) ordered before the async proxy
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    __syncwarp();
+    __syncthreads();
+    c.epoch = words[2];
+    if (trc && threadIdx.x == 0) trc[9] = globaltimer();
+
+    if (*routed_flag) {
+        uint32_t stage = 0, phase = 0, acc_phase = 0;
+        if (warp == 0) {
+            // the producer runs through both phases: the down weights do
+            // not depend on h, so they load while gate/up finishes
+            if (dec_produce<true>(a, c, &tmGU, stage, phase, lane))
+                dec_produce<false>(a, c, &tmDN, stage, phase, lane);
+        } else {
+            bool ok = true;
+            if (warp == 1) ok = dec_mma<true>(a, c, stage, phase, acc_phase, nullptr, lane);
+            else dec_epilogue<true>(a, c, acc_phase);
+            // the (at most two) experts of this CTA's down range, then wait
+            // for their h (16 gate/up tiles each) and stage it as B rows
+            if (threadIdx.x == 32) {
+                int MT, KB, seg_rows;
+                dec_shape<false>(a, MT, KB, seg_rows);
                 SegIter it;
-                it.init(k * (a.H / 256), a.I / 128, (int)gridDim.x, (int)blockIdx.x);
+                it.init(k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
                 Seg sg;
                 int n = 0;
-                slot_s[0] = slot_s[1] = -1;
                 while (it.next(sg)) {  // ranges are contiguous: expert indices ascend
-                    const int s = sg.tile / (a.H / 256);
-                    if (n > 0 && slot_s[n - 1] == s) continue;
-                    if (n == 2) {  // more than two experts in one CTA's range: not supported
-                        raise_flag(a.err, ERR_TIMEOUT);
-                        *abort_flag = 1;
+                    const int sx = sg.tile / MT;
+                    if (n > 0 && slot_s[n - 1] == sx) continue;
+                    if (n == 2) {  // more than two experts in one range: not supported
+                        c.give_up(a);
                         break;
                     }
-                    slot_s[n++] = s;
+                    slot_s[n++] = sx;
                 }
             }
-            __syncthreads();
-            for (int sl = 0; sl < 2; ++sl) {
-                const int s = slot_s[sl];
-                if (s < 0) continue;
-                for (int i = threadIdx.x; i < a.I / 16; i += kTcThreads) {  // 16 codes per thread
-                    const uint4 v = __ldcg(reinterpret_cast<const uint4*>(a.hq + (size_t)s * a.I) + i);
-                    const int c = i * 16;
-                    *reinterpret_cast<uint4*>(smem + kDecResOff + sl * 32768 + (c / 128) * kDecBTile + (c % 128)) = v;
+            __syncwarp();
+            work_bar();  // the gate/up epilogue is done: no MMA reads the token row any more
+            if (warp == 1) {
+                // wait for the h flags of this CTA's experts (16 gate/up tiles
+                // each), then bring their h rows and scale rows in with bulk
+                // copies; the MMA thread waits on h_bar before its first MMA
+                const int mt_gu = a.I / 128;  // <= 16: lanes 0-15 slot 0, 16-31 slot 1
+                const int sx = slot_s[lane >> 4];
+                bool fok = true;
+                if (sx >= 0 && (lane & 15) < mt_gu)
+                    fok = flag_wait(a.h_flag + sx * mt_gu + (lane & 15), c.epoch, c.abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, fok) && lane == 0) c.give_up(a);
+                if (lane == 0) {
+                    // the copies read global memory other CTAs wrote through the generic proxy
+                    asm volatile("fence.proxy.async.global;" ::: "memory");
+                    const uint32_t hb = c.h_bar();
+                    const uint32_t srow = (uint32_t)(a.I / 128) * 16;
+                    const int nsl = slot_s[1] >= 0 ? 2 : 1;
+                    mbar_arrive_expect_tx(hb, (uint32_t)nsl * ((uint32_t)a.I + srow));
+                    for (int sl = 0; sl < nsl; ++sl) {
+                        bulk_load(smem_u32(smem + kDecResOff + sl * kDecSlotBytes), a.hq + (size_t)slot_s[sl] * a.I,
+                                  (uint32_t)a.I, hb);
+                        bulk_load(smem_u32(smem + kDecTokScaleOff + sl * kDecTokScaleSlot),
+                                  a.hs + (size_t)slot_s[sl] * srow, srow, hb);
+                    }
                 }
-                for (int b = threadIdx.x; b < a.I / 32; b += kTcThreads)
-                    smem[kDecSfbOff + sl * kDecSfbSlot + (b / 4) * 16 + (b % 4)] = a.hs[(size_t)s * (a.I / 32) + b];
+                __syncwarp();
             }
-            asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-            __syncthreads();
-            if (tr0) trc[2] = globaltimer();
-            decode_phase<false>(a, &tmDN, a.down_sf, smem, bar0, tmem, seg_e, seg_j, seg_w, slot_s, stage,
-                                phase, acc_phase, abort_flag, last_flag, a.sk_cnt_dn);
-        } else {
-            raise_flag(a.err, ERR_TIMEOUT);
+            if (warp == 1) {
+                if (ok && !*c.abort_flag) dec_mma<false>(a, c, stage, phase, acc_phase, nullptr, lane);
+            } else {
+                dec_epilogue<false>(a, c, acc_phase);
+            }
         }
     } else {
         // no valid routing (ERR_BAD_ID is raised): every row is dropped, as
@@ -899,12 +1086,13 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         for (int i = blockIdx.x * kTcThreads + threadIdx.x; i < a.H; i += gridDim.x * kTcThreads)
             a.out[i] = 0.f;
     }
+    __syncwarp();  // the producer / MMA lane rejoins its warp before the CTA barrier
     __syncthreads();
-    if (tr0) trc[1] = globaltimer();
-    if (*abort_flag) spin_ns(200000);
+    if (trc && threadIdx.x == 0) trc[1] = globaltimer();
+    if (*c.abort_flag) spin_ns(200000);
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(c.tmem, 512);
     }
 }
 
@@ -1125,10 +1313,11 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     a.hs = L->hs;
     a.y = L->y;
     a.sk_part = L->sk_partials;
-    a.sk_cnt_gu = L->sk_counters;
-    a.sk_cnt_dn = L->sk_counters + L->num_sms;
-    a.cmb_cnt = L->sk_counters + 4 * L->num_sms;
-    a.gbar = reinterpret_cast<unsigned*>(L->sk_counters + 4 * L->num_sms + 32);
+    int32_t* dw = L->sk_counters + kSkZeroed(L);
+    a.launches = reinterpret_cast<unsigned long long*>(dw);
+    a.piece_flag = reinterpret_cast<uint32_t*>(dw + 2);
+    a.h_flag = a.piece_flag + 4 * L->num_sms;
+    a.y_flag = a.h_flag + kDecMaxTiles;
     a.err = L->d_err;
     a.trace = L->trace;
     cudaLaunchConfig_t cfg = {};
@@ -1136,11 +1325,17 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = kDecSmem;
     cfg.stream = s;
-    cudaLaunchAttribute attr[1];
+    // cooperative (all CTAs co-resident for the grid barrier) and
+    // programmatic dependent launch: a CTA takes its SM as soon as the
+    // previous kernel's CTA there exits, runs its prologue and waits in
+    // griddepcontrol.wait for that kernel's completion
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeCooperative;
     attr[0].val.cooperative = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     L->launches += 1;
     return cudaLaunchKernelEx(&cfg, k_decode, st->gu, st->down, a);
 }

@@ -72,11 +72,14 @@ constexpr int kChunk = 4;      // tokens per CUDA-core GEMM work item
 constexpr int kFrontMaxT = 32; // batches up to this size use the one-CTA front kernel
 constexpr int kFusedCombineMaxT = 32;  // and the combine fused into the down GEMM
 
-// split-tile counters: 4 GEMM launches x num_sms, then one per 256-feature
-// block of the fused combine (H / 256 <= 32)
-// block of the fused combine (H / 256 <= 32), then the decode kernel's grid
-// barrier words (arrival count, generation)
-inline int kSkCounters(const moe_layer* L) { return 4 * L->num_sms + 32 + 8; }
+// split-tile counters of the grouped GEMMs (4 launches x num_sms, then one
+// per 256-feature block of the fused combine, H / 256 <= 32): zeroed by every
+// grouped forward
+inline int kSkZeroed(const moe_layer* L) { return 4 * L->num_sms + 32; }
+// then the words of the one-token decode kernel, zeroed only at creation: a
+// 64-bit launch counter, piece flags [2][num_sms][2], h flags [128], y flags [128]
+inline int kDecWords(const moe_layer* L) { return 2 + 4 * L->num_sms + 256; }
+inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L); }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
 // stream; the kernels synchronise on it with pdl_wait().

@@ -214,7 +214,7 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
     return launch_pdl(k_permute, dim3(1), dim3(1024), smem, s, ids, R, L->cfg.n_experts, offsets, row_src,
                       row_dst, L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
                       L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err, L->sk_counters,
-                      L->sk_counters ? kSkCounters(L) : 0);
+                      L->sk_counters ? kSkZeroed(L) : 0);
 }
 
 // The same counting sort with caller-chosen bookkeeping buffers (no layer):
@@ -378,7 +378,7 @@ cudaError_t launch_front(moe_layer* L, const float* logits, int32_t* ids, float*
                       L->cfg.top_k, L->cfg.n_experts, L->cfg.hidden, d, L->offsets, L->row_src, L->row_dst,
                       L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
                       L->cfg.has_shared ? L->sh_desc : nullptr, L->d_err, L->sk_counters,
-                      L->sk_counters ? kSkCounters(L) : 0,
+                      L->sk_counters ? kSkZeroed(L) : 0,
                       L->trace ? L->trace + (size_t)4 * L->num_sms * 12 : nullptr);
 }
 

@@ -183,7 +183,7 @@ extern "C" int probe_mma(const uint8_t* a, const uint8_t* b, const uint8_t* sfa,
 // global time the load was issued and the time the consumer saw it land.
 __global__ void __launch_bounds__(64, 1)
 k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int stages, int mode, int pf,
-         unsigned long long* stamps, int* ok_out, int layout, uint32_t box_tx, uint32_t slot) {
+         unsigned long long* stamps, int* ok_out, int layout, uint32_t box_tx, uint32_t slot, const uint8_t* sf_src) {
     extern __shared__ uint8_t raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + stages * slot + 16384 + 1024);
@@ -196,7 +196,7 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
         *abort_flag = 0;
         fence_mbar_init();
     }
-    if (warp == 1) tmem_alloc(smem_u32(tslot), 256);
+    if (warp == 1) tmem_alloc(smem_u32(tslot), 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -213,12 +213,20 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                 prefetch_tile_l2(&tmA, (j % KB) * 128, (blockIdx.x + (j / KB) * gridDim.x) * 128);
             }
             if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
-            mbar_arrive_expect_tx(b0 + 8 * s, box_tx);
+            mbar_arrive_expect_tx(b0 + 8 * s, box_tx + ((mode & 128) ? 1024u : 0u));
             if (blockIdx.x == 0 && i < 256) stamps[2 * i] = globaltimer();
+            // bit 7: a second, 1 KB bulk copy per stage (a scale-atom pair) into the B area
+            if (mode & 128)
+                bulk_load(smem_u32(sm + stages * slot + 1024 * s), sf_src + ((size_t)blockIdx.x * total + i) * 1024,
+                          1024, b0 + 8 * s);
             if (layout == 1)  // contiguous 8 KB tiles: 64-byte rows back to back
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, 0, (blockIdx.x * tiles_per_cta * KB + i) * 128, b0 + 8 * s);
             else if (layout == 3)  // 256-row fp4 box (two 128-row tiles per copy)
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row, b0 + 8 * s);
+            else if (layout == 5)  // 256-row fp4 box, CTAs on disjoint 256-row tiles
+                tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row * 2, b0 + 8 * s);
+            else if (layout == 6)  // contiguous 16 KB tiles: 256 rows of 64 bytes back to back
+                tma_load_2d(smem_u32(sm + s * slot), &tmA, 0, (blockIdx.x * tiles_per_cta * KB + i) * 256, b0 + 8 * s);
             else
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row, b0 + 8 * s);
         }
@@ -230,14 +238,22 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
             if (blockIdx.x == 0 && i < 256) stamps[2 * i + 1] = globaltimer();
             if (mode & 1) {
                 // bit 2: no tcgen05 fence; bit 3: 16 MMAs per stage; bit 4: N = 128;
-                // bit 5: unscaled kind::f8f6f4 instead of the block-scaled MMA
+                // bit 5: unscaled kind::f8f6f4 instead of the block-scaled MMA;
+                // bit 6: operands swapped (the weight tile as B, N = 256)
+                // (mode bit 7, an extra 1 KB bulk copy per stage, is on the producer side)
                 if (!(mode & 4)) tc_fence_after();
                 const uint32_t a = smem_u32(sm + s * slot), b = smem_u32(sm + stages * slot);
                 const uint32_t nn = (mode & 16) ? 128 : 32;
                 const int reps = (mode & 8) ? 4 : 1;
                 for (int rr = 0; rr < reps; ++rr)
                     for (int kk = 0; kk < 4; ++kk) {
-                        if (mode & 32) {
+                        if (mode & 64) {
+                            // operands swapped: A = a fixed e4m3 tile (the token side), B = the
+                            // streamed 256-row fp4 weight tile, N = 256: one MMA per K=32 step
+                            mma_mx(tmem, desc_sw128(b + 32 * kk), desc_sw128(a + 32 * kk),
+                                   idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
+                                   (kk > 0 || rr > 0) ? 1u : 0u);
+                        } else if (mode & 32) {
                             const uint32_t id = (kFmtE2M1 << 7) | (kFmtE4M3 << 10) | ((nn >> 3) << 17) | (8u << 24) | (1u << 4);
                             asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
                                          "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n}"
@@ -257,12 +273,14 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
     }
     __syncthreads();
     if (*abort_flag) { spin_ns(200000); if (threadIdx.x == 0) atomicExch(ok_out, 0); }
-    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 256); }
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 512); }
 }
 
 // layout 0: fp4 [rows][4096] box 128x128 (rows 2 KB apart); 1: fp4 viewed as
 // contiguous 64-byte rows (each box = 8 KB contiguous); 2: uint8 [rows][4096]
-// box 128x128 (16 KB); 3: fp4 box 128 x 256 rows (16 KB of codes, 32 KB slot).
+// box 128x128 (16 KB); 3: fp4 box 128 x 256 rows (16 KB of codes, 32 KB slot),
+// neighbouring CTAs' boxes overlapping by 128 rows; 5: as 3 on disjoint
+// 256-row tiles; 6: 256-row boxes over contiguous 16 KB tiles.
 extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tiles_per_cta, int stages, int mode,
                             int pf, unsigned long long* stamps, int* ok, float* ms, int layout) {
     CUtensorMap ta;
@@ -270,12 +288,15 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     uint32_t tx = 8192, slot = 16384;
     if (layout == 1) r = make_map(&ta, a, 128, (uint64_t)rows * 32, 128, true);
     else if (layout == 2) { r = make_map(&ta, a, 4096, (uint64_t)rows / 2, 128, false); tx = 16384; }
-    else if (layout == 3) { r = make_map(&ta, a, 4096, (uint64_t)rows, 256, true); tx = 16384; slot = 32768; }
+    else if (layout == 3 || layout == 5) { r = make_map(&ta, a, 4096, (uint64_t)rows, 256, true); tx = 16384; slot = 32768; }
+    else if (layout == 6) { r = make_map(&ta, a, 128, (uint64_t)rows * 32, 256, true); tx = 16384; slot = 32768; }
     else r = make_map(&ta, a, 4096, (uint64_t)rows, 128, true);
     if (r) return 1000 + r;
     const long long need = (long long)(grid * (tiles_per_cta - 1) + grid) * 128 + (layout == 3 ? 128 : 0);
     if (need > (layout == 2 ? rows / 2 : rows)) return 3;
     if (layout == 1 && (long long)grid * tiles_per_cta * 32 * 128 > rows * 32) return 4;
+    if (layout == 5 && (long long)grid * tiles_per_cta * 256 > rows) return 4;
+    if (layout == 6 && (long long)grid * tiles_per_cta * 32 * 256 > rows * 32) return 4;
     if (slot == 32768 && stages > 6) return 5;
     // tiles + B tile + barrier offset + barriers/slot + 1024 alignment slack
     const int smem = stages * (int)slot + 16384 + 1024 + 512 + 1024;
@@ -284,7 +305,10 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
-    k_stream<<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot);
+    // bit 7 reads 1 KB per stage from the start of the tensor (grid * tiles * 32 KB <= its size)
+    if ((mode & 128) && (long long)grid * tiles_per_cta * 32 * 1024 > rows * 2048) return 6;
+    if ((mode & 128) && stages * 1024 > 16384) return 7;
+    k_stream<<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);
@@ -357,6 +381,83 @@ extern "C" int probe_mma_peak(int grid, int iters, int n, uint32_t a_fmt, int* o
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
     k_mma_peak<<<grid, 64, smem>>>(iters, n, a_fmt, ok);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// Issue cost of the decode kernel's per-stage MMA group: per iteration `ncp`
+// scale-factor copies (tcgen05.cp 32x128b.warpx4), four K=32 block-scaled
+// MMAs on one or two accumulators (M = 128, N = n) and optionally one
+// tcgen05.commit to an mbarrier nobody waits on.  Smem operands are fixed.
+// mode: 0 as the grouped GEMMs issue them, 1 the same scale-factor ids for
+// every kk, 2 the same operand addresses for every kk, 3 B read through the
+// decode kernel's no-swizzle descriptor (16-byte K chunks 16 bytes apart)
+__global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, int commit, int acc2,
+                                                  uint32_t a_fmt, int mode, int* ok_out) {
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    // A: 2 x 16 KB, B: 16 KB, SF atoms: 3 x 512 B, then barriers
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 49152 + 1536);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 1);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 49152 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sm)[i] = 0x38383838u;
+    for (int i = threadIdx.x; i < 1536 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sm + 49152)[i] = 0x7F7F7F7Fu;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(bar), 1);
+        mbar_init(smem_u32(bar + 1), 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (threadIdx.x == 0) {
+        const uint32_t a = smem_u32(sm), b = smem_u32(sm + 32768), sf = smem_u32(sm + 49152);
+        for (int it = 0; it < iters; ++it) {
+            for (int j = 0; j < ncp; ++j) tmem_cp_32x128_x4(tmem + 256 + 4 * j, desc_sf(sf + 512 * j));
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk) {
+                const uint32_t sid = mode == 1 ? 0u : (uint32_t)kk;
+                const uint32_t ko = mode == 2 ? 0u : 32u * kk;
+                const uint32_t id = idesc_mx(a_fmt, kFmtE4M3, 128, (uint32_t)n, sid, sid);
+                // acc2 == 2: a separate accumulator per (row half, kk): eight
+                // independent chains of N = 16 columns
+                const uint32_t acc = (acc2 == 2) ? (it ? 1u : 0u) : ((it | kk) ? 1u : 0u);
+                const uint32_t d0 = (acc2 == 2) ? tmem + 16 * kk : tmem;
+                const uint32_t d1 = (acc2 == 2) ? tmem + 64 + 16 * kk : tmem + 128;
+                const uint64_t bd = mode == 3 ? smem_desc(b + ko, 16, 128, 0) : desc_sw128(b + ko);
+                mma_mx(d0, desc_sw128(a + ko), bd, id, tmem + 256, tmem + 264, acc);
+                if (acc2) mma_mx(d1, desc_sw128(a + 16384 + ko), bd, id, tmem + 260, tmem + 264, acc);
+            }
+            if (commit) mma_commit(smem_u32(bar + 1));
+        }
+        mma_commit(smem_u32(bar));
+        if (!mbar_wait(smem_u32(bar), 0, 2000000000ull, abort_flag)) { atomicExch(ok_out, 0); spin_ns(200000); }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+extern "C" int probe_mma_mix(int grid, int iters, int n, int ncp, int commit, int acc2, uint32_t a_fmt, int mode,
+                             int* ok, float* ms) {
+    if (n < 16 || n > (acc2 == 2 ? 16 : acc2 ? 128 : 256) || ncp < 0 || ncp > 3) return 3;
+    const int smem = 49152 + 1536 + 1024 + 64;
+    cudaFuncSetAttribute(k_mma_mix, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    if (mode < 0 || mode > 3) return 3;
+    k_mma_mix<<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);

@@ -32,18 +32,27 @@ def load():
                                  vp, C.c_int]
     lib.probe_stream_lsu.argtypes = [vp, C.c_longlong, C.c_int, C.c_int, C.c_int, vp, vp, vp]
     lib.probe_mma_peak.argtypes = [C.c_int, C.c_int, C.c_int, C.c_uint32, vp, vp]
+    lib.probe_mma_mix.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_uint32, C.c_int,
+                                  vp, vp]
     return lib
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "microbench_tc.json"))
+    ap.add_argument("--only-mix", action="store_true", help="only the per-stage MMA group issue costs")
+    ap.add_argument("--only-stream", action="store_true", help="only the 256-row weight-box TMA streams")
     args = ap.parse_args()
     lib = load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ms = C.c_float()
     ok = torch.ones(1, dtype=torch.int32, device="cuda")
     out = {"sms": sms}
+    if args.only_mix:
+        mma_mix(lib, sms, ok, ms, out)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
 
     buf = torch.zeros(4 << 30, dtype=torch.uint8, device="cuda")
     sink = torch.zeros(1, dtype=torch.int32, device="cuda")
@@ -64,6 +73,21 @@ def main():
         per = sorted((st[2 * i + 3] - st[2 * i + 1]) / 1000 for i in range(64, 200))
         return lat[len(lat) // 2], per[len(per) // 2]
 
+    if args.only_stream:
+        for layout, stages, mode in ((5, 6, 0), (5, 6, 128), (5, 6, 1 | 64), (5, 6, 1 | 64 | 128),
+                                     (6, 6, 128), (6, 6, 1 | 64 | 128)):
+            for _ in range(2):
+                ok.fill_(1)
+                rc = lib.probe_stream(A.data_ptr(), rows, sms, 8, stages, mode, 0, stamps.data_ptr(),
+                                      ok.data_ptr(), C.byref(ms), layout)
+            lat, per = stage_stats()
+            key = f"tma_layout{layout}_stages{stages}_mode{mode}"
+            out[key] = {"GBs": round(sms * 8 * 32 * 16384 / ms.value / 1e6, 1), "issue_to_land_us": lat,
+                        "us_per_stage": per, "ok": int(ok.item()), "rc": rc}
+            print(key, out[key], flush=True)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
     # layout: 0 fp4 128-row box, 1 fp4 contiguous tiles, 2 uint8 128-row box, 3 fp4 256-row box
     # mode: 1 = MMAs (N=32), |8 = 16 MMAs per stage, |16 = N=128, |32 = unscaled kind
     cases = [(0, 8192, 4, 0), (0, 8192, 8, 0), (1, 8192, 4, 0), (2, 16384, 4, 0), (2, 16384, 8, 0),
@@ -90,6 +114,7 @@ def main():
         print(f"cpasync_stages{stages}", out[f"cpasync_stages{stages}"], flush=True)
     del A
 
+    mma_mix(lib, sms, ok, ms, out)
     for fmt in (5, 0):
         for n in (32, 128, 256):
             iters = 20000 if n >= 128 else 40000
@@ -101,6 +126,23 @@ def main():
             print("mma", fmt, n, rc, int(ok.item()), round(tf, 1), flush=True)
     os.makedirs(os.path.dirname(args.out), exist_ok=True)
     json.dump(out, open(args.out, "w"), indent=1)
+
+
+def mma_mix(lib, sms, ok, ms, out):
+    """ns per iteration of [ncp scale copies + 4 (or 8) MMAs (+ commit)] on every SM."""
+    iters = 20000
+    cases = [(16, 0, 0, 0, 0), (16, 0, 0, 1, 0), (16, 3, 1, 1, 0), (16, 1, 1, 1, 0), (128, 3, 1, 1, 0),
+             (16, 0, 0, 2, 0), (16, 0, 0, 1, 1), (16, 0, 0, 1, 2), (16, 0, 0, 0, 1), (16, 3, 1, 1, 1),
+             (16, 0, 0, 1, 3), (16, 3, 1, 1, 3)]
+    for fmt in (5,):
+        for n, ncp, commit, acc2, mode in cases:
+                ok.fill_(1)
+                lib.probe_mma_mix(sms, 100, n, ncp, commit, acc2, fmt, mode, ok.data_ptr(), C.byref(ms))
+                rc = lib.probe_mma_mix(sms, iters, n, ncp, commit, acc2, fmt, mode, ok.data_ptr(), C.byref(ms))
+                key = (f"mix_f{fmt}_n{n}_cp{ncp}_commit{commit}_" + ("acc1", "acc2", "acc8split")[acc2] +
+                       ("", "_samesfid", "_sameaddr", "_nswzB")[mode])
+                out[key] = {"ns_per_iter": round(ms.value * 1e6 / iters, 2), "rc": rc, "ok": int(ok.item())}
+                print(key, out[key], flush=True)
 
 
 if __name__ == "__main__":

@@ -51,12 +51,14 @@ def _check_token(cfg, wts, layer, tk, t):
     ref = orc.layer_forward(wts, xb, rid, w.cpu().numpy().astype(np.float64))
     norm, elem = G.compare_out(out.cpu().numpy(), ref)
     assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (norm, elem)
-    # the grouped tcgen05 kernels split the same tiles over the same CTAs and
-    # add the same partial sums in the same order: identical bytes
+    # the grouped tcgen05 kernels: the same routing bit for bit; the output
+    # within the oracle tolerance of theirs (the decode kernel multiplies
+    # with the operands swapped, so fp32 sums may round differently)
     ids2, w2, out2, n2 = _route_forward(layer, lg, xb, 2)
     assert n2 > 1
     assert torch.equal(ids, ids2) and torch.equal(w, w2)
-    assert out.cpu().numpy().tobytes() == out2.cpu().numpy().tobytes()
+    o1, o2 = out.cpu().numpy().astype(np.float64), out2.cpu().numpy().astype(np.float64)
+    assert np.linalg.norm(o1 - o2) <= G.NORM_TOL * np.linalg.norm(o2)
 
 
 def test_decode_kernel_decode_shape(decode_layer):
