@@ -50,8 +50,12 @@ __device__ __forceinline__ int mxfp8_exponent(float amax) {
     return (ef == 0 || ex < -127) ? -127 : ex;   // ef <= 254 keeps ex <= 119
 }
 
-// v * 2^-ex, exact for the exponents mxfp8_exponent returns.
-__device__ __forceinline__ float scale_pow2(float v, int ex) { return ldexpf(v, -ex); }
+// v * 2^-ex for the exponents mxfp8_exponent returns (-127 <= ex <= 119):
+// 2^-ex is a normal fp32 built from its exponent field, so the product is
+// one IEEE multiplication (rounded once, as a scaling by a power of two is).
+__device__ __forceinline__ float scale_pow2(float v, int ex) {
+    return v * __uint_as_float((uint32_t)(127 - ex) << 23);
+}
 
 // Two fp32 -> two e4m3 bytes (round to nearest even, saturate to +-448),
 // first value in the low byte.

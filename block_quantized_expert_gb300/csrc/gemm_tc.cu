@@ -548,7 +548,8 @@ constexpr int kDecTokScaleSlot = 64 * 16 + 512;
 constexpr int kDecTokScaleOff = kDecResOff + kDecResBytes;  // token scale rows (2 slots)
 constexpr int kDecBarOff = kDecTokScaleOff + 2 * kDecTokScaleSlot;
 constexpr int kDecUpOff = kDecBarOff + 512;              // gate/up epilogue: the 128 up values of a tile
-constexpr int kDecSmem = kDecUpOff + 512 + 1024;
+constexpr int kDecFrontOff = kDecUpOff + 512;            // routing: logits [E], candidates [<= 256] x 2
+constexpr int kDecSmem = kDecFrontOff + 4096 + 2048 + 1024;
 // tensor memory: D in columns 0-255; weight scales, 8 per stage; the
 // token's scales of the down phase, 4 per stage; those of the gate/up
 // phase, 4 per K step for every step (copied at the phase start, while the
@@ -763,6 +764,22 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_ph
     while (it.next(sg)) {
         const int s = sg.tile / MT, m = sg.tile % MT;
         const int f0 = m * (kGateUp ? 128 : 256);
+        const bool split = sg.first_cta != sg.last_cta;
+        const bool owner = !split || (int)blockIdx.x == sg.first_cta;
+        float later = 0.f;  // the later pieces of a cut tile this CTA finishes, in K order
+        if (split && owner) {
+            // they come from the following CTAs, which met them first: wait
+            // for them and load them while this CTA's own MMAs still run
+            if (lead_warp) {
+                bool ok = true;
+                const int cc = sg.first_cta + 1 + lane;
+                if (cc <= sg.last_cta) ok = flag_wait(pflag + cc * 2 + it.slot(cc, sg.tile), c.epoch, c.abort_flag);
+                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
+            }
+            epi_bar();  // the acquire loads above make the pieces visible to the CTA
+            for (int cc = sg.first_cta + 1; cc <= sg.last_cta; ++cc)
+                later += __ldcg(a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128 + pcol + col);
+        }
         // on a timeout the epilogue goes on with whatever the accumulator
         // holds (the error is raised), so all eight warps keep meeting at
         // the same named barriers
@@ -781,29 +798,14 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_ph
             const float x = __shfl_sync(0xFFFFFFFFu, __uint_as_float(r[i]), 0);
             if (lane == i) v = x;
         }
-        if (sg.first_cta != sg.last_cta) {
-            const int slot = it.slot(blockIdx.x, sg.tile);
-            if ((int)blockIdx.x != sg.first_cta) {
-                // a later piece: park it and go on
-                a.sk_part[((size_t)blockIdx.x * 2 + slot) * 2 * 128 * 128 + pcol + col] = v;
-                epi_bar();  // the release store below publishes the whole CTA's writes
-                if (lead_warp && lane == 0) flag_set(pflag + blockIdx.x * 2 + slot, c.epoch);
-                continue;
-            }
-            // the first piece (this CTA's last segment): the later pieces are
-            // parked by the following CTAs, which met them first
-            if (lead_warp) {
-                bool ok = true;
-                const int cc = sg.first_cta + 1 + lane;
-                if (cc <= sg.last_cta) ok = flag_wait(pflag + cc * 2 + it.slot(cc, sg.tile), c.epoch, c.abort_flag);
-                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
-            }
-            epi_bar();  // the acquire loads above make the pieces visible to the CTA
-            float sum = 0.f + v;
-            for (int cc = sg.first_cta + 1; cc <= sg.last_cta; ++cc)
-                sum += __ldcg(a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128 + pcol + col);
-            v = sum;
+        if (!owner) {
+            // a later piece: park it and go on
+            a.sk_part[((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128 + pcol + col] = v;
+            epi_bar();  // the release store below publishes the whole CTA's writes
+            if (lead_warp && lane == 0) flag_set(pflag + blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile), c.epoch);
+            continue;
         }
+        if (split) v += later;
         if (kGateUp) {
             if (warp >= 6) up_s[col - 128] = v;
             epi_bar();
@@ -849,13 +851,14 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);
     uint32_t* words = reinterpret_cast<uint32_t*>(bars + 2 * kDecStages + 3);
     // words: [0] tmem base, [1] abort, [2] epoch, [3] routed, [4..7] spare,
-    // then seg_e, seg_j, seg_w, sel (8 each), slot_s (2)
+    // then seg_e, seg_j, seg_w, sel (8 each), slot_s (2), prod_e (8)
     int* seg_e = reinterpret_cast<int*>(words + 8);
     int* seg_j = seg_e + 8;
     float* seg_w = reinterpret_cast<float*>(seg_j + 8);
     int* sel = reinterpret_cast<int*>(seg_w + 8);
     int* slot_s = sel + 8;
-    float* lg = reinterpret_cast<float*>(smem);  // logits, in stage 0 before the ring starts
+    int* prod_e = slot_s + 2;  // [8] the producer warp's own copy of seg_e
+    float* lg = reinterpret_cast<float*>(smem + kDecFrontOff);  // the logits (E <= 1024)
     DecCtx c;
     c.smem = smem;
     c.bar0 = smem_u32(bars);
@@ -899,12 +902,13 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     pdl_wait();
     if (trc && threadIdx.x == 0) trc[8] = globaltimer();
 
-    // ---- this launch's epoch; x loads in flight while the logits are ranked
-    if (threadIdx.x == 0) {
+    // ---- the launch's epoch (used after the front); x loads in flight while
+    // the logits are ranked
+    unsigned long long n_launch = 0;
+    if (threadIdx.x == 32) {
         // every CTA adds one per launch: the count is a multiple of gridDim
         // between launches, so all CTAs of a launch read the same quotient
-        const unsigned long long n = atomicAdd(a.launches, 1ull);
-        words[2] = (uint32_t)(n / gridDim.x) + 1u;
+        n_launch = atomicAdd(a.launches, 1ull);
     }
     const int nch = a.H / 8;  // 8-element chunks; a 32-block is 4 chunks of 4 aligned lanes
     uint4 xr[2];
@@ -916,9 +920,11 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     // top-k by rank (larger logit first, equal logits by lower index; NaN
     // never selected), in two rounds: each warp ranks a 32-logit chunk among
     // itself and keeps its local top k as candidates -- every global top-k
-    // logit is one -- then warp 0 ranks each candidate among all candidates.
+    // logit is one -- then thread t ranks candidate t among all candidates.
     const int nchunk = (E + 31) / 32;
-    int* cand = reinterpret_cast<int*>(smem + 4096);  // [nchunk][k], after the logits
+    const int nc = nchunk * k;                             // <= 256
+    int* ci = reinterpret_cast<int*>(smem + kDecFrontOff + 4096);   // candidate experts (-1: none)
+    float* cv = reinterpret_cast<float*>(smem + kDecFrontOff + 5120);  // their logits (NaN: none)
     for (int chk = warp; chk < nchunk; chk += kTcThreads / 32) {
         const int e = chk * 32 + lane;
         const float v = e < E ? __ldg(a.logits + e) : __int_as_float(0x7FC00000);
@@ -929,56 +935,17 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
             const float u = __shfl_sync(0xFFFFFFFFu, v, l2);
             r += (u > v || (u == v && l2 < lane)) ? 1 : 0;
         }
-        if (lane < k) cand[chk * k + lane] = -1;
+        if (lane < k) {
+            ci[chk * k + lane] = -1;
+            cv[chk * k + lane] = __int_as_float(0x7FC00000);
+        }
         __syncwarp();
-        if (v == v && r < k) cand[chk * k + r] = e;
+        if (v == v && r < k) {
+            ci[chk * k + r] = e;
+            cv[chk * k + r] = v;
+        }
     }
     __syncthreads();
-    if (warp == 0) {
-        const int nc = nchunk * k;
-        for (int t = lane; t < nc; t += 32) {
-            const int e = cand[t];
-            if (e < 0) continue;
-            const float v = lg[e];
-            int r = 0;
-            for (int t2 = 0; t2 < nc; ++t2) {
-                const int e2 = cand[t2];
-                if (e2 < 0) continue;
-                const float u = lg[e2];
-                r += (u > v || (u == v && e2 < e)) ? 1 : 0;
-            }
-            if (r < k) sel[r] = e;
-        }
-        __syncwarp();
-        // routing weights: lane j < k takes the j-th selection; w_j =
-        // w_scale * s_j / (s_0 + ... + s_{k-1}), s = sqrt(softplus(logit)), in fp32
-        const int e = lane < k ? sel[lane] : 0;
-        const bool ok = __all_sync(0xFFFFFFFFu, e >= 0);
-        float sv = 0.f;
-        if (lane < k && ok) {
-            const float l = lg[e];
-            sv = sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))));
-        }
-        float sum = 0.f;
-        for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, sv, j);
-        const float wj = ok ? a.w_scale * sv / sum : 0.0f;
-        if (lane < k && blockIdx.x == 0) {
-            a.ids_out[lane] = ok ? e : -1;
-            a.w_out[lane] = wj;
-        }
-        // position in ascending expert order (the combine order; ids are distinct)
-        int pos = 0;
-        for (int j = 0; j < k; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
-        if (lane < k) {
-            seg_e[pos] = e;
-            seg_w[pos] = wj;
-            seg_j[pos] = lane;
-        }
-        if (lane == 0) {
-            if (!ok && blockIdx.x == 0) raise_flag(a.err, ERR_BAD_ID);
-            *routed_flag = ok;
-        }
-    }
     // ---- quantise x into the resident B row (MXFP8, 32-blocks)
 #pragma unroll
     for (int r = 0; r < 2; ++r) {
@@ -1008,22 +975,77 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         // the scale row of K step b / 4: block b % 4, once per lane quarter
         smem[kDecTokScaleOff + (b / 4) * 16 + 4 * (ch & 3) + (b % 4)] = (uint8_t)(ex + 127);
     }
-    // generic-proxy writes (B row, scales; the logits' stage-0 bytes TMA
-    // overwrites next) ordered before the async proxy
+    // the quantised row and scales were written through the generic proxy;
+    // the MMAs read them through the async proxy
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-    __syncwarp();
+    for (int t = threadIdx.x; t < nc; t += kTcThreads) {
+        const int e = ci[t];
+        if (e < 0) continue;
+        const float v = cv[t];
+        int r = 0;
+#pragma unroll 8
+        for (int t2 = 0; t2 < nc; ++t2) {  // empty slots hold NaN: never counted
+            const float u = cv[t2];
+            r += (int)(u > v) | ((int)(u == v) & (int)(ci[t2] < e));
+        }
+        if (r < k) sel[r] = e;
+    }
     __syncthreads();
-    c.epoch = words[2];
-    if (trc && threadIdx.x == 0) trc[9] = globaltimer();
-
-    if (*routed_flag) {
-        uint32_t stage = 0, phase = 0, acc_phase = 0;
-        if (warp == 0) {
-            // the producer runs through both phases: the down weights do
-            // not depend on h, so they load while gate/up finishes
-            if (dec_produce<true>(a, c, &tmGU, stage, phase, lane))
-                dec_produce<false>(a, c, &tmDN, stage, phase, lane);
-        } else {
+    uint32_t stage = 0, phase = 0, acc_phase = 0;
+    if (warp == 0) {
+        // the producer starts as soon as the experts are known, on its own
+        // copy of them in ascending order (the other warps still finish the
+        // routing weights)
+        const int e = lane < k ? sel[lane] : 0;
+        if (__all_sync(0xFFFFFFFFu, e >= 0)) {
+            int pos = 0;
+            for (int j = 0; j < k; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
+            if (lane < k) prod_e[pos] = e;
+            __syncwarp();
+            DecCtx cp = c;
+            cp.seg_e = prod_e;
+            // it runs through both phases: the down weights do not depend on
+            // h, so they load while gate/up finishes
+            if (dec_produce<true>(a, cp, &tmGU, stage, phase, lane))
+                dec_produce<false>(a, cp, &tmDN, stage, phase, lane);
+        }
+    } else {
+        if (threadIdx.x == 32) words[2] = (uint32_t)(n_launch / gridDim.x) + 1u;
+        if (warp == 2) {
+            // routing weights: lane j < k takes the j-th selection; w_j =
+            // w_scale * s_j / (s_0 + ... + s_{k-1}), s = sqrt(softplus(logit)), in fp32
+            const int e = lane < k ? sel[lane] : 0;
+            const bool ok = __all_sync(0xFFFFFFFFu, e >= 0);
+            float sv = 0.f;
+            if (lane < k && ok) {
+                const float l = lg[e];
+                sv = sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))));
+            }
+            float sum = 0.f;
+            for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, sv, j);
+            const float wj = ok ? a.w_scale * sv / sum : 0.0f;
+            if (lane < k && blockIdx.x == 0) {
+                a.ids_out[lane] = ok ? e : -1;
+                a.w_out[lane] = wj;
+            }
+            // position in ascending expert order (the combine order; ids are distinct)
+            int pos = 0;
+            for (int j = 0; j < k; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
+            if (lane < k) {
+                seg_e[pos] = e;
+                seg_w[pos] = wj;
+                seg_j[pos] = lane;
+            }
+            if (lane == 0) {
+                if (!ok && blockIdx.x == 0) raise_flag(a.err, ERR_BAD_ID);
+                *routed_flag = ok;
+            }
+        }
+        __syncwarp();
+        work_bar();  // the routing of warps 1-9 (the producer is on its way)
+        c.epoch = words[2];
+        if (trc && threadIdx.x == 32) trc[9] = globaltimer();
+        if (*routed_flag) {
             bool ok = true;
             if (warp == 1) ok = dec_mma<true>(a, c, stage, phase, acc_phase, nullptr, lane);
             else dec_epilogue<true>(a, c, acc_phase);
@@ -1079,12 +1101,12 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
             } else {
                 dec_epilogue<false>(a, c, acc_phase);
             }
+        } else {
+            // no valid routing (ERR_BAD_ID is raised): every row is dropped,
+            // as in the grouped path, and the output is zero
+            for (int i = blockIdx.x * (kTcThreads - 32) + threadIdx.x - 32; i < a.H; i += gridDim.x * (kTcThreads - 32))
+                a.out[i] = 0.f;
         }
-    } else {
-        // no valid routing (ERR_BAD_ID is raised): every row is dropped, as
-        // in the grouped path, and the output is zero
-        for (int i = blockIdx.x * kTcThreads + threadIdx.x; i < a.H; i += gridDim.x * kTcThreads)
-            a.out[i] = 0.f;
     }
     __syncwarp();  // the producer / MMA lane rejoins its warp before the CTA barrier
     __syncthreads();
