@@ -576,7 +576,7 @@ struct DecArgs {
     uint8_t* hs;          // [k][I/32] UE8M0 (scratch)
     float* y;             // [k][H] down outputs (scratch)
     float* sk_part;       // [G][2][2][128][128] partial accumulators of cut tiles
-    unsigned long long* launches;  // launch counter (epoch = value / gridDim.x)
+    unsigned long long* launches;  // launch counter: this launch's flags hold its value + 1
     uint32_t* piece_flag;  // [2 phases][G][2]: a cut tile's piece parked by CTA c in slot s
     uint32_t* h_flag;      // [kDecMaxTiles]: h of gate/up tile t written
     uint32_t* y_flag;      // [kDecMaxTiles]: y of down tile t written
@@ -906,9 +906,9 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     // the logits are ranked
     unsigned long long n_launch = 0;
     if (threadIdx.x == 32) {
-        // every CTA adds one per launch: the count is a multiple of gridDim
-        // between launches, so all CTAs of a launch read the same quotient
-        n_launch = atomicAdd(a.launches, 1ull);
+        // the launch counter: read here by every CTA (the previous launch,
+        // which advanced it, has completed), advanced once at this launch's end
+        n_launch = *reinterpret_cast<volatile unsigned long long*>(a.launches);
     }
     const int nch = a.H / 8;  // 8-element chunks; a 32-block is 4 chunks of 4 aligned lanes
     uint4 xr[2];
@@ -1010,7 +1010,7 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
                 dec_produce<false>(a, cp, &tmDN, stage, phase, lane);
         }
     } else {
-        if (threadIdx.x == 32) words[2] = (uint32_t)(n_launch / gridDim.x) + 1u;
+        if (threadIdx.x == 32) words[2] = (uint32_t)n_launch + 1u;
         if (warp == 2) {
             // routing weights: lane j < k takes the j-th selection; w_j =
             // w_scale * s_j / (s_0 + ... + s_{k-1}), s = sqrt(softplus(logit)), in fp32
@@ -1111,6 +1111,8 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     __syncwarp();  // the producer / MMA lane rejoins its warp before the CTA barrier
     __syncthreads();
     if (trc && threadIdx.x == 0) trc[1] = globaltimer();
+    // the next launch reads the counter only after this grid has completed
+    if (blockIdx.x == 0 && threadIdx.x == 32) *a.launches = n_launch + 1ull;
     if (*c.abort_flag) spin_ns(200000);
     if (warp == 1) {
         tc_fence_after();
