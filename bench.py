@@ -48,6 +48,8 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--trace", action="store_true",
                     help="after timing, trace one more call of the GEMM kernels (stderr)")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="a smaller expert set with the same per-token work (for profiler captures)")
     return ap.parse_args()
 
 
@@ -493,6 +495,9 @@ def main():
     world = int(os.environ.get("WORLD_SIZE", 1))
     local_rank = int(os.environ.get("LOCAL_RANK", 0))
     cfg = CONFIGS[args.config]
+    if args.experts is not None:
+        import dataclasses
+        cfg = dataclasses.replace(cfg, E=args.experts, name=f"{cfg.name}_e{args.experts}")
     if args.impl == "reference":
         res = run_reference(args, cfg, rank, world)
     else:

@@ -512,19 +512,25 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 // down, combine -- so nothing of the token goes through a kernel boundary.
 // Every CTA routes the token itself (ranks of the fp32 logits, the selection
 // k_route makes, hence the same experts and weights everywhere) and
-// quantises x straight into a resident shared-memory B row.  The weights
-// stream through the TMA / tcgen05 pipeline of k_gemm_tc, split stream-K
-// over all SMs; the producer runs on from the gate/up weights into the down
-// weights (they do not depend on h).
+// quantises x straight into a resident shared-memory row.  The weights
+// stream through a TMA / tcgen05 pipeline like k_gemm_tc's, split stream-K
+// over all SMs.
+//
+// The k experts (ascending) may form groups whose phases run gate/up(0),
+// gate/up(1), ..., down(0), down(1), ... so that one group's h hand-off
+// overlaps the next group's streaming; with one accumulator the extra tile
+// boundaries cost more than that saves (measured), so there is one group.
+// The producer runs through all phases (the weights do not depend on h) and
+// fetches the h of a group's experts before that group's down weights.
 //
 // Cross-CTA hand-offs go through flags that hold the launch's epoch (a
 // 64-bit launch counter that only grows), so nothing is ever reset: a tile
 // cut between CTAs is finished by the CTA holding its first K-steps (it
-// reaches that piece last), which waits for the other pieces' flags and adds
-// the pieces in K order; a gate/up tile's owner publishes h and an h flag;
-// a CTA starts its down phase once the h flags of its experts are set; the
-// owner of the last expert's tile of each 256-feature block waits for the
-// other experts' y flags and writes the combined output.
+// reaches that piece last), which adds the later pieces (parked by the
+// following CTAs, which met them first) to its own; a gate/up tile's owner
+// publishes h and an h flag; the owner of the last expert's tile of each
+// 256-feature block waits for the other experts' y flags and writes the
+// combined output.
 
 // Orientation: with a single token the MMA cost is per instruction, not
 // per column, so the weights are the B operand (N = 256: one MMA per K=32
@@ -538,29 +544,31 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 // features, 128-255 the matching up features; down columns are 256 outputs.
 constexpr int kDecStageBytes = 32768 + 1024;  // 256 weight rows + their scale atoms
 constexpr int kDecStages = 6;
-constexpr int kDecResOff = kDecStages * kDecStageBytes;  // A rows: x (H <= 4096) or h of two experts
-constexpr int kDecSlotBytes = 2048 + 256;                // one h row (I <= 2048) + what the aliased rows reach
-constexpr int kDecResBytes = 2 * kDecSlotBytes;          // also covers x: 4096 + 512
+constexpr int kDecGroups = 1;
+constexpr int kDecSlotBytes = 2048 + 256;     // one h row (I <= 2048) + what the aliased rows reach
+constexpr int kDecXOff = kDecStages * kDecStageBytes;            // the x row (H <= 4096) + reach
+constexpr int kDecHOff = kDecXOff + 4096 + 512;                   // h rows [group][2 slots]
 // Token scales: the source rows of the A scale copies, one 16-byte row per K
 // step holding the step's four block scales once per lane quarter (the token
 // rows 0, 32, 64, 96); a copy reads 512 bytes from its row.
-constexpr int kDecTokScaleSlot = 64 * 16 + 512;
-constexpr int kDecTokScaleOff = kDecResOff + kDecResBytes;  // token scale rows (2 slots)
-constexpr int kDecBarOff = kDecTokScaleOff + 2 * kDecTokScaleSlot;
+constexpr int kDecXScaleBytes = 32 * 16 + 512;
+constexpr int kDecHScaleBytes = 16 * 16 + 512;
+constexpr int kDecTokScaleOff = kDecHOff + 2 * kDecGroups * kDecSlotBytes;  // x's, then h's [group][slot]
+constexpr int kDecBarOff = kDecTokScaleOff + kDecXScaleBytes + 2 * kDecGroups * kDecHScaleBytes;
 constexpr int kDecUpOff = kDecBarOff + 512;              // gate/up epilogue: the 128 up values of a tile
 constexpr int kDecFrontOff = kDecUpOff + 512;            // routing: logits [E], candidates [<= 256] x 2
 constexpr int kDecSmem = kDecFrontOff + 4096 + 2048 + 1024;
 // tensor memory: D in columns 0-255; weight scales, 8 per stage; the
-// token's scales of the down phase, 4 per stage; those of the gate/up
-// phase, 4 per K step for every step (copied at the phase start, while the
-// first weights are still in flight)
+// token's scales of the down phases, 4 per stage; those of the gate/up
+// phases, 4 per K step for every step (copied at the start, while the first
+// weights are still in flight)
 constexpr uint32_t kDecSfbCol = 256;
 constexpr uint32_t kDecSfaStageCol = kDecSfbCol + 8 * kDecStages;
 constexpr uint32_t kDecSfaResCol = kDecSfaStageCol + 4 * kDecStages;
 static_assert(kDecSfaResCol + 4 * 32 <= 512, "tensor memory budget");
 constexpr int kDecMaxTiles = 128;             // k * (I / 128) and k * (H / 256) for k <= 8, H <= 4096, I <= 2048
 static_assert(kDecSmem <= 232448, "shared memory budget");
-static_assert(kDecStageBytes % 1024 == 0, "128-byte swizzled A tiles need 1024-byte alignment");
+static_assert(kDecStageBytes % 1024 == 0, "128-byte swizzled weight tiles need 1024-byte alignment");
 
 struct DecArgs {
     const float* logits;  // [E]
@@ -573,16 +581,30 @@ struct DecArgs {
     const uint8_t* gu_sf;
     const uint8_t* down_sf;
     uint8_t* hq;          // [k][I] e4m3 (scratch)
-    uint8_t* hs;          // [k][I/32] UE8M0 (scratch)
+    uint8_t* hs;          // [k][I/128][16] scale rows (scratch)
     float* y;             // [k][H] down outputs (scratch)
     float* sk_part;       // [G][2][2][128][128] partial accumulators of cut tiles
     unsigned long long* launches;  // launch counter: this launch's flags hold its value + 1
-    uint32_t* piece_flag;  // [2 phases][G][2]: a cut tile's piece parked by CTA c in slot s
+    uint32_t* piece_flag;  // [4 phases][G][2]: a cut tile's piece parked by CTA c in slot s
     uint32_t* h_flag;      // [kDecMaxTiles]: h of gate/up tile t written
     uint32_t* y_flag;      // [kDecMaxTiles]: y of down tile t written
     uint32_t* err;
     unsigned long long* trace;  // [gridDim][12] ns timestamps, or null
 };
+
+// One phase: the gate/up or down tiles of experts s_lo .. s_lo + n_s - 1
+// (ascending order); idx = 2 * (down) + group names its flags and columns.
+struct DecPhase {
+    int s_lo, n_s, idx;
+};
+
+__device__ __forceinline__ int dec_groups(int k) { return k >= kDecGroups ? kDecGroups : 1; }
+
+__device__ __forceinline__ DecPhase dec_phase(int k, bool down, int g) {
+    const int G = dec_groups(k);
+    const int lo = g * k / G, hi = (g + 1) * k / G;
+    return DecPhase{lo, hi - lo, (down ? 2 : 0) + g};
+}
 
 // Shared state of one decode CTA.
 struct DecCtx {
@@ -593,12 +615,12 @@ struct DecCtx {
     const int* seg_e;    // [k] experts, ascending
     const int* seg_j;    // [k] their position in the router output
     const float* seg_w;  // [k] their weights
-    const int* slot_s;   // [2] down phase: the experts whose h sits in B slots 0 / 1
     __device__ uint32_t full_bar(int st) const { return bar0 + 8u * st; }
     __device__ uint32_t empty_bar(int st) const { return bar0 + 8u * (kDecStages + st); }
     __device__ uint32_t tmem_full() const { return bar0 + 8u * (2 * kDecStages); }
     __device__ uint32_t tmem_empty() const { return bar0 + 8u * (2 * kDecStages) + 8u; }
-    __device__ uint32_t h_bar() const { return bar0 + 8u * (2 * kDecStages) + 16u; }  // down-phase A rows landed
+    // a group's h rows and scale rows have landed
+    __device__ uint32_t h_bar(int g) const { return bar0 + 8u * (2 * kDecStages) + 16u + 8u * g; }
     __device__ void give_up(const DecArgs& a) const {
         *abort_flag = 1;
         raise_flag(a.err, ERR_TIMEOUT);
@@ -610,6 +632,25 @@ __device__ __forceinline__ void dec_shape(const DecArgs& a, int& MT, int& KB, in
     MT = kGateUp ? a.I / 128 : a.H / 256;
     KB = (kGateUp ? a.H : a.I) / 128;
     seg_rows = kGateUp ? 2 * a.I : a.H;
+}
+
+// The (at most two) experts of this CTA's range of a down phase, in range
+// order: slots[0], slots[1] (-1: none).  False if the range spans more.
+__device__ bool dec_slots(const DecArgs& a, const DecPhase& ph, int (&slots)[2]) {
+    int MT, KB, seg_rows;
+    dec_shape<false>(a, MT, KB, seg_rows);
+    SegIter it;
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    Seg sg;
+    int n = 0;
+    slots[0] = slots[1] = -1;
+    while (it.next(sg)) {  // ranges are contiguous: expert indices ascend
+        const int sx = ph.s_lo + sg.tile / MT;
+        if (n > 0 && slots[n - 1] == sx) continue;
+        if (n == 2) return false;
+        slots[n++] = sx;
+    }
+    return true;
 }
 
 // Warps 1-9 (all but the TMA producer).
@@ -639,18 +680,18 @@ __device__ bool flag_wait(const uint32_t* f, uint32_t v, volatile int* abort) {
 }
 
 // TMA producer (warp 0; lane 0 waits and issues): the weight tiles and
-// scale atoms of this CTA's stream-K range, into the stage ring.
+// scale atoms of this CTA's stream-K range of one phase, into the ring.
 template <bool kGateUp>
-__device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap* tmA, uint32_t& stage,
-                            uint32_t& phase, int lane) {
+__device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap* tmA, const DecPhase& ph,
+                            uint32_t& stage, uint32_t& phase, int lane) {
     int MT, KB, seg_rows;
     dec_shape<kGateUp>(a, MT, KB, seg_rows);
     const uint8_t* sfa = kGateUp ? a.gu_sf : a.down_sf;
     SegIter it;
-    it.init(a.k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
     Seg sg;
     while (it.next(sg)) {
-        const int s = sg.tile / MT, m = sg.tile % MT;
+        const int s = ph.s_lo + sg.tile / MT, m = sg.tile % MT;
         const int arow = c.seg_e[s] * seg_rows + m * 256;
         const size_t atom_a = (size_t)(arow / 256) * KB;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
@@ -672,40 +713,83 @@ __device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap
     return true;
 }
 
-// MMA issuer (warp 1; lane 0 waits and issues): per K=32 step one M = 128,
-// N = 256 MMA of the resident token row against the streamed weight tile.
-template <bool kGateUp>
-__device__ bool dec_mma(const DecArgs& a, const DecCtx& c, uint32_t& stage, uint32_t& phase,
-                        uint32_t& acc_phase, unsigned long long* wait_ns, int lane) {
-    int MT, KB, seg_rows;
-    dec_shape<kGateUp>(a, MT, KB, seg_rows);
-    const uint32_t res_base = smem_u32(c.smem + kDecResOff);
-    const uint32_t tok_base = smem_u32(c.smem + kDecTokScaleOff);
-    unsigned long long none = 0;
-    if (kGateUp) {
-        if (lane == 0) {
-            tc_fence_after();
-            for (int kb = 0; kb < KB; ++kb)
-                tmem_cp_32x128_x4(c.tmem + kDecSfaResCol + kb * 4, desc_sf(tok_base + kb * 16));
-        }
-        __syncwarp();
-    } else if (!warp_wait(c.h_bar(), 0, c.abort_flag, false, none, lane)) {  // h rows and scales
+// Before a down phase's weights (producer warp): wait for the h flags of the
+// phase's experts in this CTA's range (their gate/up tiles, I / 128 <= 16
+// each), then bring their h rows and scale rows in with bulk copies that
+// complete on the group's h barrier.
+__device__ bool dec_fetch_h(const DecArgs& a, const DecCtx& c, const DecPhase& ph, int g, int lane) {
+    int slots[2];
+    if (!dec_slots(a, ph, slots)) {  // more than two experts in one range: not supported
         if (lane == 0) c.give_up(a);
         return false;
     }
+    const int mt_gu = a.I / 128;  // lanes 0-15 slot 0, 16-31 slot 1
+    const int sx = slots[lane >> 4];
+    bool ok = true;
+    if (sx >= 0 && (lane & 15) < mt_gu) ok = flag_wait(a.h_flag + sx * mt_gu + (lane & 15), c.epoch, c.abort_flag);
+    if (!__all_sync(0xFFFFFFFFu, ok)) {
+        if (lane == 0) c.give_up(a);
+        return false;
+    }
+    if (lane == 0) {
+        // the copies read global memory other CTAs wrote through the generic proxy
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        const uint32_t hb = c.h_bar(g);
+        const uint32_t srow = (uint32_t)mt_gu * 16;
+        const int nsl = slots[1] >= 0 ? 2 : 1;
+        mbar_arrive_expect_tx(hb, (uint32_t)nsl * ((uint32_t)a.I + srow));
+        for (int sl = 0; sl < nsl; ++sl) {
+            bulk_load(smem_u32(c.smem + kDecHOff + (2 * g + sl) * kDecSlotBytes), a.hq + (size_t)slots[sl] * a.I,
+                      (uint32_t)a.I, hb);
+            bulk_load(smem_u32(c.smem + kDecTokScaleOff + kDecXScaleBytes + (2 * g + sl) * kDecHScaleBytes),
+                      a.hs + (size_t)slots[sl] * srow, srow, hb);
+        }
+    }
+    __syncwarp();
+    return true;
+}
+
+// MMA issuer (warp 1; lane 0 waits and issues): per K=32 step one M = 128,
+// N = 256 MMA of the resident token row against the streamed weight tile.
+template <bool kGateUp>
+__device__ bool dec_mma(const DecArgs& a, const DecCtx& c, const DecPhase& ph, int g, uint32_t& stage,
+                        uint32_t& phase, uint32_t& acc_phase, int lane) {
+    int MT, KB, seg_rows;
+    dec_shape<kGateUp>(a, MT, KB, seg_rows);
+    const uint32_t tok_base = smem_u32(c.smem + kDecTokScaleOff);
+    unsigned long long none = 0;
+    int slots[2] = {-1, -1};
+    if (kGateUp) {
+        if (g == 0) {  // x's scales for every K step, once
+            if (lane == 0) {
+                tc_fence_after();
+                for (int kb = 0; kb < KB; ++kb)
+                    tmem_cp_32x128_x4(c.tmem + kDecSfaResCol + kb * 4, desc_sf(tok_base + kb * 16));
+            }
+            __syncwarp();
+        }
+    } else {
+        dec_slots(a, ph, slots);
+        if (!warp_wait(c.h_bar(g), 0, c.abort_flag, false, none, lane)) {  // the group's h rows
+            if (lane == 0) c.give_up(a);
+            return false;
+        }
+    }
     SegIter it;
-    it.init(a.k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
     Seg sg;
     while (it.next(sg)) {
-        const int s = sg.tile / MT;
-        const int sl = (!kGateUp && c.slot_s[1] == s) ? 1 : 0;
+        const int s = ph.s_lo + sg.tile / MT;
+        const int sl = (!kGateUp && slots[1] == s) ? 1 : 0;
+        const uint32_t a_base = kGateUp ? smem_u32(c.smem + kDecXOff)
+                                        : smem_u32(c.smem + kDecHOff + (2 * g + sl) * kDecSlotBytes);
+        const uint32_t sa_base = tok_base + kDecXScaleBytes + (2 * g + sl) * kDecHScaleBytes;
         if (!warp_wait(c.tmem_empty(), acc_phase ^ 1u, c.abort_flag, false, none, lane)) {
             if (lane == 0) c.give_up(a);
             return false;
         }
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-            if (!warp_wait(c.full_bar(stage), phase, c.abort_flag, wait_ns != nullptr,
-                           wait_ns ? *wait_ns : none, lane)) {
+            if (!warp_wait(c.full_bar(stage), phase, c.abort_flag, false, none, lane)) {
                 if (lane == 0) c.give_up(a);
                 return false;
             }
@@ -713,11 +797,11 @@ __device__ bool dec_mma(const DecArgs& a, const DecCtx& c, uint32_t& stage, uint
                 tc_fence_after();
                 const uint32_t st = smem_u32(c.smem + stage * kDecStageBytes);
                 const uint32_t sfb_col = c.tmem + kDecSfbCol + stage * 8;  // weight rows 0-127, 128-255
-                const uint32_t at = res_base + sl * kDecSlotBytes + kb * 128;
+                const uint32_t at = a_base + kb * 128;
                 uint32_t sfa_col = c.tmem + kDecSfaResCol + kb * 4;
                 if (!kGateUp) {
                     sfa_col = c.tmem + kDecSfaStageCol + stage * 4;
-                    tmem_cp_32x128_x4(sfa_col, desc_sf(tok_base + sl * kDecTokScaleSlot + kb * 16));
+                    tmem_cp_32x128_x4(sfa_col, desc_sf(sa_base + kb * 16));
                 }
                 tmem_cp_32x128_x4(sfb_col, desc_sf(st + 32768));
                 tmem_cp_32x128_x4(sfb_col + 4, desc_sf(st + 32768 + 512));
@@ -747,11 +831,11 @@ __device__ bool dec_mma(const DecArgs& a, const DecCtx& c, uint32_t& stage, uint
 // SiLU(g) * u and requantise it to MXFP8 (32 features = one warp).  Down: y,
 // or for the last expert's tile of a feature block the combined output.
 template <bool kGateUp>
-__device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_phase) {
+__device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& ph, uint32_t& acc_phase) {
     int MT, KB, seg_rows;
     dec_shape<kGateUp>(a, MT, KB, seg_rows);
-    uint32_t* pflag = a.piece_flag + (kGateUp ? 0 : 2 * gridDim.x);
-    const int pcol = kGateUp ? 0 : 256;  // the two phases park pieces in different columns
+    uint32_t* pflag = a.piece_flag + ph.idx * 2 * gridDim.x;
+    const int pcol = ph.idx * 256;  // the phases park pieces in different columns
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int q = warp & 3;
     const int col = 32 * (warp - 2) + lane;  // this thread's D column (0-255)
@@ -759,17 +843,20 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_ph
     float* up_s = reinterpret_cast<float*>(c.smem + kDecUpOff);
     const bool lead_warp = warp == 2;
     SegIter it;
-    it.init(a.k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
     Seg sg;
     while (it.next(sg)) {
-        const int s = sg.tile / MT, m = sg.tile % MT;
+        const int s = ph.s_lo + sg.tile / MT, m = sg.tile % MT;
+        const int gt = s * MT + m;  // the tile's index over all experts (its flags)
         const int f0 = m * (kGateUp ? 128 : 256);
         const bool split = sg.first_cta != sg.last_cta;
         const bool owner = !split || (int)blockIdx.x == sg.first_cta;
         float later = 0.f;  // the later pieces of a cut tile this CTA finishes, in K order
         if (split && owner) {
             // they come from the following CTAs, which met them first: wait
-            // for them and load them while this CTA's own MMAs still run
+            // for them and load them while this CTA's own MMAs still run (the
+            // piece is this CTA's last of the phase, so no later tile waits
+            // for the accumulator meanwhile)
             if (lead_warp) {
                 bool ok = true;
                 const int cc = sg.first_cta + 1 + lane;
@@ -800,9 +887,10 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_ph
         }
         if (!owner) {
             // a later piece: park it and go on
-            a.sk_part[((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128 + pcol + col] = v;
+            const int slot = it.slot(blockIdx.x, sg.tile);
+            a.sk_part[((size_t)blockIdx.x * 2 + slot) * 2 * 128 * 128 + pcol + col] = v;
             epi_bar();  // the release store below publishes the whole CTA's writes
-            if (lead_warp && lane == 0) flag_set(pflag + blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile), c.epoch);
+            if (lead_warp && lane == 0) flag_set(pflag + blockIdx.x * 2 + slot, c.epoch);
             continue;
         }
         if (split) v += later;
@@ -820,11 +908,11 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_ph
                 if (lane < 4) a.hs[((size_t)s * (a.I / 128) + blk / 4) * 16 + 4 * lane + blk % 4] = (uint8_t)(ex + 127);
             }
             epi_bar();
-            if (lead_warp && lane == 0) flag_set(a.h_flag + sg.tile, c.epoch);
+            if (lead_warp && lane == 0) flag_set(a.h_flag + gt, c.epoch);
         } else if (s < a.k - 1) {
             a.y[(size_t)c.seg_j[s] * a.H + f0 + col] = v;
             epi_bar();
-            if (lead_warp && lane == 0) flag_set(a.y_flag + sg.tile, c.epoch);
+            if (lead_warp && lane == 0) flag_set(a.y_flag + gt, c.epoch);
         } else {
             // the last expert's tile of block m: combine the block in
             // ascending expert order, this tile's y from registers
@@ -833,7 +921,7 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, uint32_t& acc_ph
                 if (lane < a.k - 1) ok = flag_wait(a.y_flag + lane * MT + m, c.epoch, c.abort_flag);
                 if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
             }
-            epi_bar();  // the acquire loads above make the pieces visible to the CTA
+            epi_bar();
             float o = 0.f;
             for (int ss = 0; ss < a.k - 1; ++ss)
                 o += c.seg_w[ss] * __ldcg(a.y + (size_t)c.seg_j[ss] * a.H + f0 + col);
@@ -849,15 +937,14 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kDecBarOff);
-    uint32_t* words = reinterpret_cast<uint32_t*>(bars + 2 * kDecStages + 3);
+    uint32_t* words = reinterpret_cast<uint32_t*>(bars + 2 * kDecStages + 2 + kDecGroups);
     // words: [0] tmem base, [1] abort, [2] epoch, [3] routed, [4..7] spare,
-    // then seg_e, seg_j, seg_w, sel (8 each), slot_s (2), prod_e (8)
+    // then seg_e, seg_j, seg_w, sel, prod_e (8 each)
     int* seg_e = reinterpret_cast<int*>(words + 8);
     int* seg_j = seg_e + 8;
     float* seg_w = reinterpret_cast<float*>(seg_j + 8);
     int* sel = reinterpret_cast<int*>(seg_w + 8);
-    int* slot_s = sel + 8;
-    int* prod_e = slot_s + 2;  // [8] the producer warp's own copy of seg_e
+    int* prod_e = sel + 8;  // [8] the producer warp's own copy of seg_e
     float* lg = reinterpret_cast<float*>(smem + kDecFrontOff);  // the logits (E <= 1024)
     DecCtx c;
     c.smem = smem;
@@ -866,7 +953,6 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     c.seg_e = seg_e;
     c.seg_j = seg_j;
     c.seg_w = seg_w;
-    c.slot_s = slot_s;
     volatile int* routed_flag = reinterpret_cast<volatile int*>(words + 3);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int k = a.k, E = a.E;
@@ -878,18 +964,19 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         }
         mbar_init(c.tmem_full(), 1);
         mbar_init(c.tmem_empty(), kEpiWarps);
-        mbar_init(c.h_bar(), 1);
+        for (int g = 0; g < kDecGroups; ++g) mbar_init(c.h_bar(g), 1);
         *c.abort_flag = 0;
         fence_mbar_init();
         prefetch_tmap(&tmGU);
         prefetch_tmap(&tmDN);
     }
     if (threadIdx.x < 8) sel[threadIdx.x] = -1;
-    if (threadIdx.x < 2) slot_s[threadIdx.x] = -1;
     if (warp == 1) tmem_alloc(smem_u32(words), 512);
-    // zero the resident token rows and scale rows
-    for (int i = threadIdx.x; i < (kDecResBytes + 2 * kDecTokScaleSlot) / 16; i += kTcThreads)
-        reinterpret_cast<uint4*>(smem + kDecResOff)[i] = make_uint4(0, 0, 0, 0);
+    // zero the x row and its scale rows (the h rows arrive whole)
+    for (int i = threadIdx.x; i < (4096 + 512) / 16; i += kTcThreads)
+        reinterpret_cast<uint4*>(smem + kDecXOff)[i] = make_uint4(0, 0, 0, 0);
+    for (int i = threadIdx.x; i < kDecXScaleBytes / 16; i += kTcThreads)
+        reinterpret_cast<uint4*>(smem + kDecTokScaleOff)[i] = make_uint4(0, 0, 0, 0);
     __syncwarp();
     tc_fence_before();
     __syncthreads();
@@ -971,7 +1058,7 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
             hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
         }
         const int h = ch * 8, b = ch >> 2;
-        *reinterpret_cast<uint2*>(smem + kDecResOff + h) = make_uint2(lo, hi);
+        *reinterpret_cast<uint2*>(smem + kDecXOff + h) = make_uint2(lo, hi);
         // the scale row of K step b / 4: block b % 4, once per lane quarter
         smem[kDecTokScaleOff + (b / 4) * 16 + 4 * (ch & 3) + (b % 4)] = (uint8_t)(ex + 127);
     }
@@ -990,6 +1077,7 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         }
         if (r < k) sel[r] = e;
     }
+    if (threadIdx.x == 32) words[2] = (uint32_t)n_launch + 1u;  // this launch's flag value
     __syncthreads();
     uint32_t stage = 0, phase = 0, acc_phase = 0;
     if (warp == 0) {
@@ -1004,13 +1092,18 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
             __syncwarp();
             DecCtx cp = c;
             cp.seg_e = prod_e;
-            // it runs through both phases: the down weights do not depend on
-            // h, so they load while gate/up finishes
-            if (dec_produce<true>(a, cp, &tmGU, stage, phase, lane))
-                dec_produce<false>(a, cp, &tmDN, stage, phase, lane);
+            cp.epoch = words[2];
+            const int G = dec_groups(k);
+            // it runs through all phases (the weights do not depend on h),
+            // fetching each group's h before that group's down weights
+            bool ok = true;
+            for (int g = 0; g < G && ok; ++g) ok = dec_produce<true>(a, cp, &tmGU, dec_phase(k, false, g), stage, phase, lane);
+            for (int g = 0; g < G && ok; ++g) {
+                const DecPhase ph = dec_phase(k, true, g);
+                ok = dec_fetch_h(a, cp, ph, g, lane) && dec_produce<false>(a, cp, &tmDN, ph, stage, phase, lane);
+            }
         }
     } else {
-        if (threadIdx.x == 32) words[2] = (uint32_t)n_launch + 1u;
         if (warp == 2) {
             // routing weights: lane j < k takes the j-th selection; w_j =
             // w_scale * s_j / (s_0 + ... + s_{k-1}), s = sqrt(softplus(logit)), in fp32
@@ -1046,60 +1139,17 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         c.epoch = words[2];
         if (trc && threadIdx.x == 32) trc[9] = globaltimer();
         if (*routed_flag) {
+            const int G = dec_groups(k);
             bool ok = true;
-            if (warp == 1) ok = dec_mma<true>(a, c, stage, phase, acc_phase, nullptr, lane);
-            else dec_epilogue<true>(a, c, acc_phase);
-            // the (at most two) experts of this CTA's down range, then wait
-            // for their h (16 gate/up tiles each) and stage it as B rows
-            if (threadIdx.x == 32) {
-                int MT, KB, seg_rows;
-                dec_shape<false>(a, MT, KB, seg_rows);
-                SegIter it;
-                it.init(k * MT, KB, (int)gridDim.x, (int)blockIdx.x);
-                Seg sg;
-                int n = 0;
-                while (it.next(sg)) {  // ranges are contiguous: expert indices ascend
-                    const int sx = sg.tile / MT;
-                    if (n > 0 && slot_s[n - 1] == sx) continue;
-                    if (n == 2) {  // more than two experts in one range: not supported
-                        c.give_up(a);
-                        break;
-                    }
-                    slot_s[n++] = sx;
-                }
+            for (int g = 0; g < G; ++g) {
+                const DecPhase ph = dec_phase(k, false, g);
+                if (warp == 1) ok = ok && dec_mma<true>(a, c, ph, g, stage, phase, acc_phase, lane);
+                else dec_epilogue<true>(a, c, ph, acc_phase);
             }
-            __syncwarp();
-            work_bar();  // the gate/up epilogue is done: no MMA reads the token row any more
-            if (warp == 1) {
-                // wait for the h flags of this CTA's experts (16 gate/up tiles
-                // each), then bring their h rows and scale rows in with bulk
-                // copies; the MMA thread waits on h_bar before its first MMA
-                const int mt_gu = a.I / 128;  // <= 16: lanes 0-15 slot 0, 16-31 slot 1
-                const int sx = slot_s[lane >> 4];
-                bool fok = true;
-                if (sx >= 0 && (lane & 15) < mt_gu)
-                    fok = flag_wait(a.h_flag + sx * mt_gu + (lane & 15), c.epoch, c.abort_flag);
-                if (!__all_sync(0xFFFFFFFFu, fok) && lane == 0) c.give_up(a);
-                if (lane == 0) {
-                    // the copies read global memory other CTAs wrote through the generic proxy
-                    asm volatile("fence.proxy.async.global;" ::: "memory");
-                    const uint32_t hb = c.h_bar();
-                    const uint32_t srow = (uint32_t)(a.I / 128) * 16;
-                    const int nsl = slot_s[1] >= 0 ? 2 : 1;
-                    mbar_arrive_expect_tx(hb, (uint32_t)nsl * ((uint32_t)a.I + srow));
-                    for (int sl = 0; sl < nsl; ++sl) {
-                        bulk_load(smem_u32(smem + kDecResOff + sl * kDecSlotBytes), a.hq + (size_t)slot_s[sl] * a.I,
-                                  (uint32_t)a.I, hb);
-                        bulk_load(smem_u32(smem + kDecTokScaleOff + sl * kDecTokScaleSlot),
-                                  a.hs + (size_t)slot_s[sl] * srow, srow, hb);
-                    }
-                }
-                __syncwarp();
-            }
-            if (warp == 1) {
-                if (ok && !*c.abort_flag) dec_mma<false>(a, c, stage, phase, acc_phase, nullptr, lane);
-            } else {
-                dec_epilogue<false>(a, c, acc_phase);
+            for (int g = 0; g < G; ++g) {
+                const DecPhase ph = dec_phase(k, true, g);
+                if (warp == 1) ok = ok && !*c.abort_flag && dec_mma<false>(a, c, ph, g, stage, phase, acc_phase, lane);
+                else dec_epilogue<false>(a, c, ph, acc_phase);
             }
         } else {
             // no valid routing (ERR_BAD_ID is raised): every row is dropped,
@@ -1340,7 +1390,7 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     int32_t* dw = L->sk_counters + kSkZeroed(L);
     a.launches = reinterpret_cast<unsigned long long*>(dw);
     a.piece_flag = reinterpret_cast<uint32_t*>(dw + 2);
-    a.h_flag = a.piece_flag + 4 * L->num_sms;
+    a.h_flag = a.piece_flag + 8 * L->num_sms;
     a.y_flag = a.h_flag + kDecMaxTiles;
     a.err = L->d_err;
     a.trace = L->trace;

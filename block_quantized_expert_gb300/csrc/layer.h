@@ -77,8 +77,9 @@ constexpr int kFusedCombineMaxT = 32;  // and the combine fused into the down GE
 // grouped forward
 inline int kSkZeroed(const moe_layer* L) { return 4 * L->num_sms + 32; }
 // then the words of the one-token decode kernel, zeroed only at creation: a
-// 64-bit launch counter, piece flags [2][num_sms][2], h flags [128], y flags [128]
-inline int kDecWords(const moe_layer* L) { return 2 + 4 * L->num_sms + 256; }
+// 64-bit launch counter, piece flags [4 phases][num_sms][2], h flags [128],
+// y flags [128]
+inline int kDecWords(const moe_layer* L) { return 2 + 8 * L->num_sms + 256; }
 inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L); }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the

@@ -395,7 +395,8 @@ extern "C" int probe_mma_peak(int grid, int iters, int n, uint32_t a_fmt, int* o
 // tcgen05.commit to an mbarrier nobody waits on.  Smem operands are fixed.
 // mode: 0 as the grouped GEMMs issue them, 1 the same scale-factor ids for
 // every kk, 2 the same operand addresses for every kk, 3 B read through the
-// decode kernel's no-swizzle descriptor (16-byte K chunks 16 bytes apart)
+// decode kernel's no-swizzle descriptor (16-byte K chunks 16 bytes apart),
+// 4 the decode kernel's orientation (weights as the N = 256 B operand)
 __global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, int commit, int acc2,
                                                   uint32_t a_fmt, int mode, int* ok_out) {
     extern __shared__ uint8_t raw[];
@@ -433,6 +434,15 @@ __global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, in
                 const uint32_t acc = (acc2 == 2) ? (it ? 1u : 0u) : ((it | kk) ? 1u : 0u);
                 const uint32_t d0 = (acc2 == 2) ? tmem + 16 * kk : tmem;
                 const uint32_t d1 = (acc2 == 2) ? tmem + 64 + 16 * kk : tmem + 128;
+                if (mode == 4) {
+                    // the decode kernel's orientation: A = one aliased token row
+                    // (no swizzle, 8-row groups at stride 0), B = a 256-row
+                    // weight tile, N = 256: one MMA per K=32 step
+                    mma_mx(tmem, smem_desc(b + ko, 16, 0, 0), desc_sw128(a + ko),
+                           idesc_mx(kFmtE4M3, a_fmt, 128, 256, kk, kk), tmem + 256, tmem + 260,
+                           (it | kk) ? 1u : 0u);
+                    continue;
+                }
                 const uint64_t bd = mode == 3 ? smem_desc(b + ko, 16, 128, 0) : desc_sw128(b + ko);
                 mma_mx(d0, desc_sw128(a + ko), bd, id, tmem + 256, tmem + 264, acc);
                 if (acc2) mma_mx(d1, desc_sw128(a + 16384 + ko), bd, id, tmem + 260, tmem + 264, acc);
@@ -456,7 +466,7 @@ extern "C" int probe_mma_mix(int grid, int iters, int n, int ncp, int commit, in
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
-    if (mode < 0 || mode > 3) return 3;
+    if (mode < 0 || mode > 4) return 3;
     k_mma_mix<<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
