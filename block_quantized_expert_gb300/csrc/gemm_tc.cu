@@ -135,32 +135,34 @@ struct Seg {
 };
 
 struct SegIter {
+    // 32-bit arithmetic: a split happens only with fewer than 4 * G tiles of
+    // at most 64 K-stages, so c * total stays below 2^23
     int tiles, KB, G, c;
     bool split;
-    long long total, g, gend;
+    int total, g, gend;
     int t;
 
     __device__ void init(int tiles_, int KB_, int G_, int c_) {
         tiles = tiles_; KB = KB_; G = G_; c = c_;
-        total = (long long)tiles * KB;
+        total = tiles * KB;
         // fewer than four waves of whole tiles would leave SMs idle: split,
         // as long as every CTA still gets at least 4 K-stages
-        split = tiles < 4 * G && total >= 4LL * G;
-        if (split) { g = (long long)c * total / G; gend = (long long)(c + 1) * total / G; }
+        split = tiles < 4 * G && total >= 4 * G;
+        if (split) { g = c * total / G; gend = (c + 1) * total / G; }
         t = c;
     }
-    __device__ int owner(long long gs) const {  // CTA whose range holds global stage gs
-        return (int)(((gs + 1) * G + total - 1) / total - 1);
+    __device__ int owner(int gs) const {  // CTA whose range holds global stage gs
+        return ((gs + 1) * G + total - 1) / total - 1;
     }
-    __device__ long long range_begin(int cc) const { return (long long)cc * total / G; }
+    __device__ int range_begin(int cc) const { return cc * total / G; }
     __device__ bool next(Seg& s) {
         if (split) {
             if (g >= gend) return false;
-            s.tile = (int)(g / KB);
-            s.kb0 = (int)(g % KB);
-            s.kb1 = (int)min((long long)KB, s.kb0 + (gend - g));
-            s.first_cta = owner((long long)s.tile * KB);
-            s.last_cta = owner((long long)s.tile * KB + KB - 1);
+            s.tile = g / KB;
+            s.kb0 = g % KB;
+            s.kb1 = min(KB, s.kb0 + (gend - g));
+            s.first_cta = owner(s.tile * KB);
+            s.last_cta = owner(s.tile * KB + KB - 1);
             g += s.kb1 - s.kb0;
             return true;
         }
@@ -171,7 +173,7 @@ struct SegIter {
     }
     // partial-accumulator slot of CTA cc's piece of `tile` (0: its first segment)
     __device__ int slot(int cc, int tile) const {
-        return (int)(range_begin(cc) / KB) == tile ? 0 : 1;
+        return range_begin(cc) / KB == tile ? 0 : 1;
     }
 };
 
