@@ -470,7 +470,9 @@ def run_e2e(args, cfg, layer, tk, S, K, W, world, dev):
     return {"value": round(world * K * cfg.T / (ms * 1e-3), 1), "unit": UNIT,
             "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
             "d2h_bytes_per_step": cfg.T * cfg.H * 4,
-            "path": "moe_forward_host (pinned host in/out, CUDA graphs)"}
+            "path": ("moe_forward_host (pinned host in/out, CUDA graphs; one token: the decode kernel "
+                     "reads x and logits and writes out in mapped host memory, no copy nodes)"
+                     if cfg.T == 1 else "moe_forward_host (pinned host in/out, CUDA graphs)")}
 
 
 # ------------------------------------------------------------- CPU oracle --

@@ -44,6 +44,19 @@ Sizes sizes_of(const moe_config& c) {
     return z;
 }
 
+// Device address of page-locked (mapped) host memory; false for device or
+// pageable memory.
+bool mapped_host(const void* p, const void** dp) {
+    cudaPointerAttributes at{};
+    if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return false;
+    *dp = at.devicePointer;
+    return true;
+}
+
 const char* check_config(const moe_config* c) {
     if (!c) return "config is NULL";
     if (c->hidden <= 0 || c->hidden % 128) return "hidden must be a positive multiple of 128";
@@ -417,6 +430,21 @@ moe_status moe_forward_host(moe_layer* L, const uint16_t* x, const float* logits
     if (!x || !logits || !out) return fail(L, MOE_ERR_INVALID_ARG, "NULL pointer");
     if (moe_status st = check_T(L, T)) return st;
     cudaStream_t s = (cudaStream_t)stream;
+    // one token on the one-kernel decode path with page-locked buffers: the
+    // kernel reads x and the logits and writes out in host memory directly
+    // (mapped), so no copy is enqueued at all
+    if (L->gemm_path == 0 && L->tc != nullptr && T == 1 && moe::decode_supported(L)) {
+        const void *dx = nullptr, *dl = nullptr, *dout = nullptr;
+        if (mapped_host(x, &dx) && mapped_host(logits, &dl) && mapped_host(out, &dout) && aligned(dx, 16) &&
+            aligned(dout, 16)) {
+            L->stage_ev_set = 0;
+            cudaError_t e = moe::launch_decode(L, static_cast<const float*>(dl), static_cast<const uint16_t*>(dx),
+                                               L->ids_stage, L->w_stage, static_cast<float*>(const_cast<void*>(dout)),
+                                               s);
+            L->trace = nullptr;
+            return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward_host");
+        }
+    }
     const size_t H = L->cfg.hidden, E = L->cfg.n_experts;
     cudaError_t e = cudaMemcpyAsync(L->x_stage, x, (size_t)T * H * 2, cudaMemcpyHostToDevice, s);
     if (e == cudaSuccess)

@@ -123,3 +123,50 @@ def test_decode_kernel_unroutable_token(tiny_layer):
     # the layer stays usable
     tk = G.tokens(0, n=1)
     _check_token(cfg, wts, layer, tk, 0)
+
+
+def test_decode_host_entry_zero_copy_and_staged(decode_layer):
+    """moe_forward_host for one token: page-locked buffers are read and
+    written in place by the decode kernel (one launch, no copies), pageable
+    buffers go through the staging copies; both give the device entry's
+    bytes, eagerly and replayed from a CUDA graph."""
+    cfg, wts, layer = decode_layer
+    bqe.moe_set_gemm_path(layer, 0)
+    tk = G.tokens(1, n=3)
+    for t in range(3):
+        lg, xb = tk.logits[t:t + 1].astype(np.float32), tk.x_bits[t:t + 1]
+        _, _, out_d, _ = _route_forward(layer, lg, xb, 0)
+        ref = out_d.cpu().numpy().tobytes()
+        for pinned in (True, False):
+            xh = torch.from_numpy(xb.view(np.int16).copy())
+            lh = torch.from_numpy(lg.copy())
+            oh = torch.full((1, cfg.H), 7.0, dtype=torch.float32)
+            if pinned:
+                xh, lh, oh = xh.pin_memory(), lh.pin_memory(), oh.pin_memory()
+            n0 = bqe.moe_kernel_launches(layer)
+            bqe.moe_forward_host(layer, xh, lh, oh)
+            torch.cuda.synchronize()
+            bqe.moe_check(layer)
+            assert bqe.moe_kernel_launches(layer) - n0 == 1
+            assert oh.numpy().tobytes() == ref, pinned
+    # graph of the zero-copy call: new host inputs written between replays
+    xh = torch.zeros((1, cfg.H), dtype=torch.int16).pin_memory()
+    lh = torch.zeros((1, cfg.E), dtype=torch.float32).pin_memory()
+    oh = torch.zeros((1, cfg.H), dtype=torch.float32).pin_memory()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        bqe.moe_forward_host(layer, xh, lh, oh)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            bqe.moe_forward_host(layer, xh, lh, oh)
+    for t in range(3):
+        lg, xb = tk.logits[t:t + 1].astype(np.float32), tk.x_bits[t:t + 1]
+        xh.copy_(torch.from_numpy(xb.view(np.int16).copy()))
+        lh.copy_(torch.from_numpy(lg.copy()))
+        oh.fill_(7.0)
+        g.replay()
+        torch.cuda.synchronize()
+        bqe.moe_check(layer)
+        _, _, out_d, _ = _route_forward(layer, lg, xb, 0)
+        assert oh.numpy().tobytes() == out_d.cpu().numpy().tobytes()
