@@ -182,6 +182,49 @@ int orc_route_learned(const float* logits, int T, int E, int k, double w_scale,
     return 0;
 }
 
+/* Tail pruning of a learned routing with variance-preserving rescaling
+ * (guide, section 3.2 item 3: top-k below 6 and the adaptive tail with
+ * L2-quadrature rescaling, and the general factor alpha_gen(rho); RFC on CPU
+ * kernels, item 5: adaptive pruning below a weight threshold).
+ *
+ * For each token, in router order (descending score): expert 0 is kept;
+ * expert j >= 1 is kept while j < keep and w_j >= min_w -- the first one that
+ * fails ends the kept prefix of length m.  With
+ *   A = (1 - rho) * sum_{j<k} w_j^2 + rho * (sum_{j<k} w_j)^2,
+ *   B = (1 - rho) * sum_{j<m} w_j^2 + rho * (sum_{j<m} w_j)^2,
+ * the kept weights become sqrt(A / B) * w_j (rho = 0: the L2 factor, which
+ * keeps the sum of squares; rho = 1: the linear L1 factor, which keeps the
+ * sum); the pruned slots become id -1, weight 0.  In place on [T][k].      */
+int orc_route_prune(int32_t* ids, double* w, int T, int k, int keep, double min_w, double rho) {
+    if (k < 1 || keep < 1 || !(rho >= 0.0 && rho <= 1.0)) return 1;
+    for (int t = 0; t < T; ++t) {
+        int32_t* id = ids + (size_t)t * k;
+        double* wt = w + (size_t)t * k;
+        int m = 1;
+        while (m < k && m < keep && wt[m] >= min_w) ++m;
+        if (m == k) continue;
+        double s1a = 0.0, s2a = 0.0, s1k = 0.0, s2k = 0.0;
+        for (int j = 0; j < k; ++j) {
+            s1a += wt[j];
+            s2a += wt[j] * wt[j];
+            if (j < m) {
+                s1k += wt[j];
+                s2k += wt[j] * wt[j];
+            }
+        }
+        double alpha = sqrt(((1.0 - rho) * s2a + rho * s1a * s1a) / ((1.0 - rho) * s2k + rho * s1k * s1k));
+        for (int j = 0; j < k; ++j) {
+            if (j < m) {
+                wt[j] *= alpha;
+            } else {
+                id[j] = -1;
+                wt[j] = 0.0;
+            }
+        }
+    }
+    return 0;
+}
+
 /* Hash router: ids[t] = tid2eid[token_ids[t]] (table order), w = w_scale/k. */
 int orc_route_hash(const int32_t* token_ids, int T, const int32_t* tid2eid, int V, int k,
                    double w_scale, int32_t* ids, double* w) {
@@ -201,13 +244,16 @@ int orc_route_hash(const int32_t* token_ids, int T, const int32_t* tid2eid, int 
 /* ------------------------------------------------------------------------ */
 
 /* Stable counting sort of the rows r = t*k + j by expert ids[r]:
- * offsets[e] = number of rows with expert < e (offsets[E] = T*k);
- * row_src[p] = the row placed at position p; row_dst[r] = its position.  */
+ * offsets[e] = number of rows with expert < e (offsets[E] = the number of
+ * rows placed); row_src[p] = the row placed at position p; row_dst[r] = its
+ * position.  An id of -1 is an empty slot (a pruned expert): its row is not
+ * placed and row_dst[r] = -1.                                              */
 int orc_permute(const int32_t* ids, int T, int k, int E,
                 int32_t* offsets, int32_t* row_src, int32_t* row_dst) {
     int R = T * k;
     for (int e = 0; e <= E; ++e) offsets[e] = 0;
     for (int r = 0; r < R; ++r) {
+        if (ids[r] == -1) continue;
         if (ids[r] < 0 || ids[r] >= E) return 1;
         offsets[ids[r] + 1] += 1;
     }
@@ -216,6 +262,10 @@ int orc_permute(const int32_t* ids, int T, int k, int E,
     if (!cursor) return 2;
     for (int e = 0; e < E; ++e) cursor[e] = offsets[e];
     for (int r = 0; r < R; ++r) {
+        if (ids[r] == -1) {
+            row_dst[r] = -1;
+            continue;
+        }
         int p = cursor[ids[r]]++;
         row_src[p] = r;
         row_dst[r] = p;
@@ -299,9 +349,11 @@ static void expert_ffn(const orc_layer* L, int e, const double* xd, double* hbuf
 
 /* Forward of the tokens listed in tok[0..n) of a batch of T tokens:
  * out[i][H] = sum over the token's k routed experts in ascending expert
- * order of w * expert(x) (+ the shared expert, if present, unweighted).
+ * order of w * expert(x) (+ the shared expert, if present, unweighted); an
+ * id of -1 is an empty slot (a pruned expert) and adds nothing.
  * hq_out [n][k][I] / hs_out [n][k][I/32] (optional) receive the MXFP8 bytes
- * of h for the routed experts, in the token's own (j) order.               */
+ * of h for the routed experts, in the token's own (j) order (zero for an
+ * empty slot).                                                             */
 int orc_layer_forward(const orc_layer* L, const uint16_t* x, const int32_t* ids,
                       const double* w, int T, const int32_t* tok, int n, double* out,
                       uint8_t* hq_out, uint8_t* hs_out) {
@@ -312,7 +364,7 @@ int orc_layer_forward(const orc_layer* L, const uint16_t* x, const int32_t* ids,
         if (tok[i] < 0 || tok[i] >= T) return 1;
         for (int j = 0; j < k; ++j) {
             int e = ids[(size_t)tok[i] * k + j];
-            if (e < 0 || e >= E) return 1;
+            if (e != -1 && (e < 0 || e >= E)) return 1;
         }
     }
     int status = 0;
@@ -345,6 +397,11 @@ int orc_layer_forward(const orc_layer* L, const uint16_t* x, const int32_t* ids,
             for (int a = 0; a < k; ++a) {
                 int j = order[a];
                 int e = ids[(size_t)t * k + j];
+                if (e == -1) {
+                    if (hq_out) memset(hq_out + ((size_t)i * k + j) * I, 0, (size_t)I);
+                    if (hs_out) memset(hs_out + ((size_t)i * k + j) * (I / 32), 0, (size_t)I / 32);
+                    continue;
+                }
                 expert_ffn(L, e, xd, hbuf, hq, hs, y);
                 double wt = w[(size_t)t * k + j];
                 for (int c = 0; c < H; ++c) o[c] += wt * y[c];

@@ -70,6 +70,7 @@ def lib():
             L.orc_mxfp8_quantize.argtypes = [f64p, C.c_int, u8p, u8p]
             L.orc_quantize_bf16.argtypes = [u16p, C.c_int, C.c_int, u8p, u8p]
             L.orc_route_learned.argtypes = [f32p, C.c_int, C.c_int, C.c_int, C.c_double, i32p, f64p]
+            L.orc_route_prune.argtypes = [i32p, f64p, C.c_int, C.c_int, C.c_int, C.c_double, C.c_double]
             L.orc_route_hash.argtypes = [i32p, C.c_int, i32p, C.c_int, C.c_int, C.c_double, i32p, f64p]
             L.orc_permute.argtypes = [i32p, C.c_int, C.c_int, C.c_int, i32p, i32p, i32p]
             L.orc_layer_forward.argtypes = [C.POINTER(OrcLayer), u16p, i32p, f64p, C.c_int, i32p,
@@ -128,6 +129,19 @@ def route_learned(logits: np.ndarray, k: int, w_scale: float = 1.5):
     w = np.empty((T, k), np.float64)
     if lib().orc_route_learned(lg, T, E, k, float(w_scale), ids, w):
         raise ValueError("orc_route_learned failed")
+    return ids, w
+
+
+def route_prune(ids: np.ndarray, w: np.ndarray, keep: int, min_w: float = 0.0, rho: float = 0.0):
+    """Tail pruning of a learned routing (moe_oracle.c: orc_route_prune) on
+    copies of ids [T][k] / w [T][k]: kept prefix rescaled by
+    sqrt(((1-rho) S2_all + rho S1_all^2) / ((1-rho) S2_kept + rho S1_kept^2)),
+    pruned slots id -1, weight 0."""
+    ids = np.array(ids, dtype=np.int32, order="C", copy=True)
+    w = np.array(w, dtype=np.float64, order="C", copy=True)
+    T, k = ids.shape
+    if lib().orc_route_prune(ids, w, T, k, int(keep), float(min_w), float(rho)):
+        raise ValueError("orc_route_prune: bad arguments")
     return ids, w
 
 
