@@ -50,7 +50,14 @@ def parse():
                     help="after timing, trace one more call of the GEMM kernels (stderr)")
     ap.add_argument("--experts", type=int, default=None,
                     help="a smaller expert set with the same per-token work (for profiler captures)")
-    return ap.parse_args()
+    ap.add_argument("--prune", default=None, metavar="KEEP[,MIN_W[,RHO]]",
+                    help="tail pruning of the learned router (moe_set_route_prune), e.g. 5 or 6,0.11")
+    args = ap.parse_args()
+    args.prune_t = None
+    if args.prune:
+        v = args.prune.split(",")
+        args.prune_t = (int(v[0]), float(v[1]) if len(v) > 1 else 0.0, float(v[2]) if len(v) > 2 else 0.0)
+    return args
 
 
 def default_steps(cfg):
@@ -64,7 +71,9 @@ def config_json(cfg, args, world):
             "shared_expert": cfg.shared, "weights": "MXFP4 e2m1 + UE8M0 /32",
             "activations": "MXFP8 e4m3 + UE8M0 /32", "gemm_path": args.path,
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
-            "l2": "inputs larger than L2 (3.4 GB expert set; fresh tokens each step)"}
+            "l2": "inputs larger than L2 (3.4 GB expert set; fresh tokens each step)",
+            **({"route_prune": {"keep": args.prune_t[0], "min_w": args.prune_t[1], "rho": args.prune_t[2]}}
+               if args.prune_t else {})}
 
 
 def algorithmic_bytes(cfg, touched, rows):
@@ -160,6 +169,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     layer = bqe.moe_create(mc, dw)
     del dw
     bqe.moe_set_gemm_path(layer, {"auto": 0, "cc": 1, "tc": 2}[args.path])
+    if args.prune_t:
+        bqe.moe_set_route_prune(layer, *args.prune_t)
 
     # distinct inputs: one token per step for decode, else a few batches cycled
     S = (K + W) if cfg.T == 1 else min(K + W, 4)
@@ -183,11 +194,14 @@ def run_ours(args, cfg, rank, world, local_rank):
             bqe.moe_route_forward(layer, lg_all[j], x_all[j], ids, wt, out)
 
     # experts touched per input batch (for the algorithmic byte count)
-    touched, rows = [], cfg.T * cfg.k
+    touched, kept = [], []
     for j in range(min(S, 64)):
         step(j)
-        touched.append(len(np.unique(ids.cpu().numpy())))
+        idn = ids.cpu().numpy()
+        touched.append(len(np.unique(idn[idn >= 0])))  # -1: a pruned slot
+        kept.append(int((idn >= 0).sum()))
     avg_touched = float(np.mean(touched))
+    rows = int(round(np.mean(kept)))
     for i in range(W):
         step(i)
     bqe.moe_check(layer)
@@ -281,7 +295,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
 
     roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": profiled_traffic(cfg, dom),
+            "frac": round(achieved / peak, 4), "traffic": None if args.prune_t else profiled_traffic(cfg, dom),
             "kernel_ms": round(kernel_ms, 6), "algorithmic_bytes_per_launch": int(byts[dom]),
             "peak_source": peak_src}
     if dom != "layer":
@@ -322,7 +336,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     if not args.no_e2e:
         res["e2e"] = run_e2e(args, cfg, layer, tk, S, K, W, world, dev)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, w, tk, args.cpu_seconds)
+        res["cpu_baseline"] = cpu_baseline(cfg, w, tk, args.cpu_seconds, args.prune_t)
     layer.close()
     if world > 1:
         dist.destroy_process_group()
@@ -476,7 +490,7 @@ def run_e2e(args, cfg, layer, tk, S, K, W, world, dev):
 
 
 # ------------------------------------------------------------- CPU oracle --
-def oracle_rate(cfg, w, tk, seconds):
+def oracle_rate(cfg, w, tk, seconds, prune=None):
     """Tokens/s of the fp64 oracle (route + layer) on the host cores, on a
     sample sized to about `seconds` of work."""
     from oracle import oracle as orc
@@ -491,6 +505,8 @@ def oracle_rate(cfg, w, tk, seconds):
         lg, xb = tk.logits[:tok], tk.x_bits[:tok]
         t = time.perf_counter()
         ids, wt = orc.route_learned(lg, cfg.k, cfg.w_scale)
+        if prune:
+            ids, wt = orc.route_prune(ids, wt, *prune)
         orc.layer_forward(w, xb, ids, wt)
         return tok, time.perf_counter() - t
 
@@ -501,8 +517,8 @@ def oracle_rate(cfg, w, tk, seconds):
     return n, t, orc.max_threads(), T
 
 
-def cpu_baseline(cfg, w, tk, seconds):
-    n, t, cores, T = oracle_rate(cfg, w, tk, seconds)
+def cpu_baseline(cfg, w, tk, seconds, prune=None):
+    n, t, cores, T = oracle_rate(cfg, w, tk, seconds, prune)
     return {"value": round(n / t, 3), "unit": UNIT, "cores": cores, "kind": "oracle",
             "sample": f"{n} tokens of the {cfg.name} workload (tokens are independent; "
                       f"route + layer per token), {t:.1f} s"}
@@ -518,7 +534,7 @@ def run_reference(args, cfg, rank, world):
     w = make_weights(cfg)
     tk = make_tokens(cfg, n=min(cfg.T * (K + W), 4096) if cfg.T == 1 else cfg.T)
     budget = 60.0
-    n, t, cores, T = oracle_rate(cfg, w, tk, budget)
+    n, t, cores, T = oracle_rate(cfg, w, tk, budget, args.prune_t)
     value = n / t
     steps_done = max(1, n // cfg.T)
     res = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,

@@ -23,7 +23,8 @@ _STATUS = {1: "MOE_ERR_INVALID_ARG", 2: "MOE_ERR_UNSUPPORTED", 3: "MOE_ERR_OOM",
 EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_permute",
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
-           "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace", "moe_route_forward")
+           "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace", "moe_route_forward",
+           "moe_set_route_prune")
 
 
 class MoeError(RuntimeError):
@@ -78,6 +79,7 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_permute_noalloc": ([vp, i, i, i, vp, vp, vp, vp], i),
         "moe_set_trace": ([vp, vp, C.c_size_t], i),
         "moe_route_forward": ([vp, vp, vp, i, vp, vp, vp, vp], i),
+        "moe_set_route_prune": ([vp, i, f, f], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -189,6 +191,13 @@ def moe_destroy(layer: Layer):
 
 def moe_set_gemm_path(layer: Layer, path: int):
     _check(load_library().moe_set_gemm_path(layer.ptr, int(path)), layer.ptr)
+
+
+def moe_set_route_prune(layer: Layer, keep: int, min_w: float = 0.0, rho: float = 0.0):
+    """Tail pruning of the learned router: keep at most `keep` experts, stop at
+    the first weight below `min_w`, rescale the kept weights for correlation
+    `rho` (0: L2 quadrature, 1: linear).  keep >= k with min_w <= 0: off."""
+    _check(load_library().moe_set_route_prune(layer.ptr, int(keep), float(min_w), float(rho)), layer.ptr)
 
 
 def moe_set_stage_events(layer: Layer, events):

@@ -300,6 +300,9 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         return st;
     }
     L->gemm_path = 0;
+    L->prune_keep = L->cfg.top_k;
+    L->prune_min_w = 0.f;
+    L->prune_rho = 0.f;
     *out = L;
     return MOE_OK;
 }
@@ -338,6 +341,17 @@ moe_status moe_set_gemm_path(moe_layer* L, int path) {
     if (path < 0 || path > 2) return fail(L, MOE_ERR_INVALID_ARG, "path must be 0, 1 or 2");
     if (path == 2 && !L->tc) return fail(L, MOE_ERR_UNSUPPORTED, "tensor-core path unavailable");
     L->gemm_path = path;
+    return MOE_OK;
+}
+
+moe_status moe_set_route_prune(moe_layer* L, int keep, float min_w, float rho) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (keep < 1) return fail(L, MOE_ERR_INVALID_ARG, "keep must be >= 1");
+    if (!std::isfinite(min_w)) return fail(L, MOE_ERR_INVALID_ARG, "min_w must be finite");
+    if (!(rho >= 0.f && rho <= 1.f)) return fail(L, MOE_ERR_INVALID_ARG, "rho must be in [0, 1]");
+    L->prune_keep = keep < L->cfg.top_k ? keep : L->cfg.top_k;
+    L->prune_min_w = min_w;
+    L->prune_rho = rho;
     return MOE_OK;
 }
 

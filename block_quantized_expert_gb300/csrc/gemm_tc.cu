@@ -575,8 +575,9 @@ static_assert(kDecStageBytes % 1024 == 0, "128-byte swizzled weight tiles need 1
 struct DecArgs {
     const float* logits;  // [E]
     const uint16_t* x;    // [H] bf16
-    int E, k, H, I;
+    int E, k, H, I;       // k: the router's top-k (experts kept after pruning: DecCtx::k)
     float w_scale;
+    RoutePrune prune;
     int32_t* ids_out;     // [k]
     float* w_out;         // [k]
     float* out;           // [H]
@@ -613,6 +614,7 @@ struct DecCtx {
     uint8_t* smem;
     uint32_t bar0, tmem;
     uint32_t epoch;      // this launch's flag value
+    int k;               // the experts kept (the router's top-k after tail pruning)
     volatile int* abort_flag;
     const int* seg_e;    // [k] experts, ascending
     const int* seg_j;    // [k] their position in the router output
@@ -911,7 +913,7 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
             }
             epi_bar();
             if (lead_warp && lane == 0) flag_set(a.h_flag + gt, c.epoch);
-        } else if (s < a.k - 1) {
+        } else if (s < c.k - 1) {
             a.y[(size_t)c.seg_j[s] * a.H + f0 + col] = v;
             epi_bar();
             if (lead_warp && lane == 0) flag_set(a.y_flag + gt, c.epoch);
@@ -920,17 +922,39 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
             // ascending expert order, this tile's y from registers
             if (lead_warp) {
                 bool ok = true;
-                if (lane < a.k - 1) ok = flag_wait(a.y_flag + lane * MT + m, c.epoch, c.abort_flag);
+                if (lane < c.k - 1) ok = flag_wait(a.y_flag + lane * MT + m, c.epoch, c.abort_flag);
                 if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
             }
             epi_bar();
             float o = 0.f;
-            for (int ss = 0; ss < a.k - 1; ++ss)
+            for (int ss = 0; ss < c.k - 1; ++ss)
                 o += c.seg_w[ss] * __ldcg(a.y + (size_t)c.seg_j[ss] * a.H + f0 + col);
-            o += c.seg_w[a.k - 1] * v;
+            o += c.seg_w[c.k - 1] * v;
             a.out[f0 + col] = o;
         }
     }
+}
+
+// The routing weights of the decode token by one warp: lane j < k takes the
+// j-th selection sel[j] (router order); w_j = w_scale * s_j / (s_0 + ... +
+// s_{k-1}), s = sqrt(softplus(logit)) in fp32 (the arithmetic of
+// route_token), then the tail pruning.  Returns the kept count m (0 when the
+// token has no valid selection); lane j gets its expert and weight.
+__device__ __forceinline__ int dec_weights(const DecArgs& a, const int* sel, const float* lg, int lane, int& e,
+                                           float& wj) {
+    const int k = a.k;
+    e = lane < k ? sel[lane] : 0;
+    const bool ok = __all_sync(0xFFFFFFFFu, e >= 0);
+    float sv = 0.f;
+    if (lane < k && ok) {
+        const float l = lg[e];
+        sv = sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))));
+    }
+    float sum = 0.f;
+    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, sv, j);
+    wj = (lane < k && ok) ? a.w_scale * sv / sum : 0.0f;
+    if (!ok) return 0;
+    return prunes(a.prune, k) ? prune_tail(wj, k, a.prune, lane) : k;
 }
 
 __global__ void __launch_bounds__(kTcThreads, 1)
@@ -1086,70 +1110,75 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         // the producer starts as soon as the experts are known, on its own
         // copy of them in ascending order (the other warps still finish the
         // routing weights)
-        const int e = lane < k ? sel[lane] : 0;
-        if (__all_sync(0xFFFFFFFFu, e >= 0)) {
+        // (with a weight threshold it needs the weights to know the kept
+        // experts: it computes them itself, as warp 2 does)
+        int e = lane < k ? sel[lane] : 0;
+        int m = __all_sync(0xFFFFFFFFu, e >= 0) ? k : 0;
+        if (m > 0 && prunes(a.prune, k)) {
+            if (a.prune.min_w > 0.f) {
+                float wj;
+                m = dec_weights(a, sel, lg, lane, e, wj);
+            } else {
+                m = a.prune.keep;  // the first `keep` of the router order
+            }
+        }
+        if (m > 0) {
             int pos = 0;
-            for (int j = 0; j < k; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
-            if (lane < k) prod_e[pos] = e;
+            for (int j = 0; j < m; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
+            if (lane < m) prod_e[pos] = e;
             __syncwarp();
             DecCtx cp = c;
             cp.seg_e = prod_e;
             cp.epoch = words[2];
-            const int G = dec_groups(k);
+            cp.k = m;
+            const int G = dec_groups(m);
             // it runs through all phases (the weights do not depend on h),
             // fetching each group's h before that group's down weights
             bool ok = true;
-            for (int g = 0; g < G && ok; ++g) ok = dec_produce<true>(a, cp, &tmGU, dec_phase(k, false, g), stage, phase, lane);
+            for (int g = 0; g < G && ok; ++g) ok = dec_produce<true>(a, cp, &tmGU, dec_phase(m, false, g), stage, phase, lane);
             for (int g = 0; g < G && ok; ++g) {
-                const DecPhase ph = dec_phase(k, true, g);
+                const DecPhase ph = dec_phase(m, true, g);
                 ok = dec_fetch_h(a, cp, ph, g, lane) && dec_produce<false>(a, cp, &tmDN, ph, stage, phase, lane);
             }
         }
     } else {
         if (warp == 2) {
-            // routing weights: lane j < k takes the j-th selection; w_j =
-            // w_scale * s_j / (s_0 + ... + s_{k-1}), s = sqrt(softplus(logit)), in fp32
-            const int e = lane < k ? sel[lane] : 0;
-            const bool ok = __all_sync(0xFFFFFFFFu, e >= 0);
-            float sv = 0.f;
-            if (lane < k && ok) {
-                const float l = lg[e];
-                sv = sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))));
-            }
-            float sum = 0.f;
-            for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, sv, j);
-            const float wj = ok ? a.w_scale * sv / sum : 0.0f;
+            int e;
+            float wj;
+            const int m = dec_weights(a, sel, lg, lane, e, wj);
             if (lane < k && blockIdx.x == 0) {
-                a.ids_out[lane] = ok ? e : -1;
+                a.ids_out[lane] = lane < m ? e : -1;  // pruned slots: -1, weight 0
                 a.w_out[lane] = wj;
             }
-            // position in ascending expert order (the combine order; ids are distinct)
+            // position among the kept experts in ascending expert order (the
+            // combine order; ids are distinct)
             int pos = 0;
-            for (int j = 0; j < k; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
-            if (lane < k) {
+            for (int j = 0; j < m; ++j) pos += (__shfl_sync(0xFFFFFFFFu, e, j) < e) ? 1 : 0;
+            if (lane < m) {
                 seg_e[pos] = e;
                 seg_w[pos] = wj;
                 seg_j[pos] = lane;
             }
             if (lane == 0) {
-                if (!ok && blockIdx.x == 0) raise_flag(a.err, ERR_BAD_ID);
-                *routed_flag = ok;
+                if (m == 0 && blockIdx.x == 0) raise_flag(a.err, ERR_BAD_ID);
+                *routed_flag = m;
             }
         }
         __syncwarp();
         work_bar();  // the routing of warps 1-9 (the producer is on its way)
         c.epoch = words[2];
+        c.k = *routed_flag;
         if (trc && threadIdx.x == 32) trc[9] = globaltimer();
-        if (*routed_flag) {
-            const int G = dec_groups(k);
+        if (c.k > 0) {
+            const int G = dec_groups(c.k);
             bool ok = true;
             for (int g = 0; g < G; ++g) {
-                const DecPhase ph = dec_phase(k, false, g);
+                const DecPhase ph = dec_phase(c.k, false, g);
                 if (warp == 1) ok = ok && dec_mma<true>(a, c, ph, g, stage, phase, acc_phase, lane);
                 else dec_epilogue<true>(a, c, ph, acc_phase);
             }
             for (int g = 0; g < G; ++g) {
-                const DecPhase ph = dec_phase(k, true, g);
+                const DecPhase ph = dec_phase(c.k, true, g);
                 if (warp == 1) ok = ok && !*c.abort_flag && dec_mma<false>(a, c, ph, g, stage, phase, acc_phase, lane);
                 else dec_epilogue<false>(a, c, ph, acc_phase);
             }
@@ -1380,6 +1409,7 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     a.H = L->cfg.hidden;
     a.I = L->cfg.inter;
     a.w_scale = L->cfg.w_scale;
+    a.prune = RoutePrune{L->prune_keep, L->prune_min_w, L->prune_rho};
     a.ids_out = ids;
     a.w_out = w;
     a.out = out;
@@ -1401,7 +1431,7 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     cfg.blockDim = dim3(kTcThreads);
     cfg.dynamicSmemBytes = kDecSmem;
     cfg.stream = s;
-    // cooperative (all CTAs co-resident for the grid barrier) and
+    // cooperative (all CTAs co-resident for the waits on each other's flags) and
     // programmatic dependent launch: a CTA takes its SM as soon as the
     // previous kernel's CTA there exits, runs its prologue and waits in
     // griddepcontrol.wait for that kernel's completion

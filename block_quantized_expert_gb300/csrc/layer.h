@@ -14,6 +14,9 @@ struct moe_layer {
     int device;
     int num_sms;
     int gemm_path;  // 0 auto, 1 CUDA cores, 2 tcgen05
+    // tail pruning of the learned routing (keep = top_k, min_w = 0: none)
+    int prune_keep;
+    float prune_min_w, prune_rho;
 
     // -------- weights (library-owned copies) --------
     // gate/up codes interleaved per 128 features: [E][I/128][gate 128 rows, up 128 rows][H/2],

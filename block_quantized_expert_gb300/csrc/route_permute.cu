@@ -12,14 +12,20 @@
 namespace moe {
 
 __global__ void __launch_bounds__(256) k_route(const float* __restrict__ logits, int T, int E,
-                                               int k, float w_scale, int32_t* __restrict__ ids,
-                                               float* __restrict__ w, uint32_t* err) {
+                                               int k, float w_scale, RoutePrune prune,
+                                               int32_t* __restrict__ ids, float* __restrict__ w,
+                                               uint32_t* err) {
     pdl_launch_dependents();
     pdl_wait();
     const int t = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (t >= T) return;
-    route_token(logits + (size_t)t * E, E, k, w_scale, ids + (size_t)t * k, w + (size_t)t * k, err, lane);
+    route_token(logits + (size_t)t * E, E, k, w_scale, prune, ids + (size_t)t * k, w + (size_t)t * k, err,
+                lane);
+}
+
+static RoutePrune route_prune_of(const moe_layer* L) {
+    return RoutePrune{L->prune_keep, L->prune_min_w, L->prune_rho};
 }
 
 cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids, float* w,
@@ -28,7 +34,7 @@ cudaError_t launch_route(moe_layer* L, const float* logits, int T, int32_t* ids,
     dim3 grid((T + warps_per_block - 1) / warps_per_block);
     L->launches += 1;
     return launch_pdl(k_route, grid, dim3(32 * warps_per_block), 0, s, logits, T, L->cfg.n_experts,
-                      L->cfg.top_k, L->cfg.w_scale, ids, w, L->d_err);
+                      L->cfg.top_k, L->cfg.w_scale, route_prune_of(L), ids, w, L->d_err);
 }
 
 // Hash-routed layers (guide, section 1: tid2eid maps a token id to its k
@@ -121,7 +127,7 @@ __device__ void permute_body(
     for (int r = tid; r < R; r += 1024) {
         int e = ids[r];
         if (e >= 0 && e < E) atomicAdd(&cnt[e], 1);
-        else bad = 1;
+        else if (e != -1) bad = 1;  // -1: an empty slot (pruned expert), left out quietly
     }
     __syncthreads();
 
@@ -313,7 +319,8 @@ __global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x
 // token), the counting sort and the quantisation, each phase after a barrier.
 // Saves two kernel boundaries on the decode path.
 __global__ void __launch_bounds__(1024) k_front(
-    const float* __restrict__ logits, float w_scale, int32_t* __restrict__ ids, float* __restrict__ wts,
+    const float* __restrict__ logits, float w_scale, RoutePrune prune, int32_t* __restrict__ ids,
+    float* __restrict__ wts,
     const uint16_t* __restrict__ x, int T, int k, int E, int H, QuantDst qd, int32_t* __restrict__ offsets,
     int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
     int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan, int32_t* __restrict__ chunk_scan,
@@ -328,7 +335,7 @@ __global__ void __launch_bounds__(1024) k_front(
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (logits) {
         if (warp < T)
-            route_token(logits + (size_t)warp * E, E, k, w_scale, ids + (size_t)warp * k,
+            route_token(logits + (size_t)warp * E, E, k, w_scale, prune, ids + (size_t)warp * k,
                         wts + (size_t)warp * k, err, lane);
         __syncthreads();
     }
@@ -374,7 +381,8 @@ cudaError_t launch_front(moe_layer* L, const float* logits, int32_t* ids, float*
     }
     const size_t smem = (size_t)48 * L->cfg.n_experts;
     L->launches += 1;
-    return launch_pdl(k_front, dim3(1), dim3(1024), smem, s, logits, L->cfg.w_scale, ids, w, x, T,
+    return launch_pdl(k_front, dim3(1), dim3(1024), smem, s, logits, L->cfg.w_scale, route_prune_of(L), ids, w,
+                      x, T,
                       L->cfg.top_k, L->cfg.n_experts, L->cfg.hidden, d, L->offsets, L->row_src, L->row_dst,
                       L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
                       L->cfg.has_shared ? L->sh_desc : nullptr, L->d_err, L->sk_counters,

@@ -106,7 +106,11 @@ moe_status moe_destroy(moe_layer* layer);
  *   ids     device i32 [T][k]  experts by descending score s = sqrt(softplus
  *           (logit)); equal scores go to the lower expert index
  *   w       device f32 [T][k]  w_j = w_scale * s_j / sum of the k scores
- * 1 <= T <= max_tokens.  The top-k is plain (one expert group).             */
+ * 1 <= T <= max_tokens.  The top-k is plain (one expert group).  With tail
+ * pruning set (moe_set_route_prune) the pruned slots of a token come last
+ * with id -1 and weight 0, and the kept weights are rescaled.  A token with
+ * no valid selection (e.g. NaN logits) gets ids -1 and raises the device
+ * flag.                                                                     */
 moe_status moe_route(moe_layer* layer, const float* logits, int T, int32_t* ids, float* w,
                      moe_stream_t stream);
 
@@ -121,12 +125,13 @@ moe_status moe_route_hash(moe_layer* layer, const int32_t* token_ids, const int3
 
 /* Token -> expert grouping (the grouping MUL_MAT_ID does; guide, section 2):
  * a stable counting sort of the rows r = t*k + j by expert ids[r].
- *   ids      device i32 [T][k], values in [0, E)
+ *   ids      device i32 [T][k], values in [0, E), or -1 for an empty slot
  *   offsets  device i32 [E+1]  offsets[e] = rows with expert < e
  *   row_src  device i32 [T*k]  row placed at sorted position p (ascending r
- *            within an expert's segment)
+ *            within an expert's segment); entries past offsets[E] unused
  *   row_dst  device i32 [T*k]  inverse: sorted position of row r
- * Ids outside [0, E) are left out (row_dst = -1) and raise the device flag. */
+ * An id of -1 (a pruned expert) is left out quietly (row_dst = -1); other
+ * ids outside [0, E) are left out and raise the device flag.               */
 moe_status moe_permute(moe_layer* layer, const int32_t* ids, int T, int32_t* offsets,
                        int32_t* row_src, int32_t* row_dst, moe_stream_t stream);
 
@@ -140,7 +145,8 @@ moe_status moe_quantize(moe_layer* layer, const uint16_t* x, int T, uint8_t* q, 
 /* The layer: permute, quantise, SwiGLU gate/up with MXFP8 requantisation of
  * h, down projection, and the weighted combine in ascending expert order,
  * plus the shared expert when present.
- *   x    device u16 [T][H] bf16;  ids device i32 [T][k] in [0, E);
+ *   x    device u16 [T][H] bf16;  ids device i32 [T][k] in [0, E), or -1
+ *        for an empty slot, which adds nothing;
  *   w    device f32 [T][k];       out device f32 [T][H] (overwritten).     */
 moe_status moe_forward(moe_layer* layer, const uint16_t* x, int T, const int32_t* ids,
                        const float* w, float* out, moe_stream_t stream);
@@ -214,6 +220,24 @@ unsigned long long moe_kernel_launches(const moe_layer* layer);
  * kernels only (never the decode kernel).  All compute the same layer; the
  * choice only affects speed and the order of fp32 additions.               */
 moe_status moe_set_gemm_path(moe_layer* layer, int path);
+
+/* Tail pruning of the learned router (guide, section 3.2 item 3: top-k
+ * below the layer's k and the adaptive tail, with L2-quadrature rescaling;
+ * RFC on CPU kernels, item 5: dropping experts under a weight threshold).
+ * Applies to moe_route, moe_route_forward and moe_forward_host from the
+ * next call on; the hash router is never pruned.  Per token, in router
+ * order: expert 0 is kept; expert j >= 1 while j < keep and w_j >= min_w
+ * (the first that fails ends the kept prefix of m experts).  The kept
+ * weights are multiplied by
+ *   sqrt(((1 - rho) S2 + rho S1^2) / ((1 - rho) S2' + rho S1'^2)),
+ * S1, S2 = sum of w and of w^2 over all k, S1', S2' over the kept experts:
+ * rho = 0 keeps the sum of squares (orthogonal expert outputs), rho = 1
+ * the sum (linear rescaling).  The pruned slots get id -1 and weight 0 and
+ * their experts' weights are never read.
+ *   1 <= keep (keep >= k: no count limit); min_w finite (<= 0: no
+ *   threshold); 0 <= rho <= 1.  keep >= k with min_w <= 0 turns it off (the
+ *   default).  MOE_ERR_INVALID_ARG otherwise, the setting unchanged.       */
+moe_status moe_set_route_prune(moe_layer* layer, int keep, float min_w, float rho);
 
 /* Token -> expert grouping without a layer and without any allocation.
  * The paper has no counterpart: this entry point exists for callers that

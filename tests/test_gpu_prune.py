@@ -1,0 +1,157 @@
+"""Routed-expert tail pruning on the GPU (moe_set_route_prune) against the
+fp64 oracle: the router's kept experts and rescaled weights, the grouping
+with empty slots, the grouped tensor-core and CUDA-core layer, and the
+whole-layer decode kernel.
+
+DeepSeek-V4-Flash guide, section 3.2 item 3 (top-5 / adaptive tail with
+L2-quadrature rescaling, alpha_gen(rho)); RFC on CPU kernels, item 5."""
+import numpy as np
+import pytest
+import torch
+
+import block_quantized_expert_gb300 as bqe
+from oracle import oracle as orc
+from tests import _gpu as G
+from workloads import CONFIGS
+from workloads.generate import make_hash_table
+
+pytestmark = pytest.mark.gpu
+
+# (keep, min_w, rho): top-5 and top-4 in quadrature, the guide's adaptive
+# tail (min_w = 0.11), a correlated factor, a linear factor with a threshold
+SETTINGS = [(5, 0.0, 0.0), (4, 0.0, 0.0), (6, 0.11, 0.0), (6, 0.2, 0.3), (3, 0.15, 1.0)]
+W_TOL = 32 * 2.0 ** -24  # relative to w_scale: fp32 weights, then one fp32 factor
+
+
+@pytest.fixture(scope="module")
+def decode_layer():
+    cfg = CONFIGS[1]
+    w = G.weights_np(1)
+    layer = G.make_layer(cfg, w, max_tokens=64)
+    yield cfg, w, layer
+    bqe.moe_set_route_prune(layer, cfg.k)
+
+
+def _oracle(lg, cfg, setting):
+    ids, w = orc.route_learned(lg, cfg.k, cfg.w_scale)
+    keep, min_w, rho = setting
+    pid, pw = orc.route_prune(ids, w, keep, min_w, rho)
+    # tokens whose keep decision sits within fp32 reach of the threshold are
+    # not compared (the decision is taken in fp32 on the GPU, fp64 here)
+    clear = (np.abs(w - min_w) > 1e-5).all(axis=1) if min_w > 0 else np.ones(len(w), bool)
+    return pid, pw, clear
+
+
+@pytest.mark.parametrize("setting", SETTINGS)
+@pytest.mark.parametrize("cfg_id,n", [(1, 256), (3, 512)])
+def test_route_prune_matches_oracle(decode_layer, setting, cfg_id, n):
+    cfg, _, layer = decode_layer
+    lg = G.tokens(cfg_id, n=n).logits[:64]
+    bqe.moe_set_route_prune(layer, *setting)
+    ids, w = G.route_dev(layer, lg, cfg.k)
+    bqe.moe_check(layer)  # empty slots raise nothing
+    pid, pw, clear = _oracle(lg, cfg, setting)
+    assert clear.mean() > 0.8
+    got_i, got_w = ids.cpu().numpy(), w.cpu().numpy()
+    assert np.array_equal(got_i[clear], pid[clear])
+    assert np.abs(got_w[clear] - pw[clear]).max() <= W_TOL * cfg.w_scale
+    assert (got_w[got_i < 0] == 0).all()
+    assert (pid[clear] < 0).any() or setting[1] > 0  # the count limits prune something
+
+
+def test_permute_with_empty_slots(decode_layer):
+    cfg, _, layer = decode_layer
+    lg = G.tokens(1, n=64).logits
+    bqe.moe_set_route_prune(layer, 6, 0.2, 0.0)
+    ids, _ = G.route_dev(layer, lg, cfg.k)
+    off = torch.empty(cfg.E + 1, dtype=torch.int32, device=G.DEV)
+    src = torch.empty(64 * cfg.k, dtype=torch.int32, device=G.DEV)
+    dst = torch.empty(64 * cfg.k, dtype=torch.int32, device=G.DEV)
+    bqe.moe_permute(layer, ids, off, src, dst)
+    bqe.moe_check(layer)
+    ro, rs, rd = orc.permute(ids.cpu().numpy(), cfg.E)
+    n = int(ro[-1])
+    assert n < 64 * cfg.k
+    assert np.array_equal(off.cpu().numpy(), ro)
+    assert np.array_equal(src.cpu().numpy()[:n], rs[:n])
+    assert np.array_equal(dst.cpu().numpy(), rd)
+
+
+@pytest.mark.parametrize("path", [0, 1, 2])
+@pytest.mark.parametrize("T", [1, 32])
+def test_layer_with_pruned_routing(decode_layer, path, T):
+    """moe_route_forward with pruning on every GEMM path (T = 1 on the
+    automatic path is the decode kernel) against the oracle on the same
+    (GPU-chosen, oracle-checked) routing."""
+    cfg, wts, layer = decode_layer
+    bqe.moe_set_gemm_path(layer, path)
+    tk = G.tokens(1, n=T)
+    for setting in ((5, 0.0, 0.0), (6, 0.2, 0.3)):
+        bqe.moe_set_route_prune(layer, *setting)
+        ids = torch.empty((T, cfg.k), dtype=torch.int32, device=G.DEV)
+        w = torch.empty((T, cfg.k), dtype=torch.float32, device=G.DEV)
+        out = torch.empty((T, cfg.H), dtype=torch.float32, device=G.DEV)
+        n0 = bqe.moe_kernel_launches(layer)
+        bqe.moe_route_forward(layer, G.to_dev(tk.logits.astype(np.float32)),
+                              G.to_dev(tk.x_bits.astype(np.uint16), torch.int16), ids, w, out)
+        bqe.moe_check(layer)
+        if path == 0 and T == 1:
+            assert bqe.moe_kernel_launches(layer) - n0 == 1
+        pid, pw, clear = _oracle(tk.logits, cfg, setting)
+        gi, gw = ids.cpu().numpy(), w.cpu().numpy()
+        assert np.array_equal(gi[clear], pid[clear])
+        assert np.abs(gw[clear] - pw[clear]).max() <= W_TOL * cfg.w_scale
+        ref = orc.layer_forward(wts, tk.x_bits, gi, gw.astype(np.float64))
+        norm, elem = G.compare_out(out.cpu().numpy(), ref)
+        assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (setting, norm, elem)
+    bqe.moe_set_route_prune(layer, cfg.k)
+    bqe.moe_set_gemm_path(layer, 0)
+
+
+def test_decode_kernel_pruned_equals_grouped(decode_layer):
+    """The decode kernel and the grouped tcgen05 kernels choose the same
+    experts and weights bit for bit under pruning."""
+    cfg, wts, layer = decode_layer
+    tk = G.tokens(1, n=6)
+    for setting in SETTINGS:
+        bqe.moe_set_route_prune(layer, *setting)
+        for t in range(6):
+            res = []
+            for path in (0, 2):
+                bqe.moe_set_gemm_path(layer, path)
+                ids = torch.empty((1, cfg.k), dtype=torch.int32, device=G.DEV)
+                w = torch.empty((1, cfg.k), dtype=torch.float32, device=G.DEV)
+                out = torch.empty((1, cfg.H), dtype=torch.float32, device=G.DEV)
+                bqe.moe_route_forward(layer, G.to_dev(tk.logits[t:t + 1].astype(np.float32)),
+                                      G.to_dev(tk.x_bits[t:t + 1].astype(np.uint16), torch.int16), ids, w, out)
+                bqe.moe_check(layer)
+                res.append((ids, w, out.cpu().numpy().astype(np.float64)))
+            assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+            o1, o2 = res[0][2], res[1][2]
+            assert np.linalg.norm(o1 - o2) <= G.NORM_TOL * np.linalg.norm(o2)
+    bqe.moe_set_route_prune(layer, cfg.k)
+    bqe.moe_set_gemm_path(layer, 0)
+
+
+def test_hash_route_is_never_pruned(decode_layer):
+    cfg, _, layer = decode_layer
+    bqe.moe_set_route_prune(layer, 2, 0.3, 0.0)
+    tk = G.tokens(2, n=32)
+    ids = torch.empty((32, cfg.k), dtype=torch.int32, device=G.DEV)
+    w = torch.empty((32, cfg.k), dtype=torch.float32, device=G.DEV)
+    tab = make_hash_table(CONFIGS[2])
+    bqe.moe_route_hash(layer, G.to_dev(tk.token_ids), G.to_dev(tab), ids, w)
+    bqe.moe_check(layer)
+    assert (ids.cpu().numpy() >= 0).all()
+    assert (w.cpu().numpy() == np.float32(cfg.w_scale / cfg.k)).all()
+    bqe.moe_set_route_prune(layer, cfg.k)
+
+
+def test_prune_setter_validates(decode_layer):
+    cfg, _, layer = decode_layer
+    for bad in ((0, 0.0, 0.0), (5, float("nan"), 0.0), (5, float("inf"), 0.0), (5, 0.0, -0.1),
+                (5, 0.0, 1.5)):
+        with pytest.raises(bqe.MoeError) as ei:
+            bqe.moe_set_route_prune(layer, *bad)
+        assert ei.value.status == bqe.MOE_ERR_INVALID_ARG
+    bqe.moe_set_route_prune(layer, 99)  # more than k: no count limit
