@@ -17,9 +17,12 @@ from workloads.generate import make_hash_table
 
 pytestmark = pytest.mark.gpu
 
-# (keep, min_w, rho): top-5 and top-4 in quadrature, the guide's adaptive
-# tail (min_w = 0.11), a correlated factor, a linear factor with a threshold
-SETTINGS = [(5, 0.0, 0.0), (4, 0.0, 0.0), (6, 0.11, 0.0), (6, 0.2, 0.3), (3, 0.15, 1.0)]
+# (keep, min_w, rho): top-5 and top-4 in quadrature, adaptive tails, a
+# correlated factor, a linear factor.  The synthetic N(0, 1) logits give flat
+# weights (w_6 ~ 0.22-0.25 of w_scale 1.5, unlike the trained router's power
+# law, where the guide's min_w = 0.11 applies), so the thresholds sit inside
+# that range to prune a varying number of experts.
+SETTINGS = [(5, 0.0, 0.0), (4, 0.0, 0.0), (6, 0.24, 0.0), (6, 0.245, 0.3), (3, 0.25, 1.0)]
 W_TOL = 32 * 2.0 ** -24  # relative to w_scale: fp32 weights, then one fp32 factor
 
 
@@ -56,13 +59,14 @@ def test_route_prune_matches_oracle(decode_layer, setting, cfg_id, n):
     assert np.array_equal(got_i[clear], pid[clear])
     assert np.abs(got_w[clear] - pw[clear]).max() <= W_TOL * cfg.w_scale
     assert (got_w[got_i < 0] == 0).all()
-    assert (pid[clear] < 0).any() or setting[1] > 0  # the count limits prune something
+    assert (pid[clear] < 0).any()
+    assert (pid[clear] >= 0).sum(1).min() < (pid[clear] >= 0).sum(1).max() or setting[1] == 0
 
 
 def test_permute_with_empty_slots(decode_layer):
     cfg, _, layer = decode_layer
     lg = G.tokens(1, n=64).logits
-    bqe.moe_set_route_prune(layer, 6, 0.2, 0.0)
+    bqe.moe_set_route_prune(layer, 6, 0.245, 0.0)
     ids, _ = G.route_dev(layer, lg, cfg.k)
     off = torch.empty(cfg.E + 1, dtype=torch.int32, device=G.DEV)
     src = torch.empty(64 * cfg.k, dtype=torch.int32, device=G.DEV)
@@ -86,7 +90,7 @@ def test_layer_with_pruned_routing(decode_layer, path, T):
     cfg, wts, layer = decode_layer
     bqe.moe_set_gemm_path(layer, path)
     tk = G.tokens(1, n=T)
-    for setting in ((5, 0.0, 0.0), (6, 0.2, 0.3)):
+    for setting in ((5, 0.0, 0.0), (6, 0.245, 0.3)):
         bqe.moe_set_route_prune(layer, *setting)
         ids = torch.empty((T, cfg.k), dtype=torch.int32, device=G.DEV)
         w = torch.empty((T, cfg.k), dtype=torch.float32, device=G.DEV)
