@@ -946,13 +946,10 @@ __device__ __forceinline__ int dec_weights(const DecArgs& a, const int* sel, con
     e = lane < k ? sel[lane] : 0;
     const bool ok = __all_sync(0xFFFFFFFFu, e >= 0);
     float sv = 0.f;
-    if (lane < k && ok) {
-        const float l = lg[e];
-        sv = sqrtf(fmaxf(l, 0.f) + log1pf(expf(-fabsf(l))));
-    }
+    if (lane < k && ok) sv = sqrt_softplus(lg[e]);
     float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, sv, j);
-    wj = (lane < k && ok) ? a.w_scale * sv / sum : 0.0f;
+    for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xFFFFFFFFu, sv, j));
+    wj = (lane < k && ok) ? route_weight(a.w_scale, sv, sum) : 0.0f;
     if (!ok) return 0;
     return prunes(a.prune, k) ? prune_tail(wj, k, a.prune, lane) : k;
 }

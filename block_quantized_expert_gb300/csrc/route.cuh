@@ -20,6 +20,19 @@ struct RoutePrune {
 
 __device__ __forceinline__ bool prunes(const RoutePrune& p, int k) { return p.keep < k || p.min_w > 0.f; }
 
+// The routing arithmetic is written with explicit round-to-nearest
+// operations, so that no call site contracts a product and a sum into one
+// fused operation: every kernel that routes a token (the routing kernels and
+// the whole-layer decode kernel) gets the same fp32 bits.
+// s = sqrt(softplus(l)), softplus(l) = max(l, 0) + log1p(exp(-|l|)).
+__device__ __forceinline__ float sqrt_softplus(float l) {
+    return __fsqrt_rn(__fadd_rn(fmaxf(l, 0.f), log1pf(expf(-fabsf(l)))));
+}
+// w = w_scale * s / sum
+__device__ __forceinline__ float route_weight(float w_scale, float s, float sum) {
+    return __fdiv_rn(__fmul_rn(w_scale, s), sum);
+}
+
 // Lane j < k holds w_j (router order, descending).  Expert 0 is kept, expert
 // j >= 1 while j < keep and w_j >= min_w: the first that fails ends the kept
 // prefix of length m (returned).  Kept weights are multiplied by
@@ -36,17 +49,18 @@ __device__ __forceinline__ int prune_tail(float& wj, int k, const RoutePrune& p,
         for (int j = 0; j < k; ++j) {
             const float v = __shfl_sync(0xFFFFFFFFu, wj, j);
             const float v2 = __fmul_rn(v, v);
-            s1a += v;
-            s2a += v2;
+            s1a = __fadd_rn(s1a, v);
+            s2a = __fadd_rn(s2a, v2);
             if (j < m) {
-                s1k += v;
-                s2k += v2;
+                s1k = __fadd_rn(s1k, v);
+                s2k = __fadd_rn(s2k, v2);
             }
         }
-        const float num = (1.f - p.rho) * s2a + p.rho * __fmul_rn(s1a, s1a);
-        const float den = (1.f - p.rho) * s2k + p.rho * __fmul_rn(s1k, s1k);
-        const float alpha = sqrtf(num / den);
-        wj = lane < m ? wj * alpha : 0.f;
+        const float r1 = __fsub_rn(1.f, p.rho);
+        const float num = __fadd_rn(__fmul_rn(r1, s2a), __fmul_rn(p.rho, __fmul_rn(s1a, s1a)));
+        const float den = __fadd_rn(__fmul_rn(r1, s2k), __fmul_rn(p.rho, __fmul_rn(s1k, s1k)));
+        const float alpha = __fsqrt_rn(__fdiv_rn(num, den));
+        wj = lane < m ? __fmul_rn(wj, alpha) : 0.f;
     }
     return m;
 }
@@ -86,11 +100,10 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
         if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     }
     float s = 0.f;
-    if (lane < k && my_sel >= 0)
-        s = sqrtf(fmaxf(my_logit, 0.f) + log1pf(expf(-fabsf(my_logit))));
+    if (lane < k && my_sel >= 0) s = sqrt_softplus(my_logit);
     float sum = 0.f;
-    for (int j = 0; j < k; ++j) sum += __shfl_sync(0xFFFFFFFFu, s, j);
-    float wj = (lane < k && ok) ? w_scale * s / sum : 0.0f;
+    for (int j = 0; j < k; ++j) sum = __fadd_rn(sum, __shfl_sync(0xFFFFFFFFu, s, j));
+    float wj = (lane < k && ok) ? route_weight(w_scale, s, sum) : 0.0f;
     int m = k;
     if (ok && prunes(prune, k)) m = prune_tail(wj, k, prune, lane);
     if (lane < k) {
