@@ -407,10 +407,15 @@ def trace_report(bqe, layer, step, i, dev):
                                    "exit_us": round((fr[2] - t0) / 1e3, 2)}), file=sys.stderr, flush=True)
     if t[0, :, 9].max() > 0:  # the whole-layer decode kernel
         e0 = t[0, :, 0].min()
-        rep = {"launch": "decode"}
-        for key, c, f in (("first_entry_us", 0, np.min), ("wait_end_us", 8, np.min),
-                          ("routed_us", 9, np.max), ("last_exit_us", 1, np.max)):
-            rep[key] = round((f(t[0, :, c]) - e0) / 1e3, 2)
+        rep = {"launch": "decode", "percentiles": [0, 50, 100]}
+        for key, c in (("entry", 0), ("wait_end", 8), ("routed", 9), ("producer_start", 2),
+                       ("first_weights", 3), ("gateup_issued", 4), ("gateup_written", 10),
+                       ("h_flags_seen", 5), ("h_landed", 6), ("down_issued", 7), ("down_written", 11),
+                       ("exit", 1)):
+            v = t[0, :, c]
+            v = v[v > 0]
+            if v.size:
+                rep[key] = [round((np.percentile(v, p) - e0) / 1e3, 2) for p in (0, 50, 100)]
         print("TRACE", json.dumps(rep), file=sys.stderr, flush=True)
         return
     names = ["gateup", "down", "shared_gateup", "shared_down"]

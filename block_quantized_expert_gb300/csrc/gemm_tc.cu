@@ -1,22 +1,28 @@
 // gemm_tc.cu -- grouped expert GEMMs on the sm_103a block-scaled tensor cores
 // (tcgen05.mma kind::mxf8f6f4, one UE8M0 scale per 32 K-elements).
 //
-// Orientation: weights are the MMA's A operand (M = 128 weight rows = output
-// features), the routed tokens of one expert segment its B operand (N = 32..128
-// token rows), so the fp32 accumulator D[feature][token] lives in tensor
-// memory with one feature per TMEM lane.  MXFP4 weights are e2m1 (A format
-// 5), the shared expert's fp8 weights e4m3 (A format 0); activations are
-// e4m3.  Per 128-wide K step a TMA producer fills one pipeline stage with
-// the weight tile(s) (fp4 unpacked by TMA into the 16-byte-aligned form the
-// MMA reads), the token tile and three 512-byte scale-factor atoms; the MMA
-// thread copies the atoms into tensor memory (tcgen05.cp) and issues four
-// K=32 MMAs per accumulator; four epilogue warps read the accumulators back.
+// Orientation: the routed tokens of one expert segment are the MMA's A
+// operand (M = 128 token rows) and a 256-row weight tile its B operand (N =
+// 256), so one MMA per K=32 step covers the whole tile: the MMA cost is per
+// instruction far more than per column (measured), and N = 256 is the
+// widest shape.  The fp32 accumulator D[token][weight row] lives in tensor
+// memory with one token row per TMEM lane.  Activations are e4m3; MXFP4
+// weights are e2m1 (B format 5), the shared expert's fp8 weights e4m3 (B
+// format 0).  Per 128-wide K step a TMA producer fills one pipeline stage
+// with the weight tile (fp4 unpacked by TMA into the 16-byte-aligned form
+// the MMA reads), the token rows (a 32-, 64- or 128-row box: rows past the
+// box hold stale data whose accumulator rows are never read) and three
+// 512-byte scale-factor atoms; the MMA thread copies the atoms into tensor
+// memory (tcgen05.cp) and issues four K=32 MMAs; eight epilogue warps read
+// the accumulator back, one token row per thread.
 //
-// Gate/up (guide, section 4): two accumulators (gate, up) per tile; the
-// epilogue forms h = SiLU(g) * u in fp32 and requantises it to MXFP8 along
-// the feature axis (32 features = one warp), writing h codes and scale atoms
-// in the padded row space the down GEMM reads.  Down: one accumulator; the
-// epilogue writes fp32 rows y[row][feature] for the fixed-order combine.
+// Gate/up (guide, section 4): a weight tile is 128 gate rows and the
+// matching 128 up rows, so a thread holds g and u of its token for 64
+// features; it forms h = SiLU(g) * u in fp32 and requantises it to MXFP8
+// along the feature axis (two 32-feature blocks, each within the thread),
+// writing h codes and scale atoms in the padded row space the down GEMM
+// reads.  Down: the epilogue writes fp32 rows y[row][feature] for the
+// fixed-order combine.
 //
 // Persistent grid of one CTA per SM; tiles enumerated (token tile u, weight
 // tile m) with m fastest, so CTAs running together share a token tile and
@@ -74,8 +80,9 @@ struct TcArgs {
     int32_t* cmb_cnt;          // [N_out / 256] tiles finished per block (start at 0)
 };
 
-// One pipeline stage: a 256-row weight tile (two 128-row MMA operands), up to
-// 128 token rows, a pair of weight scale atoms and one activation scale atom.
+// One pipeline stage: a 256-row weight tile (the B operand), up to 128 token
+// rows (the A operand), a pair of weight scale atoms and one activation
+// scale atom.
 struct TcCfg {
     static constexpr int kStages = 4;
     static constexpr int kABytes = 32768;  // 256 rows x 128 B (e2m1 in 16-byte slots, or e4m3)
@@ -85,9 +92,8 @@ struct TcCfg {
     static constexpr int kBarOff = kStages * kStageBytes;
     static constexpr int kSmem = kBarOff + 256 + 1024;  // + barriers + alignment slack
     static constexpr uint32_t kTmemCols = 512;
-    static constexpr uint32_t kAcc1Col = 128;
-    static constexpr uint32_t kSfBase = 256;
-    static constexpr uint32_t kSfPerStage = 12;  // A rows 0-127, A rows 128-255, B: 4 columns each
+    static constexpr uint32_t kSfBase = 256;     // D: columns 0-255
+    static constexpr uint32_t kSfPerStage = 12;  // tokens (A), weight rows 0-127, 128-255 (B): 4 columns each
     static_assert(kSfBase + kStages * kSfPerStage <= kTmemCols, "tensor memory budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
@@ -95,7 +101,7 @@ struct TcCfg {
 // warp 0: TMA, warp 1: MMA, warps 2-9: epilogue.  Ten warps put three on two
 // of the four SM sub-partitions, whose 16K registers cap a thread at 168.
 constexpr int kTcThreads = 320;
-constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, each half of the token columns
+constexpr int kEpiWarps = 8;     // two per TMEM lane quarter, each half of the weight columns
 
 struct Tile {
     int e, n0, nvalid, nt, arow, f0, p0;
@@ -177,25 +183,47 @@ struct SegIter {
     }
 };
 
-// Token n of a tile from its two accumulator values: gate/up -> h = SiLU(g) * u
-// requantised to MXFP8 across the warp's 32 features; down -> two fp32 outputs.
+// Token row n of a tile (one epilogue thread of column half hf) from its 128
+// accumulator values.  Gate/up: v[0..63] are g and v[64..127] u of features
+// f0 + 64 hf + (0..63); h = SiLU(g) * u is requantised to MXFP8 in two
+// 32-feature blocks.  Down: v are the fp32 outputs f0 + 128 hf + (0..127).
 template <bool kGateUp>
-__device__ __forceinline__ void emit_token(const TcArgs& a, const Tile& T, int n, int q, int lane,
-                                           float v0, float v1) {
+__device__ __forceinline__ void emit_row(const TcArgs& a, const Tile& T, int n, int hf, uint32_t (&v)[128]) {
     const int p = T.p0 + n;
-    const int fm = 32 * q + lane;
     if (kGateUp) {
-        const float h = silu_mul(v0, v1);
-        const int ex = mxfp8_exponent(warp_max(fabsf(h)));
-        const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
-        a.hq[(size_t)p * a.N_out + T.f0 + fm] = (uint8_t)code;
-        if (lane == 0) a.hs[sf_atom_offset(p, (T.f0 + 32 * q) / 32, a.N_out)] = (uint8_t)(ex + 127);
+        const int fb = T.f0 + 64 * hf;
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+            // h replaces g in v[32 c .. 32 c + 31]
+            float amax = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float h = silu_mul(__uint_as_float(v[32 * c + j]), __uint_as_float(v[64 + 32 * c + j]));
+                v[32 * c + j] = __float_as_uint(h);
+                amax = fmaxf(amax, fabsf(h));
+            }
+            const int ex = mxfp8_exponent(amax);
+            const uint32_t* h = v + 32 * c;
+            uint32_t w[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                w[i] = f32x2_to_e4m3x2(scale_pow2(__uint_as_float(h[4 * i]), ex),
+                                       scale_pow2(__uint_as_float(h[4 * i + 1]), ex)) |
+                       (f32x2_to_e4m3x2(scale_pow2(__uint_as_float(h[4 * i + 2]), ex),
+                                        scale_pow2(__uint_as_float(h[4 * i + 3]), ex)) << 16);
+            uint4* dst = reinterpret_cast<uint4*>(a.hq + (size_t)p * a.N_out + fb + 32 * c);
+            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            a.hs[sf_atom_offset(p, (fb + 32 * c) / 32, a.N_out)] = (uint8_t)(ex + 127);
+        }
     } else {
         const int row = a.pos_row ? __ldg(a.pos_row + p) : p;
         if (row >= 0) {
-            float* yr = a.y + (size_t)row * a.N_out + T.f0;
-            yr[fm] = v0;
-            yr[128 + fm] = v1;
+            float4* yr = reinterpret_cast<float4*>(a.y + (size_t)row * a.N_out + T.f0 + 128 * hf);
+#pragma unroll
+            for (int i = 0; i < 32; ++i)
+                yr[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
+                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
         }
     }
 }
@@ -385,21 +413,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
                 ++n_stages;
                 if (lane == 0) {
                     tc_fence_after();
-                    const uint32_t st = smem_u32(smem + stage * Cfg::kStageBytes);
-                    const uint32_t bt = st + Cfg::kABytes;
+                    const uint32_t st = smem_u32(smem + stage * Cfg::kStageBytes);  // weights (B)
+                    const uint32_t xt = st + Cfg::kABytes;                           // token rows (A)
                     const uint32_t sf = st + Cfg::kSfOff;
                     const uint32_t sf_col = tmem + Cfg::kSfBase + stage * Cfg::kSfPerStage;
-                    tmem_cp_32x128_x4(sf_col, desc_sf(sf));
-                    tmem_cp_32x128_x4(sf_col + 4, desc_sf(sf + 512));
-                    tmem_cp_32x128_x4(sf_col + 8, desc_sf(sf + 1024));
+                    tmem_cp_32x128_x4(sf_col, desc_sf(sf + 1024));     // token scales
+                    tmem_cp_32x128_x4(sf_col + 4, desc_sf(sf));        // weight rows 0-127
+                    tmem_cp_32x128_x4(sf_col + 8, desc_sf(sf + 512));  // weight rows 128-255
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk) {
-                        const uint32_t id = idesc_mx(kAFmt, kFmtE4M3, 128, (uint32_t)T.nt, kk, kk);
-                        const uint64_t bd = desc_sw128(bt + 32 * kk);
+                        const uint32_t id = idesc_mx(kFmtE4M3, kAFmt, 128, 256, kk, kk);
                         const uint32_t acc = (kb > sg.kb0 || kk) ? 1u : 0u;
-                        mma_mx(tmem, desc_sw128(st + 32 * kk), bd, id, sf_col, sf_col + 8, acc);
-                        mma_mx(tmem + Cfg::kAcc1Col, desc_sw128(st + 16384 + 32 * kk), bd, id, sf_col + 4,
-                               sf_col + 8, acc);
+                        mma_mx(tmem, desc_sw128(xt + 32 * kk), desc_sw128(st + 32 * kk), id, sf_col, sf_col + 4, acc);
                     }
                     mma_commit(empty_bar(stage));
                 }
@@ -414,15 +439,18 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         if (tr && lane == 0) { trc[3] = w_full; trc[4] = w_acc; trc[7] = n_stages; }
     } else {
         // ---------------------------------------------------- epilogue --
-        // Warp w (2..9) reads TMEM lanes of quarter w % 4 and token columns
-        // [64 * h, 64 * h + 64), h = (w - 2) / 4: it copies both accumulators'
-        // columns to registers, frees the accumulator for the next tile, and
-        // only then does the SwiGLU / requantisation or the stores.
+        // Warp w (2..9) reads TMEM lanes of quarter w % 4 (token rows n =
+        // 32 (w % 4) + lane of the tile) and weight columns of half h = (w -
+        // 2) / 4: gate/up -> gate columns 64 h .. + 63 and the matching up
+        // columns 128 + 64 h .. + 63; down -> columns 128 h .. + 127.  It
+        // copies them to registers, frees the accumulator for the next tile,
+        // and only then does the SwiGLU / requantisation or the stores.
         const int q = warp & 3;
         const int hf = (warp - 2) >> 2;
-        const int fm = 32 * q + lane;
-        const int cb = 64 * hf;
-        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)cb;
+        const int n = 32 * q + lane;
+        const uint32_t c0 = kGateUp ? 64u * hf : 128u * hf;
+        const uint32_t c1 = kGateUp ? 128u + 64u * hf : 128u * hf + 64u;
+        const uint32_t tq = tmem + ((uint32_t)(32 * q) << 16);
         const bool leader = warp == 2 && lane == 0;
         uint32_t acc_phase = 0;
         unsigned long long w_tf = 0, t_work = 0;
@@ -435,40 +463,33 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const uint64_t tw0 = tr ? globaltimer() : 0;
             tc_fence_after();
             acc_phase ^= 1u;
-            uint32_t v0[4][16], v1[4][16];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                if (cb + 16 * j < T.nt) {  // warp-uniform
-                    tmem_ld16(tq + 16 * j, v0[j]);
-                    tmem_ld16(tq + Cfg::kAcc1Col + 16 * j, v1[j]);
-                }
+            const bool rows_here = 32 * q < T.nvalid;  // warp-uniform: this quarter holds valid rows
+            uint32_t v[128];  // fp32 bits
+            if (rows_here) {
+                tmem_ld32(tq + c0, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+                tmem_ld32(tq + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
+                tmem_ld32(tq + c1, *reinterpret_cast<uint32_t(*)[32]>(&v[64]));
+                tmem_ld32(tq + c1 + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[96]));
+                tmem_ld_wait();
             }
-            tmem_ld_wait();
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(tmem_empty);
-            const int nv = min(64, T.nvalid - cb);  // valid columns of this warp (may be <= 0)
+            const bool valid = n < T.nvalid;
             if (sg.first_cta == sg.last_cta) {
-#pragma unroll
-                for (int i = 0; i < 64; i += 4) {
-                    if (i >= nv) break;  // warp-uniform
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        if (i + k < nv)
-                            emit_token<kGateUp>(a, T, cb + i + k, q, lane, __uint_as_float(v0[(i + k) >> 4][(i + k) & 15]),
-                                                __uint_as_float(v1[(i + k) >> 4][(i + k) & 15]));
-                }
+                if (valid) emit_row<kGateUp>(a, T, n, hf, v);
                 if (!kGateUp && a.cmb_out) tile_done_combine(a, T.f0, leader, last_flag, warp, lane);
                 if (tr) t_work += globaltimer() - tw0;
                 continue;
             }
-            // a piece of a split tile: park the partial sums, count arrivals
-            float* part = a.sk_part + ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 2 * 128 * 128;
+            // a piece of a split tile: park the partial sums ([column][row]),
+            // count arrivals
+            float* part = a.sk_part + ((size_t)blockIdx.x * 2 + it.slot(blockIdx.x, sg.tile)) * 256 * 128;
+            if (rows_here) {
 #pragma unroll
-            for (int i = 0; i < 64; ++i) {
-                if (cb + i < T.nt) {
-                    part[(size_t)(cb + i) * 128 + fm] = __uint_as_float(v0[i >> 4][i & 15]);
-                    part[(size_t)(128 + cb + i) * 128 + fm] = __uint_as_float(v1[i >> 4][i & 15]);
+                for (int j = 0; j < 64; ++j) {
+                    part[(size_t)(c0 + j) * 128 + n] = __uint_as_float(v[j]);
+                    part[(size_t)(c1 + j) * 128 + n] = __uint_as_float(v[64 + j]);
                 }
             }
             __threadfence();
@@ -481,14 +502,20 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             if (!*last_flag) continue;
             __threadfence();
             // the last piece to arrive sums all pieces in K order and finishes the tile
-            for (int n = cb; n < min(T.nvalid, cb + 64); ++n) {
-                float s0 = 0.f, s1 = 0.f;
+            if (valid) {
+                // the sums replace the parked values in v
+#pragma unroll
+                for (int j = 0; j < 128; ++j) v[j] = 0u;  // +0.0f
                 for (int cc = sg.first_cta; cc <= sg.last_cta; ++cc) {
-                    const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 2 * 128 * 128;
-                    s0 += __ldcg(pp + (size_t)n * 128 + fm);
-                    s1 += __ldcg(pp + (size_t)(128 + n) * 128 + fm);
+                    const float* pp = a.sk_part + ((size_t)cc * 2 + it.slot(cc, sg.tile)) * 256 * 128;
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        v[j] = __float_as_uint(__uint_as_float(v[j]) + __ldcg(pp + (size_t)(c0 + j) * 128 + n));
+                        v[64 + j] =
+                            __float_as_uint(__uint_as_float(v[64 + j]) + __ldcg(pp + (size_t)(c1 + j) * 128 + n));
+                    }
                 }
-                emit_token<kGateUp>(a, T, n, q, lane, s0, s1);
+                emit_row<kGateUp>(a, T, n, hf, v);
             }
             epi_bar();  // everyone has read the slots before the counter is reused
             if (leader) a.sk_cnt[sg.first_cta] = 0;

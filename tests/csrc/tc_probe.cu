@@ -423,6 +423,28 @@ __global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, in
     if (threadIdx.x == 0) {
         const uint32_t a = smem_u32(sm), b = smem_u32(sm + 32768), sf = smem_u32(sm + 49152);
         for (int it = 0; it < iters; ++it) {
+            if (mode >= 5) {
+                // the decode gate/up pattern: A's scales resident (column
+                // 256), the weight tile's two scale atoms copied per stage
+                // into stage-indexed columns; mode 5 copies them right before
+                // the stage's MMAs, mode 6 one stage ahead (before the MMAs
+                // of the previous stage)
+                const uint32_t cur = tmem + 264 + 8 * (it & 1), nxt = tmem + 264 + 8 * ((it + 1) & 1);
+                if (mode == 5 || it == 0) {
+                    tmem_cp_32x128_x4(cur, desc_sf(sf));
+                    tmem_cp_32x128_x4(cur + 4, desc_sf(sf + 512));
+                }
+                if (mode == 6 && it + 1 < iters) {
+                    tmem_cp_32x128_x4(nxt, desc_sf(sf));
+                    tmem_cp_32x128_x4(nxt + 4, desc_sf(sf + 512));
+                }
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_mx(tmem, smem_desc(b + 32 * kk, 16, 0, 0), desc_sw128(a + 32 * kk),
+                           idesc_mx(kFmtE4M3, a_fmt, 128, 256, kk, kk), tmem + 256, cur, (it | kk) ? 1u : 0u);
+                if (commit) mma_commit(smem_u32(bar + 1));
+                continue;
+            }
             for (int j = 0; j < ncp; ++j) tmem_cp_32x128_x4(tmem + 256 + 4 * j, desc_sf(sf + 512 * j));
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk) {
@@ -466,7 +488,7 @@ extern "C" int probe_mma_mix(int grid, int iters, int n, int ncp, int commit, in
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
-    if (mode < 0 || mode > 4) return 3;
+    if (mode < 0 || mode > 6) return 3;
     k_mma_mix<<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
