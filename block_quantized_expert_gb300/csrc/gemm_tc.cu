@@ -211,19 +211,18 @@ __device__ __forceinline__ void emit_row(const TcArgs& a, const Tile& T, int n, 
                                        scale_pow2(__uint_as_float(h[4 * i + 1]), ex)) |
                        (f32x2_to_e4m3x2(scale_pow2(__uint_as_float(h[4 * i + 2]), ex),
                                         scale_pow2(__uint_as_float(h[4 * i + 3]), ex)) << 16);
-            uint4* dst = reinterpret_cast<uint4*>(a.hq + (size_t)p * a.N_out + fb + 32 * c);
-            dst[0] = make_uint4(w[0], w[1], w[2], w[3]);
-            dst[1] = make_uint4(w[4], w[5], w[6], w[7]);
+            st_global_v8(a.hq + (size_t)p * a.N_out + fb + 32 * c, w[0], w[1], w[2], w[3], w[4], w[5], w[6], w[7]);
             a.hs[sf_atom_offset(p, (fb + 32 * c) / 32, a.N_out)] = (uint8_t)(ex + 127);
         }
     } else {
         const int row = a.pos_row ? __ldg(a.pos_row + p) : p;
         if (row >= 0) {
-            float4* yr = reinterpret_cast<float4*>(a.y + (size_t)row * a.N_out + T.f0 + 128 * hf);
+            // whole 32-byte sectors per store: each thread writes its own row
+            float* yr = a.y + (size_t)row * a.N_out + T.f0 + 128 * hf;
 #pragma unroll
-            for (int i = 0; i < 32; ++i)
-                yr[i] = make_float4(__uint_as_float(v[4 * i]), __uint_as_float(v[4 * i + 1]),
-                                    __uint_as_float(v[4 * i + 2]), __uint_as_float(v[4 * i + 3]));
+            for (int i = 0; i < 16; ++i)
+                st_global_v8(yr + 8 * i, v[8 * i], v[8 * i + 1], v[8 * i + 2], v[8 * i + 3], v[8 * i + 4],
+                             v[8 * i + 5], v[8 * i + 6], v[8 * i + 7]);
         }
     }
 }
