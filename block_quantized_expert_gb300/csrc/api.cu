@@ -152,8 +152,9 @@ cudaError_t forward_kernels(moe_layer* L, const float* logits, const uint16_t* x
         return e;
     }
     if (e == cudaSuccess && small) {
-        e = M(1, moe::launch_front(L, logits, ids, w, x, T, s));
-        if (e == cudaSuccess) e = M(2, cudaSuccess);
+        const bool front_quant = T <= moe::kFrontQuantMaxT;
+        e = M(1, moe::launch_front(L, logits, ids, w, front_quant ? x : nullptr, T, s));
+        if (e == cudaSuccess) e = M(2, front_quant ? cudaSuccess : moe::launch_quantize_scatter(L, x, T, s));
     } else {
         if (e == cudaSuccess && logits) e = moe::launch_route(L, logits, T, ids, w, s);
         if (e == cudaSuccess) e = M(1, moe::launch_permute(L, ids, T, L->offsets, L->row_src, L->row_dst, s));

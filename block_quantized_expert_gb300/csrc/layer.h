@@ -74,6 +74,10 @@ namespace moe {
 constexpr int kChunk = 4;      // tokens per CUDA-core GEMM work item
 constexpr int kFrontMaxT = 32; // batches up to this size use the one-CTA front kernel
 constexpr int kFusedCombineMaxT = 32;  // and the combine fused into the down GEMM
+// the front kernel quantises x itself up to this size; larger batches
+// quantise in a grid-wide kernel (one SM is instruction-bound on the
+// scattered stores: about 1 us per token of T = 32, top-6, H = 4096)
+constexpr int kFrontQuantMaxT = 4;
 
 // split-tile counters of the grouped GEMMs (4 launches x num_sms, then one
 // per 256-feature block of the fused combine, H / 256 <= 32): zeroed by every
@@ -114,7 +118,7 @@ cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* off
 cudaError_t launch_quantize_canonical(moe_layer* L, const uint16_t* x, int T, uint8_t* q,
                                       uint8_t* sc, cudaStream_t s);
 cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cudaStream_t s);
-// route (if logits) + permute + quantise in one CTA, for T <= kFrontMaxT
+// route (if logits) + permute (+ quantise, if x) in one CTA, for T <= kFrontMaxT
 cudaError_t launch_front(moe_layer* L, const float* logits, int32_t* ids, float* w, const uint16_t* x,
                          int T, cudaStream_t s);
 cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int T,

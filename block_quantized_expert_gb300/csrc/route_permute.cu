@@ -253,20 +253,35 @@ struct QuantDst {
     uint8_t* xs_tok;
 };
 
-// One warp-task: 256 elements (8 blocks) of token row t.
-template <int kMode>
-__device__ __forceinline__ void quantize_task(const uint16_t* __restrict__ x, int H, const QuantDst& d,
-                                              int task, int lane) {
+// One warp-task: 256 elements (8 blocks) of token row t; this lane's 8.
+struct QTask {
+    int t, b, h;
+    bool active;
+};
+
+__device__ __forceinline__ QTask q_task(int H, int task, int lane) {
     const int tasks_per_row = (H + 255) / 256;
-    const int t = task / tasks_per_row;
-    const int b = (task % tasks_per_row) * 8 + (lane >> 2);  // 32-block index
+    QTask q;
+    q.t = task / tasks_per_row;
+    q.b = (task % tasks_per_row) * 8 + (lane >> 2);  // 32-block index
+    q.active = q.b < H / 32;
+    q.h = q.b * 32 + (lane & 3) * 8;
+    return q;
+}
+
+__device__ __forceinline__ uint4 q_load(const uint16_t* __restrict__ x, int H, const QTask& q) {
+    return q.active ? *reinterpret_cast<const uint4*>(x + (size_t)q.t * H + q.h) : make_uint4(0, 0, 0, 0);
+}
+
+// Quantise this lane's 8 elements (raw: their bf16 bits) and store them.
+template <int kMode>
+__device__ __forceinline__ void q_store(int H, const QuantDst& d, const QTask& q, uint4 raw, int lane) {
+    const int t = q.t, b = q.b, h = q.h;
     const int part = lane & 3;
-    const bool active = b < H / 32;
-    const int h = b * 32 + part * 8;
+    const bool active = q.active;
     float v[8];
     float amax = 0.0f;
     if (active) {
-        uint4 raw = *reinterpret_cast<const uint4*>(x + (size_t)t * H + h);
         uint32_t wv[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -306,6 +321,13 @@ __device__ __forceinline__ void quantize_task(const uint16_t* __restrict__ x, in
 }
 
 template <int kMode>
+__device__ __forceinline__ void quantize_task(const uint16_t* __restrict__ x, int H, const QuantDst& d,
+                                              int task, int lane) {
+    const QTask q = q_task(H, task, lane);
+    q_store<kMode>(H, d, q, q_load(x, H, q), lane);
+}
+
+template <int kMode>
 __global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x, int T, int H,
                                                   QuantDst d) {
     pdl_launch_dependents();
@@ -316,8 +338,8 @@ __global__ void __launch_bounds__(256) k_quantize(const uint16_t* __restrict__ x
 }
 
 // Small batches in one CTA (T <= kFrontMaxT): optional routing (one warp per
-// token), the counting sort and the quantisation, each phase after a barrier.
-// Saves two kernel boundaries on the decode path.
+// token), the counting sort and (x non-null) the quantisation, each phase
+// after a barrier.  Saves kernel boundaries on the decode path.
 __global__ void __launch_bounds__(1024) k_front(
     const float* __restrict__ logits, float w_scale, RoutePrune prune, int32_t* __restrict__ ids,
     float* __restrict__ wts,
@@ -342,8 +364,33 @@ __global__ void __launch_bounds__(1024) k_front(
     permute_body(ids, T * k, E, offsets, row_src, row_dst, counts, poff, tile_scan, chunk_scan, row_pos,
                  pos_row, sh_desc, T, err, zero, n_zero, dyn);
     __syncthreads();
+    if (!x) {  // quantised by a grid-wide kernel after this one
+        if (trace && threadIdx.x == 0) trace[2] = tc_globaltimer();
+        return;
+    }
+    // the rows' padded positions, just written by this CTA, from shared
+    // memory; each warp's x loads for up to kBatch tasks in flight at once
+    __shared__ int32_t s_rp[kFrontMaxT * kMaxTopK];
+    for (int r = threadIdx.x; r < T * k; r += blockDim.x) s_rp[r] = row_pos[r];
+    __syncthreads();
+    QuantDst qs = qd;
+    qs.row_pos = s_rp;
     const int tasks = T * ((H + 255) / 256);
-    for (int task = warp; task < tasks; task += 32) quantize_task<1>(x, H, qd, task, lane);
+    constexpr int kBatch = 8;
+    for (int base = warp; base < tasks; base += 32 * kBatch) {
+        uint4 raw[kBatch];
+        QTask qt[kBatch];
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i) {
+            const int task = base + 32 * i;
+            qt[i] = q_task(H, task < tasks ? task : 0, lane);
+            qt[i].active = qt[i].active && task < tasks;
+            raw[i] = q_load(x, H, qt[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < kBatch; ++i)
+            if (base + 32 * i < tasks) q_store<1>(H, qs, qt[i], raw[i], lane);  // warp-uniform
+    }
     if (trace) {
         __syncthreads();
         if (threadIdx.x == 0) trace[2] = tc_globaltimer();
