@@ -237,10 +237,15 @@ __device__ void combine_block(const TcArgs& a, int f0, int i) {
     for (int t = 0; t < a.cmb_T; ++t) {
         int order[kMaxTopK];
         int idv[kMaxTopK];
+        float yv[kMaxTopK];
 #pragma unroll
         for (int j = 0; j < kMaxTopK; ++j) {
             order[j] = j;
             idv[j] = (j < k) ? __ldg(a.cmb_ids + (size_t)t * k + j) : INT_MAX;
+            // every row's value in flight at once (a dropped row's y is not read)
+            yv[j] = (j < k && __ldg(a.cmb_row_pos + t * k + j) >= 0)
+                        ? __ldcg(a.y + (size_t)(t * k + j) * a.N_out + f0 + i)
+                        : 0.f;
         }
 #pragma unroll
         for (int x = 1; x < kMaxTopK; ++x)
@@ -254,8 +259,12 @@ __device__ void combine_block(const TcArgs& a, int f0, int i) {
         for (int x = 0; x < kMaxTopK; ++x) {
             if (x < k) {
                 const int r = t * k + order[x];
-                if (__ldg(a.cmb_row_pos + r) < 0) continue;  // dropped row (bad id)
-                acc += __ldg(a.cmb_w + r) * __ldcg(a.y + (size_t)r * a.N_out + f0 + i);
+                if (__ldg(a.cmb_row_pos + r) < 0) continue;  // dropped row (bad id, empty slot)
+                float v = 0.f;
+#pragma unroll
+                for (int j = 0; j < kMaxTopK; ++j)
+                    if (j == order[x]) v = yv[j];
+                acc += __ldg(a.cmb_w + r) * v;
             }
         }
         a.cmb_out[(size_t)t * a.N_out + f0 + i] = acc;

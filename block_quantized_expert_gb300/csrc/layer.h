@@ -73,7 +73,10 @@ namespace moe {
 
 constexpr int kChunk = 4;      // tokens per CUDA-core GEMM work item
 constexpr int kFrontMaxT = 32; // batches up to this size use the one-CTA front kernel
-constexpr int kFusedCombineMaxT = 32;  // and the combine fused into the down GEMM
+// the combine fused into the down GEMM up to this size: the CTA that
+// finishes a feature block combines it for every token, a tail that grows
+// with T (at T = 32 a separate combine kernel is faster, measured)
+constexpr int kFusedCombineMaxT = 4;
 // the front kernel quantises x itself up to this size; larger batches
 // quantise in a grid-wide kernel (one SM is instruction-bound on the
 // scattered stores: about 1 us per token of T = 32, top-6, H = 4096)
