@@ -80,6 +80,7 @@ size_t workspace_bytes(const moe_config& c) {
     size_t b = 0;
     b += 5 * (E + 1) * 4;                        // counts, offsets, poff, tile_scan, chunk_scan
     b += 3 * z.R * 4 + z.Rp * 4 + 8 * 4;         // row_src, row_dst, row_pos, pos_row, sh_desc
+    b += (z.R + 1023) / 1024 * E * 4;            // perm_cnt
     b += z.Rp * H + z.Rp * H / 32;               // xq, xs
     b += z.Rp * I + z.Rp * I / 32;               // hq, hs
     b += z.R * H * 4;                            // y
@@ -104,7 +105,7 @@ void free_all(moe_layer* L) {
                     L->sh_gu_q, L->sh_gate_s, L->sh_up_s, L->sh_down_q, L->sh_down_s,
                     L->gu_sf, L->down_sf, L->sh_gu_sf, L->sh_down_sf,
                     L->counts, L->offsets, L->poff, L->tile_scan, L->chunk_scan, L->row_src,
-                    L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->xq, L->xs, L->xq_tok,
+                    L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->perm_cnt, L->xq, L->xs, L->xq_tok,
                     L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
                     L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err,
                     L->sk_counters, L->sk_partials};
@@ -230,6 +231,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     A(&L->tile_scan, (E + 1) * 4); A(&L->chunk_scan, (E + 1) * 4);
     A(&L->row_src, z.R * 4); A(&L->row_dst, z.R * 4); A(&L->row_pos, z.R * 4);
     A(&L->pos_row, z.Rp * 4); A(&L->sh_desc, 8 * 4);
+    A(&L->perm_cnt, (z.R + 1023) / 1024 * E * 4);
     A(&L->xq, z.Rp * H); A(&L->xs, z.Rp * H / 32);
     A(&L->hq, z.Rp * I); A(&L->hs, z.Rp * I / 32);
     A(&L->y, z.R * H * 4);

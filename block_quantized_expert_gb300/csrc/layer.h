@@ -41,6 +41,7 @@ struct moe_layer {
     int32_t* row_pos;     // [R]  padded position of row r (-1 if dropped)
     int32_t* pos_row;     // [Rp] row at padded position p (-1 = padding)
     int32_t* sh_desc;     // shared-expert segment: counts[1], poff[2], tiles[2], chunks[2]
+    int32_t* perm_cnt;    // [R/1024 chunks][E] expert counts of the grid-wide sort
     uint8_t* xq;          // [Rp][H]   MXFP8 codes of x, permuted rows
     uint8_t* xs;          // atoms of [Rp][H/32]
     uint8_t* xq_tok;      // [T][H]    MXFP8 codes of x, token order (shared expert)

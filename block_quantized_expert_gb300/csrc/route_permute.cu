@@ -96,6 +96,46 @@ __device__ Int4Scan block_exclusive_scan4(Int4Scan v, Int4Scan* warp_tot, Int4Sc
     return {base.a + inc.a - v.a, base.b + inc.b - v.b, base.c + inc.c - v.c, base.d + inc.d - v.d};
 }
 
+// One chunk of the stable counting sort (1024 threads): rows [base, base +
+// 1024) of R, each placed at its expert's start + cursor[e] (rows of e in
+// earlier chunks) + rows of e in earlier warps of this chunk (per-warp counts
+// wc) + in earlier lanes (match_any); cursor then advances by this chunk's
+// counts.  Rows without a valid expert get row_dst = row_pos = -1.
+__device__ void place_chunk(const int32_t* __restrict__ ids, int R, int E, int base, int* cursor,
+                            const int* s_off, const int* s_poff, uint8_t* wc, int32_t* __restrict__ row_src,
+                            int32_t* __restrict__ row_dst, int32_t* __restrict__ row_pos,
+                            int32_t* __restrict__ pos_row) {
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
+    __syncthreads();
+    const int r = base + tid;
+    int e = (r < R) ? ids[r] : -1;
+    if (e >= E) e = -1;
+    const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
+    const int rank = __popc(grp & ((1u << lane) - 1u));
+    if (e >= 0 && rank == 0) wc[warp * E + e] = (uint8_t)__popc(grp);
+    __syncthreads();
+    if (e >= 0) {
+        int before = cursor[e] + rank;
+        for (int w2 = 0; w2 < warp; ++w2) before += wc[w2 * E + e];
+        const int p = s_off[e] + before, pp = s_poff[e] + before;
+        row_src[p] = r;
+        row_dst[r] = p;
+        row_pos[r] = pp;
+        pos_row[pp] = r;
+    } else if (r < R) {
+        row_dst[r] = -1;
+        row_pos[r] = -1;
+    }
+    __syncthreads();
+    for (int e2 = tid; e2 < E; e2 += 1024) {
+        int add = 0;
+        for (int w2 = 0; w2 < 32; ++w2) add += wc[w2 * E + e2];
+        cursor[e2] += add;
+    }
+    __syncthreads();
+}
+
 // Stable counting sort of the rows r = t*k + j by expert, in one CTA of 1024
 // threads: histogram, scan, then the rows in chunks of 1024 in ascending r,
 // each row's rank = rows of the same expert in earlier chunks (cursor) +
@@ -167,36 +207,8 @@ __device__ void permute_body(
     const int Rp = total.b;
     for (int p = tid; p < Rp; p += 1024) pos_row[p] = -1;
 
-    for (int base = 0; base < R; base += 1024) {
-        for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
-        __syncthreads();
-        const int r = base + tid;
-        int e = (r < R) ? ids[r] : -1;
-        if (e >= E) e = -1;
-        const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
-        const int rank = __popc(grp & ((1u << lane) - 1u));
-        if (e >= 0 && rank == 0) wc[warp * E + e] = (uint8_t)__popc(grp);
-        __syncthreads();
-        if (e >= 0) {
-            int before = cursor[e] + rank;
-            for (int w2 = 0; w2 < warp; ++w2) before += wc[w2 * E + e];
-            const int p = s_off[e] + before, pp = s_poff[e] + before;
-            row_src[p] = r;
-            row_dst[r] = p;
-            row_pos[r] = pp;
-            pos_row[pp] = r;
-        } else if (r < R) {
-            row_dst[r] = -1;
-            row_pos[r] = -1;
-        }
-        __syncthreads();
-        for (int e2 = tid; e2 < E; e2 += 1024) {
-            int add = 0;
-            for (int w2 = 0; w2 < 32; ++w2) add += wc[w2 * E + e2];
-            cursor[e2] += add;
-        }
-        __syncthreads();
-    }
+    for (int base = 0; base < R; base += 1024)
+        place_chunk(ids, R, E, base, cursor, s_off, s_poff, wc, row_src, row_dst, row_pos, pos_row);
 }
 
 __global__ void __launch_bounds__(1024) k_permute(
@@ -212,10 +224,32 @@ __global__ void __launch_bounds__(1024) k_permute(
                  pos_row, sh_desc, T, err, zero, n_zero, dyn);
 }
 
+__global__ void k_perm_count(const int32_t* __restrict__ ids, int R, int E, int32_t* __restrict__ chunk_cnt);
+__global__ void k_perm_place(const int32_t* __restrict__ ids, int R, int E, const int32_t* __restrict__ chunk_cnt,
+                             int32_t* __restrict__ offsets, int32_t* __restrict__ row_src,
+                             int32_t* __restrict__ row_dst, int32_t* __restrict__ counts,
+                             int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan,
+                             int32_t* __restrict__ chunk_scan, int32_t* __restrict__ row_pos,
+                             int32_t* __restrict__ pos_row, int32_t* __restrict__ sh_desc, int T, uint32_t* err,
+                             int32_t* __restrict__ zero, int n_zero);
+
 cudaError_t launch_permute(moe_layer* L, const int32_t* ids, int T, int32_t* offsets,
                            int32_t* row_src, int32_t* row_dst, cudaStream_t s) {
     const int R = T * L->cfg.top_k;
-    const size_t smem = (size_t)48 * L->cfg.n_experts;
+    const int E = L->cfg.n_experts;
+    const size_t smem = (size_t)48 * E;
+    if (R > 8 * 1024) {  // one CTA per 1024-row chunk (two launches: pays from about 8 chunks on)
+        const int C = (R + 1023) / 1024;
+        L->launches += 2;
+        cudaError_t e = launch_pdl(k_perm_count, dim3(C), dim3(1024), (size_t)4 * E, s, ids, R, E,
+                                   L->perm_cnt);
+        if (e != cudaSuccess) return e;
+        return launch_pdl(k_perm_place, dim3(C), dim3(1024), smem, s, ids, R, E,
+                          (const int32_t*)L->perm_cnt, offsets, row_src, row_dst, L->counts, L->poff,
+                          L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
+                          L->cfg.has_shared ? L->sh_desc : nullptr, T, L->d_err, L->sk_counters,
+                          L->sk_counters ? kSkZeroed(L) : 0);
+    }
     L->launches += 1;
     return launch_pdl(k_permute, dim3(1), dim3(1024), smem, s, ids, R, L->cfg.n_experts, offsets, row_src,
                       row_dst, L->counts, L->poff, L->tile_scan, L->chunk_scan, L->row_pos, L->pos_row,
@@ -236,6 +270,108 @@ cudaError_t launch_permute_raw(const int32_t* ids, int T, int k, int E, int32_t*
 }
 
 
+
+// The same sort over one CTA per 1024-row chunk (large batches), in two
+// kernels: the chunks' expert counts, then every CTA scans them (its chunk's
+// rows of expert e start after the rows of e in earlier chunks) and places
+// its own rows with place_chunk.  The result is the one-CTA sort's.
+__global__ void __launch_bounds__(1024) k_perm_count(const int32_t* __restrict__ ids, int R, int E,
+                                                      int32_t* __restrict__ chunk_cnt) {
+    extern __shared__ int sc[];  // [E]
+    pdl_launch_dependents();
+    pdl_wait();
+    for (int e = threadIdx.x; e < E; e += 1024) sc[e] = 0;
+    __syncthreads();
+    const int r = blockIdx.x * 1024 + threadIdx.x;
+    if (r < R) {
+        const int e = ids[r];
+        if (e >= 0 && e < E) atomicAdd(&sc[e], 1);
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += 1024) chunk_cnt[(size_t)blockIdx.x * E + e] = sc[e];
+}
+
+__global__ void __launch_bounds__(1024) k_perm_place(
+    const int32_t* __restrict__ ids, int R, int E, const int32_t* __restrict__ chunk_cnt,
+    int32_t* __restrict__ offsets, int32_t* __restrict__ row_src, int32_t* __restrict__ row_dst,
+    int32_t* __restrict__ counts, int32_t* __restrict__ poff, int32_t* __restrict__ tile_scan,
+    int32_t* __restrict__ chunk_scan, int32_t* __restrict__ row_pos, int32_t* __restrict__ pos_row,
+    int32_t* __restrict__ sh_desc, int T, uint32_t* err, int32_t* __restrict__ zero, int n_zero) {
+    extern __shared__ int dyn[];  // tot, cursor, s_off, s_poff [E]; wc [32][E] bytes
+    int* tot = dyn;
+    int* cursor = dyn + E;
+    int* s_off = dyn + 2 * E;
+    int* s_poff = dyn + 3 * E;
+    uint8_t* wc = reinterpret_cast<uint8_t*>(dyn + 4 * E);
+    __shared__ Int4Scan warp_tot[32];
+    __shared__ Int4Scan total;
+    __shared__ int bad;
+    pdl_launch_dependents();
+    pdl_wait();
+    const int tid = threadIdx.x, C = gridDim.x, c = blockIdx.x;
+    if (tid == 0) bad = 0;
+    for (int e = tid; e < E; e += 1024) {
+        int t = 0, b = 0;
+        for (int cc = 0; cc < C; ++cc) {
+            const int v = chunk_cnt[(size_t)cc * E + e];
+            t += v;
+            if (cc < c) b += v;
+        }
+        tot[e] = t;
+        cursor[e] = b;
+    }
+    if (c == 0)
+        for (int i = tid; i < n_zero; i += 1024) zero[i] = 0;  // the GEMMs' split-tile counters
+    __syncthreads();
+    {
+        const int r = c * 1024 + tid;
+        const int e = r < R ? ids[r] : -1;
+        if (e != -1 && (e < 0 || e >= E)) bad = 1;  // -1: an empty slot, left out quietly
+    }
+    Int4Scan v = {0, 0, 0, 0};
+    if (tid < E) {
+        const int n = tot[tid];
+        v = {n, (n + kRowTile - 1) / kRowTile * kRowTile, (n + kRowTile - 1) / kRowTile,
+             (n + kChunk - 1) / kChunk};
+    }
+    Int4Scan ex = block_exclusive_scan4(v, warp_tot, &total);  // (its barriers order `bad` too)
+    if (tid < E) {
+        s_off[tid] = ex.a;
+        s_poff[tid] = ex.b;
+        if (c == 0) {
+            offsets[tid] = ex.a;
+            counts[tid] = v.a;
+            poff[tid] = ex.b;
+            tile_scan[tid] = ex.c;
+            chunk_scan[tid] = ex.d;
+        }
+    }
+    if (tid == 0) {
+        if (c == 0) {
+            offsets[E] = total.a;
+            poff[E] = total.b;
+            tile_scan[E] = total.c;
+            chunk_scan[E] = total.d;
+            if (sh_desc) {  // the shared expert's single segment: all T tokens
+                sh_desc[0] = T;
+                sh_desc[1] = 0;
+                sh_desc[2] = (T + kRowTile - 1) / kRowTile * kRowTile;
+                sh_desc[3] = 0;
+                sh_desc[4] = (T + kRowTile - 1) / kRowTile;
+                sh_desc[5] = 0;
+                sh_desc[6] = (T + kChunk - 1) / kChunk;
+            }
+        }
+        if (bad) raise_flag(err, ERR_BAD_ID);
+    }
+    __syncthreads();
+    // the padding positions of every C-th expert segment read as no row
+    for (int e = c; e < E; e += C) {
+        const int lo = s_poff[e] + tot[e], hi = s_poff[e] + (tot[e] + kRowTile - 1) / kRowTile * kRowTile;
+        for (int p = lo + tid; p < hi; p += 1024) pos_row[p] = -1;
+    }
+    place_chunk(ids, R, E, c * 1024, cursor, s_off, s_poff, wc, row_src, row_dst, row_pos, pos_row);
+}
 
 // --------------------------------------------------------------- quantise --
 // MXFP8 of bf16 rows.  A group of 4 lanes owns one 32-block (8 elements per
@@ -481,15 +617,24 @@ __global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids
             if (idv[order[b - 1]] > idv[order[b]]) {
                 int tmp = order[b]; order[b] = order[b - 1]; order[b - 1] = tmp;
             }
+    // every row's y and weight in flight at once (addresses in ascending
+    // expert order), then summed in that order; a dropped row adds nothing
+    float4 yv[kMaxTopK];
+    float wv[kMaxTopK];
+    bool live[kMaxTopK];
+#pragma unroll
+    for (int a = 0; a < kMaxTopK; ++a) {
+        const int r = t * k + order[a];
+        live[a] = a < k && row_pos[r] >= 0;
+        yv[a] = live[a] ? *reinterpret_cast<const float4*>(y + (size_t)r * H + c) : make_float4(0.f, 0.f, 0.f, 0.f);
+        wv[a] = live[a] ? w[r] : 0.f;
+    }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int a = 0; a < kMaxTopK; ++a) {
-        if (a < k) {
-            const int r = t * k + order[a];
-            if (row_pos[r] < 0) continue;
-            const float wt = w[r];
-            const float4 v = *reinterpret_cast<const float4*>(y + (size_t)r * H + c);
-            acc.x += wt * v.x; acc.y += wt * v.y; acc.z += wt * v.z; acc.w += wt * v.w;
+        if (live[a]) {
+            const float wt = wv[a];
+            acc.x += wt * yv[a].x; acc.y += wt * yv[a].y; acc.z += wt * yv[a].z; acc.w += wt * yv[a].w;
         }
     }
     if (y_sh) {
@@ -588,6 +733,10 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = max_carveout(k_quantize<0>);
     if (e == cudaSuccess) e = max_carveout(k_quantize<1>);
     if (e == cudaSuccess) e = max_carveout(k_combine);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(k_perm_place, cudaFuncAttributeMaxDynamicSharedMemorySize, 48 * kMaxExperts);
+    if (e == cudaSuccess) e = max_carveout(k_perm_place);
+    if (e == cudaSuccess) e = max_carveout(k_perm_count);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_front, cudaFuncAttributeMaxDynamicSharedMemorySize, 48 * kMaxExperts);
     if (e == cudaSuccess) e = max_carveout(k_front);
