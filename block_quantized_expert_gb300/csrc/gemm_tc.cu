@@ -558,7 +558,8 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 // overlaps the next group's streaming; with one accumulator the extra tile
 // boundaries cost more than that saves (measured), so there is one group.
 // The producer runs through all phases (the weights do not depend on h) and
-// fetches the h of a group's experts before that group's down weights.
+// fetches the h of a group's experts once that group's first down weights are
+// on their way.
 //
 // Cross-CTA hand-offs go through flags that hold the launch's epoch (a
 // 64-bit launch counter that only grows), so nothing is ever reset: a tile
@@ -718,10 +719,15 @@ __device__ bool flag_wait(const uint32_t* f, uint32_t v, volatile int* abort) {
     return true;
 }
 
+__device__ bool dec_fetch_h(const DecArgs& a, const DecCtx& c, const DecPhase& ph, int g, int lane);
+
 // TMA producer (warp 0; lane 0 waits and issues): the weight tiles and
-// scale atoms of this CTA's stream-K range of one phase, into the ring.
+// scale atoms of this CTA's stream-K range of one phase, into the ring.  A
+// down phase fetches group g's h after its first kDecStages weight loads:
+// those land during the gate/up -> down hand-off (the weights do not depend
+// on h), so the down MMAs find a full ring when h arrives.
 template <bool kGateUp>
-__device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap* tmA, const DecPhase& ph,
+__device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap* tmA, const DecPhase& ph, int g,
                             uint32_t& stage, uint32_t& phase, int lane) {
     int MT, KB, seg_rows;
     dec_shape<kGateUp>(a, MT, KB, seg_rows);
@@ -729,11 +735,18 @@ __device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap
     SegIter it;
     it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
     Seg sg;
+    int issued = 0;
+    bool h_done = kGateUp;
     while (it.next(sg)) {
         const int s = ph.s_lo + sg.tile / MT, m = sg.tile % MT;
         const int arow = c.seg_e[s] * seg_rows + m * 256;
         const size_t atom_a = (size_t)(arow / 256) * KB;
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
+            if (!h_done && issued == kDecStages) {
+                if (!dec_fetch_h(a, c, ph, g, lane)) return false;
+                h_done = true;
+            }
+            ++issued;
             unsigned long long none = 0;
             if (!warp_wait(c.empty_bar(stage), phase ^ 1u, c.abort_flag, false, none, lane)) {
                 if (lane == 0) c.give_up(a);
@@ -749,10 +762,10 @@ __device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap
             if (++stage == kDecStages) { stage = 0; phase ^= 1u; }
         }
     }
-    return true;
+    return h_done || dec_fetch_h(a, c, ph, g, lane);
 }
 
-// Before a down phase's weights (producer warp): wait for the h flags of the
+// Before a down phase's MMAs (producer warp): wait for the h flags of the
 // phase's experts in this CTA's range (their gate/up tiles, I / 128 <= 16
 // each), then bring their h rows and scale rows in with bulk copies that
 // complete on the group's h barrier.
@@ -1165,13 +1178,13 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
             cp.k = m;
             const int G = dec_groups(m);
             // it runs through all phases (the weights do not depend on h),
-            // fetching each group's h before that group's down weights
+            // fetching each group's h once that group's first down weights
+            // are on their way
             bool ok = true;
-            for (int g = 0; g < G && ok; ++g) ok = dec_produce<true>(a, cp, &tmGU, dec_phase(m, false, g), stage, phase, lane);
-            for (int g = 0; g < G && ok; ++g) {
-                const DecPhase ph = dec_phase(m, true, g);
-                ok = dec_fetch_h(a, cp, ph, g, lane) && dec_produce<false>(a, cp, &tmDN, ph, stage, phase, lane);
-            }
+            for (int g = 0; g < G && ok; ++g)
+                ok = dec_produce<true>(a, cp, &tmGU, dec_phase(m, false, g), g, stage, phase, lane);
+            for (int g = 0; g < G && ok; ++g)
+                ok = dec_produce<false>(a, cp, &tmDN, dec_phase(m, true, g), g, stage, phase, lane);
         }
     } else {
         if (warp == 2) {
