@@ -1068,12 +1068,18 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         // which advanced it, has completed), advanced once at this launch's end
         n_launch = *reinterpret_cast<volatile unsigned long long*>(a.launches);
     }
+    // x is loaded (and later quantised) by warps 1-9 alone: chunk (tid - 32)
+    // + 288 r, so each warp holds 32 consecutive 8-element chunks
     const int nch = a.H / 8;  // 8-element chunks; a 32-block is 4 chunks of 4 aligned lanes
+    constexpr int kXThreads = kTcThreads - 32;
+    static_assert(2 * kXThreads >= 4096 / 8, "two rounds of chunks cover H <= 4096");
     uint4 xr[2];
+    if (warp > 0) {
 #pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int ch = threadIdx.x + r * kTcThreads;
-        if (ch < nch) xr[r] = *reinterpret_cast<const uint4*>(a.x + (size_t)ch * 8);
+        for (int r = 0; r < 2; ++r) {
+            const int ch = threadIdx.x - 32 + r * kXThreads;
+            if (ch < nch) xr[r] = *reinterpret_cast<const uint4*>(a.x + (size_t)ch * 8);
+        }
     }
     // top-k by rank (larger logit first, equal logits by lower index; NaN
     // never selected), in two rounds: each warp ranks a 32-logit chunk among
@@ -1104,38 +1110,6 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
         }
     }
     __syncthreads();
-    // ---- quantise x into the resident B row (MXFP8, 32-blocks)
-#pragma unroll
-    for (int r = 0; r < 2; ++r) {
-        const int ch = threadIdx.x + r * kTcThreads;
-        if (ch - lane >= nch) continue;  // warp-uniform (nch is a multiple of 32)
-        const uint32_t wv[4] = {xr[r].x, xr[r].y, xr[r].z, xr[r].w};
-        float v[8];
-        float amax = 0.f;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            v[2 * i] = __uint_as_float(wv[i] << 16);
-            v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-        }
-#pragma unroll
-        for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
-        amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
-        const int ex = mxfp8_exponent(amax);
-        uint32_t lo = 0, hi = 0;
-#pragma unroll
-        for (int i = 0; i < 2; ++i) {
-            lo |= f32x2_to_e4m3x2(scale_pow2(v[2 * i], ex), scale_pow2(v[2 * i + 1], ex)) << (16 * i);
-            hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
-        }
-        const int h = ch * 8, b = ch >> 2;
-        *reinterpret_cast<uint2*>(smem + kDecXOff + h) = make_uint2(lo, hi);
-        // the scale row of K step b / 4: block b % 4, once per lane quarter
-        smem[kDecTokScaleOff + (b / 4) * 16 + 4 * (ch & 3) + (b % 4)] = (uint8_t)(ex + 127);
-    }
-    // the quantised row and scales were written through the generic proxy;
-    // the MMAs read them through the async proxy
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     for (int t = threadIdx.x; t < nc; t += kTcThreads) {
         const int e = ci[t];
         if (e < 0) continue;
@@ -1187,6 +1161,39 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
                 ok = dec_produce<false>(a, cp, &tmDN, dec_phase(m, true, g), g, stage, phase, lane);
         }
     } else {
+        // ---- quantise x into the resident token row (MXFP8, 32-blocks),
+        // while the producer streams the first weights
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int ch = threadIdx.x - 32 + r * kXThreads;
+            if (ch - lane >= nch) continue;  // warp-uniform (nch is a multiple of 32)
+            const uint32_t wv[4] = {xr[r].x, xr[r].y, xr[r].z, xr[r].w};
+            float v[8];
+            float amax = 0.f;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[2 * i] = __uint_as_float(wv[i] << 16);
+                v[2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
+            }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) amax = fmaxf(amax, fabsf(v[i]));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+            amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+            const int ex = mxfp8_exponent(amax);
+            uint32_t lo = 0, hi = 0;
+#pragma unroll
+            for (int i = 0; i < 2; ++i) {
+                lo |= f32x2_to_e4m3x2(scale_pow2(v[2 * i], ex), scale_pow2(v[2 * i + 1], ex)) << (16 * i);
+                hi |= f32x2_to_e4m3x2(scale_pow2(v[4 + 2 * i], ex), scale_pow2(v[5 + 2 * i], ex)) << (16 * i);
+            }
+            const int h = ch * 8, b = ch >> 2;
+            *reinterpret_cast<uint2*>(smem + kDecXOff + h) = make_uint2(lo, hi);
+            // the scale row of K step b / 4: block b % 4, once per lane quarter
+            smem[kDecTokScaleOff + (b / 4) * 16 + 4 * (ch & 3) + (b % 4)] = (uint8_t)(ex + 127);
+        }
+        // the quantised row and scales were written through the generic proxy;
+        // the MMAs read them through the async proxy
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         if (warp == 2) {
             int e;
             float wj;
