@@ -515,7 +515,10 @@ def oracle_rate(cfg, w, tk, seconds, prune=None):
         orc.layer_forward(w, xb, ids, wt)
         return tok, time.perf_counter() - t
 
-    n0, t0 = run(min(4, n_all))
+    # calibrate on two tokens per thread (the oracle runs tokens in parallel),
+    # after a first call that loads the library and its tables
+    run(min(2, n_all))
+    n0, t0 = run(min(2 * orc.max_threads(), n_all))
     per = t0 / n0
     n = int(max(4, min(n_all, seconds / max(per, 1e-9))))
     n, t = run(n)
