@@ -30,7 +30,8 @@ static EncodeTiledFn encode() {
     return reinterpret_cast<EncodeTiledFn>(p);
 }
 
-static int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows, bool fp4) {
+static int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t rows, uint32_t box_rows, bool fp4,
+                    bool swizzle = true) {
     EncodeTiledFn enc = encode();
     if (!enc) return -1;
     cuuint64_t dims[2] = {cols, rows};
@@ -39,7 +40,8 @@ static int make_map(CUtensorMap* m, const void* base, uint64_t cols, uint64_t ro
     cuuint32_t estr[2] = {1, 1};
     CUresult r = enc(m, fp4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : CU_TENSOR_MAP_DATA_TYPE_UINT8, 2,
                      const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                     CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+                     swizzle ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? 0 : (int)r;
 }
 
@@ -223,7 +225,7 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, 0, (blockIdx.x * tiles_per_cta * KB + i) * 128, b0 + 8 * s);
             else if (layout == 3)  // 256-row fp4 box (two 128-row tiles per copy)
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row, b0 + 8 * s);
-            else if (layout == 5)  // 256-row fp4 box, CTAs on disjoint 256-row tiles
+            else if (layout == 5 || layout == 7)  // 256-row fp4 box, CTAs on disjoint 256-row tiles
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row * 2, b0 + 8 * s);
             else if (layout == 6)  // contiguous 16 KB tiles: 256 rows of 64 bytes back to back
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, 0, (blockIdx.x * tiles_per_cta * KB + i) * 256, b0 + 8 * s);
@@ -250,7 +252,11 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                         if (mode & 64) {
                             // operands swapped: A = a fixed e4m3 tile (the token side), B = the
                             // streamed 256-row fp4 weight tile, N = 256: one MMA per K=32 step
-                            mma_mx(tmem, desc_sw128(b + 32 * kk), desc_sw128(a + 32 * kk),
+                            // bit 8: the weight tile read through a no-swizzle
+                            // descriptor (layout 7 writes it unswizzled; timing only)
+                            const uint64_t bd = (mode & 256) ? smem_desc(a + 32 * kk, 128, 1024, 0)
+                                                             : desc_sw128(a + 32 * kk);
+                            mma_mx(tmem, desc_sw128(b + 32 * kk), bd,
                                    idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
                                    (kk > 0 || rr > 0) ? 1u : 0u);
                         } else if (mode & 32) {
@@ -289,13 +295,14 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     if (layout == 1) r = make_map(&ta, a, 128, (uint64_t)rows * 32, 128, true);
     else if (layout == 2) { r = make_map(&ta, a, 4096, (uint64_t)rows / 2, 128, false); tx = 16384; }
     else if (layout == 3 || layout == 5) { r = make_map(&ta, a, 4096, (uint64_t)rows, 256, true); tx = 16384; slot = 32768; }
+    else if (layout == 7) { r = make_map(&ta, a, 4096, (uint64_t)rows, 256, true, false); tx = 16384; slot = 32768; }
     else if (layout == 6) { r = make_map(&ta, a, 128, (uint64_t)rows * 32, 256, true); tx = 16384; slot = 32768; }
     else r = make_map(&ta, a, 4096, (uint64_t)rows, 128, true);
     if (r) return 1000 + r;
     const long long need = (long long)(grid * (tiles_per_cta - 1) + grid) * 128 + (layout == 3 ? 128 : 0);
     if (need > (layout == 2 ? rows / 2 : rows)) return 3;
     if (layout == 1 && (long long)grid * tiles_per_cta * 32 * 128 > rows * 32) return 4;
-    if (layout == 5 && (long long)grid * tiles_per_cta * 256 > rows) return 4;
+    if ((layout == 5 || layout == 7) && (long long)grid * tiles_per_cta * 256 > rows) return 4;
     if (layout == 6 && (long long)grid * tiles_per_cta * 32 * 256 > rows * 32) return 4;
     if (slot == 32768 && stages > 6) return 5;
     // tiles + B tile + barrier offset + barriers/slot + 1024 alignment slack
@@ -423,6 +430,21 @@ __global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, in
     if (threadIdx.x == 0) {
         const uint32_t a = smem_u32(sm), b = smem_u32(sm + 32768), sf = smem_u32(sm + 49152);
         for (int it = 0; it < iters; ++it) {
+            if (mode >= 7) {
+                // mode 7: the decode orientation with the weight tile (B) in
+                // the no-swizzle K-major layout [K chunk][256 rows][16 B];
+                // mode 8: A a real swizzled 128-row tile, B swizzled (the
+                // grouped kernel's orientation)
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk) {
+                    const uint64_t ad = mode == 7 ? smem_desc(b + 32 * kk, 16, 0, 0) : desc_sw128(b + 32 * kk);
+                    const uint64_t bd = mode == 7 ? smem_desc(a + 8192 * kk, 4096, 128, 0) : desc_sw128(a + 32 * kk);
+                    mma_mx(tmem, ad, bd, idesc_mx(kFmtE4M3, a_fmt, 128, 256, kk, kk), tmem + 256, tmem + 260,
+                           (it | kk) ? 1u : 0u);
+                }
+                if (commit) mma_commit(smem_u32(bar + 1));
+                continue;
+            }
             if (mode >= 5) {
                 // the decode gate/up pattern: A's scales resident (column
                 // 256), the weight tile's two scale atoms copied per stage
@@ -488,7 +510,7 @@ extern "C" int probe_mma_mix(int grid, int iters, int n, int ncp, int commit, in
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
-    if (mode < 0 || mode > 6) return 3;
+    if (mode < 0 || mode > 8) return 3;
     k_mma_mix<<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
