@@ -65,6 +65,30 @@ def default_steps(cfg):
     return {1: 32768, 2: 1024, 3: 256, 4: 32}[cfg.index]
 
 
+# ------------------------------------------------------------------ ranks --
+# Replicas: every rank runs its own layer on its own tokens (no exchange);
+# the job's time is the slowest rank's and its rate counts every rank's tokens.
+def rank_seed(cfg, rank):
+    """Token seed of a rank: each replica draws its own tokens."""
+    return cfg.default_seed + 7919 * rank
+
+
+def max_over_ranks(ms, world, dev):
+    """The slowest rank's time (all ranks get it)."""
+    if world == 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    tm = torch.tensor([ms], dtype=torch.float64, device=dev)
+    dist.all_reduce(tm, op=dist.ReduceOp.MAX)
+    return float(tm.item())
+
+
+def job_rate(world, tokens_per_rank, ms):
+    """Tokens per second of the whole job: every rank's tokens over the slowest rank's time."""
+    return round(world * tokens_per_rank / (ms * 1e-3), 1)
+
+
 def config_json(cfg, args, world):
     return {"workload": cfg.name, "hidden": cfg.H, "inter": cfg.I, "experts": cfg.E,
             "top_k": cfg.k, "tokens_per_step": cfg.T, "router": cfg.router,
@@ -174,7 +198,7 @@ def run_ours(args, cfg, rank, world, local_rank):
 
     # distinct inputs: one token per step for decode, else a few batches cycled
     S = (K + W) if cfg.T == 1 else min(K + W, 4)
-    tk = make_tokens(cfg, seed=cfg.default_seed + 7919 * rank, n=S * cfg.T)
+    tk = make_tokens(cfg, seed=rank_seed(cfg, rank), n=S * cfg.T)
     x_all = torch.from_numpy(tk.x_bits.view(np.int16).reshape(S, cfg.T, cfg.H).copy()).to(dev)
     lg_all = torch.from_numpy(tk.logits.reshape(S, cfg.T, cfg.E).copy()).to(dev)
     hashed = cfg.router == "hash"
@@ -256,11 +280,7 @@ def run_ours(args, cfg, rank, world, local_rank):
     if world > 1:
         dist.barrier()
     clk_rows = sampler.stop()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
     bqe.moe_check(layer)
 
     if args.trace:
@@ -313,14 +333,13 @@ def run_ours(args, cfg, rank, world, local_rank):
                          "peak_source": ("measured bf16_tflops_sustained x 2 (fp8 / bf16 nominal ratio)"
                                          if "bf16_tflops_sustained" in peaks else "fallback 1.7 PF/s x 2")})
 
-    tokens = K * cfg.T
-    value = world * tokens / (ms * 1e-3)
+    value = job_rate(world, K * cfg.T, ms)
     # rows in the timed region within the clock sampling
     in_region = [r for r in clk_rows if _ts_in(r[0], wall0, wall1)]
     clocks = ClockSampler.summary(in_region if in_region else clk_rows)
     clocks["window"] = "timed region" if in_region else "around the timed region"
 
-    res = {"metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world,
+    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
            "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
            "dtype": "mxfp4 x mxfp8 -> f32 accumulate", "data": "synthetic (seeded)",
@@ -481,12 +500,8 @@ def run_e2e(args, cfg, layer, tk, S, K, W, world, dev):
             g.replay()
         t1.record(stream)
     torch.cuda.synchronize()
-    ms = t0.elapsed_time(t1)
-    if world > 1:
-        tm = torch.tensor([ms], device=dev)
-        dist.all_reduce(tm, op=dist.ReduceOp.MAX)
-        ms = float(tm.item())
-    return {"value": round(world * K * cfg.T / (ms * 1e-3), 1), "unit": UNIT,
+    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    return {"value": job_rate(world, K * cfg.T, ms), "unit": UNIT,
             "h2d_bytes_per_step": cfg.T * cfg.H * 2 + cfg.T * cfg.E * 4,
             "d2h_bytes_per_step": cfg.T * cfg.H * 4,
             "path": ("moe_forward_host (pinned host in/out, CUDA graphs; one token: the decode kernel "
