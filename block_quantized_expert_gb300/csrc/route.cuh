@@ -74,19 +74,24 @@ __device__ __forceinline__ int prune_tail(float& wj, int k, const RoutePrune& p,
 // w_j = w_scale * s_j / sum (guide, section 3.2); then the tail pruning, if
 // any (pruned slots: id -1, weight 0).
 // Routing of one token by one warp: writes ids_t[0..k) and w_t[0..k).
-__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, float w_scale,
-                            const RoutePrune& prune, int32_t* __restrict__ ids_t,
-                            float* __restrict__ w_t, uint32_t* err, int lane) {
+// The k argmax passes of route_token over the lane's logits held in
+// registers (kPer per lane: experts lane, lane + 32, ...; E <= 32 kPer).
+template <int kPer>
+__device__ __forceinline__ bool route_select(const float* __restrict__ row, int E, int k, int lane, int& my_sel,
+                                             float& my_logit) {
+    float lv[kPer];
+#pragma unroll
+    for (int i = 0; i < kPer; ++i) lv[i] = lane + 32 * i < E ? __ldg(row + lane + 32 * i) : 0.f;
     uint32_t taken = 0;  // bit i <-> expert lane + 32 i
-    int my_sel = -1;     // lane j keeps the j-th selection
-    float my_logit = 0.f;
     bool ok = true;
     for (int j = 0; j < k; ++j) {
         float best = -INFINITY;
         int bi = INT_MAX;
-        for (int i = 0, e = lane; e < E; ++i, e += 32) {
-            if ((taken >> i) & 1u) continue;
-            float v = __ldg(row + e);
+#pragma unroll
+        for (int i = 0; i < kPer; ++i) {
+            const int e = lane + 32 * i;
+            if (e >= E || ((taken >> i) & 1u)) continue;
+            const float v = lv[i];
             if (v > best || (v == best && e < bi)) { best = v; bi = e; }
         }
 #pragma unroll
@@ -99,6 +104,16 @@ __device__ __forceinline__ void route_token(const float* __restrict__ row, int E
         if (lane == j) { my_sel = bi; my_logit = best; }
         if (bi >= 0 && (bi & 31) == lane) taken |= 1u << (bi >> 5);
     }
+    return ok;
+}
+
+__device__ __forceinline__ void route_token(const float* __restrict__ row, int E, int k, float w_scale,
+                            const RoutePrune& prune, int32_t* __restrict__ ids_t,
+                            float* __restrict__ w_t, uint32_t* err, int lane) {
+    int my_sel = -1;     // lane j keeps the j-th selection
+    float my_logit = 0.f;
+    const bool ok = E <= 256 ? route_select<8>(row, E, k, lane, my_sel, my_logit)
+                             : route_select<32>(row, E, k, lane, my_sel, my_logit);
     float s = 0.f;
     if (lane < k && my_sel >= 0) s = sqrt_softplus(my_logit);
     float sum = 0.f;
