@@ -84,6 +84,17 @@ def max_over_ranks(ms, world, dev):
     return float(tm.item())
 
 
+def chunk_spread(ms_per_step):
+    """Median, min, max and std of the per-step time over the timed region's
+    graph chunks; spread_pct = (max - min) / median (above 15 % is flagged)."""
+    a = np.asarray(ms_per_step, dtype=np.float64)
+    med = float(np.median(a))
+    spread = float((a.max() - a.min()) / med * 100.0) if med > 0 else 0.0
+    return {"chunks": int(a.size), "median_ms": round(med, 6), "min_ms": round(float(a.min()), 6),
+            "max_ms": round(float(a.max()), 6), "std_ms": round(float(a.std()), 6),
+            "spread_pct": round(spread, 2), "spread_over_15pct": spread > 15.0}
+
+
 def job_rate(world, tokens_per_rank, ms):
     """Tokens per second of the whole job: every rank's tokens over the slowest rank's time."""
     return round(world * tokens_per_rank / (ms * 1e-3), 1)
@@ -270,13 +281,22 @@ def run_ours(args, cfg, rank, world, local_rank):
     t0 = torch.cuda.Event(enable_timing=True)
     t1 = torch.cuda.Event(enable_timing=True)
     wall0 = time.time()
+    # an event after every graph (chunk of args.graph_chunk steps) gives the
+    # spread of the per-step time across the timed region
+    chunk_ev = [torch.cuda.Event(enable_timing=True) for _ in graphs]
     with torch.cuda.stream(stream):
         t0.record(stream)
-        for g in graphs:
+        for g, ce in zip(graphs, chunk_ev):
             g.replay()
+            ce.record(stream)
         t1.record(stream)
     torch.cuda.synchronize()
     wall1 = time.time()
+    chunk_ms, prev = [], t0
+    for ci, ce in enumerate(chunk_ev):
+        n_steps = min(args.graph_chunk, K - ci * args.graph_chunk)
+        chunk_ms.append(prev.elapsed_time(ce) / n_steps)
+        prev = ce
     if world > 1:
         dist.barrier()
     clk_rows = sampler.stop()
@@ -345,6 +365,7 @@ def run_ours(args, cfg, rank, world, local_rank):
            "dtype": "mxfp4 x mxfp8 -> f32 accumulate", "data": "synthetic (seeded)",
            "config": config_json(cfg, args, world),
            "gpu_launches": int(launches),
+           "per_step_spread": chunk_spread(chunk_ms),
            "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
            "experts_touched_per_step": avg_touched,
            "roofline": dict(roof, **{
