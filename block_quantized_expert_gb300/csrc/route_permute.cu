@@ -591,6 +591,11 @@ cudaError_t launch_quantize_scatter(moe_layer* L, const uint16_t* x, int T, cuda
 // out[t] = sum over the token's experts in ascending expert order (equal ids
 // in j order) of w * y[row] (+ the shared expert): a fixed fp32 order, no
 // atomics (guide, section 3.2, the FFN output equation).
+// One thread per token and group of kCmbQ float4 columns, 128 features apart
+// (every load of a warp is 512 contiguous bytes of one row; a warp covers
+// 128 kCmbQ features, so H must be a multiple of that): the token's ids, row
+// positions and weights are read once for them all.
+template <int kCmbQ>
 __global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids,
                                                  const float* __restrict__ w,
                                                  const int32_t* __restrict__ row_pos,
@@ -599,10 +604,11 @@ __global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids
                                                  int k, float* __restrict__ out) {
     pdl_launch_dependents();
     pdl_wait();
-    const int H4 = H / 4;
+    const int G = H / (4 * kCmbQ);  // column groups per token
     const long long i = (long long)blockIdx.x * blockDim.x + threadIdx.x;
-    if (i >= (long long)T * H4) return;
-    const int t = (int)(i / H4), c = (int)(i % H4) * 4;
+    if (i >= (long long)T * G) return;
+    const int t = (int)(i / G), g = (int)(i % G);
+    const int c = (g / 32) * (128 * kCmbQ) + (g % 32) * 4;  // first column; then + 128 q
     int order[kMaxTopK];
     int idv[kMaxTopK];
 #pragma unroll
@@ -619,39 +625,55 @@ __global__ void __launch_bounds__(256) k_combine(const int32_t* __restrict__ ids
             }
     // every row's y and weight in flight at once (addresses in ascending
     // expert order), then summed in that order; a dropped row adds nothing
-    float4 yv[kMaxTopK];
-    float wv[kMaxTopK];
     bool live[kMaxTopK];
+    float wv[kMaxTopK];
+    int rr[kMaxTopK];
 #pragma unroll
     for (int a = 0; a < kMaxTopK; ++a) {
-        const int r = t * k + order[a];
-        live[a] = a < k && row_pos[r] >= 0;
-        yv[a] = live[a] ? *reinterpret_cast<const float4*>(y + (size_t)r * H + c) : make_float4(0.f, 0.f, 0.f, 0.f);
-        wv[a] = live[a] ? w[r] : 0.f;
+        rr[a] = t * k + order[a];
+        live[a] = a < k && row_pos[rr[a]] >= 0;
+        wv[a] = live[a] ? w[rr[a]] : 0.f;
     }
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float4 acc[kCmbQ];
+#pragma unroll
+    for (int q = 0; q < kCmbQ; ++q) acc[q] = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int a = 0; a < kMaxTopK; ++a) {
-        if (live[a]) {
-            const float wt = wv[a];
-            acc.x += wt * yv[a].x; acc.y += wt * yv[a].y; acc.z += wt * yv[a].z; acc.w += wt * yv[a].w;
+        if (!live[a]) continue;
+        float4 yv[kCmbQ];
+#pragma unroll
+        for (int q = 0; q < kCmbQ; ++q)
+            yv[q] = *reinterpret_cast<const float4*>(y + (size_t)rr[a] * H + c + 128 * q);
+        const float wt = wv[a];
+#pragma unroll
+        for (int q = 0; q < kCmbQ; ++q) {
+            acc[q].x += wt * yv[q].x; acc[q].y += wt * yv[q].y; acc[q].z += wt * yv[q].z; acc[q].w += wt * yv[q].w;
         }
     }
     if (y_sh) {
-        const float4 v = *reinterpret_cast<const float4*>(y_sh + (size_t)t * H + c);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+#pragma unroll
+        for (int q = 0; q < kCmbQ; ++q) {
+            const float4 v = *reinterpret_cast<const float4*>(y_sh + (size_t)t * H + c + 128 * q);
+            acc[q].x += v.x; acc[q].y += v.y; acc[q].z += v.z; acc[q].w += v.w;
+        }
     }
-    *reinterpret_cast<float4*>(out + (size_t)t * H + c) = acc;
+#pragma unroll
+    for (int q = 0; q < kCmbQ; ++q) *reinterpret_cast<float4*>(out + (size_t)t * H + c + 128 * q) = acc[q];
 }
 
 cudaError_t launch_combine(moe_layer* L, const int32_t* ids, const float* w, int T,
                            float* out, cudaStream_t s) {
-    const long long n = (long long)T * (L->cfg.hidden / 4);
+    const int H = L->cfg.hidden;  // a multiple of 256
+    const int q = H % 512 == 0 ? 4 : 2;
+    const long long n = (long long)T * (H / (4 * q));
+    const dim3 grid((unsigned)((n + 255) / 256));
     L->launches += 1;
-    return launch_pdl(k_combine, dim3((unsigned)((n + 255) / 256)), dim3(256), 0, s, ids, w,
-                      (const int32_t*)L->row_pos, (const float*)L->y,
-                      (const float*)(L->cfg.has_shared ? L->y_sh : nullptr), T, L->cfg.hidden,
-                      L->cfg.top_k, out);
+    const float* ysh = L->cfg.has_shared ? L->y_sh : nullptr;
+    if (q == 4)
+        return launch_pdl(k_combine<4>, grid, dim3(256), 0, s, ids, w, (const int32_t*)L->row_pos,
+                          (const float*)L->y, ysh, T, H, L->cfg.top_k, out);
+    return launch_pdl(k_combine<2>, grid, dim3(256), 0, s, ids, w, (const int32_t*)L->row_pos,
+                      (const float*)L->y, ysh, T, H, L->cfg.top_k, out);
 }
 
 // ----------------------------------------------------------- test helpers --
@@ -732,7 +754,8 @@ cudaError_t kernels_init() {
     if (e == cudaSuccess) e = max_carveout(k_route_hash);
     if (e == cudaSuccess) e = max_carveout(k_quantize<0>);
     if (e == cudaSuccess) e = max_carveout(k_quantize<1>);
-    if (e == cudaSuccess) e = max_carveout(k_combine);
+    if (e == cudaSuccess) e = max_carveout(k_combine<2>);
+    if (e == cudaSuccess) e = max_carveout(k_combine<4>);
     if (e == cudaSuccess)
         e = cudaFuncSetAttribute(k_perm_place, cudaFuncAttributeMaxDynamicSharedMemorySize, 48 * kMaxExperts);
     if (e == cudaSuccess) e = max_carveout(k_perm_place);
