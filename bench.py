@@ -457,6 +457,15 @@ def trace_report(bqe, layer, step, i, dev):
             if v.size:
                 rep[key] = [round((np.percentile(v, p) - e0) / 1e3, 2) for p in (0, 50, 100)]
         print("TRACE", json.dumps(rep), file=sys.stderr, flush=True)
+        if t[0, :, 11].max() <= 0:  # the phase stamps are not compiled in
+            return
+        # the CTAs that finish last: their stamps (us from the first entry)
+        last = np.argsort(-t[0, :, 11])[:8]
+        slow = {int(b): [round((t[0, b, c] - e0) / 1e3, 2) if t[0, b, c] > 0 else None
+                         for c in (2, 3, 4, 10, 5, 6, 7, 11)] for b in last}
+        print("TRACE", json.dumps({"launch": "decode_last_ctas", "columns": [
+            "producer_start", "first_weights", "gateup_issued", "gateup_written", "down_loads_start",
+            "h_landed", "down_issued", "down_written"], "ctas": slow}), file=sys.stderr, flush=True)
         return
     names = ["gateup", "down", "shared_gateup", "shared_down"]
     for j in range(4):
