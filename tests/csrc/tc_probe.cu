@@ -256,7 +256,9 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                             // descriptor (layout 7 writes it unswizzled; timing only)
                             const uint64_t bd = (mode & 256) ? smem_desc(a + 32 * kk, 128, 1024, 0)
                                                              : desc_sw128(a + 32 * kk);
-                            mma_mx(tmem, desc_sw128(b + 32 * kk), bd,
+                            // bit 9: the token operand one aliased 8-row group (no swizzle, stride 0)
+                            const uint64_t ad = (mode & 512) ? smem_desc(b + 32 * kk, 16, 0, 0) : desc_sw128(b + 32 * kk);
+                            mma_mx(tmem, ad, bd,
                                    idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
                                    (kk > 0 || rr > 0) ? 1u : 0u);
                         } else if (mode & 32) {
@@ -583,6 +585,221 @@ extern "C" int probe_stream_lsu(const uint8_t* a, long long rows, int grid, int 
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
     k_stream_lsu<<<grid, 160, smem>>>(a, tiles_per_cta, 32, stages, stamps, ok);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// Contention probe: warp 1 (lane 0) runs the decode kernel's MMA loop (four
+// N = 256 block-scaled MMAs per iteration on resident operands) while warps
+// 2-9 keep shared memory busy: load = 1 writes 16 bytes per thread per step
+// into a 32 KB region (generic-proxy stores), load = 2 reads it, load = 0
+// idles.  stamps[blockIdx.x] = the MMA loop's wall time (ns).
+__global__ void __launch_bounds__(320, 1) k_contend(int iters, int load, unsigned long long* stamps, int* ok_out) {
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    // [0, 32K) weights (B), [32K, 48K) token tile (A), [48K, 49.5K) scale atoms,
+    // [64K, 96K) the busy region, then barriers
+    uint64_t* bar = reinterpret_cast<uint64_t*>(sm + 98304);
+    uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
+    volatile int* stop = reinterpret_cast<volatile int*>(slot + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(slot + 2);
+    const int warp = threadIdx.x >> 5;
+    for (int i = threadIdx.x; i < 98304 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(sm)[i] = 0x38383838u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (threadIdx.x == 0) {
+        mbar_init(smem_u32(bar), 1);
+        *stop = 0;
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(slot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *slot;
+    if (threadIdx.x == 32) {
+        const uint32_t b = smem_u32(sm), a = smem_u32(sm + 32768), sf = smem_u32(sm + 49152);
+        tmem_cp_32x128_x4(tmem + 256, desc_sf(sf));
+        tmem_cp_32x128_x4(tmem + 260, desc_sf(sf + 512));
+        tmem_cp_32x128_x4(tmem + 264, desc_sf(sf + 1024));
+        const unsigned long long t0 = globaltimer();
+        for (int it = 0; it < iters; ++it) {
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_mx(tmem, smem_desc(a + 32 * kk, 16, 0, 0), desc_sw128(b + 32 * kk),
+                       idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260, (it | kk) ? 1u : 0u);
+        }
+        mma_commit(smem_u32(bar));
+        const bool ok = mbar_wait(smem_u32(bar), 0, 2000000000ull, abort_flag);
+        stamps[blockIdx.x] = globaltimer() - t0;
+        if (!ok) atomicExch(ok_out, 0);
+        *stop = 1;
+    } else if (warp >= 2) {
+        const int t = threadIdx.x - 64;
+        uint4* busy = reinterpret_cast<uint4*>(sm + 65536);
+        uint4 acc = make_uint4(0, 0, 0, 0);
+        const unsigned long long t0 = globaltimer();
+        for (int i = 0; !*stop && globaltimer() - t0 < 200000000ull; ++i) {
+#pragma unroll 8
+            for (int j = 0; j < 8; ++j) {
+                const int idx = (t + 256 * ((i * 8 + j) & 7)) & 2047;  // 2048 x 16 B = 32 KB
+                if (load == 1) {
+                    busy[idx] = make_uint4(i, j, t, 0);
+                } else if (load == 2) {
+                    const uint4 v = busy[idx];
+                    acc.x ^= v.x; acc.y += v.y;
+                }
+            }
+        }
+        if (acc.x == 0x12345678u) stamps[gridDim.x + blockIdx.x] = acc.y;  // keeps the reads
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+extern "C" int probe_contend(int grid, int iters, int load, unsigned long long* stamps, int* ok, float* ms) {
+    const int smem = 98304 + 64 + 1024;
+    cudaFuncSetAttribute(k_contend, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_contend<<<grid, 320, smem>>>(iters, load, stamps, ok);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// Weight stream with the copies done by the load/store units instead of the
+// TMA: warps 0-7 (one weight row per thread) load each 16 KB stage (256 rows
+// x 64 bytes of packed fp4, plus the stage's 1 KB of scale atoms) into
+// registers kLd stages ahead and store them into the 16-byte-slot, 128-byte-
+// swizzled layout the MMA reads (8 data bytes per slot); warp 8 issues the
+// decode kernel's MMAs (four N = 256 per stage, two scale copies) with
+// mode & 1, else frees the stage at once.  Global layout: rows of 2048 bytes
+// (K = 4096), CTA c streams rows [256 (c + G t), +256) x 32 K steps.
+constexpr int kLd = 6;
+__global__ void __launch_bounds__(320, 1)
+k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, int tiles_per_cta, int stages,
+             int mode, int* ok_out) {
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    const int slot = 32768 + 1024;  // padded weights + scale atoms
+    uint8_t* tok = sm + stages * slot;  // 4 KB token area (A, aliased)
+    uint64_t* bars = reinterpret_cast<uint64_t*>(tok + 4096);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * stages);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t b0 = smem_u32(bars);
+    for (int i = threadIdx.x; i < 4096 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(tok)[i] = 0x38383838u;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < stages; ++s) { mbar_init(b0 + 8 * s, 256); mbar_init(b0 + 8 * (stages + s), 1); }
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (warp == 9) tmem_alloc(smem_u32(tslot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    const int total = tiles_per_cta * 32;
+    if (warp < 8) {
+        // four lanes per row (16 bytes each, a row's 64 bytes contiguous):
+        // thread p covers rows p / 4 + 64 j (j < 4), chunk c = p % 4
+        const int p = threadIdx.x, c = p & 3, r0 = p >> 2;
+        uint4 reg[kLd][4];
+        uint4 sreg[kLd];
+        auto load = [&](int i, int q) {
+            const long long row0 = (long long)(blockIdx.x + (i / 32) * gridDim.x) * 256;
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+                reg[q][j] = __ldcs(reinterpret_cast<const uint4*>(w + (row0 + r0 + 64 * j) * 2048 + (i % 32) * 64) + c);
+            if (p < 64) sreg[q] = __ldcs(reinterpret_cast<const uint4*>(sf_src + ((size_t)blockIdx.x * total + i) * 1024) + p);
+        };
+#pragma unroll
+        for (int q = 0; q < kLd; ++q)
+            if (q < total) load(q, q);
+        bool run = true;
+        for (int i0 = 0; i0 < total && run; i0 += kLd) {
+#pragma unroll
+            for (int q = 0; q < kLd; ++q) {  // compile-time register slot q
+                const int i = i0 + q;
+                if (i >= total) break;
+                const int s = i % stages;
+                const uint32_t ph = (uint32_t)((i / stages) & 1);
+                if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) {
+                    *abort_flag = 1;
+                    run = false;
+                    break;
+                }
+                uint8_t* st = sm + s * slot;
+                // packed chunk c of row r holds 32 codes = element slots 2c, 2c + 1
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const int r = r0 + 64 * j;
+                    const uint32_t e0 = (2 * c) ^ (r & 7), e1 = (2 * c + 1) ^ (r & 7);
+                    uint8_t* line = st + (r >> 3) * 1024 + (r & 7) * 128;
+                    *reinterpret_cast<uint2*>(line + e0 * 16) = make_uint2(reg[q][j].x, reg[q][j].y);
+                    *reinterpret_cast<uint2*>(line + e1 * 16) = make_uint2(reg[q][j].z, reg[q][j].w);
+                }
+                if (p < 64) reinterpret_cast<uint4*>(st + 32768)[p] = sreg[q];
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                mbar_arrive(b0 + 8 * s);
+                if (i + kLd < total) load(i + kLd, q);
+            }
+        }
+    } else if (warp == 8 && lane == 0) {
+        const uint32_t a = smem_u32(tok);
+        for (int i = 0; i < total; ++i) {
+            const int s = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            if (!mbar_wait(b0 + 8 * s, ph, 200000000ull, abort_flag)) { *abort_flag = 1; break; }
+            if (mode & 1) {
+                tc_fence_after();
+                const uint32_t st = smem_u32(sm + s * slot);
+                tmem_cp_32x128_x4(tmem + 260, desc_sf(st + 32768));
+                tmem_cp_32x128_x4(tmem + 264, desc_sf(st + 32768 + 512));
+#pragma unroll
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_mx(tmem, smem_desc(a + 32 * kk, 16, 0, 0), desc_sw128(st + 32 * kk),
+                           idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260, (i | kk) ? 1u : 0u);
+                mma_commit(b0 + 8 * (stages + s));
+            } else {
+                mbar_arrive(b0 + 8 * (stages + s));
+            }
+        }
+        if (mode & 1) {  // the last MMAs complete before the CTA frees its tensor memory
+            const int s = (total - 1) % stages;
+            mbar_wait(b0 + 8 * (stages + s), (uint32_t)(((total - 1) / stages) & 1), 200000000ull, abort_flag);
+        }
+    }
+    __syncwarp();
+    __syncthreads();
+    if (*abort_flag) { spin_ns(200000); if (threadIdx.x == 0) atomicExch(ok_out, 0); }
+    if (warp == 9) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+extern "C" int probe_stream_ldg(const uint8_t* w, long long bytes, const uint8_t* sf, long long sf_bytes, int grid,
+                                int tiles_per_cta, int stages, int mode, int* ok, float* ms) {
+    if ((long long)grid * tiles_per_cta * 256 * 2048 > bytes) return 3;
+    if ((long long)grid * tiles_per_cta * 32 * 1024 > sf_bytes) return 4;
+    if (stages < 2 || stages > 6) return 5;
+    const int smem = stages * (32768 + 1024) + 4096 + 16 * stages + 16 + 1024;
+    cudaFuncSetAttribute(k_stream_ldg, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_stream_ldg<<<grid, 320, smem>>>(w, sf, tiles_per_cta, stages, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);

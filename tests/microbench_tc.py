@@ -32,6 +32,8 @@ def load():
                                  vp, C.c_int]
     lib.probe_stream_lsu.argtypes = [vp, C.c_longlong, C.c_int, C.c_int, C.c_int, vp, vp, vp]
     lib.probe_mma_peak.argtypes = [C.c_int, C.c_int, C.c_int, C.c_uint32, vp, vp]
+    lib.probe_contend.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp]
+    lib.probe_stream_ldg.argtypes = [vp, C.c_longlong, vp, C.c_longlong, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp]
     lib.probe_mma_mix.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_uint32, C.c_int,
                                   vp, vp]
     return lib
@@ -42,12 +44,45 @@ def main():
     ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "microbench_tc.json"))
     ap.add_argument("--only-mix", action="store_true", help="only the per-stage MMA group issue costs")
     ap.add_argument("--only-stream", action="store_true", help="only the 256-row weight-box TMA streams")
+    ap.add_argument("--only-ldg", action="store_true",
+                    help="weight stream copied by the load/store units instead of the TMA, with / without MMAs")
+    ap.add_argument("--only-contend", action="store_true",
+                    help="MMA loop time with shared-memory stores / loads by other warps")
     args = ap.parse_args()
     lib = load()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     ms = C.c_float()
     ok = torch.ones(1, dtype=torch.int32, device="cuda")
     out = {"sms": sms}
+    if args.only_ldg:
+        tiles = 8
+        W = torch.zeros(sms * tiles * 256 * 2048, dtype=torch.uint8, device="cuda")
+        SF = torch.full((sms * tiles * 32 * 1024,), 127, dtype=torch.uint8, device="cuda")
+        for stages, mode in ((6, 0), (6, 1), (4, 1), (5, 1), (6, 1)):
+            for _ in range(2):
+                ok.fill_(1)
+                rc = lib.probe_stream_ldg(W.data_ptr(), W.numel(), SF.data_ptr(), SF.numel(), sms, tiles, stages,
+                                          mode, ok.data_ptr(), C.byref(ms))
+            key = f"ldg_stages{stages}_mode{mode}"
+            out[key] = {"GBs": round(sms * tiles * 32 * (16384 + 1024) / ms.value / 1e6, 1),
+                        "us_per_stage": round(ms.value * 1e3 / (tiles * 32), 3), "rc": rc, "ok": int(ok.item())}
+            print(key, out[key], flush=True)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
+    if args.only_contend:
+        stamps = torch.zeros(2 * sms, dtype=torch.int64, device="cuda")
+        iters = 4000
+        for busy in (0, 1, 2, 0):
+            ok.fill_(1)
+            rc = lib.probe_contend(sms, iters, busy, stamps.data_ptr(), ok.data_ptr(), C.byref(ms))
+            ns = stamps[:sms].float().mean().item() / iters
+            key = f"contend_load{busy}"
+            out[key] = {"ns_per_mma_group": round(ns, 1), "rc": rc, "ok": int(ok.item())}
+            print(key, out[key], flush=True)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
     if args.only_mix:
         mma_mix(lib, sms, ok, ms, out)
         os.makedirs(os.path.dirname(args.out), exist_ok=True)
@@ -75,7 +110,8 @@ def main():
 
     if args.only_stream:
         for layout, stages, mode in ((5, 6, 0), (5, 6, 128), (5, 6, 1 | 64), (5, 6, 1 | 64 | 128),
-                                     (6, 6, 128), (6, 6, 1 | 64 | 128), (7, 6, 0), (7, 6, 1 | 64 | 256)):
+                                     (6, 6, 128), (6, 6, 1 | 64 | 128), (7, 6, 0), (7, 6, 1 | 64 | 256),
+                                     (5, 6, 1 | 64 | 512), (5, 6, 1 | 64 | 128 | 512)):
             for _ in range(2):
                 ok.fill_(1)
                 rc = lib.probe_stream(A.data_ptr(), rows, sms, 8, stages, mode, 0, stamps.data_ptr(),
