@@ -170,3 +170,44 @@ def test_decode_host_entry_zero_copy_and_staged(decode_layer):
         bqe.moe_check(layer)
         _, _, out_d, _ = _route_forward(layer, lg, xb, 0)
         assert oh.numpy().tobytes() == out_d.cpu().numpy().tobytes()
+
+
+def test_two_layers_interleaved_in_one_graph(decode_layer, tiny_layer):
+    """Decode calls of two layers alternating on one stream (each kernel
+    launched while the previous layer's still runs, as consecutive layers
+    of a model are): every call gives the bytes of the same call made alone."""
+    cfg_a, _, la = decode_layer
+    cfg_b, _, lb = tiny_layer
+    bqe.moe_set_gemm_path(la, 0)
+    bqe.moe_set_gemm_path(lb, 0)
+    ta, tb = G.tokens(1, n=3), G.tokens(0, n=3)
+
+    def bufs(cfg, tk, t):
+        return (G.to_dev(tk.logits[t:t + 1].astype(np.float32)), G.to_dev(tk.x_bits[t:t + 1].astype(np.uint16), torch.int16),
+                torch.empty((1, cfg.k), dtype=torch.int32, device=G.DEV),
+                torch.empty((1, cfg.k), dtype=torch.float32, device=G.DEV),
+                torch.empty((1, cfg.H), dtype=torch.float32, device=G.DEV))
+
+    calls = []
+    for t in range(3):
+        calls.append((la, bufs(cfg_a, ta, t)))
+        calls.append((lb, bufs(cfg_b, tb, t)))
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        for L, (lg, xb, ids, w, out) in calls:  # warm-up, eager
+            bqe.moe_route_forward(L, lg, xb, ids, w, out)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            for L, (lg, xb, ids, w, out) in calls:
+                bqe.moe_route_forward(L, lg, xb, ids, w, out)
+    g.replay()
+    torch.cuda.synchronize()
+    bqe.moe_check(la)
+    bqe.moe_check(lb)
+    for L, (lg, xb, ids, w, out) in calls:
+        ids1, w1, out1 = torch.empty_like(ids), torch.empty_like(w), torch.empty_like(out)
+        bqe.moe_route_forward(L, lg, xb, ids1, w1, out1)
+        torch.cuda.synchronize()
+        assert torch.equal(ids, ids1) and torch.equal(w, w1)
+        assert out.cpu().numpy().tobytes() == out1.cpu().numpy().tobytes()
