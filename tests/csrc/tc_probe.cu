@@ -688,8 +688,10 @@ extern "C" int probe_contend(int grid, int iters, int load, unsigned long long* 
 // (K = 4096), CTA c streams rows [256 (c + G t), +256) x 32 K steps.
 constexpr int kLd = 6;
 __global__ void __launch_bounds__(320, 1)
-k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, int tiles_per_cta, int stages,
-             int mode, int* ok_out) {
+k_stream_ldg(const __grid_constant__ CUtensorMap tmW, const uint8_t* __restrict__ w,
+             const uint8_t* __restrict__ sf_src, int tiles_per_cta, int stages, int mode, int* ok_out) {
+    // mode bit 1 (hybrid): odd stages are copied by the TMA (warp 9), even
+    // stages by the load/store units; `stages` must then be even
     extern __shared__ uint8_t raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     const int slot = 32768 + 1024;  // padded weights + scale atoms
@@ -701,7 +703,10 @@ k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, 
     const uint32_t b0 = smem_u32(bars);
     for (int i = threadIdx.x; i < 4096 / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(tok)[i] = 0x38383838u;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < stages; ++s) { mbar_init(b0 + 8 * s, 256); mbar_init(b0 + 8 * (stages + s), 1); }
+        for (int s = 0; s < stages; ++s) {
+            mbar_init(b0 + 8 * s, ((mode & 2) && (s & 1)) ? 1 : 256);
+            mbar_init(b0 + 8 * (stages + s), 1);
+        }
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -716,6 +721,8 @@ k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, 
         // four lanes per row (16 bytes each, a row's 64 bytes contiguous):
         // thread p covers rows p / 4 + 64 j (j < 4), chunk c = p % 4
         const int p = threadIdx.x, c = p & 3, r0 = p >> 2;
+        const int step = (mode & 2) ? 2 : 1;        // LSU stage j is global stage step * j
+        const int n_lsu = (total + step - 1) / step;
         uint4 reg[kLd][4];
         uint4 sreg[kLd];
         auto load = [&](int i, int q) {
@@ -727,13 +734,14 @@ k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, 
         };
 #pragma unroll
         for (int q = 0; q < kLd; ++q)
-            if (q < total) load(q, q);
+            if (q < n_lsu) load(step * q, q);
         bool run = true;
-        for (int i0 = 0; i0 < total && run; i0 += kLd) {
+        for (int j0 = 0; j0 < n_lsu && run; j0 += kLd) {
 #pragma unroll
             for (int q = 0; q < kLd; ++q) {  // compile-time register slot q
-                const int i = i0 + q;
-                if (i >= total) break;
+                const int j = j0 + q;
+                if (j >= n_lsu) break;
+                const int i = step * j;
                 const int s = i % stages;
                 const uint32_t ph = (uint32_t)((i / stages) & 1);
                 if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) {
@@ -754,8 +762,21 @@ k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, 
                 if (p < 64) reinterpret_cast<uint4*>(st + 32768)[p] = sreg[q];
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 mbar_arrive(b0 + 8 * s);
-                if (i + kLd < total) load(i + kLd, q);
+                if (j + kLd < n_lsu) load(step * (j + kLd), q);
             }
+        }
+    } else if (warp == 9 && lane == 0 && (mode & 2)) {
+        // the TMA's share: the odd stages
+        for (int i = 1; i < total; i += 2) {
+            const int s = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) { *abort_flag = 1; break; }
+            uint8_t* st = sm + s * slot;
+            const uint32_t fb = b0 + 8 * s;
+            mbar_arrive_expect_tx(fb, 16384u + 1024u);
+            const int row = (blockIdx.x + (i / 32) * gridDim.x) * 256;
+            tma_load_2d(smem_u32(st), &tmW, (i % 32) * 128, row, fb);
+            bulk_load(smem_u32(st + 32768), sf_src + ((size_t)blockIdx.x * total + i) * 1024, 1024, fb);
         }
     } else if (warp == 8 && lane == 0) {
         const uint32_t a = smem_u32(tok);
@@ -791,6 +812,9 @@ k_stream_ldg(const uint8_t* __restrict__ w, const uint8_t* __restrict__ sf_src, 
 extern "C" int probe_stream_ldg(const uint8_t* w, long long bytes, const uint8_t* sf, long long sf_bytes, int grid,
                                 int tiles_per_cta, int stages, int mode, int* ok, float* ms) {
     if ((long long)grid * tiles_per_cta * 256 * 2048 > bytes) return 3;
+    if ((mode & 2) && (stages & 1)) return 8;
+    CUtensorMap tw;
+    if (int r = make_map(&tw, w, 4096, (uint64_t)(bytes / 2048), 256, true)) return 1000 + r;
     if ((long long)grid * tiles_per_cta * 32 * 1024 > sf_bytes) return 4;
     if (stages < 2 || stages > 6) return 5;
     const int smem = stages * (32768 + 1024) + 4096 + 16 * stages + 16 + 1024;
@@ -799,7 +823,7 @@ extern "C" int probe_stream_ldg(const uint8_t* w, long long bytes, const uint8_t
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
-    k_stream_ldg<<<grid, 320, smem>>>(w, sf, tiles_per_cta, stages, mode, ok);
+    k_stream_ldg<<<grid, 320, smem>>>(tw, w, sf, tiles_per_cta, stages, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);

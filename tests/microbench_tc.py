@@ -58,7 +58,7 @@ def main():
         tiles = 8
         W = torch.zeros(sms * tiles * 256 * 2048, dtype=torch.uint8, device="cuda")
         SF = torch.full((sms * tiles * 32 * 1024,), 127, dtype=torch.uint8, device="cuda")
-        for stages, mode in ((6, 0), (6, 1), (4, 1), (5, 1), (6, 1)):
+        for stages, mode in ((6, 0), (4, 1), (6, 2), (6, 3), (4, 3), (4, 2)):
             for _ in range(2):
                 ok.fill_(1)
                 rc = lib.probe_stream_ldg(W.data_ptr(), W.numel(), SF.data_ptr(), SF.numel(), sms, tiles, stages,
