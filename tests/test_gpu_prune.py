@@ -159,3 +159,45 @@ def test_prune_setter_validates(decode_layer):
             bqe.moe_set_route_prune(layer, *bad)
         assert ei.value.status == bqe.MOE_ERR_INVALID_ARG
     bqe.moe_set_route_prune(layer, 99)  # more than k: no count limit
+
+
+def test_decode_graph_replay_with_varying_kept_counts(decode_layer):
+    """The decode kernel replayed from one CUDA graph over tokens whose kept
+    expert counts differ (an adaptive threshold): the stream-K split changes
+    from launch to launch, and every replay gives the bytes of the eager call."""
+    cfg, _, layer = decode_layer
+    bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_route_prune(layer, 6, 0.245, 0.0)
+    tk = G.tokens(1, n=8)
+    ids0, w0 = orc.route_learned(tk.logits, cfg.k, cfg.w_scale)
+    kept = (orc.route_prune(ids0, w0, 6, 0.245, 0.0)[0] >= 0).sum(1)
+    assert len(set(kept.tolist())) > 1  # the tokens keep different numbers of experts
+    lg = torch.zeros((1, cfg.E), dtype=torch.float32, device=G.DEV)
+    xb = torch.zeros((1, cfg.H), dtype=torch.int16, device=G.DEV)
+    ids = torch.empty((1, cfg.k), dtype=torch.int32, device=G.DEV)
+    w = torch.empty((1, cfg.k), dtype=torch.float32, device=G.DEV)
+    out = torch.empty((1, cfg.H), dtype=torch.float32, device=G.DEV)
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        bqe.moe_route_forward(layer, lg, xb, ids, w, out)
+        s.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            bqe.moe_route_forward(layer, lg, xb, ids, w, out)
+    try:
+        for t in range(8):
+            lg.copy_(G.to_dev(tk.logits[t:t + 1].astype(np.float32)))
+            xb.copy_(G.to_dev(tk.x_bits[t:t + 1].astype(np.uint16), torch.int16))
+            g.replay()
+            torch.cuda.synchronize()
+            bqe.moe_check(layer)
+            assert int((ids >= 0).sum()) == int(kept[t])
+            ids_e = torch.empty_like(ids)
+            w_e = torch.empty_like(w)
+            out_e = torch.empty_like(out)
+            bqe.moe_route_forward(layer, lg, xb, ids_e, w_e, out_e)
+            torch.cuda.synchronize()
+            assert torch.equal(ids, ids_e) and torch.equal(w, w_e)
+            assert out.cpu().numpy().tobytes() == out_e.cpu().numpy().tobytes()
+    finally:
+        bqe.moe_set_route_prune(layer, cfg.k)
