@@ -105,19 +105,31 @@ __device__ void place_chunk(const int32_t* __restrict__ ids, int R, int E, int b
                             const int* s_off, const int* s_poff, uint8_t* wc, int32_t* __restrict__ row_src,
                             int32_t* __restrict__ row_dst, int32_t* __restrict__ row_pos,
                             int32_t* __restrict__ pos_row) {
+    // wc[e * 32 + w]: rows of expert e in warp w of this chunk (one byte each,
+    // 32 contiguous bytes = 8 words per expert, summed four at a time)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int i = tid; i < 32 * E; i += 1024) wc[i] = 0;
+    uint32_t* wcw = reinterpret_cast<uint32_t*>(wc);
+    for (int i = tid; i < 8 * E; i += 1024) wcw[i] = 0u;
     __syncthreads();
     const int r = base + tid;
     int e = (r < R) ? ids[r] : -1;
     if (e >= E) e = -1;
     const unsigned grp = __match_any_sync(0xFFFFFFFFu, e);
     const int rank = __popc(grp & ((1u << lane) - 1u));
-    if (e >= 0 && rank == 0) wc[warp * E + e] = (uint8_t)__popc(grp);
+    if (e >= 0 && rank == 0) wc[e * 32 + warp] = (uint8_t)__popc(grp);
     __syncthreads();
     if (e >= 0) {
+        // rows of e in warps 0 .. warp-1: whole words, then the low bytes of one
         int before = cursor[e] + rank;
-        for (int w2 = 0; w2 < warp; ++w2) before += wc[w2 * E + e];
+        const uint32_t* we = wcw + e * 8;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int lo = 4 * i;
+            if (lo >= warp) break;
+            uint32_t v = we[i];
+            if (warp - lo < 4) v &= (1u << (8 * (warp - lo))) - 1u;
+            before += (int)__dp4a(v, 0x01010101u, 0u);
+        }
         const int p = s_off[e] + before, pp = s_poff[e] + before;
         row_src[p] = r;
         row_dst[r] = p;
@@ -129,9 +141,10 @@ __device__ void place_chunk(const int32_t* __restrict__ ids, int R, int E, int b
     }
     __syncthreads();
     for (int e2 = tid; e2 < E; e2 += 1024) {
-        int add = 0;
-        for (int w2 = 0; w2 < 32; ++w2) add += wc[w2 * E + e2];
-        cursor[e2] += add;
+        uint32_t add = 0u;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) add = __dp4a(wcw[e2 * 8 + i], 0x01010101u, add);
+        cursor[e2] += (int)add;
     }
     __syncthreads();
 }
