@@ -457,7 +457,7 @@ moe_status moe_forward_host(moe_layer* L, const uint16_t* x, const float* logits
             L->stage_ev_set = 0;
             cudaError_t e = moe::launch_decode(L, static_cast<const float*>(dl), static_cast<const uint16_t*>(dx),
                                                L->ids_stage, L->w_stage, static_cast<float*>(const_cast<void*>(dout)),
-                                               s);
+                                               s, true);
             L->trace = nullptr;
             return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward_host");
         }

@@ -627,6 +627,8 @@ struct DecArgs {
     uint32_t* piece_flag;  // [4 phases][G][2]: a cut tile's piece parked by CTA c in slot s
     uint32_t* h_flag;      // [kDecMaxTiles]: h of gate/up tile t written
     uint32_t* y_flag;      // [kDecMaxTiles]: y of down tile t written
+    uint16_t* x_stage;     // x in host memory: CTA 0's device copy of it for the others, else null
+    uint32_t* x_flag;      // x_stage written
     uint32_t* err;
     unsigned long long* trace;  // [gridDim][12] ns timestamps, or null
 };
@@ -1073,8 +1075,11 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
     const int nch = a.H / 8;  // 8-element chunks; a 32-block is 4 chunks of 4 aligned lanes
     constexpr int kXThreads = kTcThreads - 32;
     static_assert(2 * kXThreads >= 4096 / 8, "two rounds of chunks cover H <= 4096");
-    uint4 xr[2];
-    if (warp > 0) {
+    // (x in host memory: CTA 0 alone reads it, the others take its device copy
+    // later -- x is first needed by the MMAs, well after the routing)
+    const bool x_staged = a.x_stage != nullptr;
+    uint4 xr[2] = {make_uint4(0, 0, 0, 0), make_uint4(0, 0, 0, 0)};
+    if (warp > 0 && (!x_staged || blockIdx.x == 0)) {
 #pragma unroll
         for (int r = 0; r < 2; ++r) {
             const int ch = threadIdx.x - 32 + r * kXThreads;
@@ -1161,6 +1166,26 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
                 ok = dec_produce<false>(a, cp, &tmDN, dec_phase(m, true, g), g, stage, phase, lane);
         }
     } else {
+        if (x_staged) {
+            if (blockIdx.x == 0) {
+                // publish the raw x: stores, the barrier over warps 1-9, one release
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int ch = threadIdx.x - 32 + r * kXThreads;
+                    if (ch < nch) *reinterpret_cast<uint4*>(a.x_stage + (size_t)ch * 8) = xr[r];
+                }
+                work_bar();
+                if (threadIdx.x == 32) flag_set(a.x_flag, words[2]);
+            } else {
+                if (threadIdx.x == 32 && !flag_wait(a.x_flag, words[2], c.abort_flag)) c.give_up(a);
+                work_bar();  // the acquire above, then the whole of warps 1-9
+#pragma unroll
+                for (int r = 0; r < 2; ++r) {
+                    const int ch = threadIdx.x - 32 + r * kXThreads;
+                    if (ch < nch) xr[r] = __ldcg(reinterpret_cast<const uint4*>(a.x_stage + (size_t)ch * 8));
+                }
+            }
+        }
         // ---- quantise x into the resident token row (MXFP8, 32-blocks),
         // while the producer streams the first weights
 #pragma unroll
@@ -1451,7 +1476,7 @@ bool decode_supported(const moe_layer* L) {
 
 // One token: route + layer in the cooperative decode kernel.
 cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w,
-                          float* out, cudaStream_t s) {
+                          float* out, cudaStream_t s, bool x_in_host) {
     const TcState* st = static_cast<const TcState*>(L->tc);
     DecArgs a{};
     a.logits = logits;
@@ -1476,6 +1501,8 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     a.piece_flag = reinterpret_cast<uint32_t*>(dw + 2);
     a.h_flag = a.piece_flag + 8 * L->num_sms;
     a.y_flag = a.h_flag + kDecMaxTiles;
+    a.x_flag = a.y_flag + kDecMaxTiles;
+    a.x_stage = x_in_host ? L->x_stage : nullptr;
     a.err = L->d_err;
     a.trace = L->trace;
     cudaLaunchConfig_t cfg = {};

@@ -90,7 +90,7 @@ inline int kSkZeroed(const moe_layer* L) { return 4 * L->num_sms + 32; }
 // then the words of the one-token decode kernel, zeroed only at creation: a
 // 64-bit launch counter, piece flags [4 phases][num_sms][2], h flags [128],
 // y flags [128]
-inline int kDecWords(const moe_layer* L) { return 2 + 8 * L->num_sms + 256; }
+inline int kDecWords(const moe_layer* L) { return 2 + 8 * L->num_sms + 256 + 32; }
 inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L); }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
@@ -141,8 +141,11 @@ cudaError_t cc_init();
 // Tensor-core path.
 cudaError_t tc_init(moe_layer* L);
 bool decode_supported(const moe_layer* L);
+// x_in_host: x is mapped host memory; one CTA copies it to the layer's
+// staging buffer for the others (one read of x over the host link, not one
+// per CTA)
 cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w,
-                          float* out, cudaStream_t s);
+                          float* out, cudaStream_t s, bool x_in_host = false);
 void tc_free(moe_layer* L);
 // cmb_ids != null: fuse the combine into the down GEMM (out = sum over the
 // token's experts in ascending order of w * y); requires no shared expert.
