@@ -178,11 +178,26 @@ extern "C" int probe_mma(const uint8_t* a, const uint8_t* b, const uint8_t* sfa,
 // Microbenchmarks (timing only; results are not checked for values).
 // ------------------------------------------------------------------------
 
+// Block-scaled MMA with the A operand read from tensor memory (128 lanes x
+// K/4 columns of 8-bit codes) instead of shared memory.
+__device__ __forceinline__ void mma_mx_ta(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                          uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate) {
+    asm volatile(
+        "{\n.reg .pred p;\nsetp.ne.b32 p, %6, 0;\n"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X"
+        " [%0], [%1], %2, %3, [%4], [%5], p;\n}"
+        ::"r"(d_tmem), "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
 // Streams `tiles_per_cta` x KB fp4 weight tiles (128 x 128) per CTA through a
 // `stages`-deep TMA pipeline.  mode bit 0: issue one M=128,N=32 block-scaled
 // MMA group per stage (else the consumer frees the stage at once); bit 1:
 // prefetch tiles into L2 `pf` stages ahead.  CTA 0 records, per stage, the
 // global time the load was issued and the time the consumer saw it land.
+// kTA: the token operand of the swapped MMAs (mode bit 6) in tensor memory
+// (its own instantiation: kernels holding that MMA form time differently)
+template <bool kTA>
 __global__ void __launch_bounds__(64, 1)
 k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int stages, int mode, int pf,
          unsigned long long* stamps, int* ok_out, int layout, uint32_t box_tx, uint32_t slot, const uint8_t* sf_src) {
@@ -258,6 +273,12 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                                                              : desc_sw128(a + 32 * kk);
                             // bit 9: the token operand one aliased 8-row group (no swizzle, stride 0)
                             const uint64_t ad = (mode & 512) ? smem_desc(b + 32 * kk, 16, 0, 0) : desc_sw128(b + 32 * kk);
+                            // bit 10: the token operand in tensor memory (columns 384 + 8 kk)
+                            if constexpr (kTA)
+                                mma_mx_ta(tmem, tmem + 384 + 8 * kk, bd,
+                                          idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
+                                          (kk > 0 || rr > 0) ? 1u : 0u);
+                            else
                             mma_mx(tmem, ad, bd,
                                    idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
                                    (kk > 0 || rr > 0) ? 1u : 0u);
@@ -309,7 +330,8 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     if (slot == 32768 && stages > 6) return 5;
     // tiles + B tile + barrier offset + barriers/slot + 1024 alignment slack
     const int smem = stages * (int)slot + 16384 + 1024 + 512 + 1024;
-    cudaFuncSetAttribute(k_stream, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(k_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(k_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaEvent_t e0, e1;
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
@@ -317,7 +339,10 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     // bit 7 reads 1 KB per stage from the start of the tensor (grid * tiles * 32 KB <= its size)
     if ((mode & 128) && (long long)grid * tiles_per_cta * 32 * 1024 > rows * 2048) return 6;
     if ((mode & 128) && stages * 1024 > 16384) return 7;
-    k_stream<<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
+    if (mode & 1024)
+        k_stream<true><<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
+    else
+        k_stream<false><<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);
@@ -406,6 +431,7 @@ extern "C" int probe_mma_peak(int grid, int iters, int n, uint32_t a_fmt, int* o
 // every kk, 2 the same operand addresses for every kk, 3 B read through the
 // decode kernel's no-swizzle descriptor (16-byte K chunks 16 bytes apart),
 // 4 the decode kernel's orientation (weights as the N = 256 B operand)
+template <bool kTA>
 __global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, int commit, int acc2,
                                                   uint32_t a_fmt, int mode, int* ok_out) {
     extern __shared__ uint8_t raw[];
@@ -436,9 +462,16 @@ __global__ void __launch_bounds__(64, 1) k_mma_mix(int iters, int n, int ncp, in
                 // mode 7: the decode orientation with the weight tile (B) in
                 // the no-swizzle K-major layout [K chunk][256 rows][16 B];
                 // mode 8: A a real swizzled 128-row tile, B swizzled (the
-                // grouped kernel's orientation)
+                // grouped kernel's orientation); mode 9: as 8 with A in tensor
+                // memory (columns 384 + 8 kk)
 #pragma unroll
                 for (int kk = 0; kk < 4; ++kk) {
+                    if constexpr (kTA) {
+                        mma_mx_ta(tmem, tmem + 384 + 8 * kk, desc_sw128(a + 32 * kk),
+                                  idesc_mx(kFmtE4M3, a_fmt, 128, 256, kk, kk), tmem + 256, tmem + 260,
+                                  (it | kk) ? 1u : 0u);
+                        continue;
+                    }
                     const uint64_t ad = mode == 7 ? smem_desc(b + 32 * kk, 16, 0, 0) : desc_sw128(b + 32 * kk);
                     const uint64_t bd = mode == 7 ? smem_desc(a + 8192 * kk, 4096, 128, 0) : desc_sw128(a + 32 * kk);
                     mma_mx(tmem, ad, bd, idesc_mx(kFmtE4M3, a_fmt, 128, 256, kk, kk), tmem + 256, tmem + 260,
@@ -507,13 +540,17 @@ extern "C" int probe_mma_mix(int grid, int iters, int n, int ncp, int commit, in
                              int* ok, float* ms) {
     if (n < 16 || n > (acc2 == 2 ? 16 : acc2 ? 128 : 256) || ncp < 0 || ncp > 3) return 3;
     const int smem = 49152 + 1536 + 1024 + 64;
-    cudaFuncSetAttribute(k_mma_mix, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (mode < 0 || mode > 9) return 3;
+    cudaFuncSetAttribute(k_mma_mix<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaFuncSetAttribute(k_mma_mix<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaEvent_t e0, e1;
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
     cudaEventRecord(e0);
-    if (mode < 0 || mode > 8) return 3;
-    k_mma_mix<<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, mode, ok);
+    if (mode == 9)
+        k_mma_mix<true><<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, 8, ok);
+    else
+        k_mma_mix<false><<<grid, 64, smem>>>(iters, n, ncp, commit, acc2, a_fmt, mode, ok);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);

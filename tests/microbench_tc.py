@@ -111,7 +111,8 @@ def main():
     if args.only_stream:
         for layout, stages, mode in ((5, 6, 0), (5, 6, 128), (5, 6, 1 | 64), (5, 6, 1 | 64 | 128),
                                      (6, 6, 128), (6, 6, 1 | 64 | 128), (7, 6, 0), (7, 6, 1 | 64 | 256),
-                                     (5, 6, 1 | 64 | 512), (5, 6, 1 | 64 | 128 | 512)):
+                                     (5, 6, 1 | 64 | 512), (5, 6, 1 | 64 | 128 | 512), (5, 6, 1 | 64 | 1024),
+                                     (5, 6, 1 | 64 | 128 | 1024)):
             for _ in range(2):
                 ok.fill_(1)
                 rc = lib.probe_stream(A.data_ptr(), rows, sms, 8, stages, mode, 0, stamps.data_ptr(),
@@ -171,7 +172,7 @@ def mma_mix(lib, sms, ok, ms, out):
              (16, 0, 0, 2, 0), (16, 0, 0, 1, 1), (16, 0, 0, 1, 2), (16, 0, 0, 0, 1), (16, 3, 1, 1, 1),
              (16, 0, 0, 1, 3), (16, 3, 1, 1, 3), (16, 0, 0, 0, 4), (16, 2, 1, 0, 4), (16, 3, 1, 0, 4),
              (16, 0, 1, 0, 5), (16, 0, 1, 0, 6), (16, 0, 0, 0, 5), (16, 0, 0, 0, 6), (16, 0, 0, 0, 7),
-             (16, 0, 0, 0, 8)]
+             (16, 0, 0, 0, 8), (16, 0, 0, 0, 9)]
     for fmt in (5,):
         for n, ncp, commit, acc2, mode in cases:
                 ok.fill_(1)
@@ -179,7 +180,8 @@ def mma_mix(lib, sms, ok, ms, out):
                 rc = lib.probe_mma_mix(sms, iters, n, ncp, commit, acc2, fmt, mode, ok.data_ptr(), C.byref(ms))
                 key = (f"mix_f{fmt}_n{n}_cp{ncp}_commit{commit}_" + ("acc1", "acc2", "acc8split")[acc2] +
                        ("", "_samesfid", "_sameaddr", "_nswzB", "_swapN256", "_swapN256_sfres_cpnow",
-                        "_swapN256_sfres_cpahead", "_swapN256_nswzB", "_swapN256_realA")[mode])
+                        "_swapN256_sfres_cpahead", "_swapN256_nswzB", "_swapN256_realA",
+                        "_swapN256_tmemA")[mode])
                 out[key] = {"ns_per_iter": round(ms.value * 1e6 / iters, 2), "rc": rc, "ok": int(ok.item())}
                 print(key, out[key], flush=True)
 
