@@ -198,18 +198,20 @@ __device__ __forceinline__ void mma_mx_ta(uint32_t d_tmem, uint32_t a_tmem, uint
 // kTA: the token operand of the swapped MMAs (mode bit 6) in tensor memory
 // (its own instantiation: kernels holding that MMA form time differently)
 template <bool kTA>
-__global__ void __launch_bounds__(64, 1)
+__global__ void __launch_bounds__(96, 1)
 k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int stages, int mode, int pf,
          unsigned long long* stamps, int* ok_out, int layout, uint32_t box_tx, uint32_t slot, const uint8_t* sf_src) {
     extern __shared__ uint8_t raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(sm + stages * slot + 16384 + 1024);
-    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * stages);
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * stages + 2);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t b0 = smem_u32(bars);
     if (threadIdx.x == 0) {
         for (int s = 0; s < stages; ++s) { mbar_init(b0 + 8 * s, 1); mbar_init(b0 + 8 * (stages + s), 1); }
+        mbar_init(b0 + 8 * (2 * stages), 1);
+        mbar_init(b0 + 8 * (2 * stages + 1), 1);
         *abort_flag = 0;
         fence_mbar_init();
     }
@@ -226,10 +228,28 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
             const uint32_t ph = (uint32_t)((i / stages) & 1);
             const int row = (blockIdx.x + (i / KB) * gridDim.x) * 128, kb = i % KB;
             if ((mode & 2) && i + pf < total) {
+                // the tile the load of stage j will read (the coordinates of the branches below)
                 const int j = i + pf;
-                prefetch_tile_l2(&tmA, (j % KB) * 128, (blockIdx.x + (j / KB) * gridDim.x) * 128);
+                const int jrow = (blockIdx.x + (j / KB) * gridDim.x) * 128, jkb = j % KB;
+                if (layout == 1)
+                    prefetch_tile_l2(&tmA, 0, (blockIdx.x * tiles_per_cta * KB + j) * 128);
+                else if (layout == 5 || layout == 7)
+                    prefetch_tile_l2(&tmA, jkb * 128, jrow * 2);
+                else if (layout == 6)
+                    prefetch_tile_l2(&tmA, 0, (blockIdx.x * tiles_per_cta * KB + j) * 256);
+                else
+                    prefetch_tile_l2(&tmA, jkb * 128, jrow);
             }
-            if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
+            if (mode & 65536) {
+                // bit 16: the producer polls the free barrier politely (a
+                // 64 ns sleep between tests, bounded like mbar_wait)
+                const uint64_t t0 = globaltimer();
+                while (!mbar_try_wait(b0 + 8 * (stages + s), ph ^ 1u)) {
+                    if (*abort_flag || globaltimer() - t0 > 200000000ull) { ok = false; *abort_flag = 1; break; }
+                    __nanosleep(64);
+                }
+                if (!ok) break;
+            } else if (!mbar_wait(b0 + 8 * (stages + s), ph ^ 1u, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
             mbar_arrive_expect_tx(b0 + 8 * s, box_tx + ((mode & 128) ? 1024u : 0u));
             if (blockIdx.x == 0 && i < 256) stamps[2 * i] = globaltimer();
             // bit 7: a second, 1 KB bulk copy per stage (a scale-atom pair) into the B area
@@ -247,12 +267,60 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
             else
                 tma_load_2d(smem_u32(sm + s * slot), &tmA, kb * 128, row, b0 + 8 * s);
         }
+    } else if (warp == 2 && lane == 0 && (mode & 32768)) {
+        // observer: the time each stage lands (it consumes nothing; on a
+        // missed phase it stops observing)
+        for (int i = 0; i < total && i < 256; ++i) {
+            const int s = i % stages;
+            const uint32_t ph = (uint32_t)((i / stages) & 1);
+            if (!mbar_wait(b0 + 8 * s, ph, 5000000ull, abort_flag)) break;
+            if (blockIdx.x == 0) stamps[768 + i] = globaltimer();
+        }
+    } else if (warp == 1 && lane == 0 && (mode & 262144)) {
+        // bit 18: stages in groups of `pf` (1-4) -- wait for all of them,
+        // then issue their MMAs (swapped operands, 4 per stage) and commits
+        const int G = pf < 1 ? 1 : (pf > 4 ? 4 : pf);
+        for (int i = 0; i < total && ok; i += G) {
+            const int n = total - i < G ? total - i : G;
+            for (int j = 0; j < n && ok; ++j) {
+                const int s = (i + j) % stages;
+                const uint32_t ph = (uint32_t)(((i + j) / stages) & 1);
+                if (!mbar_wait(b0 + 8 * s, ph, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; }
+            }
+            if (!ok) break;
+            if (blockIdx.x == 0 && i < 256) stamps[2 * i + 1] = globaltimer();
+            tc_fence_after();
+            for (int j = 0; j < n; ++j) {
+                const int s = (i + j) % stages;
+                const uint32_t a = smem_u32(sm + s * slot), b = smem_u32(sm + stages * slot);
+                for (int kk = 0; kk < 4; ++kk)
+                    mma_mx(tmem, desc_sw128(b + 32 * kk), desc_sw128(a + 32 * kk),
+                           idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
+                           (kk > 0 || j > 0) ? 1u : 0u);
+                mma_commit(b0 + 8 * (stages + s));
+            }
+        }
+        if (ok) {
+            mma_commit(b0 + 8 * (2 * stages + 1));
+            if (!mbar_wait(b0 + 8 * (2 * stages + 1), 0, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; }
+        }
     } else if (warp == 1 && lane == 0) {
         for (int i = 0; i < total && ok; ++i) {
             const int s = i % stages;
             const uint32_t ph = (uint32_t)((i / stages) & 1);
             if (!mbar_wait(b0 + 8 * s, ph, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
             if (blockIdx.x == 0 && i < 256) stamps[2 * i + 1] = globaltimer();
+            if (mode & 16384) {
+                // no MMAs: hold the slot for `pf` ns of wall time, then free it
+                // (bit 17: free it first, then spin)
+                if (mode & 131072) mbar_arrive(b0 + 8 * (stages + s));
+                const uint64_t t0 = globaltimer();
+                while (globaltimer() - t0 < (uint64_t)pf) {}
+                if (blockIdx.x == 0 && i < 256) stamps[512 + i] = globaltimer();
+                if (!(mode & 131072)) mbar_arrive(b0 + 8 * (stages + s));
+                if (blockIdx.x == 0 && i < 256) stamps[1024 + i] = globaltimer();
+                continue;
+            }
             if (mode & 1) {
                 // bit 2: no tcgen05 fence; bit 3: 16 MMAs per stage; bit 4: N = 128;
                 // bit 5: unscaled kind::f8f6f4 instead of the block-scaled MMA;
@@ -269,8 +337,11 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                             // streamed 256-row fp4 weight tile, N = 256: one MMA per K=32 step
                             // bit 8: the weight tile read through a no-swizzle
                             // descriptor (layout 7 writes it unswizzled; timing only)
-                            const uint64_t bd = (mode & 256) ? smem_desc(a + 32 * kk, 128, 1024, 0)
-                                                             : desc_sw128(a + 32 * kk);
+                            // bit 11: the MMAs read a static 256-row tile instead of the
+                            // landed stage (after the barrier and tail; timing only)
+                            const uint32_t wt = (mode & 2048) ? smem_u32(sm + stages * slot + 16384 + 2048) : a;
+                            const uint64_t bd = (mode & 256) ? smem_desc(wt + 32 * kk, 128, 1024, 0)
+                                                             : desc_sw128(wt + 32 * kk);
                             // bit 9: the token operand one aliased 8-row group (no swizzle, stride 0)
                             const uint64_t ad = (mode & 512) ? smem_desc(b + 32 * kk, 16, 0, 0) : desc_sw128(b + 32 * kk);
                             // bit 10: the token operand in tensor memory (columns 384 + 8 kk)
@@ -279,9 +350,11 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                                           idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
                                           (kk > 0 || rr > 0) ? 1u : 0u);
                             else
+                            // bit 13: accumulate across stages (only the first MMA of the
+                            // stream starts the accumulator), else each stage restarts it
                             mma_mx(tmem, ad, bd,
                                    idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260,
-                                   (kk > 0 || rr > 0) ? 1u : 0u);
+                                   (kk > 0 || rr > 0 || ((mode & 8192) && i > 0)) ? 1u : 0u);
                         } else if (mode & 32) {
                             const uint32_t id = (kFmtE2M1 << 7) | (kFmtE4M3 << 10) | ((nn >> 3) << 17) | (8u << 24) | (1u << 4);
                             asm volatile("{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
@@ -294,10 +367,24 @@ k_stream(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int KB, int
                                    (kk > 0 || rr > 0) ? 1u : 0u);
                         }
                     }
-                mma_commit(b0 + 8 * (stages + s));
+                // stamps[512 + i]: the stage's MMAs and commit issued (CTA 0)
+                if (blockIdx.x == 0 && i < 256) stamps[512 + i] = globaltimer();
+                // bit 12 (with bit 11: the MMAs read no slot): free the slot
+                // once its MMAs are issued, and commit to a barrier nobody waits on
+                if (mode & 4096) {
+                    mma_commit(b0 + 8 * (2 * stages));
+                    mbar_arrive(b0 + 8 * (stages + s));
+                } else {
+                    mma_commit(b0 + 8 * (stages + s));
+                }
             } else {
                 mbar_arrive(b0 + 8 * (stages + s));
             }
+        }
+        // every MMA issued has completed before the tensor memory is freed
+        if ((mode & 1) && ok) {
+            mma_commit(b0 + 8 * (2 * stages + 1));
+            if (!mbar_wait(b0 + 8 * (2 * stages + 1), 0, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; }
         }
     }
     __syncthreads();
@@ -329,7 +416,9 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     if (layout == 6 && (long long)grid * tiles_per_cta * 32 * 256 > rows * 32) return 4;
     if (slot == 32768 && stages > 6) return 5;
     // tiles + B tile + barrier offset + barriers/slot + 1024 alignment slack
-    const int smem = stages * (int)slot + 16384 + 1024 + 512 + 1024;
+    const int smem = stages * (int)slot + 16384 + 1024 + 512 + 1024 + ((mode & 2048) ? 2048 + 32768 : 0);
+    if (smem > 232448) return 8;
+    if ((mode & 4096) && !(mode & 2048)) return 9;  // a slot freed early must not be read
     cudaFuncSetAttribute(k_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaFuncSetAttribute(k_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     cudaEvent_t e0, e1;
@@ -340,15 +429,180 @@ extern "C" int probe_stream(const uint8_t* a, long long rows, int grid, int tile
     if ((mode & 128) && (long long)grid * tiles_per_cta * 32 * 1024 > rows * 2048) return 6;
     if ((mode & 128) && stages * 1024 > 16384) return 7;
     if (mode & 1024)
-        k_stream<true><<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
+        k_stream<true><<<grid, 96, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
     else
-        k_stream<false><<<grid, 64, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
+        k_stream<false><<<grid, 96, smem>>>(ta, tiles_per_cta, 32, stages, mode, pf, stamps, ok, layout, tx, slot, a);
     cudaEventRecord(e1);
     int rc = (int)cudaDeviceSynchronize();
     cudaEventElapsedTime(ms, e0, e1);
     cudaEventDestroy(e0);
     cudaEventDestroy(e1);
     return rc;
+}
+
+// The TMA weight stream (its consumer frees every stage at once) and an
+// independent MMA loop on resident operands, side by side in one CTA per SM:
+// does either engine slow the other when neither waits on the other's data?
+// which: 1 the stream alone, 2 the MMAs alone, 3 both.  The stream moves
+// 256-row fp4 boxes (16 KB of codes into 32 KB slots, 6 stages, CTAs on
+// disjoint tiles); an MMA group is 4 block-scaled N = 256 MMAs (an aliased
+// token A, a swizzled 256-row B) and a commit, two groups in flight.
+// times[4 b ..]: stream start, stream end, MMA start, MMA end (ns).
+__global__ void __launch_bounds__(96, 1)
+k_stream_indep(const __grid_constant__ CUtensorMap tmA, int tiles_per_cta, int groups, int which,
+               unsigned long long* times, int* ok_out) {
+    constexpr int kStages = 6, kSlot = 32768, KB = 32;
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* bt = sm + kStages * kSlot;  // resident B (32 KB), then A (1 KB)
+    uint8_t* at = bt + 32768;
+    uint64_t* bars = reinterpret_cast<uint64_t*>(at + 1024);  // full[6], empty[6], mma[2]
+    uint32_t* tslot = reinterpret_cast<uint32_t*>(bars + 2 * kStages + 2);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t b0 = smem_u32(bars), bm = b0 + 8 * 2 * kStages;
+    for (int i = threadIdx.x; i < (32768 + 1024) / 4; i += blockDim.x) reinterpret_cast<uint32_t*>(bt)[i] = 0x38383838u;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < 2 * kStages + 2; ++s) mbar_init(b0 + 8 * s, 1);
+        *abort_flag = 0;
+        fence_mbar_init();
+    }
+    if (warp == 1) tmem_alloc(smem_u32(tslot), 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tslot;
+    bool ok = true;
+    const int total = tiles_per_cta * KB;
+    unsigned long long* tm = times + 4 * (size_t)blockIdx.x;
+    if (warp == 0 && lane == 0 && (which & 1)) {
+        tm[0] = globaltimer();
+        for (int i = 0; i < total && ok; ++i) {
+            const int s = i % kStages;
+            const uint32_t ph = (uint32_t)((i / kStages) & 1);
+            const int row = (blockIdx.x + (i / KB) * gridDim.x) * 128, kb = i % KB;
+            if (!mbar_wait(b0 + 8 * (kStages + s), ph ^ 1u, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
+            mbar_arrive_expect_tx(b0 + 8 * s, 16384u);
+            tma_load_2d(smem_u32(sm + s * kSlot), &tmA, kb * 128, row * 2, b0 + 8 * s);
+        }
+    } else if (warp == 1 && lane == 0 && (which & 1)) {
+        for (int i = 0; i < total && ok; ++i) {
+            const int s = i % kStages;
+            const uint32_t ph = (uint32_t)((i / kStages) & 1);
+            if (!mbar_wait(b0 + 8 * s, ph, 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; break; }
+            mbar_arrive(b0 + 8 * (kStages + s));
+        }
+        tm[1] = globaltimer();
+    } else if (warp == 2 && lane == 0 && (which & 2)) {
+        const uint32_t a = smem_u32(at), b = smem_u32(bt);
+        tm[2] = globaltimer();
+        for (int it = 0; it < groups && ok; ++it) {
+            // (which bit 2: B is ring slot it % 6, whatever the stream is doing to it)
+            const uint32_t bb = (which & 4) ? smem_u32(sm + (it % kStages) * kSlot) : b;
+            // group it commits to barrier it % 2; before issuing it, wait for
+            // group it - 2 (the previous commit to the same barrier)
+            if (it >= 2 && !mbar_wait(bm + 8 * (it & 1), (uint32_t)(((it - 2) >> 1) & 1), 200000000ull, abort_flag)) {
+                ok = false; *abort_flag = 1; break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)
+                mma_mx(tmem, smem_desc(a + 32 * kk, 16, 0, 0), desc_sw128(bb + 32 * kk),
+                       idesc_mx(kFmtE4M3, kFmtE2M1, 128, 256, kk, kk), tmem + 256, tmem + 260, (it | kk) ? 1u : 0u);
+            mma_commit(bm + 8 * (it & 1));
+        }
+        for (int it = groups - 2 > 0 ? groups - 2 : 0; it < groups && ok; ++it)
+            if (!mbar_wait(bm + 8 * (it & 1), (uint32_t)((it >> 1) & 1), 200000000ull, abort_flag)) { ok = false; *abort_flag = 1; }
+        tm[3] = globaltimer();
+    }
+    __syncthreads();
+    if (*abort_flag) { spin_ns(200000); if (threadIdx.x == 0) atomicExch(ok_out, 0); }
+    if (warp == 1) { tc_fence_after(); tmem_dealloc(tmem, 512); }
+}
+
+extern "C" int probe_stream_indep(const uint8_t* a, long long rows, int grid, int tiles_per_cta, int groups,
+                                  int which, unsigned long long* times, int* ok, float* ms) {
+    CUtensorMap ta;
+    if (make_map(&ta, a, 4096, (uint64_t)rows, 256, true)) return 2;
+    if ((long long)grid * tiles_per_cta * 256 > rows || groups < 2 || which < 1 || which > 7) return 3;
+    const int smem = 6 * 32768 + 32768 + 1024 + 256 + 1024;
+    cudaFuncSetAttribute(k_stream_indep, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    cudaEventRecord(e0);
+    k_stream_indep<<<grid, 96, smem>>>(ta, tiles_per_cta, groups, which, times, ok);
+    cudaEventRecord(e1);
+    int rc = (int)cudaDeviceSynchronize();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// Cost of single-thread primitives in SM clock cycles (clock64), one CTA
+// per SM: res[4 b + 0] a try_wait on a completed phase, [1] a test_wait on
+// it, [2] a %globaltimer read, [3] an arrive on another barrier followed by
+// a try_wait on the completed one.  park: where the rest of warp 0 is while
+// lane 0 runs the loops -- 0 exited; 1 at the CTA barrier (with warp 1);
+// 2 at a warp barrier; 3 running the same loops (converged warp); 4 at a
+// warp shuffle.  Every lane of a warp meets the same barrier instruction
+// (the CTA barrier is an aligned one).
+__global__ void __launch_bounds__(64, 1) k_prim(int iters, int park, unsigned long long* res) {
+    __shared__ __align__(8) uint64_t bars[2];
+    const int lane = threadIdx.x & 31;
+    const bool w0 = threadIdx.x < 32;
+    if (park == 0 && (!w0 || lane != 0)) return;
+    if ((park == 2 || park == 4) && !w0) return;
+    const uint32_t b0 = smem_u32(&bars[0]), b1 = smem_u32(&bars[1]);
+    if (w0 && lane == 0) {
+        mbar_init(b0, 1);
+        mbar_init(b1, (1 << 20) - 1);  // the largest count
+        fence_mbar_init();
+        mbar_arrive(b0);  // phase 0 of b0 completes
+    }
+    if (w0 && park != 0) __syncwarp();  // (park 0: lane 0 is alone in its warp)
+    uint32_t acc = 0;
+    unsigned long long g = 0;
+    if (w0 && (lane == 0 || park == 3)) {
+        unsigned long long* r = res + 4 * (size_t)blockIdx.x;
+        long long t0 = clock64();
+        for (int i = 0; i < iters; ++i) acc += mbar_try_wait(b0, 0) ? 1u : 0u;
+        long long t1 = clock64();
+        if (lane == 0) r[0] = (unsigned long long)(t1 - t0);
+        t0 = clock64();
+        for (int i = 0; i < iters; ++i) {
+            uint32_t ok;
+            asm volatile("{\n.reg .pred p;\nmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+                         "selp.u32 %0, 1, 0, p;\n}" : "=r"(ok) : "r"(b0), "r"(0u) : "memory");
+            acc += ok;
+        }
+        t1 = clock64();
+        if (lane == 0) r[1] = (unsigned long long)(t1 - t0);
+        t0 = clock64();
+        for (int i = 0; i < iters; ++i) g += globaltimer();
+        t1 = clock64();
+        if (lane == 0) r[2] = (unsigned long long)(t1 - t0);
+        t0 = clock64();
+        for (int i = 0; i < iters; ++i) {  // b1 never completes (iters < its count)
+            if (lane == 0) mbar_arrive(b1);
+            acc += mbar_try_wait(b0, 0) ? 1u : 0u;
+        }
+        t1 = clock64();
+        if (lane == 0) r[3] = (unsigned long long)(t1 - t0);
+        if (acc == 0xFFFFFFFFu && g == 1) r[0] = 0;  // keep the loops
+    }
+    if (park == 4) acc = __shfl_sync(0xFFFFFFFFu, acc, 0);
+    if (park == 2) __syncwarp();
+    if (park == 1 || park == 3) __syncthreads();
+    if (acc == 0xFFFFFFFEu) res[0] = 0;
+}
+
+extern "C" int probe_prim(int grid, int iters, int park, unsigned long long* res) {
+    if (iters < 1 || iters >= (1 << 20) - 1) return 3;
+    k_prim<<<grid, 64>>>(iters, park, res);
+    return (int)cudaDeviceSynchronize();
 }
 
 // Plain HBM read stream: every thread sums 16-byte loads, grid-strided.

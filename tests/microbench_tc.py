@@ -34,6 +34,8 @@ def load():
     lib.probe_mma_peak.argtypes = [C.c_int, C.c_int, C.c_int, C.c_uint32, vp, vp]
     lib.probe_contend.argtypes = [C.c_int, C.c_int, C.c_int, vp, vp, vp]
     lib.probe_stream_ldg.argtypes = [vp, C.c_longlong, vp, C.c_longlong, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp]
+    lib.probe_stream_indep.argtypes = [vp, C.c_longlong, C.c_int, C.c_int, C.c_int, C.c_int, vp, vp, vp]
+    lib.probe_prim.argtypes = [C.c_int, C.c_int, C.c_int, vp]
     lib.probe_mma_mix.argtypes = [C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_uint32, C.c_int,
                                   vp, vp]
     return lib
@@ -46,6 +48,12 @@ def main():
     ap.add_argument("--only-stream", action="store_true", help="only the 256-row weight-box TMA streams")
     ap.add_argument("--only-ldg", action="store_true",
                     help="weight stream copied by the load/store units instead of the TMA, with / without MMAs")
+    ap.add_argument("--only-pf", action="store_true",
+                    help="the 256-row weight-box stream with MMAs and an L2 prefetch running ahead of the ring")
+    ap.add_argument("--only-prim", action="store_true",
+                    help="cycles per mbarrier wait on a completed phase and per %%globaltimer read")
+    ap.add_argument("--only-indep", action="store_true",
+                    help="TMA stream and an independent MMA loop, alone and side by side")
     ap.add_argument("--only-contend", action="store_true",
                     help="MMA loop time with shared-memory stores / loads by other warps")
     args = ap.parse_args()
@@ -67,6 +75,47 @@ def main():
             out[key] = {"GBs": round(sms * tiles * 32 * (16384 + 1024) / ms.value / 1e6, 1),
                         "us_per_stage": round(ms.value * 1e3 / (tiles * 32), 3), "rc": rc, "ok": int(ok.item())}
             print(key, out[key], flush=True)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
+    if args.only_prim:
+        iters = 4096
+        res = torch.zeros(4 * sms, dtype=torch.int64, device="cuda")
+        for park in (0, 2, 4, 3, 1):
+            for _ in range(2):
+                res.zero_()
+                rc = lib.probe_prim(sms, iters, park, res.data_ptr())
+            r = res.view(sms, 4).double().median(dim=0).values / iters
+            key = f"prim_cycles_park{park}"
+            out[key] = {"try_wait_completed": round(r[0].item(), 1), "test_wait_completed": round(r[1].item(), 1),
+                        "globaltimer_read": round(r[2].item(), 1), "arrive_then_try_wait": round(r[3].item(), 1),
+                        "rc": rc}
+            print(key, out[key], flush=True)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
+    if args.only_indep:
+        tiles, groups = 8, 224
+        W = torch.zeros(sms * tiles * 256 * 2048, dtype=torch.uint8, device="cuda")
+        times = torch.zeros(4 * sms, dtype=torch.int64, device="cuda")
+        for which in (1, 2, 3, 1, 2, 3, 6, 7):
+            times.zero_()
+            ok.fill_(1)
+            rc = lib.probe_stream_indep(W.data_ptr(), W.numel() // 2048, sms, tiles, groups, which,
+                                        times.data_ptr(), ok.data_ptr(), C.byref(ms))
+            t = times.view(sms, 4).cpu().double()
+            rec = {"rc": rc, "ok": int(ok.item()), "kernel_ms": round(ms.value, 4)}
+            if which & 1:
+                d = (t[:, 1] - t[:, 0]) / 1e3
+                rec["stream_us_per_stage_median"] = round(d.median().item() / (tiles * 32), 4)
+                rec["stream_us_per_stage_max"] = round(d.max().item() / (tiles * 32), 4)
+                rec["stream_TBs"] = round(sms * tiles * 32 * 16384 / (d.max().item() * 1e-6) / 1e12, 3)
+            if which & 2:
+                d = (t[:, 3] - t[:, 2]) / 1e3
+                rec["mma_ns_per_group_median"] = round(d.median().item() * 1e3 / groups, 1)
+            key = f"indep_which{which}"
+            out[key] = rec
+            print(key, rec, flush=True)
         os.makedirs(os.path.dirname(args.out), exist_ok=True)
         json.dump(out, open(args.out, "w"), indent=1)
         return
@@ -100,13 +149,51 @@ def main():
 
     rows = sms * 128 * 16
     A = torch.zeros(rows * 2048, dtype=torch.uint8, device="cuda")
-    stamps = torch.zeros(512, dtype=torch.int64, device="cuda")
+    stamps = torch.zeros(1280, dtype=torch.int64, device="cuda")
 
     def stage_stats():
         st = stamps.cpu().tolist()
         lat = sorted((st[2 * i + 1] - st[2 * i]) / 1000 for i in range(64, 200))
         per = sorted((st[2 * i + 3] - st[2 * i + 1]) / 1000 for i in range(64, 200))
         return lat[len(lat) // 2], per[len(per) // 2]
+
+    if args.only_pf:
+        for layout, stages, mode, pf in ((5, 6, 1 | 64 | 262144, 1), (5, 6, 1 | 64 | 262144, 2),
+                                         (5, 6, 1 | 64 | 262144, 3), (5, 5, 1 | 64 | 262144, 2),
+                                         (5, 6, 1 | 64 | 128 | 262144, 2),
+                                         (5, 5, 1 | 64, 0), (5, 5, 1 | 64 | 2048, 0), (5, 5, 1 | 64 | 2048 | 4096, 0),
+                                         (5, 6, 1 | 64, 0), (5, 6, 1 | 64 | 2, 6), (5, 6, 1 | 64 | 2, 12),
+                                         (5, 6, 1 | 64 | 2, 24), (5, 6, 1 | 64 | 2, 48), (5, 6, 1 | 64 | 128 | 2, 12),
+                                         (5, 6, 2, 12), (5, 6, 0, 0)):
+            for _ in range(2):
+                ok.fill_(1)
+                rc = lib.probe_stream(A.data_ptr(), rows, sms, 8, stages, mode, pf, stamps.data_ptr(),
+                                      ok.data_ptr(), C.byref(ms), layout)
+            lat, per = stage_stats()
+            st = stamps.cpu().tolist()
+            iss = sorted((st[512 + i] - st[2 * i + 1]) / 1000 for i in range(64, 200)) if mode & (1 | 16384) else [0]
+            obs = {}
+            if mode & 32768:
+                land = [st[768 + i] for i in range(256)]
+                rel = [st[512 + i] for i in range(256)]
+                med = lambda v: sorted(v)[len(v) // 2] if v else None
+                obs = {"land_gap_us": med([(land[i + 1] - land[i]) / 1000 for i in range(64, 200)]),
+                       "seen_after_land_us": med([(st[2 * i + 1] - land[i]) / 1000 for i in range(64, 200)]),
+                       "next_land_after_release_us": med([(land[i + 1] - rel[i]) / 1000 for i in range(64, 200)])
+                       if mode & (1 | 16384) else None,
+                       "true_issue_to_land_us": med([(land[i] - st[2 * i]) / 1000 for i in range(64, 200)])}
+                if mode & 16384:
+                    obs["arrive_us"] = med([(st[1024 + i] - st[512 + i]) / 1000 for i in range(64, 200)])
+                    obs["wait_done_after_arrive_us"] = med([(st[2 * i + 3] - st[1024 + i]) / 1000 for i in range(64, 200)])
+            key = f"tma_layout{layout}_stages{stages}_mode{mode}_pf{pf}"
+            out[key] = {"GBs": round(sms * 8 * 32 * 16384 / ms.value / 1e6, 1), "issue_to_land_us": lat,
+                        "us_per_stage_cta0_median": per, "us_per_stage_mean": round(ms.value * 1e3 / (8 * 32), 3),
+                        "mma_issue_us_median": iss[len(iss) // 2], "mma_issue_us_max": iss[-1], **obs,
+                        "ok": int(ok.item()), "rc": rc}
+            print(key, out[key], flush=True)
+        os.makedirs(os.path.dirname(args.out), exist_ok=True)
+        json.dump(out, open(args.out, "w"), indent=1)
+        return
 
     if args.only_stream:
         for layout, stages, mode in ((5, 6, 0), (5, 6, 128), (5, 6, 1 | 64), (5, 6, 1 | 64 | 128),
