@@ -148,12 +148,12 @@ struct SegIter {
     int total, g, gend;
     int t;
 
-    __device__ void init(int tiles_, int KB_, int G_, int c_) {
+    __device__ void init(int tiles_, int KB_, int G_, int c_, int min_stages = 4) {
         tiles = tiles_; KB = KB_; G = G_; c = c_;
         total = tiles * KB;
         // fewer than four waves of whole tiles would leave SMs idle: split,
-        // as long as every CTA still gets at least 4 K-stages
-        split = tiles < 4 * G && total >= 4 * G;
+        // as long as every CTA still gets at least min_stages K-stages
+        split = tiles < 4 * G && total >= min_stages * G;
         if (split) { g = c * total / G; gend = (c + 1) * total / G; }
         t = c;
     }
@@ -583,6 +583,9 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
 constexpr int kDecStageBytes = 32768 + 1024;  // 256 weight rows + their scale atoms
 constexpr int kDecStages = 6;
 constexpr int kDecGroups = 1;
+// stream-K split of a decode phase down to one K-stage per CTA: one kept
+// expert has only 512 gate/up and 256 down stages for the whole grid
+constexpr int kDecMinStages = 1;
 constexpr int kDecSlotBytes = 2048 + 256;     // one h row (I <= 2048) + what the aliased rows reach
 constexpr int kDecXOff = kDecStages * kDecStageBytes;            // the x row (H <= 4096) + reach
 constexpr int kDecHOff = kDecXOff + 4096 + 512;                   // h rows [group][2 slots]
@@ -682,7 +685,7 @@ __device__ bool dec_slots(const DecArgs& a, const DecPhase& ph, int (&slots)[2])
     int MT, KB, seg_rows;
     dec_shape<false>(a, MT, KB, seg_rows);
     SegIter it;
-    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x, kDecMinStages);
     Seg sg;
     int n = 0;
     slots[0] = slots[1] = -1;
@@ -735,7 +738,7 @@ __device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap
     dec_shape<kGateUp>(a, MT, KB, seg_rows);
     const uint8_t* sfa = kGateUp ? a.gu_sf : a.down_sf;
     SegIter it;
-    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x, kDecMinStages);
     Seg sg;
     int issued = 0;
     bool h_done = kGateUp;
@@ -830,7 +833,7 @@ __device__ bool dec_mma(const DecArgs& a, const DecCtx& c, const DecPhase& ph, i
         }
     }
     SegIter it;
-    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x, kDecMinStages);
     Seg sg;
     while (it.next(sg)) {
         const int s = ph.s_lo + sg.tile / MT;
@@ -897,7 +900,7 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
     float* up_s = reinterpret_cast<float*>(c.smem + kDecUpOff);
     const bool lead_warp = warp == 2;
     SegIter it;
-    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x);
+    it.init(ph.n_s * MT, KB, (int)gridDim.x, (int)blockIdx.x, kDecMinStages);
     Seg sg;
     while (it.next(sg)) {
         const int s = ph.s_lo + sg.tile / MT, m = sg.tile % MT;

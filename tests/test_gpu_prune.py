@@ -21,8 +21,10 @@ pytestmark = pytest.mark.gpu
 # correlated factor, a linear factor.  The synthetic N(0, 1) logits give flat
 # weights (w_6 ~ 0.22-0.25 of w_scale 1.5, unlike the trained router's power
 # law, where the guide's min_w = 0.11 applies), so the thresholds sit inside
-# that range to prune a varying number of experts.
-SETTINGS = [(5, 0.0, 0.0), (4, 0.0, 0.0), (6, 0.24, 0.0), (6, 0.245, 0.3), (3, 0.25, 1.0)]
+# that range to prune a varying number of experts.  Keeping one expert
+# spreads its tiles over the whole grid (each CTA a one- to four-stage piece).
+SETTINGS = [(5, 0.0, 0.0), (4, 0.0, 0.0), (6, 0.24, 0.0), (6, 0.245, 0.3), (3, 0.25, 1.0), (2, 0.0, 0.0),
+            (1, 0.0, 0.0)]
 W_TOL = 32 * 2.0 ** -24  # relative to w_scale: fp32 weights, then one fp32 factor
 
 
