@@ -89,8 +89,9 @@ size_t workspace_bytes(const moe_config& c) {
     }
     b += T * H * 2 + T * E * 4 + T * H * 4 + 2 * T * k * 4;  // staging
     b += 256;                                    // error word
-    // split-tile counters and partial accumulators (sized for up to 256 SMs)
-    b += (size_t)(4 * 256 + 32) * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
+    // split-tile counters, decode flags and partial accumulators (sized for up to 256 SMs)
+    b += (size_t)((4 * 256 + 32) + (2 + 8 * 256 + 256 + 32)) * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
+    b += (size_t)128 * 256 * 8;                  // decode down outputs with their epoch
     return b;
 }
 
@@ -108,7 +109,7 @@ void free_all(moe_layer* L) {
                     L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->perm_cnt, L->xq, L->xs, L->xq_tok,
                     L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
                     L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err,
-                    L->sk_counters, L->sk_partials};
+                    L->sk_counters, L->sk_partials, L->dec_yw};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     moe::tc_free(L);
@@ -245,6 +246,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     A(&L->d_err, 256);
     A(&L->sk_counters, (size_t)moe::kSkCounters(L) * 4);
     A(&L->sk_partials, (size_t)L->num_sms * 2 * 2 * 128 * 128 * 4);
+    A(&L->dec_yw, (size_t)128 * 256 * 8);
     if (a != cudaSuccess) {
         cudaGetLastError();
         free_all(L);
@@ -282,10 +284,11 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
             a = moe::pack_sf_pairs(L->sh_down_s, nullptr, L->sh_down_sf, 1, (int)(H / 256), (int)I, 3, s);
     }
     // a defined workspace: padding rows of the activation buffers read as zero
-    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters};
+    // (and the epoch-tagged decode words start at epoch 0, which no launch uses)
+    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters, L->dec_yw};
     size_t zn[] = {z.Rp * H, z.Rp * H / 32, z.Rp * I, z.Rp * I / 32, 256, z.Rp * 4,
-                   (size_t)moe::kSkCounters(L) * 4};
-    for (int i = 0; i < 7 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
+                   (size_t)moe::kSkCounters(L) * 4, (size_t)128 * 256 * 8};
+    for (int i = 0; i < 8 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
     if (c.has_shared) {
         void* zs[] = {L->xq_tok, L->xs_tok, L->hq_sh, L->hs_sh};
         size_t zsn[] = {z.Tpad * H, z.Tpad * H / 32, z.Tpad * I, z.Tpad * I / 32};

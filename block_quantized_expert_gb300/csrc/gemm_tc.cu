@@ -624,7 +624,8 @@ struct DecArgs {
     const uint8_t* down_sf;
     uint8_t* hq;          // [k][I] e4m3 (scratch)
     uint8_t* hs;          // [k][I/128][16] scale rows (scratch)
-    float* y;             // [k][H] down outputs (scratch)
+    float* y;             // [k][H] down outputs (scratch; unused by the decode kernel)
+    unsigned long long* yw;  // [kDecMaxTiles][256] down tile outputs: epoch << 32 | fp32 bits
     float* sk_part;       // [G][2][2][128][128] partial accumulators of cut tiles
     unsigned long long* launches;  // launch counter: this launch's flags hold its value + 1
     uint32_t* piece_flag;  // [4 phases][G][2]: a cut tile's piece parked by CTA c in slot s
@@ -725,6 +726,28 @@ __device__ bool flag_wait(const uint32_t* f, uint32_t v, volatile int* abort) {
 }
 
 __device__ bool dec_fetch_h(const DecArgs& a, const DecCtx& c, const DecPhase& ph, int g, int lane);
+
+// A value and its launch's epoch in one 64-bit word: a single-copy atomic
+// store / load, so a reader that sees the epoch sees the value with it (no
+// flag, no second round trip).
+__device__ __forceinline__ void word_set(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.relaxed.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+__device__ __forceinline__ unsigned long long word_get(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+// Wait (bounded, like flag_wait) until *p carries epoch e; returns the word.
+__device__ bool word_wait(const unsigned long long* p, uint32_t e, volatile int* abort, unsigned long long& v) {
+    const uint64_t t0 = globaltimer();
+    while ((uint32_t)(v >> 32) != e) {
+        if (globaltimer() - t0 > kWaitLimitNs || *abort) return false;
+        __nanosleep(32);
+        v = word_get(p);
+    }
+    return true;
+}
 
 // TMA producer (warp 0; lane 0 waits and issues): the weight tiles and
 // scale atoms of this CTA's stream-K range of one phase, into the ring.  A
@@ -967,21 +990,25 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
             epi_bar();
             if (lead_warp && lane == 0) flag_set(a.h_flag + gt, c.epoch);
         } else if (s < c.k - 1) {
-            a.y[(size_t)c.seg_j[s] * a.H + f0 + col] = v;
-            epi_bar();
-            if (lead_warp && lane == 0) flag_set(a.y_flag + gt, c.epoch);
+            word_set(a.yw + (size_t)gt * 256 + col, ((unsigned long long)c.epoch << 32) | __float_as_uint(v));
         } else {
             // the last expert's tile of block m: combine the block in
-            // ascending expert order, this tile's y from registers
-            if (lead_warp) {
-                bool ok = true;
-                if (lane < c.k - 1) ok = flag_wait(a.y_flag + lane * MT + m, c.epoch, c.abort_flag);
-                if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
-            }
-            epi_bar();
+            // ascending expert order, this tile's y from registers, the
+            // others' from their epoch-tagged words (all loads in flight
+            // at once; a word of an earlier launch is polled again)
+            unsigned long long yv[kMaxTopK - 1];
+#pragma unroll
+            for (int ss = 0; ss < kMaxTopK - 1; ++ss)
+                if (ss < c.k - 1) yv[ss] = word_get(a.yw + (size_t)(ss * MT + m) * 256 + col);
             float o = 0.f;
-            for (int ss = 0; ss < c.k - 1; ++ss)
-                o += c.seg_w[ss] * __ldcg(a.y + (size_t)c.seg_j[ss] * a.H + f0 + col);
+            bool ok = true;
+#pragma unroll
+            for (int ss = 0; ss < kMaxTopK - 1; ++ss) {
+                if (ss >= c.k - 1) break;
+                ok = ok && word_wait(a.yw + (size_t)(ss * MT + m) * 256 + col, c.epoch, c.abort_flag, yv[ss]);
+                o += c.seg_w[ss] * __uint_as_float((uint32_t)yv[ss]);
+            }
+            if (!ok) c.give_up(a);
             o += c.seg_w[c.k - 1] * v;
             a.out[f0 + col] = o;
         }
@@ -1498,6 +1525,7 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     a.hq = L->hq;
     a.hs = L->hs;
     a.y = L->y;
+    a.yw = L->dec_yw;
     a.sk_part = L->sk_partials;
     int32_t* dw = L->sk_counters + kSkZeroed(L);
     a.launches = reinterpret_cast<unsigned long long*>(dw);

@@ -60,6 +60,7 @@ struct moe_layer {
     uint32_t* d_err;      // sticky device error flags
     int32_t* sk_counters; // [4][num_sms] arrival counters of split tiles (zeroed per forward)
     float* sk_partials;   // [num_sms][2][2][128][128] partial accumulators of split tiles
+    unsigned long long* dec_yw;  // [128 tiles][256] decode down outputs: launch epoch << 32 | fp32 bits
 
     void* tc;             // tensor-core kernel state (tensor maps), or null
     unsigned long long launches;  // kernels enqueued so far
