@@ -240,7 +240,7 @@ moe_status moe_set_gemm_path(moe_layer* layer, int path);
 moe_status moe_set_route_prune(moe_layer* layer, int keep, float min_w, float rho);
 
 /* Token -> expert grouping without a layer and without any allocation.
- * The paper has no counterpart: this entry point exists for callers that
+ * The method's description has no counterpart: this entry point exists for callers that
  * cannot call cudaMalloc -- code running inside another framework's memory
  * arena that forbids foreign allocations, serving loops that freeze device
  * memory after start-up, or engines that only want the grouping for their

@@ -2,7 +2,7 @@
 """Microbenchmarks of the sm_103a building blocks (tests/csrc/tc_probe.cu):
 a plain HBM read stream, the block-scaled MMA issue rate, and TMA weight
 streaming with and without MMAs.  Prints one line per case and writes all
-results as JSON (default gpurun_out/microbench_tc.json).  Timing only.
+results as JSON (default tests/_build/microbench_tc.json).  Timing only.
 
     python tests/microbench_tc.py [--out PATH]
 """
@@ -43,7 +43,7 @@ def load():
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--out", default=os.path.join(ROOT, "gpurun_out", "microbench_tc.json"))
+    ap.add_argument("--out", default=os.path.join(HERE, "_build", "microbench_tc.json"))
     ap.add_argument("--only-mix", action="store_true", help="only the per-stage MMA group issue costs")
     ap.add_argument("--only-stream", action="store_true", help="only the 256-row weight-box TMA streams")
     ap.add_argument("--only-ldg", action="store_true",
