@@ -738,15 +738,26 @@ __device__ __forceinline__ unsigned long long word_get(const unsigned long long*
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-// Wait (bounded, like flag_wait) until *p carries epoch e; returns the word.
-__device__ bool word_wait(const unsigned long long* p, uint32_t e, volatile int* abort, unsigned long long& v) {
+// Wait (bounded, like flag_wait) until the n <= N words p[i * stride]
+// carry epoch e, v[i] holding each word's first read.  Every round re-reads
+// all words still of an earlier launch together: one round trip per round,
+// not one per word.
+template <int N>
+__device__ bool words_wait(const unsigned long long* p, size_t stride, int n, uint32_t e, volatile int* abort,
+                           unsigned long long (&v)[N]) {
     const uint64_t t0 = globaltimer();
-    while ((uint32_t)(v >> 32) != e) {
+    while (true) {
+        uint32_t pending = 0;
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if (i < n && (uint32_t)(v[i] >> 32) != e) pending |= 1u << i;
+        if (!pending) return true;
         if (globaltimer() - t0 > kWaitLimitNs || *abort) return false;
         __nanosleep(32);
-        v = word_get(p);
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+            if ((pending >> i) & 1u) v[i] = word_get(p + (size_t)i * stride);
     }
-    return true;
 }
 
 // TMA producer (warp 0; lane 0 waits and issues): the weight tiles and
@@ -997,17 +1008,14 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
             // others' from their epoch-tagged words (all loads in flight
             // at once; a word of an earlier launch is polled again)
             unsigned long long yv[kMaxTopK - 1];
+            const unsigned long long* yp = a.yw + (size_t)m * 256 + col;  // expert ss: + ss * MT * 256
+#pragma unroll
+            for (int ss = 0; ss < kMaxTopK - 1; ++ss) yv[ss] = ss < c.k - 1 ? word_get(yp + (size_t)ss * MT * 256) : 0ull;
+            const bool ok = words_wait(yp, (size_t)MT * 256, c.k - 1, c.epoch, c.abort_flag, yv);
+            float o = 0.f;
 #pragma unroll
             for (int ss = 0; ss < kMaxTopK - 1; ++ss)
-                if (ss < c.k - 1) yv[ss] = word_get(a.yw + (size_t)(ss * MT + m) * 256 + col);
-            float o = 0.f;
-            bool ok = true;
-#pragma unroll
-            for (int ss = 0; ss < kMaxTopK - 1; ++ss) {
-                if (ss >= c.k - 1) break;
-                ok = ok && word_wait(a.yw + (size_t)(ss * MT + m) * 256 + col, c.epoch, c.abort_flag, yv[ss]);
-                o += c.seg_w[ss] * __uint_as_float((uint32_t)yv[ss]);
-            }
+                if (ss < c.k - 1) o += c.seg_w[ss] * __uint_as_float((uint32_t)yv[ss]);
             if (!ok) c.give_up(a);
             o += c.seg_w[c.k - 1] * v;
             a.out[f0 + col] = o;
