@@ -90,7 +90,7 @@ size_t workspace_bytes(const moe_config& c) {
     b += T * H * 2 + T * E * 4 + T * H * 4 + 2 * T * k * 4;  // staging
     b += 256;                                    // error word
     // split-tile counters, decode flags and partial accumulators (sized for up to 256 SMs)
-    b += (size_t)((4 * 256 + 32) + (2 + 8 * 256 + 256 + 32)) * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
+    b += (size_t)((4 * 256 + 32) + (2 + 8 * 256 + 128 + 32)) * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
     b += (size_t)128 * 256 * 8;                  // decode down outputs with their epoch
     return b;
 }

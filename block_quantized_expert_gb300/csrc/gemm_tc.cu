@@ -624,13 +624,11 @@ struct DecArgs {
     const uint8_t* down_sf;
     uint8_t* hq;          // [k][I] e4m3 (scratch)
     uint8_t* hs;          // [k][I/128][16] scale rows (scratch)
-    float* y;             // [k][H] down outputs (scratch; unused by the decode kernel)
     unsigned long long* yw;  // [kDecMaxTiles][256] down tile outputs: epoch << 32 | fp32 bits
     float* sk_part;       // [G][2][2][128][128] partial accumulators of cut tiles
     unsigned long long* launches;  // launch counter: this launch's flags hold its value + 1
     uint32_t* piece_flag;  // [4 phases][G][2]: a cut tile's piece parked by CTA c in slot s
     uint32_t* h_flag;      // [kDecMaxTiles]: h of gate/up tile t written
-    uint32_t* y_flag;      // [kDecMaxTiles]: y of down tile t written
     uint16_t* x_stage;     // x in host memory: CTA 0's device copy of it for the others, else null
     uint32_t* x_flag;      // x_stage written
     uint32_t* err;
@@ -1532,15 +1530,13 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     a.down_sf = L->down_sf;
     a.hq = L->hq;
     a.hs = L->hs;
-    a.y = L->y;
     a.yw = L->dec_yw;
     a.sk_part = L->sk_partials;
     int32_t* dw = L->sk_counters + kSkZeroed(L);
     a.launches = reinterpret_cast<unsigned long long*>(dw);
     a.piece_flag = reinterpret_cast<uint32_t*>(dw + 2);
     a.h_flag = a.piece_flag + 8 * L->num_sms;
-    a.y_flag = a.h_flag + kDecMaxTiles;
-    a.x_flag = a.y_flag + kDecMaxTiles;
+    a.x_flag = a.h_flag + kDecMaxTiles;
     a.x_stage = x_in_host ? L->x_stage : nullptr;
     a.err = L->d_err;
     a.trace = L->trace;

@@ -90,8 +90,8 @@ constexpr int kFrontQuantMaxT = 4;
 inline int kSkZeroed(const moe_layer* L) { return 4 * L->num_sms + 32; }
 // then the words of the one-token decode kernel, zeroed only at creation: a
 // 64-bit launch counter, piece flags [4 phases][num_sms][2], h flags [128],
-// y flags [128]
-inline int kDecWords(const moe_layer* L) { return 2 + 8 * L->num_sms + 256 + 32; }
+// the staged-x flag (+ spare)
+inline int kDecWords(const moe_layer* L) { return 2 + 8 * L->num_sms + 128 + 32; }
 inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L); }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
