@@ -540,9 +540,10 @@ def run_e2e(args, cfg, layer, tk, S, K, W, world, dev):
 
 
 # ------------------------------------------------------------- CPU oracle --
-def oracle_rate(cfg, w, tk, seconds, prune=None):
+def oracle_rate(cfg, w, tk, seconds, prune=None, max_tokens=None, warmup_calls=1):
     """Tokens/s of the fp64 oracle (route + layer) on the host cores, on a
-    sample sized to about `seconds` of work."""
+    sample sized to about `seconds` of work and at most `max_tokens` tokens,
+    after `warmup_calls` untimed calls on one token each."""
     from oracle import oracle as orc
 
     for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s"):
@@ -561,11 +562,13 @@ def oracle_rate(cfg, w, tk, seconds, prune=None):
         return tok, time.perf_counter() - t
 
     # calibrate on two tokens per thread (the oracle runs tokens in parallel),
-    # after a first call that loads the library and its tables
-    run(min(2, n_all))
-    n0, t0 = run(min(2 * orc.max_threads(), n_all))
+    # after the warm-up calls (the first loads the library and its tables)
+    for _ in range(max(1, warmup_calls)):
+        run(1)
+    cap = n_all if max_tokens is None else max(1, min(n_all, max_tokens))
+    n0, t0 = run(min(2 * orc.max_threads(), cap))
     per = t0 / n0
-    n = int(max(4, min(n_all, seconds / max(per, 1e-9))))
+    n = int(max(min(4, cap), min(cap, seconds / max(per, 1e-9))))
     n, t = run(n)
     return n, t, orc.max_threads(), T
 
@@ -587,18 +590,22 @@ def run_reference(args, cfg, rank, world):
     w = make_weights(cfg)
     tk = make_tokens(cfg, n=min(cfg.T * (K + W), 4096) if cfg.T == 1 else cfg.T)
     budget = 60.0
-    n, t, cores, T = oracle_rate(cfg, w, tk, budget, args.prune_t)
+    # W untimed warm-up steps (one token each), then at most K steps' tokens,
+    # bounded to about `budget` seconds (tokens are independent; the oracle
+    # runs them in parallel over the host cores)
+    n, t, cores, T = oracle_rate(cfg, w, tk, budget, args.prune_t, max_tokens=K * cfg.T, warmup_calls=W)
     value = n / t
     steps_done = max(1, n // cfg.T)
     res = {"metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
-           "steps": steps_done, "warmup": 1, "ms_per_step": 1e3 * t / steps_done,
+           "steps": steps_done, "warmup": W, "ms_per_step": 1e3 * t * cfg.T / n,
            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
            "data": "synthetic (seeded)", "config": config_json(cfg, args, world),
            "impl": "reference",
            "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": cores,
                             "kind": "oracle",
-                            "sample": f"{n} tokens ({steps_done} of {K} steps, time-bounded "
-                                      f"~{budget:.0f} s) of the {cfg.name} workload"},
+                            "sample": f"{n} tokens (of the {K * cfg.T} in {K} steps; time-bounded "
+                                      f"~{budget:.0f} s) of the {cfg.name} workload after {W} "
+                                      f"warm-up tokens"},
            "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                    "d2h_bytes_per_step": 0}}
     return res
