@@ -157,7 +157,8 @@ moe_status moe_forward(moe_layer* layer, const uint16_t* x, int T, const int32_t
  * counting sort and the quantisation in one kernel.  One token on the
  * automatic path runs as one cooperative kernel of one CTA per SM (route,
  * quantise, gate/up, down, combine; hand-offs between CTAs through bounded
- * flag waits); moe_hidden does not report h after such a call.            */
+ * waits on flags or on epoch-tagged data); moe_hidden does not report h
+ * after such a call.                                                       */
 moe_status moe_route_forward(moe_layer* layer, const float* logits, const uint16_t* x, int T,
                              int32_t* ids, float* w, float* out, moe_stream_t stream);
 
@@ -167,7 +168,8 @@ moe_status moe_route_forward(moe_layer* layer, const float* logits, const uint16
  * on `stream` (page-locked host buffers make the copies overlap); read out
  * only after synchronising the stream.  One token on the automatic path with
  * all three buffers page-locked (16-byte aligned x and out) enqueues no copy:
- * the decode kernel reads and writes the host memory in place (mapped).    */
+ * the decode kernel reads and writes the host memory in place (mapped; one
+ * CTA reads x over the host link and hands a device copy to the others).   */
 moe_status moe_forward_host(moe_layer* layer, const uint16_t* x, const float* logits, int T,
                             float* out, moe_stream_t stream);
 
