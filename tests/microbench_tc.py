@@ -164,7 +164,11 @@ def main():
                                          (5, 5, 1 | 64, 0), (5, 5, 1 | 64 | 2048, 0), (5, 5, 1 | 64 | 2048 | 4096, 0),
                                          (5, 6, 1 | 64, 0), (5, 6, 1 | 64 | 2, 6), (5, 6, 1 | 64 | 2, 12),
                                          (5, 6, 1 | 64 | 2, 24), (5, 6, 1 | 64 | 2, 48), (5, 6, 1 | 64 | 128 | 2, 12),
-                                         (5, 6, 2, 12), (5, 6, 0, 0)):
+                                         (5, 6, 2, 12), (5, 6, 0, 0),
+                                         (5, 6, 1 | 64 | 4, 0), (5, 6, 1 | 64 | 8192, 0),
+                                         (5, 6, 16384, 150), (5, 6, 16384, 290), (5, 6, 16384, 450),
+                                         (5, 6, 16384 | 32768, 290), (5, 6, 16384 | 32768 | 131072, 290),
+                                         (5, 6, 16384 | 32768 | 65536, 290), (5, 6, 1 | 64 | 32768, 0)):
             for _ in range(2):
                 ok.fill_(1)
                 rc = lib.probe_stream(A.data_ptr(), rows, sms, 8, stages, mode, pf, stamps.data_ptr(),
