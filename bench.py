@@ -45,6 +45,8 @@ def parse():
     ap.add_argument("--graph-chunk", type=int, default=256, help="steps per CUDA graph")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="skip the time-boxed records of the other workloads (default run only)")
     ap.add_argument("--cpu-seconds", type=float, default=12.0)
     ap.add_argument("--trace", action="store_true",
                     help="after timing, trace one more call of the GEMM kernels (stderr)")
@@ -180,12 +182,203 @@ class ClockSampler:
 
 
 # --------------------------------------------------------------- our path --
+def _upload_weights(w, dev):
+    import torch
+    return {n: torch.from_numpy(np.array(getattr(w, n))).to(dev)
+            for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
+                      "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")
+            if getattr(w, n) is not None}
+
+
+def make_layer(bqe, cfg, w, dev, max_tokens, path="auto", prune=None):
+    import torch
+    dw = _upload_weights(w, dev)
+    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, max_tokens, cfg.shared, cfg.w_scale)
+    layer = bqe.moe_create(mc, dw)
+    torch.cuda.synchronize(dev)
+    del dw
+    bqe.moe_set_gemm_path(layer, {"auto": 0, "cc": 1, "tc": 2}[path])
+    if prune:
+        bqe.moe_set_route_prune(layer, *prune)
+    return layer
+
+
+class Workload:
+    """Device inputs of S distinct batches of one configuration and the call
+    that runs the layer on batch i (route + layer)."""
+
+    def __init__(self, bqe, cfg, layer, dev, S, seed, router=None):
+        import torch
+        from workloads import make_hash_table, make_tokens
+        self.bqe, self.cfg, self.layer, self.S = bqe, cfg, layer, S
+        self.router = router or cfg.router
+        tk = make_tokens(cfg, seed=seed, n=S * cfg.T)
+        self.tokens = tk
+        self.x = torch.from_numpy(tk.x_bits.view(np.int16).reshape(S, cfg.T, cfg.H).copy()).to(dev)
+        self.lg = torch.from_numpy(tk.logits.reshape(S, cfg.T, cfg.E).copy()).to(dev)
+        if self.router == "hash":
+            self.tab = torch.from_numpy(make_hash_table(cfg)).to(dev)
+            self.tok = torch.from_numpy(tk.token_ids.reshape(S, cfg.T).copy()).to(dev)
+        self.ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
+        self.wt = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
+        self.out = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device=dev)
+
+    def step(self, i):
+        j = i % self.S
+        b = self.bqe
+        if self.router == "hash":
+            b.moe_route_hash(self.layer, self.tok[j], self.tab, self.ids, self.wt)
+            b.moe_forward(self.layer, self.x[j], self.ids, self.wt, self.out)
+        else:
+            b.moe_route_forward(self.layer, self.lg[j], self.x[j], self.ids, self.wt, self.out)
+
+    def touched(self, n=64):
+        """Mean experts touched and mean kept (routed) rows per batch."""
+        touched, kept = [], []
+        for j in range(min(self.S, n)):
+            self.step(j)
+            idn = self.ids.cpu().numpy()
+            touched.append(len(np.unique(idn[idn >= 0])))  # -1: a pruned slot
+            kept.append(int((idn >= 0).sum()))
+        return float(np.mean(touched)), int(round(np.mean(kept)))
+
+
+def capture(step, first, n, chunk, stream, before_step=None):
+    """CUDA graphs of n steps (chunk steps each) starting at step `first`."""
+    import torch
+    graphs = []
+    with torch.cuda.stream(stream):
+        for c0 in range(0, n, chunk):
+            g = torch.cuda.CUDAGraph()
+            stream.synchronize()
+            with torch.cuda.graph(g, stream=stream):
+                for i in range(c0, min(n, c0 + chunk)):
+                    if before_step is not None:
+                        before_step(i)
+                    step(first + i)
+            graphs.append(g)
+    return graphs
+
+
+def timed_replay(graphs, K, chunk, stream, dev, world):
+    """Replay the graphs (K steps) between two events on their stream,
+    bracketed by a barrier and a device synchronisation on both sides; an
+    event after each graph gives the per-step time of every chunk.  Returns
+    (slowest rank's ms, per-chunk ms per step, wall start, wall end)."""
+    import torch
+    import torch.distributed as dist
+    for g in graphs[:2]:
+        g.replay()
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    t0 = torch.cuda.Event(enable_timing=True)
+    t1 = torch.cuda.Event(enable_timing=True)
+    chunk_ev = [torch.cuda.Event(enable_timing=True) for _ in graphs]
+    wall0 = time.time()
+    with torch.cuda.stream(stream):
+        t0.record(stream)
+        for g, ce in zip(graphs, chunk_ev):
+            g.replay()
+            ce.record(stream)
+        t1.record(stream)
+    torch.cuda.synchronize(dev)
+    wall1 = time.time()
+    if world > 1:
+        dist.barrier()
+    chunk_ms, prev = [], t0
+    for ci, ce in enumerate(chunk_ev):
+        n_steps = min(chunk, K - ci * chunk)
+        chunk_ms.append(prev.elapsed_time(ce) / n_steps)
+        prev = ce
+    return max_over_ranks(t0.elapsed_time(t1), world, dev), chunk_ms, wall0, wall1
+
+
+STAGES = ["permute", "quantize", "gateup", "down", "combine"]
+
+
+def stage_times(bqe, layer, step, first, n, stream):
+    """Per-stage device times (ms) from a separate, untimed pass: n more
+    steps captured with the library's stage events on every step (the
+    events sit between the stage kernels, so this pass is not the timed one)."""
+    import torch
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(6)] for _ in range(n)]
+    with torch.cuda.stream(stream):
+        for e6 in evs:  # events must exist on the stream before the capture
+            for e in e6:
+                e.record(stream)
+    graphs = capture(step, first, n, n, stream, before_step=lambda i: bqe.moe_set_stage_events(layer, evs[i]))
+    for g in graphs:
+        g.replay()
+    torch.cuda.synchronize()
+    st = np.array([[e6[i].elapsed_time(e6[i + 1]) for i in range(5)] for e6 in evs])
+    return dict(zip(STAGES, st.mean(0).tolist()))
+
+
+def clocked(fn):
+    """Run fn() with nvidia-smi sampling the SM clocks; returns (fn(), clocks)."""
+    import torch
+    sampler = ClockSampler(gpu_uuid(torch.cuda.current_device()))
+    time.sleep(0.3)
+    r = fn()
+    rows = sampler.stop()
+    wall0, wall1 = r[2], r[3]
+    in_region = [row for row in rows if _ts_in(row[0], wall0, wall1)]
+    clocks = ClockSampler.summary(in_region if in_region else rows)
+    clocks["window"] = "timed region" if in_region else "around the timed region"
+    return r, clocks
+
+
+def load_peaks():
+    try:
+        return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
+    except OSError:
+        return {}
+
+
+def roofline(cfg, dom, kernel_ms, byts, rows, peaks, mma_peak=None):
+    """Roofline of the dominant kernel: algorithmic bytes (or flops) per
+    launch over its measured duration, against the measured peak."""
+    hbm = peaks.get("hbm_gbs", 6800.0)
+    achieved = byts[dom] / (kernel_ms * 1e-3) / 1e9
+    roof = {"bound": "hbm", "achieved": round(achieved, 1), "peak": hbm, "unit": "GB/s",
+            "frac": round(achieved / hbm, 4), "kernel_ms": round(kernel_ms, 6),
+            "algorithmic_bytes_per_launch": int(byts[dom]),
+            "peak_source": "measured (MEASURED_PEAKS.json hbm_gbs), of measured" if "hbm_gbs" in peaks
+            else "fallback 6.8 TB/s, of fallback"}
+    if dom in ("gateup", "down"):
+        H, I = cfg.H, cfg.I
+        flops = {"gateup": rows * 4.0 * H * I, "down": rows * 2.0 * H * I}[dom]
+        if cfg.shared and dom == "down":  # the down stage also runs the shared expert's two GEMMs
+            flops += cfg.T * 6.0 * H * I
+        tflops = flops / (kernel_ms * 1e-3) / 1e12
+        # the recipe's figure: the fp8-class block-scaled MMA at twice the
+        # measured bf16 rate (sustained: the kernel runs inside a long step)
+        tpeak = 2.0 * peaks.get("bf16_tflops_sustained", 1700.0)
+        tensor = {"tflops": round(tflops, 1), "algorithmic_flops_per_launch": flops,
+                  "peak_2x_bf16_sustained": round(tpeak, 1),
+                  "frac_2x_bf16_sustained": round(tflops / tpeak, 4)}
+        if mma_peak:
+            tensor.update({"peak_mxf8f6f4_measured": round(mma_peak, 1),
+                           "frac_mxf8f6f4_measured": round(tflops / mma_peak, 4)})
+        roof["tensor"] = tensor
+        ref = mma_peak or tpeak
+        if tflops / ref > achieved / hbm:
+            roof.update({"bound": "tensor", "achieved": round(tflops, 1), "peak": round(ref, 1),
+                         "unit": "TFLOP/s", "frac": round(tflops / ref, 4),
+                         "peak_source": ("block-scaled MMA loop (libmoe_peaks, kind::mxf8f6f4, M128 N256 "
+                                         "K32) measured in this run, of measured") if mma_peak else
+                                        "measured bf16_tflops_sustained x 2 (fp8 / bf16 nominal ratio), of measured"})
+    return roof
+
+
 def run_ours(args, cfg, rank, world, local_rank):
     import torch
     import torch.distributed as dist
 
     import block_quantized_expert_gb300 as bqe
-    from workloads import make_hash_table, make_tokens, make_weights
+    from workloads import make_weights
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
@@ -196,196 +389,143 @@ def run_ours(args, cfg, rank, world, local_rank):
     W = max(W, 3)
 
     w = make_weights(cfg)
-    dw = {n: torch.from_numpy(np.array(getattr(w, n))).to(dev)
-          for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
-                    "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")
-          if getattr(w, n) is not None}
-    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, cfg.T, cfg.shared, cfg.w_scale)
-    layer = bqe.moe_create(mc, dw)
-    del dw
-    bqe.moe_set_gemm_path(layer, {"auto": 0, "cc": 1, "tc": 2}[args.path])
-    if args.prune_t:
-        bqe.moe_set_route_prune(layer, *args.prune_t)
-
+    layer = make_layer(bqe, cfg, w, dev, cfg.T, args.path, args.prune_t)
     # distinct inputs: one token per step for decode, else a few batches cycled
     S = (K + W) if cfg.T == 1 else min(K + W, 4)
-    tk = make_tokens(cfg, seed=rank_seed(cfg, rank), n=S * cfg.T)
-    x_all = torch.from_numpy(tk.x_bits.view(np.int16).reshape(S, cfg.T, cfg.H).copy()).to(dev)
-    lg_all = torch.from_numpy(tk.logits.reshape(S, cfg.T, cfg.E).copy()).to(dev)
-    hashed = cfg.router == "hash"
-    if hashed:
-        tab = torch.from_numpy(make_hash_table(cfg)).to(dev)
-        tok_all = torch.from_numpy(tk.token_ids.reshape(S, cfg.T).copy()).to(dev)
-    ids = torch.empty((cfg.T, cfg.k), dtype=torch.int32, device=dev)
-    wt = torch.empty((cfg.T, cfg.k), dtype=torch.float32, device=dev)
-    out = torch.empty((cfg.T, cfg.H), dtype=torch.float32, device=dev)
-
-    def step(i):
-        j = i % S
-        if hashed:
-            bqe.moe_route_hash(layer, tok_all[j], tab, ids, wt)
-            bqe.moe_forward(layer, x_all[j], ids, wt, out)
-        else:
-            bqe.moe_route_forward(layer, lg_all[j], x_all[j], ids, wt, out)
-
-    # experts touched per input batch (for the algorithmic byte count)
-    touched, kept = [], []
-    for j in range(min(S, 64)):
-        step(j)
-        idn = ids.cpu().numpy()
-        touched.append(len(np.unique(idn[idn >= 0])))  # -1: a pruned slot
-        kept.append(int((idn >= 0).sum()))
-    avg_touched = float(np.mean(touched))
-    rows = int(round(np.mean(kept)))
+    wl = Workload(bqe, cfg, layer, dev, S, rank_seed(cfg, rank))
+    avg_touched, rows = wl.touched()
     for i in range(W):
-        step(i)
+        wl.step(i)
     bqe.moe_check(layer)
 
-    # the timed region: K steps as chunked CUDA graphs; stage events on every
-    # ev_every-th step
+    # the timed region: K steps as chunked CUDA graphs, nothing else inside
     stream = torch.cuda.Stream(device=dev)
-    ev_every = max(1, K // 256)
-    stage_events = []
-    graphs = []
     launches0 = bqe.moe_kernel_launches(layer)
-    with torch.cuda.stream(stream):
-        for c0 in range(0, K, args.graph_chunk):
-            g = torch.cuda.CUDAGraph()
-            evs_chunk = []
-            for i in range(c0, min(K, c0 + args.graph_chunk)):
-                if i % ev_every == 0:
-                    evs = [torch.cuda.Event(enable_timing=True) for _ in range(6)]
-                    for e in evs:
-                        e.record(stream)
-                    evs_chunk.append(evs)
-            stream.synchronize()
-            with torch.cuda.graph(g, stream=stream):
-                n_ev = 0
-                for i in range(c0, min(K, c0 + args.graph_chunk)):
-                    if i % ev_every == 0:
-                        bqe.moe_set_stage_events(layer, evs_chunk[n_ev])
-                        n_ev += 1
-                    step(W + i)
-            graphs.append(g)
-            stage_events.extend(evs_chunk)
+    graphs = capture(wl.step, W, K, args.graph_chunk, stream)
     launches = bqe.moe_kernel_launches(layer) - launches0   # kernels per replay of all graphs
-    for g in graphs[:2]:
-        g.replay()
-    torch.cuda.synchronize()
-
-    sampler = ClockSampler(gpu_uuid(dev))
-    time.sleep(0.3)
-    if world > 1:
-        dist.barrier()
-    torch.cuda.synchronize()
-    t0 = torch.cuda.Event(enable_timing=True)
-    t1 = torch.cuda.Event(enable_timing=True)
-    wall0 = time.time()
-    # an event after every graph (chunk of args.graph_chunk steps) gives the
-    # spread of the per-step time across the timed region
-    chunk_ev = [torch.cuda.Event(enable_timing=True) for _ in graphs]
-    with torch.cuda.stream(stream):
-        t0.record(stream)
-        for g, ce in zip(graphs, chunk_ev):
-            g.replay()
-            ce.record(stream)
-        t1.record(stream)
-    torch.cuda.synchronize()
-    wall1 = time.time()
-    chunk_ms, prev = [], t0
-    for ci, ce in enumerate(chunk_ev):
-        n_steps = min(args.graph_chunk, K - ci * args.graph_chunk)
-        chunk_ms.append(prev.elapsed_time(ce) / n_steps)
-        prev = ce
-    if world > 1:
-        dist.barrier()
-    clk_rows = sampler.stop()
-    ms = max_over_ranks(t0.elapsed_time(t1), world, dev)
+    (ms, chunk_ms, wall0, wall1), clocks = clocked(lambda: timed_replay(graphs, K, args.graph_chunk, stream,
+                                                                         dev, world))
     bqe.moe_check(layer)
+    del graphs
 
     if args.trace:
-        trace_report(bqe, layer, step, K + W, dev)
+        trace_report(bqe, layer, wl.step, K + W, dev)
 
-    # per-stage device times from the sampled steps
-    names = ["permute", "quantize", "gateup", "down", "combine"]
-    st = np.array([[evs[i].elapsed_time(evs[i + 1]) for i in range(5)] for evs in stage_events])
-    stage_ms = dict(zip(names, st.mean(0).tolist()))
     byts = algorithmic_bytes(cfg, avg_touched, rows)
     step_bytes = byts["gateup"] + byts["down"]
+    peaks = load_peaks()
     if launches == K:
-        # one token on the automatic path: the whole layer is one kernel, so
-        # its average duration is the timed region over the K calls (the
-        # sampled stage events around it break the back-to-back launches)
-        dom = "layer"
-        byts["layer"] = byts["gateup"] + byts["down"]
-        stage_ms["layer"] = stage_ms.pop("gateup")
-        stage_ms.pop("down")
+        # one kernel per call (the whole-layer decode kernel): its average
+        # duration is the timed region over the K calls
+        dom, kernel_ms, stage_ms = "layer", ms / K, None
+        byts["layer"] = step_bytes
         kernel = "whole-layer decode kernel (k_decode)"
     else:
+        stage_ms = stage_times(bqe, layer, wl.step, W + K, min(K, 32), stream)
         dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
-        kernel = f"{dom} GEMM"
-    kernel_ms = ms / K if dom == "layer" else stage_ms[dom]
-    achieved = byts[dom] / (kernel_ms * 1e-3) / 1e9
-    peaks = {}
-    try:
-        peaks = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
-    except OSError:
-        pass
-    peak = peaks.get("hbm_gbs", 6800.0)
-    peak_src = "measured (MEASURED_PEAKS.json hbm_gbs)" if "hbm_gbs" in peaks else "fallback 6.8 TB/s"
+        kernel_ms, kernel = stage_ms[dom], f"{dom} GEMM"
+    roof = roofline(cfg, dom, kernel_ms, byts, rows, peaks)
+    roof["kernel"] = kernel
+    roof["traffic"] = profiled_traffic(cfg, dom) if not args.prune_t else None
+    roof["hbm_frac_whole_step"] = round(step_bytes / (ms / K * 1e-3) / 1e9 / roof["peak"], 4) \
+        if roof["unit"] == "GB/s" else None
 
-    roof = {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(achieved / peak, 4), "traffic": None if args.prune_t else profiled_traffic(cfg, dom),
-            "kernel_ms": round(kernel_ms, 6), "algorithmic_bytes_per_launch": int(byts[dom]),
-            "peak_source": peak_src}
-    if dom != "layer":
-        # a GEMM stage whose multiply-adds outweigh its bytes is tensor-bound:
-        # the block-scaled fp4 x fp8 MMA runs at the fp8 rate, twice the
-        # measured bf16 peak (sustained: the kernel runs inside a long step)
-        H, I = cfg.H, cfg.I
-        flops = {"gateup": rows * 4.0 * H * I, "down": rows * 2.0 * H * I}[dom]
-        tpeak = 2.0 * peaks.get("bf16_tflops_sustained", 1700.0)
-        tflops = flops / (kernel_ms * 1e-3) / 1e12
-        if tflops / tpeak > achieved / peak:
-            roof.update({"bound": "tensor", "achieved": round(tflops, 1), "peak": round(tpeak, 1),
-                         "unit": "TFLOP/s", "frac": round(tflops / tpeak, 4), "traffic": None,
-                         "algorithmic_flops_per_launch": flops,
-                         "peak_source": ("measured bf16_tflops_sustained x 2 (fp8 / bf16 nominal ratio)"
-                                         if "bf16_tflops_sustained" in peaks else "fallback 1.7 PF/s x 2")})
-
-    value = job_rate(world, K * cfg.T, ms)
-    # rows in the timed region within the clock sampling
-    in_region = [r for r in clk_rows if _ts_in(r[0], wall0, wall1)]
-    clocks = ClockSampler.summary(in_region if in_region else clk_rows)
-    clocks["window"] = "timed region" if in_region else "around the timed region"
-
-    res = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+    res = {"metric": METRIC, "value": job_rate(world, K * cfg.T, ms), "unit": UNIT, "n_gpus": world,
            "steps": K, "warmup": W, "ms_per_step": ms / K, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None,
            "dtype": "mxfp4 x mxfp8 -> f32 accumulate", "data": "synthetic (seeded)",
            "config": config_json(cfg, args, world),
            "gpu_launches": int(launches),
            "per_step_spread": chunk_spread(chunk_ms),
-           "stage_ms": {k: round(v, 5) for k, v in stage_ms.items()},
            "experts_touched_per_step": avg_touched,
-           "roofline": dict(roof, **{
-                        "hbm_frac_whole_step": round(
-                            step_bytes / (ms / K * 1e-3) / 1e9 / peak, 4)}),
+           "roofline": roof,
            "clocks": clocks}
+    if stage_ms:
+        res["stage_ms_untimed_pass"] = {k: round(v, 5) for k, v in stage_ms.items()}
 
     if not args.no_e2e:
-        res["e2e"] = run_e2e(args, cfg, layer, tk, S, K, W, world, dev)
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        res["cpu_baseline"] = cpu_baseline(cfg, w, tk, args.cpu_seconds, args.prune_t)
+        res["e2e"] = run_e2e(args, cfg, layer, wl.tokens, S, K, W, world, dev)
     layer.close()
+    del wl
+    torch.cuda.empty_cache()
+    if rank == 0 and world == 1 and cfg.index == 1 and not args.no_per_config and not args.prune_t:
+        res["per_config"] = per_config(args, bqe, dev, peaks)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(cfg, w, wl_tokens_for_cpu(cfg, rank), args.cpu_seconds, args.prune_t)
     if world > 1:
         dist.destroy_process_group()
     return res
 
 
-# DRAM bytes per launch of the decode kernel from the committed ncu summary,
+def wl_tokens_for_cpu(cfg, rank):
+    from workloads import make_tokens
+    return make_tokens(cfg, seed=rank_seed(cfg, rank), n=max(cfg.T, min(4096, 64 * cfg.T)))
+
+
+PER_CONFIG = [  # (config, router, timed steps)
+    (2, "hash", 128), (2, "learned", 128), (3, None, 48), (4, None, 16)]
+
+
+def per_config(args, bqe, dev, peaks):
+    """One time-boxed record per other workload (batched decode with the hash
+    and the learned router, pp512, prefill 8192 with the shared expert):
+    tokens/s over the timed steps, the dominant GEMM's time from an untimed
+    instrumented pass and its roofline fraction (prefill 8192 against the
+    block-scaled MMA peak measured here, right after its timed region)."""
+    import torch
+    from block_quantized_expert_gb300 import peaks as pk
+    from workloads import CONFIGS, make_weights
+
+    recs = []
+    layer = None
+    layer_for = None
+    for ci, router, K in PER_CONFIG:
+        cfg = CONFIGS[ci]
+        t_start = time.time()
+        key = (cfg.shared, cfg.T if cfg.shared else 512)
+        if layer_for != key:
+            if layer is not None:
+                layer.close()
+                torch.cuda.empty_cache()
+            layer = make_layer(bqe, cfg, make_weights(cfg), dev, key[1], args.path)
+            layer_for = key
+        W = 3
+        wl = Workload(bqe, cfg, layer, dev, min(K + W, 4), cfg.default_seed, router=router)
+        avg_touched, rows = wl.touched(4)
+        for i in range(W):
+            wl.step(i)
+        bqe.moe_check(layer)
+        stream = torch.cuda.Stream(device=dev)
+        graphs = capture(wl.step, W, K, K, stream)
+        (ms, _, w0, w1), clocks = clocked(lambda: timed_replay(graphs, K, K, stream, dev, 1))
+        del graphs
+        mma_peak = None
+        if cfg.index == 4:
+            mma_peak = pk.mma_mx_tflops(iters=60000, reps=3)
+        stage_ms = stage_times(bqe, layer, wl.step, W + K, min(K, 16), stream)
+        bqe.moe_check(layer)
+        byts = algorithmic_bytes(cfg, avg_touched, rows)
+        dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
+        roof = roofline(cfg, dom, stage_ms[dom], byts, rows, peaks, mma_peak)
+        roof["kernel"] = f"{dom} GEMM (k_gemm_tc)"
+        recs.append({"workload": cfg.name if router is None else f"{cfg.name.rsplit('_', 1)[0]}_{router}",
+                     "tokens_per_step": cfg.T, "router": router or cfg.router, "shared_expert": cfg.shared,
+                     "value": job_rate(1, K * cfg.T, ms), "unit": UNIT, "steps": K, "warmup": W,
+                     "ms_per_step": round(ms / K, 6), "experts_touched_per_step": avg_touched,
+                     "stage_ms_untimed_pass": {k: round(v, 5) for k, v in stage_ms.items()},
+                     "roofline": roof, "clocks": clocks,
+                     "l2": "weights of the touched experts larger than L2; 4 input batches cycled",
+                     "wall_s": round(time.time() - t_start, 1)})
+        del wl
+    if layer is not None:
+        layer.close()
+    torch.cuda.empty_cache()
+    return recs
+
+
+# DRAM bytes per launch of the decode kernel from a committed ncu capture,
 # valid only for the kernel sources it was taken on
-PROFILE_COUNTERS = os.path.join(ROOT, "profiles", "decode_t1_k_decode_counters.md")
+PROFILE_COUNTERS = os.path.join(ROOT, "profiles", "decode_t1_k_decode_counters.json")
 KERNEL_SOURCES = ["gemm_tc.cu", "common.cuh", "tc_ptx.cuh", "route.cuh", "layer.h"]
 
 
@@ -402,13 +542,12 @@ def profiled_traffic(cfg, dom):
     if dom != "layer" or cfg.index != 1:
         return None
     try:
-        lines = open(PROFILE_COUNTERS).read().splitlines()
-    except OSError:
+        rec = json.load(open(PROFILE_COUNTERS))
+    except (OSError, ValueError):
         return None
-    kv = dict(l.split(":", 1) for l in lines if l.startswith(("kernel_sources_sha256:", "traffic_bytes_per_launch:")))
-    if kv.get("kernel_sources_sha256", "").strip() != kernel_sources_sha256():
+    if rec.get("kernel_sources_sha256") != kernel_sources_sha256():
         return None  # the kernel changed since the counters were taken
-    return int(kv["traffic_bytes_per_launch"].strip())
+    return int(rec["dram_bytes_per_launch"])
 
 
 def trace_report(bqe, layer, step, i, dev):

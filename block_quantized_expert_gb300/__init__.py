@@ -24,7 +24,7 @@ EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_perm
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
            "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace", "moe_route_forward",
-           "moe_set_route_prune")
+           "moe_set_route_prune", "moe_set_wait_limit", "moe_test_stall_next_decode")
 
 
 class MoeError(RuntimeError):
@@ -80,6 +80,8 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_set_trace": ([vp, vp, C.c_size_t], i),
         "moe_route_forward": ([vp, vp, vp, i, vp, vp, vp, vp], i),
         "moe_set_route_prune": ([vp, i, f, f], i),
+        "moe_set_wait_limit": ([vp, C.c_double], i),
+        "moe_test_stall_next_decode": ([vp], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -198,6 +200,17 @@ def moe_set_route_prune(layer: Layer, keep: int, min_w: float = 0.0, rho: float 
     the first weight below `min_w`, rescale the kept weights for correlation
     `rho` (0: L2 quadrature, 1: linear).  keep >= k with min_w <= 0: off."""
     _check(load_library().moe_set_route_prune(layer.ptr, int(keep), float(min_w), float(rho)), layer.ptr)
+
+
+def moe_set_wait_limit(layer: Layer, seconds: float):
+    """Wall-time limit of the layer's device-side waits (default 2 s)."""
+    _check(load_library().moe_set_wait_limit(layer.ptr, float(seconds)), layer.ptr)
+
+
+def moe_test_stall_next_decode(layer: Layer):
+    """Test hook: the next one-token decode-kernel call cannot complete its
+    hand-off, runs out its bounded waits and reports MOE_ERR_TIMEOUT."""
+    _check(load_library().moe_test_stall_next_decode(layer.ptr), layer.ptr)
 
 
 def moe_set_stage_events(layer: Layer, events):

@@ -10,6 +10,8 @@ PKG = Path(__file__).resolve().parent
 CSRC = PKG / "csrc"
 OUT_DIR = PKG / "_build"
 LIB = OUT_DIR / "libmoe.so"
+PEAKS_SRC = PKG / "peaks" / "peaks.cu"
+PEAKS_LIB = OUT_DIR / "libmoe_peaks.so"
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -59,7 +61,23 @@ def build(force: bool = False, verbose: bool = False) -> Path:
     return LIB
 
 
+def build_peaks(force: bool = False) -> Path:
+    """Compile the roofline-denominator microbenchmarks into libmoe_peaks.so."""
+    deps = [PEAKS_SRC, CSRC / "tc_ptx.cuh", Path(__file__)]
+    if not force and PEAKS_LIB.exists() and all(p.stat().st_mtime <= PEAKS_LIB.stat().st_mtime for p in deps):
+        return PEAKS_LIB
+    OUT_DIR.mkdir(parents=True, exist_ok=True)
+    tmp = PEAKS_LIB.with_suffix(f".{os.getpid()}.tmp")
+    r = subprocess.run([NVCC, *ARCH, *FLAGS, "-shared", "-o", str(tmp), str(PEAKS_SRC)],
+                       capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed for {PEAKS_SRC.name}:\n{r.stderr}")
+    os.replace(tmp, PEAKS_LIB)
+    return PEAKS_LIB
+
+
 if __name__ == "__main__":
     import sys
     build(force="--force" in sys.argv, verbose="-v" in sys.argv)
+    build_peaks(force="--force" in sys.argv)
     print(LIB)

@@ -306,6 +306,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         return st;
     }
     L->gemm_path = 0;
+    L->wait_ns = 2000000000ull;
+    L->stall_next_decode = 0;
     L->prune_keep = L->cfg.top_k;
     L->prune_min_w = 0.f;
     L->prune_rho = 0.f;
@@ -358,6 +360,20 @@ moe_status moe_set_route_prune(moe_layer* L, int keep, float min_w, float rho) {
     L->prune_keep = keep < L->cfg.top_k ? keep : L->cfg.top_k;
     L->prune_min_w = min_w;
     L->prune_rho = rho;
+    return MOE_OK;
+}
+
+moe_status moe_set_wait_limit(moe_layer* L, double seconds) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!(seconds >= 1e-4 && seconds <= 60.0)) return fail(L, MOE_ERR_INVALID_ARG, "seconds must be in [1e-4, 60]");
+    L->wait_ns = (uint64_t)(seconds * 1e9);
+    return MOE_OK;
+}
+
+moe_status moe_test_stall_next_decode(moe_layer* L) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (!moe::decode_supported(L)) return fail(L, MOE_ERR_UNSUPPORTED, "the layer has no whole-layer decode kernel");
+    L->stall_next_decode = 1;
     return MOE_OK;
 }
 
@@ -493,7 +509,7 @@ moe_status moe_check(moe_layer* L, moe_stream_t stream) {
     if (e == cudaSuccess && flags) e = cudaMemset(L->d_err, 0, 4);
     if (e != cudaSuccess) return cuda_fail(L, e, "moe_check");
     if (flags & moe::ERR_TIMEOUT)
-        return fail(L, MOE_ERR_TIMEOUT, "a device-side wait ran out of iterations");
+        return fail(L, MOE_ERR_TIMEOUT, "a device-side wait ran out of time (moe_set_wait_limit)");
     if (flags & moe::ERR_BAD_ID)
         return fail(L, MOE_ERR_INVALID_ARG, "an expert or token id was out of range");
     return MOE_OK;

@@ -47,7 +47,6 @@ using namespace tc;
 // TMA into 16-byte slots count the packed bytes (256 x 64), e4m3 256 x 128.
 constexpr uint32_t kFp4BoxTx = 16384;
 constexpr uint32_t kFp8BoxTx = 32768;
-constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 struct TcArgs {
     int n_seg;
@@ -65,6 +64,7 @@ struct TcArgs {
     float* y;                  // down: y[row][N_out]
     const int32_t* pos_row;    // down: padded position -> y row (null: identity)
     uint32_t* err;
+    uint64_t wait_ns;          // wall-time limit of every wait
     uint32_t a_tx;             // TMA bytes of one 256-row weight copy
     int32_t* sk_cnt;           // [gridDim] arrival counters of cut tiles, by first CTA (start at 0)
     float* sk_part;            // [gridDim][2][2][128][128] partial accumulators
@@ -290,12 +290,13 @@ __device__ __forceinline__ void tile_done_combine(const TcArgs& a, int f0, bool 
     if (leader) a.cmb_cnt[f0 / 256] = 0;  // counters are left at zero
 }
 
-// mbar_wait that adds the waited wall time to *acc when tracing.
+// mbar_wait (for at most limit_ns) that adds the waited wall time to *acc
+// when tracing.
 __device__ __forceinline__ bool timed_wait(uint32_t bar, uint32_t parity, volatile int* abort,
-                                           bool tr, unsigned long long& acc) {
-    if (!tr) return mbar_wait(bar, parity, kWaitLimitNs, abort);
+                                           bool tr, unsigned long long& acc, uint64_t limit_ns) {
+    if (!tr) return mbar_wait(bar, parity, limit_ns, abort);
     const uint64_t t0 = globaltimer();
-    const bool ok = mbar_wait(bar, parity, kWaitLimitNs, abort);
+    const bool ok = mbar_wait(bar, parity, limit_ns, abort);
     acc += globaltimer() - t0;
     return ok;
 }
@@ -304,9 +305,9 @@ __device__ __forceinline__ bool timed_wait(uint32_t bar, uint32_t parity, volati
 // CTA-wide barriers converged): lane 0 waits and issues, the warp learns the
 // outcome of each wait from it.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int* abort, bool tr,
-                                          unsigned long long& acc, int lane) {
+                                          unsigned long long& acc, int lane, uint64_t limit_ns) {
     int ok = 1;
-    if (lane == 0) ok = timed_wait(bar, parity, abort, tr, acc) ? 1 : 0;
+    if (lane == 0) ok = timed_wait(bar, parity, abort, tr, acc, limit_ns) ? 1 : 0;
     return __shfl_sync(0xFFFFFFFFu, ok, 0) != 0;
 }
 
@@ -383,7 +384,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             const size_t atom_a = (size_t)(T.arow / 256) * KB;
             const size_t atom_b = (size_t)(T.p0 / 128) * KB;
             for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag, tr, w_empty, lane)) {
+                if (!warp_wait(empty_bar(stage), phase ^ 1u, abort_flag, tr, w_empty, lane, a.wait_ns)) {
                     if (lane == 0) give_up();
                     ok = false;
                     break;
@@ -408,12 +409,12 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
         unsigned long long w_full = 0, w_acc = 0, n_stages = 0;
         while (ok && it.next(sg)) {
             const Tile T = decode_tile<kGateUp>(a, sg.tile);
-            if (!warp_wait(tmem_empty, acc_phase ^ 1u, abort_flag, tr, w_acc, lane)) {
+            if (!warp_wait(tmem_empty, acc_phase ^ 1u, abort_flag, tr, w_acc, lane, a.wait_ns)) {
                 if (lane == 0) give_up();
                 break;
             }
             for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-                if (!warp_wait(full_bar(stage), phase, abort_flag, tr, w_full, lane)) {
+                if (!warp_wait(full_bar(stage), phase, abort_flag, tr, w_full, lane, a.wait_ns)) {
                     if (lane == 0) give_up();
                     ok = false;
                     break;
@@ -467,7 +468,7 @@ k_gemm_tc(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUten
             // on a timeout the epilogue goes on with whatever the accumulator
             // holds (the error is raised), so all eight warps keep meeting at
             // the same named barriers
-            if (!timed_wait(tmem_full, acc_phase, abort_flag, tr, w_tf) && lane == 0) give_up();
+            if (!timed_wait(tmem_full, acc_phase, abort_flag, tr, w_tf, a.wait_ns) && lane == 0) give_up();
             const uint64_t tw0 = tr ? globaltimer() : 0;
             tc_fence_after();
             acc_phase ^= 1u;
@@ -632,6 +633,10 @@ struct DecArgs {
     uint16_t* x_stage;     // x in host memory: CTA 0's device copy of it for the others, else null
     uint32_t* x_flag;      // x_stage written
     uint32_t* err;
+    uint64_t wait_ns;      // wall-time limit of every wait
+    // test hook: the h-flag waits expect a value no CTA writes (every CTA's
+    // wait runs out after wait_ns; the call reports MOE_ERR_TIMEOUT)
+    int stall_h;
     unsigned long long* trace;  // [gridDim][12] ns timestamps, or null
 };
 
@@ -704,7 +709,7 @@ __device__ __forceinline__ void work_bar() { asm volatile("bar.sync 2, 288;" :::
 // its writers followed by one gpu-scope release store (cumulative over the
 // writes the barrier ordered before it); a waiter's acquire load followed by
 // a named barrier makes them visible to its whole CTA.  The wait gives up
-// after kWaitLimitNs or when the CTA aborts.
+// after limit_ns or when the CTA aborts.
 __device__ __forceinline__ void flag_set(uint32_t* f, uint32_t v) {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(f), "r"(v) : "memory");
 }
@@ -713,11 +718,11 @@ __device__ __forceinline__ uint32_t flag_get(const uint32_t* f) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
     return v;
 }
-__device__ bool flag_wait(const uint32_t* f, uint32_t v, volatile int* abort) {
+__device__ bool flag_wait(const uint32_t* f, uint32_t v, volatile int* abort, uint64_t limit_ns) {
     if (flag_get(f) == v) return true;
     const uint64_t t0 = globaltimer();
     while (flag_get(f) != v) {
-        if (globaltimer() - t0 > kWaitLimitNs || *abort) return false;
+        if (globaltimer() - t0 > limit_ns || *abort) return false;
         __nanosleep(32);
     }
     return true;
@@ -736,13 +741,13 @@ __device__ __forceinline__ unsigned long long word_get(const unsigned long long*
     asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
     return v;
 }
-// Wait (bounded, like flag_wait) until the n <= N words p[i * stride]
+// Wait (bounded by limit_ns, like flag_wait) until the n <= N words p[i * stride]
 // carry epoch e, v[i] holding each word's first read.  Every round re-reads
 // all words still of an earlier launch together: one round trip per round,
 // not one per word.
 template <int N>
 __device__ bool words_wait(const unsigned long long* p, size_t stride, int n, uint32_t e, volatile int* abort,
-                           unsigned long long (&v)[N]) {
+                           uint64_t limit_ns, unsigned long long (&v)[N]) {
     const uint64_t t0 = globaltimer();
     while (true) {
         uint32_t pending = 0;
@@ -750,7 +755,7 @@ __device__ bool words_wait(const unsigned long long* p, size_t stride, int n, ui
         for (int i = 0; i < N; ++i)
             if (i < n && (uint32_t)(v[i] >> 32) != e) pending |= 1u << i;
         if (!pending) return true;
-        if (globaltimer() - t0 > kWaitLimitNs || *abort) return false;
+        if (globaltimer() - t0 > limit_ns || *abort) return false;
         __nanosleep(32);
 #pragma unroll
         for (int i = 0; i < N; ++i)
@@ -785,7 +790,7 @@ __device__ bool dec_produce(const DecArgs& a, const DecCtx& c, const CUtensorMap
             }
             ++issued;
             unsigned long long none = 0;
-            if (!warp_wait(c.empty_bar(stage), phase ^ 1u, c.abort_flag, false, none, lane)) {
+            if (!warp_wait(c.empty_bar(stage), phase ^ 1u, c.abort_flag, false, none, lane, a.wait_ns)) {
                 if (lane == 0) c.give_up(a);
                 return false;
             }
@@ -815,7 +820,9 @@ __device__ bool dec_fetch_h(const DecArgs& a, const DecCtx& c, const DecPhase& p
     const int mt_gu = a.I / 128;  // lanes 0-15 slot 0, 16-31 slot 1
     const int sx = slots[lane >> 4];
     bool ok = true;
-    if (sx >= 0 && (lane & 15) < mt_gu) ok = flag_wait(a.h_flag + sx * mt_gu + (lane & 15), c.epoch, c.abort_flag);
+    // (stall_h: a value no launch writes -- the test of the bounded waits)
+    const uint32_t want = a.stall_h ? (c.epoch ^ 0x80000000u) : c.epoch;
+    if (sx >= 0 && (lane & 15) < mt_gu) ok = flag_wait(a.h_flag + sx * mt_gu + (lane & 15), want, c.abort_flag, a.wait_ns);
     if (!__all_sync(0xFFFFFFFFu, ok)) {
         if (lane == 0) c.give_up(a);
         return false;
@@ -859,7 +866,7 @@ __device__ bool dec_mma(const DecArgs& a, const DecCtx& c, const DecPhase& ph, i
         }
     } else {
         dec_slots(a, ph, slots);
-        if (!warp_wait(c.h_bar(g), 0, c.abort_flag, false, none, lane)) {  // the group's h rows
+        if (!warp_wait(c.h_bar(g), 0, c.abort_flag, false, none, lane, a.wait_ns)) {  // the group's h rows
             if (lane == 0) c.give_up(a);
             return false;
         }
@@ -873,12 +880,12 @@ __device__ bool dec_mma(const DecArgs& a, const DecCtx& c, const DecPhase& ph, i
         const uint32_t a_base = kGateUp ? smem_u32(c.smem + kDecXOff)
                                         : smem_u32(c.smem + kDecHOff + (2 * g + sl) * kDecSlotBytes);
         const uint32_t sa_base = tok_base + kDecXScaleBytes + (2 * g + sl) * kDecHScaleBytes;
-        if (!warp_wait(c.tmem_empty(), acc_phase ^ 1u, c.abort_flag, false, none, lane)) {
+        if (!warp_wait(c.tmem_empty(), acc_phase ^ 1u, c.abort_flag, false, none, lane, a.wait_ns)) {
             if (lane == 0) c.give_up(a);
             return false;
         }
         for (int kb = sg.kb0; kb < sg.kb1; ++kb) {
-            if (!warp_wait(c.full_bar(stage), phase, c.abort_flag, false, none, lane)) {
+            if (!warp_wait(c.full_bar(stage), phase, c.abort_flag, false, none, lane, a.wait_ns)) {
                 if (lane == 0) c.give_up(a);
                 return false;
             }
@@ -949,7 +956,7 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
             if (lead_warp) {
                 bool ok = true;
                 const int cc = sg.first_cta + 1 + lane;
-                if (cc <= sg.last_cta) ok = flag_wait(pflag + cc * 2 + it.slot(cc, sg.tile), c.epoch, c.abort_flag);
+                if (cc <= sg.last_cta) ok = flag_wait(pflag + cc * 2 + it.slot(cc, sg.tile), c.epoch, c.abort_flag, a.wait_ns);
                 if (!__all_sync(0xFFFFFFFFu, ok) && lane == 0) c.give_up(a);
             }
             epi_bar();  // the acquire loads above make the pieces visible to the CTA
@@ -959,7 +966,7 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
         // on a timeout the epilogue goes on with whatever the accumulator
         // holds (the error is raised), so all eight warps keep meeting at
         // the same named barriers
-        if (!mbar_wait(c.tmem_full(), acc_phase, kWaitLimitNs, c.abort_flag) && lane == 0) c.give_up(a);
+        if (!mbar_wait(c.tmem_full(), acc_phase, a.wait_ns, c.abort_flag) && lane == 0) c.give_up(a);
         tc_fence_after();
         acc_phase ^= 1u;
         uint32_t r[32];
@@ -1009,7 +1016,7 @@ __device__ void dec_epilogue(const DecArgs& a, const DecCtx& c, const DecPhase& 
             const unsigned long long* yp = a.yw + (size_t)m * 256 + col;  // expert ss: + ss * MT * 256
 #pragma unroll
             for (int ss = 0; ss < kMaxTopK - 1; ++ss) yv[ss] = ss < c.k - 1 ? word_get(yp + (size_t)ss * MT * 256) : 0ull;
-            const bool ok = words_wait(yp, (size_t)MT * 256, c.k - 1, c.epoch, c.abort_flag, yv);
+            const bool ok = words_wait(yp, (size_t)MT * 256, c.k - 1, c.epoch, c.abort_flag, a.wait_ns, yv);
             float o = 0.f;
 #pragma unroll
             for (int ss = 0; ss < kMaxTopK - 1; ++ss)
@@ -1213,7 +1220,7 @@ k_decode(const __grid_constant__ CUtensorMap tmGU, const __grid_constant__ CUten
                 work_bar();
                 if (threadIdx.x == 32) flag_set(a.x_flag, words[2]);
             } else {
-                if (threadIdx.x == 32 && !flag_wait(a.x_flag, words[2], c.abort_flag)) c.give_up(a);
+                if (threadIdx.x == 32 && !flag_wait(a.x_flag, words[2], c.abort_flag, a.wait_ns)) c.give_up(a);
                 work_bar();  // the acquire above, then the whole of warps 1-9
 #pragma unroll
                 for (int r = 0; r < 2; ++r) {
@@ -1436,6 +1443,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid,
     g.hq = L->hq;
     g.hs = L->hs;
     g.err = L->d_err;
+    g.wait_ns = L->wait_ns;
     g.a_tx = kFp4BoxTx;
     g.sk_part = L->sk_partials;
     g.sk_cnt = L->sk_counters;
@@ -1539,6 +1547,9 @@ cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, 
     a.x_flag = a.h_flag + kDecMaxTiles;
     a.x_stage = x_in_host ? L->x_stage : nullptr;
     a.err = L->d_err;
+    a.wait_ns = L->wait_ns;
+    a.stall_h = L->stall_next_decode;
+    L->stall_next_decode = 0;  // one-shot
     a.trace = L->trace;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(L->num_sms);

@@ -17,6 +17,8 @@ struct moe_layer {
     // tail pruning of the learned routing (keep = top_k, min_w = 0: none)
     int prune_keep;
     float prune_min_w, prune_rho;
+    uint64_t wait_ns;        // wall-time limit of every device-side wait
+    int stall_next_decode;   // test hook: the next decode launch's h waits cannot complete
 
     // -------- weights (library-owned copies) --------
     // gate/up codes interleaved per 128 features: [E][I/128][gate 128 rows, up 128 rows][H/2],

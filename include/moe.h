@@ -241,6 +241,27 @@ moe_status moe_set_gemm_path(moe_layer* layer, int path);
  *   default).  MOE_ERR_INVALID_ARG otherwise, the setting unchanged.       */
 moe_status moe_set_route_prune(moe_layer* layer, int keep, float min_w, float rho);
 
+/* Wall-time limit of every device-side wait of this layer's kernels (a
+ * pipeline barrier, or a flag or tagged word another CTA writes): a wait that
+ * runs out gives up instead of spinning on.  The kernel then skips its
+ * remaining work, lets its copies in flight land, frees its tensor memory and
+ * exits; the device flag it raises makes the next moe_check() return
+ * MOE_ERR_TIMEOUT (outputs of that call are undefined), and the layer stays
+ * usable.  Not part of the method: a guard against a CTA that never arrives
+ * (colibri "DeepSeek V4 target engine", "Validation": every GPU stage is
+ * checked against the CPU, and a failure must surface, not hang).
+ *   seconds in [1e-4, 60]; default 2.  MOE_ERR_INVALID_ARG otherwise.      */
+moe_status moe_set_wait_limit(moe_layer* layer, double seconds);
+
+/* Test hook of the bounded-wait path above.  The next one-token call that
+ * runs the whole-layer decode kernel (moe_route_forward or moe_forward_host
+ * with T = 1 on the automatic path) waits for its gate/up results under a
+ * value no CTA ever writes, so every CTA's wait runs out after the wait
+ * limit and the call ends with MOE_ERR_TIMEOUT at the next moe_check().
+ * One-shot: the call after it runs normally.  MOE_ERR_UNSUPPORTED if the
+ * layer has no decode kernel (shape, shared expert, or not an sm_103 GPU).  */
+moe_status moe_test_stall_next_decode(moe_layer* layer);
+
 /* Token -> expert grouping without a layer and without any allocation.
  * The method's description has no counterpart: this entry point exists for callers that
  * cannot call cudaMalloc -- code running inside another framework's memory

@@ -42,3 +42,17 @@ def test_workspace_and_config_validation_on_host():
     # NULL layer is rejected before any CUDA call
     assert lib.moe_route(None, None, 1, None, None, None) == bqe.MOE_ERR_INVALID_ARG
     assert lib.moe_destroy(None) == bqe.MOE_OK
+
+
+def test_peaks_library_exports_its_header():
+    """libmoe_peaks.so (the roofline denominators) builds and exports what
+    include/moe_peaks.h declares."""
+    from block_quantized_expert_gb300 import peaks
+
+    text = open(os.path.join(os.path.dirname(HEADER), "moe_peaks.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = sorted(set(re.findall(r"\b(peak_[a-z_]+)\s*\(", text)))
+    assert names == ["peak_mma_mx", "peak_read_stream"]
+    lib = peaks.load()
+    for n in names:
+        assert hasattr(lib, n), n

@@ -45,7 +45,11 @@ def test_combine_matches_oracle(layer, T):
         bqe.moe_check(L)  # the NaN tokens raise the routing flag
     gi = ids.cpu().numpy()
     assert (gi[dead] == -1).all()
-    ref = orc.layer_forward(w, tk.x_bits, gi, wd.cpu().numpy().astype(np.float64))
+    # the oracle's own routing; a token with only NaN logits routes nowhere
+    rid, rw = orc.route_learned(np.where(np.isnan(lg), 0.0, lg).astype(np.float32), cfg.k, cfg.w_scale)
+    rid[dead], rw[dead] = -1, 0.0
+    assert np.array_equal(gi, rid)
+    ref = orc.layer_forward(w, tk.x_bits, rid, rw)
     got = out.cpu().numpy()
     norm, elem = G.compare_out(got, ref)
     assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (norm, elem)
@@ -71,7 +75,9 @@ def test_repeated_calls_of_changing_size(layer):
         ids, wd = G.route_dev(L, tk.logits, cfg.k)
         out = G.forward_dev(L, tk.x_bits, ids, wd).cpu().numpy()
         bqe.moe_check(L)
-        ref = orc.layer_forward(w, tk.x_bits, ids.cpu().numpy(), wd.cpu().numpy().astype(np.float64))
+        rid, rw = orc.route_learned(tk.logits, cfg.k, cfg.w_scale)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        ref = orc.layer_forward(w, tk.x_bits, rid, rw)
         norm, elem = G.compare_out(out, ref)
         assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL
     bqe.moe_set_gemm_path(L, 0)

@@ -48,7 +48,7 @@ def _check_token(cfg, wts, layer, tk, t):
     rid, rw = orc.route_learned(lg, cfg.k, cfg.w_scale)
     assert np.array_equal(ids.cpu().numpy(), rid)
     assert np.abs(w.cpu().numpy() - rw).max() <= 8 * 2.0 ** -24 * cfg.w_scale
-    ref = orc.layer_forward(wts, xb, rid, w.cpu().numpy().astype(np.float64))
+    ref = orc.layer_forward(wts, xb, rid, rw)  # the oracle end to end, on its own routing
     norm, elem = G.compare_out(out.cpu().numpy(), ref)
     assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (norm, elem)
     # the grouped tcgen05 kernels: the same routing bit for bit; the output

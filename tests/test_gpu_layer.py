@@ -76,7 +76,11 @@ def _quant_check(layer, x_bits):
     assert np.array_equal(q.cpu().numpy(), rq)
 
 
-def _forward_check(layer, weights, x_bits, ids_dev, w_dev, sample, path):
+def _forward_check(layer, weights, x_bits, ids_dev, w_dev, sample, path, rid=None, rw=None, name=""):
+    """The layer output of `sample` tokens (and their requantised h codes)
+    against the oracle.  The oracle runs end to end on its own routing
+    (rid, rw from orc.route_*) where the test routed through the router;
+    tests that give the layer hand-made routing pass it to both."""
     bqe.moe_set_gemm_path(layer, path)
     out = G.forward_dev(layer, x_bits, ids_dev, w_dev).cpu().numpy()
     T, k = ids_dev.shape
@@ -85,25 +89,51 @@ def _forward_check(layer, weights, x_bits, ids_dev, w_dev, sample, path):
     hs = torch.empty((T * k, I // 32), dtype=torch.uint8, device=G.DEV)
     bqe.moe_hidden(layer, T, hq, hs)
     bqe.moe_check(layer)
-    ids = ids_dev.cpu().numpy()
-    wt = w_dev.cpu().numpy().astype(np.float64)
-    ref, rq, rsc = orc.layer_forward(weights, x_bits, ids, wt, tokens=sample, want_h=True)
+    if rid is None:
+        rid, rw = ids_dev.cpu().numpy(), w_dev.cpu().numpy().astype(np.float64)
+    assert np.array_equal(ids_dev.cpu().numpy(), rid)
+    ref, rq, rsc = orc.layer_forward(weights, x_bits, rid, rw, tokens=sample, want_h=True)
     norm, elem = G.compare_out(out[sample], ref)
     assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (norm, elem)
     hq = hq.cpu().numpy().reshape(T, k, I)[sample]
-    flips = float(np.mean(hq != rq))
+    live = rid[sample] >= 0  # h rows of routed slots
+    n_codes = int(live.sum()) * I
+    n_flips = int((hq != rq)[live].sum())
+    flips = n_flips / max(1, n_codes)
+    G.report("hq_flips", {"case": name, "path": path, "tokens": int(len(sample)), "codes": n_codes,
+                          "flips": n_flips, "fraction": flips, "norm_err": norm, "elem_err": elem})
     assert flips <= G.HQ_FLIP_TOL, flips
     return out, norm, elem, flips
+
+
+def tile_covering_sample(rid, E, extra=0, seed=0):
+    """Tokens such that every 128-row tile of every non-empty expert segment
+    (the row tiles the grouped GEMMs take, including each ragged last tile)
+    holds at least two compared rows: a random row of the tile and its last
+    row.  Segments are the oracle's stable counting sort of the rows t*k+j."""
+    off, src, _ = orc.permute(rid, E)
+    k = rid.shape[1]
+    rng = np.random.default_rng(seed)
+    toks = set()
+    for e in range(E):
+        n = int(off[e + 1] - off[e])
+        for u in range(0, n, 128):
+            m = min(128, n - u)
+            for r in (int(rng.integers(0, m)), m - 1):
+                toks.add(int(src[off[e] + u + r]) // k)
+    if extra:
+        toks.update(int(t) for t in rng.choice(rid.shape[0], extra, replace=False))
+    return np.array(sorted(toks), dtype=np.int32)
 
 
 @pytest.mark.parametrize("path", PATHS)
 def test_tiny_config_all_steps(tiny, path):
     cfg, w, layer = tiny
     tk = G.tokens(0)
-    ids, wd, _, _ = _route_check(layer, tk.logits, cfg.k)
+    ids, wd, rid, rw = _route_check(layer, tk.logits, cfg.k)
     _perm_check(layer, ids, cfg.E)
     _quant_check(layer, tk.x_bits)
-    _forward_check(layer, w, tk.x_bits, ids, wd, np.arange(cfg.T), path)
+    _forward_check(layer, w, tk.x_bits, ids, wd, np.arange(cfg.T), path, rid, rw, "tiny")
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -118,7 +148,7 @@ def test_tiny_ragged_segments_and_one_hot_expert(tiny, path):
     wt = np.tile(np.array([[0.9, 0.6]], np.float32), (T, 1))
     ids_d, w_d = G.to_dev(ids), G.to_dev(wt)
     _perm_check(layer, ids_d, cfg.E)
-    _forward_check(layer, w, tk.x_bits, ids_d, w_d, np.arange(T), path)
+    _forward_check(layer, w, tk.x_bits, ids_d, w_d, np.arange(T), path, ids, wt.astype(np.float64), "ragged")
 
 
 def test_route_ties_and_hash(tiny):
@@ -135,8 +165,8 @@ def test_decode_t1_calls(full, path):
     cfg = CONFIGS[1]
     tk = G.tokens(1, n=12)
     for t in range(12):
-        ids, wd, _, _ = _route_check(layer, tk.logits[t:t + 1], cfg.k)
-        _forward_check(layer, w, tk.x_bits[t:t + 1], ids, wd, np.array([0]), path)
+        ids, wd, rid, rw = _route_check(layer, tk.logits[t:t + 1], cfg.k)
+        _forward_check(layer, w, tk.x_bits[t:t + 1], ids, wd, np.array([0]), path, rid, rw, "decode_t1")
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -151,9 +181,9 @@ def test_batched_decode_hash_then_learned(full, path):
     rid, rw = orc.route_hash(tk.token_ids, tab, cfg.w_scale)
     assert np.array_equal(ids.cpu().numpy(), rid) and (wd.cpu().numpy() == 0.25).all()
     _perm_check(layer, ids, cfg.E)
-    _forward_check(layer, w, tk.x_bits, ids, wd, np.arange(cfg.T), path)
-    ids2, wd2, _, _ = _route_check(layer, tk.logits, cfg.k)
-    _forward_check(layer, w, tk.x_bits, ids2, wd2, np.arange(cfg.T), path)
+    _forward_check(layer, w, tk.x_bits, ids, wd, np.arange(cfg.T), path, rid, rw, "batched_hash")
+    ids2, wd2, rid2, rw2 = _route_check(layer, tk.logits, cfg.k)
+    _forward_check(layer, w, tk.x_bits, ids2, wd2, np.arange(cfg.T), path, rid2, rw2, "batched_learned")
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -161,11 +191,11 @@ def test_prefill_pp512(full, path):
     w, layer = full
     cfg = CONFIGS[3]
     tk = G.tokens(3)
-    ids, wd, _, _ = _route_check(layer, tk.logits, cfg.k)
+    ids, wd, rid, rw = _route_check(layer, tk.logits, cfg.k)
     _perm_check(layer, ids, cfg.E)
     _quant_check(layer, tk.x_bits)
-    sample = np.random.default_rng(0).choice(cfg.T, 48, replace=False).astype(np.int32)
-    _forward_check(layer, w, tk.x_bits, ids, wd, sample, path)
+    # every token: all 128-row tiles of all segments are compared
+    _forward_check(layer, w, tk.x_bits, ids, wd, np.arange(cfg.T, dtype=np.int32), path, rid, rw, "pp512")
 
 
 @pytest.mark.parametrize("path", PATHS)
@@ -173,10 +203,15 @@ def test_prefill_8192_zipf_shared(full_shared, path):
     w, layer = full_shared
     cfg = CONFIGS[4]
     tk = G.tokens(4)
-    ids, wd, _, _ = _route_check(layer, tk.logits, cfg.k)
+    ids, wd, rid, rw = _route_check(layer, tk.logits, cfg.k)
     _perm_check(layer, ids, cfg.E)
-    sample = np.random.default_rng(1).choice(cfg.T, 32, replace=False).astype(np.int32)
-    _forward_check(layer, w, tk.x_bits, ids, wd, sample, path)
+    # two rows of every 128-row tile of every segment (the Zipf head
+    # expert's ~60 tiles, the ragged tails, the one-row segments) plus 64
+    # random tokens; their shared-expert rows span every token tile too
+    sample = tile_covering_sample(rid, cfg.E, extra=64, seed=1)
+    # and one token of every 128-token tile of the shared expert's rows
+    sample = np.union1d(sample, np.arange(0, cfg.T, 128) + 77).astype(np.int32)
+    _forward_check(layer, w, tk.x_bits, ids, wd, sample, path, rid, rw, "prefill8192")
 
 
 def test_forward_is_deterministic_and_host_entry_matches(tiny):
