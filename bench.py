@@ -459,7 +459,8 @@ def run_ours(args, cfg, rank, world, local_rank):
 
 def wl_tokens_for_cpu(cfg, rank):
     from workloads import make_tokens
-    return make_tokens(cfg, seed=rank_seed(cfg, rank), n=max(cfg.T, min(4096, 64 * cfg.T)))
+    # enough tokens for the oracle's time budget (~60 tokens/s per 16 cores)
+    return make_tokens(cfg, seed=rank_seed(cfg, rank), n=max(cfg.T, 2048))
 
 
 PER_CONFIG = [  # (config, router, timed steps)
