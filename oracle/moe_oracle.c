@@ -30,7 +30,13 @@
  *    tile; activations entering a matmul are MXFP8: e4m3 elements in
  *    32-element blocks with a UE8M0 scale (colibri "Linux CUDA tier": the
  *    MXFP8 path), scale 2^(floor(log2 amax) - 8), round to nearest even,
- *    saturating at +-448, sign kept (so -0 encodes 0x80).
+ *    saturating at +-448, sign kept (so -0 encodes 0x80);
+ *  - the NVFP4-style variant of the routed experts (CISM VALIDATION "4-bit
+ *    quantization scheme study", row "E2M1 + E4M3 b16 (NVFP4 granularity)"):
+ *    e2m1 elements in 16-element blocks with an e4m3 block scale, and (the
+ *    reading taken here, since an e4m3 scale alone cannot reach the small
+ *    magnitudes of the weights) one fp32 scale per expert matrix:
+ *    value = e2m1(code) * e4m3(block scale) * matrix scale.
  *
  * Readings where the pages are silent are listed in the design notes; the
  * ones that shape this code: the top-k is plain (one expert group), ties in
@@ -286,6 +292,10 @@ typedef struct {
     const uint8_t *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
     /* shared expert (or all NULL): e4m3 [rows][K], UE8M0 [rows/128][K/128] */
     const uint8_t *sh_gate_q, *sh_gate_s, *sh_up_q, *sh_up_s, *sh_down_q, *sh_down_s;
+    /* routed-expert weight format: 0 MXFP4 (above); 1 NVFP4-style: the same
+     * payload, scales e4m3 [E][rows][K/16], and fp32 matrix scales [E]     */
+    int wfmt;
+    const float *gate_g, *up_g, *down_g;
 } orc_layer;
 
 /* Decode tables, filled once from the value functions above.               */
@@ -306,6 +316,27 @@ static double mxfp4_at(const uint8_t* q, const uint8_t* s, int K, size_t row, in
     return tab_e2m1[code] * tab_ue8m0[s[row * (size_t)(K / 32) + (size_t)(col / 32)]];
 }
 
+/* NVFP4-style element: e2m1(code) * e4m3(block scale byte) * matrix scale. */
+double orc_nvfp4_value(int code, int sbyte, double g) {
+    return orc_e2m1_value(code) * orc_e4m3_value(sbyte) * g;
+}
+
+/* Value of element (row, col) of an NVFP4-style matrix with K columns and
+ * matrix scale g.                                                           */
+static double nvfp4_at(const uint8_t* q, const uint8_t* s, int K, size_t row, int col, double g) {
+    uint8_t byte = q[row * (size_t)(K / 2) + (size_t)(col / 2)];
+    int code = (col % 2 == 0) ? (byte & 15) : (byte >> 4);
+    return tab_e2m1[code] * tab_e4m3[s[row * (size_t)(K / 16) + (size_t)(col / 16)]] * g;
+}
+
+/* Element (row, col) of routed expert e's matrix (K columns; row counted
+ * from the expert's first row) in the layer's weight format.              */
+static double routed_at(const orc_layer* L, const uint8_t* q, const uint8_t* s, const float* g, int K,
+                        int e, int rows, int row, int col) {
+    size_t r = (size_t)e * rows + row;
+    return L->wfmt == 1 ? nvfp4_at(q, s, K, r, col, (double)g[e]) : mxfp4_at(q, s, K, r, col);
+}
+
 /* Value of element (row, col) of an fp8 matrix with 128x128 tile scales.   */
 static double fp8_tile_at(const uint8_t* q, const uint8_t* s, int K, size_t row, int col) {
     double v = tab_e4m3[q[row * (size_t)K + (size_t)col]];
@@ -322,9 +353,8 @@ static void expert_ffn(const orc_layer* L, int e, const double* xd, double* hbuf
         for (int c = 0; c < H; ++c) {
             double wg, wu;
             if (e >= 0) {
-                size_t row = (size_t)e * I + j;
-                wg = mxfp4_at(L->gate_q, L->gate_s, H, row, c);
-                wu = mxfp4_at(L->up_q, L->up_s, H, row, c);
+                wg = routed_at(L, L->gate_q, L->gate_s, L->gate_g, H, e, I, j, c);
+                wu = routed_at(L, L->up_q, L->up_s, L->up_g, H, e, I, j, c);
             } else {
                 wg = fp8_tile_at(L->sh_gate_q, L->sh_gate_s, H, (size_t)j, c);
                 wu = fp8_tile_at(L->sh_up_q, L->sh_up_s, H, (size_t)j, c);
@@ -339,7 +369,7 @@ static void expert_ffn(const orc_layer* L, int e, const double* xd, double* hbuf
     for (int c = 0; c < H; ++c) {
         double acc = 0.0;
         for (int j = 0; j < I; ++j) {
-            double wd = (e >= 0) ? mxfp4_at(L->down_q, L->down_s, I, (size_t)e * H + c, j)
+            double wd = (e >= 0) ? routed_at(L, L->down_q, L->down_s, L->down_g, I, e, H, c, j)
                                  : fp8_tile_at(L->sh_down_q, L->sh_down_s, I, (size_t)c, j);
             acc += hbuf[j] * wd;
         }
@@ -359,6 +389,7 @@ int orc_layer_forward(const orc_layer* L, const uint16_t* x, const int32_t* ids,
                       uint8_t* hq_out, uint8_t* hs_out) {
     int H = L->H, I = L->I, k = L->k, E = L->E;
     if (H % 128 || I % 128 || k < 1 || k > 64) return 1;
+    if (L->wfmt != 0 && (L->wfmt != 1 || !L->gate_g || !L->up_g || !L->down_g)) return 1;
     init_tables();
     for (int i = 0; i < n; ++i) {
         if (tok[i] < 0 || tok[i] >= T) return 1;

@@ -37,7 +37,8 @@ class OrcLayer(C.Structure):
     _fields_ = [("H", C.c_int), ("I", C.c_int), ("E", C.c_int), ("k", C.c_int)] + [
         (n, C.c_void_p) for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
                                    "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s",
-                                   "sh_down_q", "sh_down_s")]
+                                   "sh_down_q", "sh_down_s")] + [
+        ("wfmt", C.c_int), ("gate_g", C.c_void_p), ("up_g", C.c_void_p), ("down_g", C.c_void_p)]
 
 
 def build(force: bool = False) -> Path:
@@ -62,6 +63,8 @@ def lib():
             L.orc_e4m3_value.argtypes = [C.c_int]
             L.orc_ue8m0_value.restype = C.c_double
             L.orc_ue8m0_value.argtypes = [C.c_int]
+            L.orc_nvfp4_value.restype = C.c_double
+            L.orc_nvfp4_value.argtypes = [C.c_int, C.c_int, C.c_double]
             L.orc_e4m3_encode.restype = C.c_int
             L.orc_e4m3_encode.argtypes = [C.c_double]
             L.orc_sqrt_softplus.restype = C.c_double
@@ -91,6 +94,11 @@ def e4m3_value(code: int) -> float:
 
 def ue8m0_value(code: int) -> float:
     return lib().orc_ue8m0_value(int(code))
+
+
+def nvfp4_value(code: int, sbyte: int, g: float) -> float:
+    """NVFP4-style element: e2m1(code) * e4m3(sbyte) * g (fp64)."""
+    return lib().orc_nvfp4_value(int(code), int(sbyte), float(g))
 
 
 def e4m3_encode(y: float) -> int:
@@ -180,6 +188,15 @@ def _layer_struct(w, k: int):
             setattr(st, n, None)
         else:
             a = np.ascontiguousarray(a, dtype=np.uint8)
+            keep.append(a)
+            setattr(st, n, a.ctypes.data)
+    st.wfmt = 1 if getattr(cfg, "wfmt", "mxfp4") == "nvfp4" else 0
+    for n in ("gate_g", "up_g", "down_g"):
+        a = getattr(w, n, None)
+        if a is None:
+            setattr(st, n, None)
+        else:
+            a = np.ascontiguousarray(a, dtype=np.float32)
             keep.append(a)
             setattr(st, n, a.ctypes.data)
     return st, keep

@@ -39,6 +39,21 @@ def dq_mxfp4(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     return e2m1_table()[codes] * np.repeat(scale, 32, axis=-1)
 
 
+def dq_nvfp4(q: np.ndarray, s: np.ndarray, g: float) -> np.ndarray:
+    """[rows, K/2] codes + [rows, K/16] e4m3 scales + matrix scale -> fp64 [rows, K]."""
+    lo, hi = q & 15, q >> 4
+    codes = np.stack([lo, hi], axis=-1).reshape(*q.shape[:-1], q.shape[-1] * 2)
+    return e2m1_table()[codes] * np.repeat(e4m3_table()[s], 16, axis=-1) * float(g)
+
+
+def dq_routed(weights, name: str, e: int) -> np.ndarray:
+    """Expert e's gate / up / down matrix, dequantised in the layer's format."""
+    q, s = getattr(weights, name + "_q")[e], getattr(weights, name + "_s")[e]
+    if getattr(weights.cfg, "wfmt", "mxfp4") == "nvfp4":
+        return dq_nvfp4(q, s, getattr(weights, name + "_g")[e])
+    return dq_mxfp4(q, s)
+
+
 def dq_fp8_tiles(q: np.ndarray, s: np.ndarray) -> np.ndarray:
     vals = e4m3_table()[q]
     scale = np.ldexp(1.0, s.astype(np.int64) - 127)
@@ -81,9 +96,8 @@ def dense_layer(weights, x_bits: np.ndarray, ids: np.ndarray, w: np.ndarray):
     T = x.shape[0]
     out = np.zeros((T, cfg.H))
     for e in range(cfg.E):
-        y, _, _ = swiglu_expert(xd, dq_mxfp4(weights.gate_q[e], weights.gate_s[e]),
-                                dq_mxfp4(weights.up_q[e], weights.up_s[e]),
-                                dq_mxfp4(weights.down_q[e], weights.down_s[e]))
+        y, _, _ = swiglu_expert(xd, dq_routed(weights, "gate", e), dq_routed(weights, "up", e),
+                                dq_routed(weights, "down", e))
         wt = np.where(ids == e, w, 0.0).sum(axis=1)       # routing weight of e per token
         out += wt[:, None] * y
     if weights.sh_gate_q is not None:

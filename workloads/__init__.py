@@ -15,5 +15,6 @@ from .generate import (  # noqa: F401
     bf16_bits_from_f32,
     bf16_bits_to_f32,
     encode_mxfp4_rows,
+    encode_nvfp4_rows,
     encode_fp8_tiles,
 )

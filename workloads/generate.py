@@ -12,6 +12,12 @@ What is drawn here, per configuration:
   32-element e2m1 blocks along K, two codes per byte (even element in the low
   nibble) and one UE8M0 scale byte per block, scale 2^(floor(log2 amax) - 2),
   round-to-nearest-even, saturating at +-6;
+* or (the NVFP4-style variant, configurations with wfmt "nvfp4"; CISM
+  VALIDATION, "4-bit quantization scheme study", row "E2M1 + E4M3 b16") the
+  same fp32 draws as e2m1 codes in 16-element blocks along K with one e4m3
+  scale per block and one fp32 scale per matrix: g = amax(matrix) / (6 * 448),
+  block scale = e4m3(amax(block) / (6 g)) rounded to nearest even, codes
+  e2m1(w / (scale * g)) rounded to nearest even, saturating at +-6;
 * the optional shared expert: fp32 draws of the same shape stored as fp8 e4m3
   with one UE8M0 scale per 128x128 tile, scale 2^(floor(log2 amax) - 8),
   round-to-nearest-even, saturating at +-448;
@@ -60,6 +66,7 @@ class LayerConfig:
     bias: Optional[str] = None   # None, "normal0.5", "zipf1.1"
     shared: bool = False
     w_scale: float = 1.5
+    wfmt: str = "mxfp4"      # routed-expert weight format: "mxfp4" or "nvfp4"
 
     @property
     def default_seed(self) -> int:
@@ -82,6 +89,12 @@ CONFIGS = {
                    bias="normal0.5"),
     4: LayerConfig(4, "prefill_t8192_zipf_shared", H=4096, I=2048, E=256, k=6, T=8192,
                    bias="zipf1.1", shared=True),
+    # the NVFP4-style weight variant of the tiny, decode and pp512 layers
+    # (the same fp32 weight draws, encoded as e2m1 + e4m3 per 16 + fp32 per matrix)
+    5: LayerConfig(5, "tiny_nvfp4", H=256, I=128, E=16, k=2, T=4, wfmt="nvfp4"),
+    6: LayerConfig(6, "decode_t1_nvfp4", H=4096, I=2048, E=256, k=6, T=1, steps=4096, wfmt="nvfp4"),
+    7: LayerConfig(7, "prefill_pp512_nvfp4", H=4096, I=2048, E=256, k=6, T=512, bias="normal0.5",
+                   wfmt="nvfp4"),
 }
 
 
@@ -146,6 +159,25 @@ def encode_mxfp4_rows(w: np.ndarray):
     return packed, (ex + 127).astype(np.uint8)
 
 
+def encode_nvfp4_rows(w: np.ndarray):
+    """fp32 [rows][K] -> (packed e2m1 [rows][K/2] u8, e4m3 block scales
+    [rows][K/16] u8, fp32 matrix scale g).  Element value = e2m1(code) *
+    e4m3(scale) * g."""
+    rows, K = w.shape
+    amax_t = np.float32(np.abs(w).max())
+    g = np.float32(amax_t / np.float32(6.0 * 448.0)) if amax_t > 0 else np.float32(1.0)
+    b = w.reshape(rows, K // 16, 16)
+    target = (np.abs(b).max(axis=2) / np.float32(6.0) / g).astype(np.float32)
+    sbyte = _rne_index(target, _E4M3_MID)                  # 0..126, saturating at 448
+    denom = (_E4M3_MAG[sbyte] * g).astype(np.float32)
+    safe = np.where(denom > 0, denom, np.float32(1.0))
+    y = np.where(denom[..., None] > 0, b / safe[..., None], np.float32(0.0)).astype(np.float32)
+    code = _e2m1_index(np.abs(y)) | (np.signbit(y).astype(np.uint8) << 3)
+    code = code.reshape(rows, K)
+    packed = (code[:, 0::2] | (code[:, 1::2] << 4)).astype(np.uint8)
+    return packed, sbyte.astype(np.uint8), g
+
+
 def encode_fp8_tiles(w: np.ndarray, tile: int = 128):
     """fp32 [R][C] -> (e4m3 [R][C] u8, UE8M0 [R/tile][C/tile] u8)."""
     R, C = w.shape
@@ -187,9 +219,15 @@ class Weights:
     sh_up_s: Optional[np.ndarray] = None
     sh_down_q: Optional[np.ndarray] = None   # u8 e4m3 [H][I]
     sh_down_s: Optional[np.ndarray] = None   # u8 [H/128][I/128]
+    # NVFP4 only: the scales above are e4m3 [E][rows][K/16], plus one fp32
+    # scale per expert matrix
+    gate_g: Optional[np.ndarray] = None      # f32 [E]
+    up_g: Optional[np.ndarray] = None
+    down_g: Optional[np.ndarray] = None
 
     ARRAYS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
-              "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")
+              "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s",
+              "gate_g", "up_g", "down_g")
 
 
 def _streams(seed: int):
@@ -207,7 +245,8 @@ def _cache_dir(cfg: LayerConfig, seed: int) -> Optional[Path]:
     root = os.environ.get("BQE_WORKLOAD_CACHE", str(Path.home() / ".cache" / "bqe_workloads"))
     if root in ("", "0", "off"):
         return None
-    return Path(root) / f"H{cfg.H}_I{cfg.I}_E{cfg.E}_s{seed}"
+    fmt = "" if cfg.wfmt == "mxfp4" else f"_{cfg.wfmt}"
+    return Path(root) / f"H{cfg.H}_I{cfg.I}_E{cfg.E}_s{seed}{fmt}"
 
 
 def make_weights(cfg: LayerConfig, seed: Optional[int] = None, threads: Optional[int] = None,
@@ -234,20 +273,25 @@ def make_weights(cfg: LayerConfig, seed: Optional[int] = None, threads: Optional
 
     st = _streams(seed)
     kids = st["weights"].spawn(3 * E)
+    nv = cfg.wfmt == "nvfp4"
+    blk = 16 if nv else 32
     w = Weights(cfg,
-                gate_q=np.empty((E, I, H // 2), np.uint8), gate_s=np.empty((E, I, H // 32), np.uint8),
-                up_q=np.empty((E, I, H // 2), np.uint8), up_s=np.empty((E, I, H // 32), np.uint8),
-                down_q=np.empty((E, H, I // 2), np.uint8), down_s=np.empty((E, H, I // 32), np.uint8))
+                gate_q=np.empty((E, I, H // 2), np.uint8), gate_s=np.empty((E, I, H // blk), np.uint8),
+                up_q=np.empty((E, I, H // 2), np.uint8), up_s=np.empty((E, I, H // blk), np.uint8),
+                down_q=np.empty((E, H, I // 2), np.uint8), down_s=np.empty((E, H, I // blk), np.uint8))
+    if nv:
+        w.gate_g, w.up_g, w.down_g = (np.empty(E, np.float32) for _ in range(3))
 
     def job(i):
         e, m = divmod(i, 3)
-        if m < 2:
-            q, s = encode_mxfp4_rows(_draw(kids[i], I, H))
-            (w.gate_q if m == 0 else w.up_q)[e] = q
-            (w.gate_s if m == 0 else w.up_s)[e] = s
+        wf = _draw(kids[i], I, H) if m < 2 else _draw(kids[i], H, I)
+        if nv:
+            q, s, g = encode_nvfp4_rows(wf)
+            (w.gate_g, w.up_g, w.down_g)[m][e] = g
         else:
-            q, s = encode_mxfp4_rows(_draw(kids[i], H, I))
-            w.down_q[e], w.down_s[e] = q, s
+            q, s = encode_mxfp4_rows(wf)
+        (w.gate_q, w.up_q, w.down_q)[m][e] = q
+        (w.gate_s, w.up_s, w.down_s)[m][e] = s
 
     nthr = threads or min(32, os.cpu_count() or 1)
     with ThreadPoolExecutor(nthr) as ex:
