@@ -186,14 +186,16 @@ def _upload_weights(w, dev):
     import torch
     return {n: torch.from_numpy(np.array(getattr(w, n))).to(dev)
             for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
-                      "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s")
-            if getattr(w, n) is not None}
+                      "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s",
+                      "gate_g", "up_g", "down_g")
+            if getattr(w, n, None) is not None}
 
 
 def make_layer(bqe, cfg, w, dev, max_tokens, path="auto", prune=None):
     import torch
     dw = _upload_weights(w, dev)
-    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, max_tokens, cfg.shared, cfg.w_scale)
+    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, max_tokens, cfg.shared, cfg.w_scale,
+                       bqe.MOE_WEIGHTS_NVFP4 if cfg.wfmt == "nvfp4" else bqe.MOE_WEIGHTS_MXFP4)
     layer = bqe.moe_create(mc, dw)
     torch.cuda.synchronize(dev)
     del dw

@@ -36,7 +36,10 @@ class MoeError(RuntimeError):
 class moe_config(C.Structure):
     _fields_ = [("hidden", C.c_int), ("inter", C.c_int), ("n_experts", C.c_int),
                 ("top_k", C.c_int), ("max_tokens", C.c_int), ("has_shared", C.c_int),
-                ("w_scale", C.c_float)]
+                ("w_scale", C.c_float), ("weight_format", C.c_int)]
+
+
+MOE_WEIGHTS_MXFP4, MOE_WEIGHTS_NVFP4 = 0, 1
 
 
 _WEIGHT_FIELDS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
@@ -44,7 +47,7 @@ _WEIGHT_FIELDS = ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
 
 
 class moe_weights(C.Structure):
-    _fields_ = [(n, C.c_void_p) for n in _WEIGHT_FIELDS]
+    _fields_ = [(n, C.c_void_p) for n in _WEIGHT_FIELDS + ("gate_g", "up_g", "down_g")]
 
 
 _lib = None
@@ -136,10 +139,11 @@ class MoeConfig:
     max_tokens: int
     has_shared: bool = False
     w_scale: float = 1.5
+    weight_format: int = MOE_WEIGHTS_MXFP4
 
     def c(self) -> moe_config:
         return moe_config(self.hidden, self.inter, self.n_experts, self.top_k, self.max_tokens,
-                          int(bool(self.has_shared)), self.w_scale)
+                          int(bool(self.has_shared)), self.w_scale, int(self.weight_format))
 
 
 class Layer:
@@ -165,12 +169,15 @@ def moe_workspace_bytes(cfg: MoeConfig) -> int:
 
 
 def moe_create(cfg: MoeConfig, weights: dict, stream=None) -> Layer:
-    """weights: dict of CUDA uint8 tensors named as the fields of moe_weights."""
+    """weights: dict of CUDA tensors named as the fields of moe_weights (uint8;
+    NVFP4 layers also float32 gate_g, up_g, down_g [E])."""
     import torch
     lib = load_library()
     H, I, E = cfg.hidden, cfg.inter, cfg.n_experts
-    shapes = {"gate_q": (E, I, H // 2), "gate_s": (E, I, H // 32), "up_q": (E, I, H // 2),
-              "up_s": (E, I, H // 32), "down_q": (E, H, I // 2), "down_s": (E, H, I // 32),
+    nv = cfg.weight_format == MOE_WEIGHTS_NVFP4
+    blk = 16 if nv else 32
+    shapes = {"gate_q": (E, I, H // 2), "gate_s": (E, I, H // blk), "up_q": (E, I, H // 2),
+              "up_s": (E, I, H // blk), "down_q": (E, H, I // 2), "down_s": (E, H, I // blk),
               "sh_gate_q": (I, H), "sh_gate_s": (I // 128, H // 128), "sh_up_q": (I, H),
               "sh_up_s": (I // 128, H // 128), "sh_down_q": (H, I), "sh_down_s": (H // 128, I // 128)}
     wt = moe_weights()
@@ -179,6 +186,8 @@ def moe_create(cfg: MoeConfig, weights: dict, stream=None) -> Layer:
             setattr(wt, n, None)
             continue
         setattr(wt, n, _ptr(weights.get(n), torch.uint8, shapes[n], n))
+    for n in ("gate_g", "up_g", "down_g"):
+        setattr(wt, n, _ptr(weights.get(n), torch.float32, (E,), n) if nv else None)
     out = C.c_void_p()
     _check(lib.moe_create(C.byref(cfg.c()), C.byref(wt), _stream(stream), C.byref(out)))
     return Layer(out.value, cfg)

@@ -69,6 +69,8 @@ const char* check_config(const moe_config* c) {
     if (c->hidden > 8192 || c->inter > 8192) return "hidden/inter larger than 8192";
     if (c->hidden % 256) return "hidden must be a multiple of 256";
     if (!std::isfinite(c->w_scale)) return "w_scale must be finite";
+    if (c->weight_format != MOE_WEIGHTS_MXFP4 && c->weight_format != MOE_WEIGHTS_NVFP4)
+        return "weight_format must be MOE_WEIGHTS_MXFP4 or MOE_WEIGHTS_NVFP4";
     return nullptr;
 }
 
@@ -109,7 +111,7 @@ void free_all(moe_layer* L) {
                     L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->perm_cnt, L->xq, L->xs, L->xq_tok,
                     L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
                     L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err,
-                    L->sk_counters, L->sk_partials, L->dec_yw};
+                    L->sk_counters, L->sk_partials, L->dec_yw, L->gate_g, L->up_g, L->down_g};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     moe::tc_free(L);
@@ -193,6 +195,8 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     if (!w) return fail(nullptr, MOE_ERR_INVALID_ARG, "weights is NULL");
     if (!w->gate_q || !w->gate_s || !w->up_q || !w->up_s || !w->down_q || !w->down_s)
         return fail(nullptr, MOE_ERR_INVALID_ARG, "a routed-expert weight pointer is NULL");
+    if (cfg->weight_format == MOE_WEIGHTS_NVFP4 && (!w->gate_g || !w->up_g || !w->down_g))
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "NVFP4 weights need gate_g, up_g and down_g");
     if (cfg->has_shared && (!w->sh_gate_q || !w->sh_gate_s || !w->sh_up_q || !w->sh_up_s ||
                             !w->sh_down_q || !w->sh_down_s))
         return fail(nullptr, MOE_ERR_INVALID_ARG, "has_shared set but a shared weight pointer is NULL");
@@ -216,12 +220,15 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     L->R_max = (int)z.R;
     L->Rp_max = (int)z.Rp;
     size_t total = 0;
-    const size_t gq = E * I * H / 2, gs = E * I * H / 32, dq = E * H * I / 2, ds = E * H * I / 32;
+    const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
+    const size_t sblk = nv ? 16 : 32;  // elements per weight block scale
+    const size_t gq = E * I * H / 2, gs = E * I * H / sblk, dq = E * H * I / 2, ds = E * H * I / sblk;
     cudaError_t a = cudaSuccess;
     auto A = [&](auto** p, size_t bytes) { if (a == cudaSuccess) a = dalloc(p, bytes, &total); };
     A(&L->gu_q, 2 * gq); A(&L->gate_s, gs); A(&L->up_s, gs);
     A(&L->down_q, dq); A(&L->down_s, ds);
-    A(&L->gu_sf, 2 * gs); A(&L->down_sf, ds);
+    A(&L->gu_sf, 2 * E * I * H / 32); A(&L->down_sf, E * H * I / 32);
+    if (nv) { A(&L->gate_g, E * 4); A(&L->up_g, E * 4); A(&L->down_g, E * 4); }
     if (c.has_shared) {
         A(&L->sh_gu_q, 2 * I * H); A(&L->sh_gate_s, (I / 128) * (H / 128));
         A(&L->sh_up_s, (I / 128) * (H / 128));
@@ -268,6 +275,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     C2(L->gu_q + blk, 2 * blk, w->up_q, blk, E * (I / 128));
     C(L->gate_s, w->gate_s, gs); C(L->up_s, w->up_s, gs);
     C(L->down_q, w->down_q, dq); C(L->down_s, w->down_s, ds);
+    if (nv) { C(L->gate_g, w->gate_g, E * 4); C(L->up_g, w->up_g, E * 4); C(L->down_g, w->down_g, E * 4); }
     if (c.has_shared) {
         C2(L->sh_gu_q, 2 * 128 * H, w->sh_gate_q, 128 * H, I / 128);
         C2(L->sh_gu_q + 128 * H, 2 * 128 * H, w->sh_up_q, 128 * H, I / 128);
@@ -275,8 +283,11 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         C(L->sh_up_s, w->sh_up_s, (I / 128) * (H / 128));
         C(L->sh_down_q, w->sh_down_q, H * I); C(L->sh_down_s, w->sh_down_s, (H / 128) * (I / 128));
     }
-    if (a == cudaSuccess) a = moe::pack_sf_pairs(L->gate_s, L->up_s, L->gu_sf, (int)E, (int)(I / 128), (int)H, 0, s);
-    if (a == cudaSuccess) a = moe::pack_sf_pairs(L->down_s, nullptr, L->down_sf, (int)E, (int)(H / 256), (int)I, 1, s);
+    // (the tensor-core scale atoms exist for MXFP4 experts only)
+    if (a == cudaSuccess && !nv)
+        a = moe::pack_sf_pairs(L->gate_s, L->up_s, L->gu_sf, (int)E, (int)(I / 128), (int)H, 0, s);
+    if (a == cudaSuccess && !nv)
+        a = moe::pack_sf_pairs(L->down_s, nullptr, L->down_sf, (int)E, (int)(H / 256), (int)I, 1, s);
     if (c.has_shared) {
         if (a == cudaSuccess)
             a = moe::pack_sf_pairs(L->sh_gate_s, L->sh_up_s, L->sh_gu_sf, 1, (int)(I / 128), (int)H, 2, s);

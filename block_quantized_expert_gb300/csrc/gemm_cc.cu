@@ -1,5 +1,11 @@
 // gemm_cc.cu -- grouped expert GEMMs on the CUDA cores (fp32 FMA over the
-// exactly dequantised MXFP4 / fp8 weights and MXFP8 activations).
+// exactly dequantised MXFP4 / NVFP4 / fp8 weights and MXFP8 activations).
+//
+// Weight kinds: 0 MXFP4 (e2m1, UE8M0 per 32), 1 fp8 e4m3 with 128x128 UE8M0
+// tiles (the shared expert), 2 NVFP4-style (e2m1, e4m3 per 16, fp32 per
+// matrix: CISM VALIDATION, "4-bit quantization scheme study", row "E2M1 +
+// E4M3 b16"): a 32-block's two halves take their own scales and the matrix
+// scale multiplies the finished dot product.
 //
 // Work item = (segment e, chunk of up to kChunk tokens of the segment,
 // 32 output features).  The chunk's activation rows are dequantised once into
@@ -19,6 +25,7 @@ struct CCArgs {
     const int32_t* poff;        // [n_seg+1] padded row starts
     const int32_t* chunk_scan;  // [n_seg+1]
     const uint8_t *w1_q, *w1_s, *w2_q, *w2_s;
+    const float *w1_g, *w2_g;   // kind 2: per-segment matrix scales [n_seg]
     const uint8_t* aq;          // activation codes [Rp][K]
     const uint8_t* as;          // activation scale atoms
     int K, N;                   // contraction length, output features
@@ -35,7 +42,7 @@ constexpr int kCCWarps = kCCThreads / 32;
 template <int kWKind>
 __device__ __forceinline__ void load_weight_block(const uint8_t* __restrict__ q, size_t row, int K,
                                                   int b, float* wv) {
-    if (kWKind == 0) {  // MXFP4: 16 bytes, even element in the low nibble
+    if (kWKind != 1) {  // MXFP4 / NVFP4: 16 bytes, even element in the low nibble
         const uint4 raw = __ldg(reinterpret_cast<const uint4*>(q + row * (size_t)(K / 2)) + b);
         const uint32_t wds[4] = {raw.x, raw.y, raw.z, raw.w};
 #pragma unroll
@@ -53,11 +60,18 @@ __device__ __forceinline__ void load_weight_block(const uint8_t* __restrict__ q,
     }
 }
 
+// The block scale of 32-block b of row `row` (kind 2: of its first 16
+// elements; weight_scale_hi: of its last 16).
 template <int kWKind>
 __device__ __forceinline__ float weight_scale(const uint8_t* __restrict__ s, size_t seg_row0,
                                               int row, int K, int b) {
     if (kWKind == 0) return ue8m0_to_f32(__ldg(s + (seg_row0 + row) * (size_t)(K / 32) + b));
+    if (kWKind == 2) return e4m3_to_f32(__ldg(s + (seg_row0 + row) * (size_t)(K / 16) + 2 * b));
     return ue8m0_to_f32(__ldg(s + (size_t)(row / 128) * (K / 128) + b / 4));
+}
+__device__ __forceinline__ float weight_scale_hi(const uint8_t* __restrict__ s, size_t seg_row0, int row,
+                                                 int K, int b) {
+    return e4m3_to_f32(__ldg(s + (seg_row0 + row) * (size_t)(K / 16) + 2 * b + 1));
 }
 
 template <int kWKind, bool kGateUp>
@@ -93,7 +107,7 @@ __global__ void __launch_bounds__(kCCThreads) k_gemm_cc(CCArgs a) {
         }
         __syncthreads();
 
-        const size_t seg_row0 = (kWKind == 0) ? (size_t)e * a.N : 0;
+        const size_t seg_row0 = (kWKind != 1) ? (size_t)e * a.N : 0;
         for (int jj = warp; jj < 32; jj += kCCWarps) {
             const int j = fb * 32 + jj;
             float acc1[kChunk], acc2[kChunk];
@@ -101,43 +115,56 @@ __global__ void __launch_bounds__(kCCThreads) k_gemm_cc(CCArgs a) {
             for (int n = 0; n < kChunk; ++n) { acc1[n] = 0.f; acc2[n] = 0.f; }
             // gate/up codes are interleaved per 128 features (gate block, then up
             // block); down codes are row-major per segment
-            const size_t prow = kGateUp ? (size_t)((kWKind == 0 ? e : 0) * (a.N / 128) + j / 128) * 256 + (j % 128)
+            const size_t prow = kGateUp ? (size_t)((kWKind != 1 ? e : 0) * (a.N / 128) + j / 128) * 256 + (j % 128)
                                         : seg_row0 + j;
             for (int b = lane; b < KB; b += 32) {
                 float w1[32];
                 load_weight_block<kWKind>(a.w1_q, prow, a.K, b, w1);
                 const float s1 = weight_scale<kWKind>(a.w1_s, seg_row0, j, a.K, b);
+                const float s1h = kWKind == 2 ? weight_scale_hi(a.w1_s, seg_row0, j, a.K, b) : s1;
                 float w2[32];
-                float s2 = 0.f;
+                float s2 = 0.f, s2h = 0.f;
                 if (kGateUp) {
                     load_weight_block<kWKind>(a.w2_q, prow + 128, a.K, b, w2);
                     s2 = weight_scale<kWKind>(a.w2_s, seg_row0, j, a.K, b);
+                    s2h = kWKind == 2 ? weight_scale_hi(a.w2_s, seg_row0, j, a.K, b) : s2;
                 }
 #pragma unroll
                 for (int n = 0; n < kChunk; ++n) {
                     if (n < nt) {
                         const float4* xv = reinterpret_cast<const float4*>(xf + n * a.K + b * 32);
-                        float p1 = 0.f, p2 = 0.f;
+                        // the two 16-element halves (one scale each for kind 2)
+                        float p1[2] = {0.f, 0.f}, p2[2] = {0.f, 0.f};
 #pragma unroll
                         for (int i = 0; i < 8; ++i) {
                             const float4 x4 = xv[i];
-                            p1 = fmaf(w1[4 * i], x4.x, p1); p1 = fmaf(w1[4 * i + 1], x4.y, p1);
-                            p1 = fmaf(w1[4 * i + 2], x4.z, p1); p1 = fmaf(w1[4 * i + 3], x4.w, p1);
+                            float& q1 = p1[i >> 2];
+                            q1 = fmaf(w1[4 * i], x4.x, q1); q1 = fmaf(w1[4 * i + 1], x4.y, q1);
+                            q1 = fmaf(w1[4 * i + 2], x4.z, q1); q1 = fmaf(w1[4 * i + 3], x4.w, q1);
                             if (kGateUp) {
-                                p2 = fmaf(w2[4 * i], x4.x, p2); p2 = fmaf(w2[4 * i + 1], x4.y, p2);
-                                p2 = fmaf(w2[4 * i + 2], x4.z, p2); p2 = fmaf(w2[4 * i + 3], x4.w, p2);
+                                float& q2 = p2[i >> 2];
+                                q2 = fmaf(w2[4 * i], x4.x, q2); q2 = fmaf(w2[4 * i + 1], x4.y, q2);
+                                q2 = fmaf(w2[4 * i + 2], x4.z, q2); q2 = fmaf(w2[4 * i + 3], x4.w, q2);
                             }
                         }
-                        acc1[n] = fmaf(p1, s1, acc1[n]);
-                        if (kGateUp) acc2[n] = fmaf(p2, s2, acc2[n]);
+                        if (kWKind == 2) {
+                            acc1[n] = fmaf(p1[1], s1h, fmaf(p1[0], s1, acc1[n]));
+                            if (kGateUp) acc2[n] = fmaf(p2[1], s2h, fmaf(p2[0], s2, acc2[n]));
+                        } else {
+                            acc1[n] = fmaf(p1[0] + p1[1], s1, acc1[n]);
+                            if (kGateUp) acc2[n] = fmaf(p2[0] + p2[1], s2, acc2[n]);
+                        }
                     }
                 }
             }
 #pragma unroll
+            // kind 2: the matrix scales multiply the finished dot products
+            const float g1 = kWKind == 2 ? __ldg(a.w1_g + e) : 1.f;
+            const float g2 = (kWKind == 2 && kGateUp) ? __ldg(a.w2_g + e) : 1.f;
             for (int n = 0; n < kChunk; ++n) {
-                const float g = warp_sum(acc1[n]);
+                const float g = warp_sum(acc1[n]) * g1;
                 if (kGateUp) {
-                    const float u = warp_sum(acc2[n]);
+                    const float u = warp_sum(acc2[n]) * g2;
                     if (lane == 0 && n < nt) hb[n * 32 + jj] = silu_mul(g, u);
                 } else {
                     if (lane == 0 && n < nt) hb[n * 32 + jj] = g;
@@ -169,6 +196,8 @@ cudaError_t cc_init() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<0, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<1, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<1, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<2, true>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(k_gemm_cc<2, false>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     return e;  // the dynamic smem request already selects the largest carveout
 }
 
@@ -190,18 +219,21 @@ cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     a.poff = L->poff;
     a.chunk_scan = L->chunk_scan;
     a.w1_q = L->gu_q; a.w1_s = L->gate_s; a.w2_q = L->gu_q; a.w2_s = L->up_s;
+    a.w1_g = L->gate_g; a.w2_g = L->up_g;
     a.aq = L->xq; a.as = L->xs;
     a.K = c.hidden; a.N = c.inter;
     a.hq = L->hq; a.hs = L->hs;
-    cudaError_t err = cc_launch<0, true>(L, a, s);
+    const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
+    cudaError_t err = nv ? cc_launch<2, true>(L, a, s) : cc_launch<0, true>(L, a, s);
     if (err == cudaSuccess && mid) err = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
     if (err != cudaSuccess) return err;
     CCArgs d = a;
     d.w1_q = L->down_q; d.w1_s = L->down_s; d.w2_q = nullptr; d.w2_s = nullptr;
+    d.w1_g = L->down_g; d.w2_g = nullptr;
     d.aq = L->hq; d.as = L->hs;
     d.K = c.inter; d.N = c.hidden;
     d.y = L->y; d.pos_row = L->pos_row;
-    err = cc_launch<0, false>(L, d, s);
+    err = nv ? cc_launch<2, false>(L, d, s) : cc_launch<0, false>(L, d, s);
     if (err != cudaSuccess || !c.has_shared) return err;
     // shared expert: one segment of all T tokens in token order
     CCArgs sg{};

@@ -1383,6 +1383,9 @@ cudaError_t tc_init(moe_layer* L) {
     cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, L->device);
     cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, L->device);
     if (major != 10 || minor != 3) return cudaSuccess;  // kernels are built for sm_103a only
+    // the block-scaled MMAs take UE8M0 scales per 32 elements: NVFP4 experts
+    // (e4m3 scales per 16) run on the CUDA-core kernels
+    if (L->cfg.weight_format != MOE_WEIGHTS_MXFP4) return cudaSuccess;
     TcState* st = new (std::nothrow) TcState;
     if (!st) return cudaErrorMemoryAllocation;
     const uint64_t H = L->cfg.hidden, I = L->cfg.inter, E = L->cfg.n_experts;

@@ -23,8 +23,10 @@ struct moe_layer {
     // -------- weights (library-owned copies) --------
     // gate/up codes interleaved per 128 features: [E][I/128][gate 128 rows, up 128 rows][H/2],
     // so one 256-row copy brings the gate and up tiles of 128 features; down codes canonical
-    // [E][H][I/2]; scales canonical [E][rows][K/32] (read by the CUDA-core kernels).
+    // [E][H][I/2]; scales canonical [E][rows][K/32] (NVFP4: e4m3 [E][rows][K/16]; read by the
+    // CUDA-core kernels).
     uint8_t *gu_q, *gate_s, *up_s, *down_q, *down_s;
+    float *gate_g, *up_g, *down_g;  // NVFP4: per-expert matrix scales [E] (null for MXFP4)
     uint8_t *sh_gu_q, *sh_gate_s, *sh_up_s, *sh_down_q, *sh_down_s;  // shared: [I/128][256][H] e4m3
     // scales as 512-byte atoms, two per 256-row block and 128-column step:
     // [blocks][K/128][2][512] (gate/up: gate, up halves; down: rows 0-127, 128-255)

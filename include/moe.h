@@ -71,19 +71,36 @@ typedef struct {
     int max_tokens;
     int has_shared;  /* 1: the shared-expert pointers of moe_weights are set */
     float w_scale;   /* routing weights of a token sum to w_scale            */
+    int weight_format; /* routed experts: MOE_WEIGHTS_MXFP4 (0, the default)
+                        * or MOE_WEIGHTS_NVFP4 (1), see moe_weights         */
 } moe_config;
+
+/* Routed-expert weight formats.  MXFP4 is what the experts ship in (colibri
+ * "DeepSeek V4 target engine", intro).  NVFP4-style (CISM VALIDATION,
+ * "4-bit quantization scheme study", row "E2M1 + E4M3 b16 (NVFP4
+ * granularity)", the best 4-bit scheme of that study): the same e2m1 codes,
+ * one e4m3 scale per 16 elements along K and one fp32 scale per expert
+ * matrix, element = e2m1 * e4m3 scale * matrix scale.  The tcgen05
+ * block-scaled MMAs take UE8M0 scales per 32 elements only, so an NVFP4
+ * layer runs its GEMMs on the CUDA cores (moe_set_gemm_path 2 returns
+ * MOE_ERR_UNSUPPORTED and a one-token call takes the grouped path).        */
+enum { MOE_WEIGHTS_MXFP4 = 0, MOE_WEIGHTS_NVFP4 = 1 };
 
 /* Device pointers to the weights, in the canonical shipping layout:
  *   gate_q, up_q  u8 [E][I][H/2]  e2m1 pairs (even element = low nibble)
  *   gate_s, up_s  u8 [E][I][H/32] UE8M0 block scales
+ *                 (NVFP4: u8 [E][I][H/16] e4m3 block scales, positive)
  *   down_q        u8 [E][H][I/2]
- *   down_s        u8 [E][H][I/32]
+ *   down_s        u8 [E][H][I/32] (NVFP4: [E][H][I/16] e4m3)
+ *   gate_g, up_g, down_g  f32 [E]: NVFP4 only, the per-matrix scales
+ *                 (ignored, may be NULL, for MXFP4)
  *   sh_gate_q, sh_up_q u8 [I][H] e4m3;  sh_gate_s, sh_up_s u8 [I/128][H/128]
  *   sh_down_q     u8 [H][I] e4m3;       sh_down_s          u8 [H/128][I/128]
  * Shared-expert pointers are ignored unless has_shared.                     */
 typedef struct {
     const uint8_t *gate_q, *gate_s, *up_q, *up_s, *down_q, *down_s;
     const uint8_t *sh_gate_q, *sh_gate_s, *sh_up_q, *sh_up_s, *sh_down_q, *sh_down_s;
+    const float *gate_g, *up_g, *down_g;
 } moe_weights;
 
 typedef struct moe_layer moe_layer;

@@ -54,15 +54,17 @@ def weights_np(cfg_id: int):
 def upload(w) -> dict:
     d = {}
     for n in ("gate_q", "gate_s", "up_q", "up_s", "down_q", "down_s",
-              "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s"):
-        a = getattr(w, n)
+              "sh_gate_q", "sh_gate_s", "sh_up_q", "sh_up_s", "sh_down_q", "sh_down_s",
+              "gate_g", "up_g", "down_g"):
+        a = getattr(w, n, None)
         if a is not None:
             d[n] = to_dev(a)
     return d
 
 
 def make_layer(cfg, w, max_tokens: int) -> bqe.Layer:
-    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, max_tokens, cfg.shared, cfg.w_scale)
+    mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, max_tokens, cfg.shared, cfg.w_scale,
+                       bqe.MOE_WEIGHTS_NVFP4 if cfg.wfmt == "nvfp4" else bqe.MOE_WEIGHTS_MXFP4)
     dw = upload(w)
     layer = bqe.moe_create(mc, dw)
     torch.cuda.synchronize()
