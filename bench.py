@@ -117,8 +117,9 @@ def algorithmic_bytes(cfg, touched, rows):
     """Bytes one layer call must move at least: the touched experts' MXFP4
     weights (payload + scales) and the activation rows in and out."""
     H, I = cfg.H, cfg.I
-    w_gu = 2 * (I * H // 2 + I * H // 32)
-    w_dn = H * I // 2 + H * I // 32
+    blk = 16 if getattr(cfg, "wfmt", "mxfp4") == "nvfp4" else 32  # elements per block scale byte
+    w_gu = 2 * (I * H // 2 + I * H // blk)
+    w_dn = H * I // 2 + H * I // blk
     act_gu = rows * (H + H // 32) + rows * (I + I // 32)
     act_dn = rows * (I + I // 32) + rows * H * 4
     return {"gateup": touched * w_gu + act_gu, "down": touched * w_dn + act_dn}
@@ -466,7 +467,8 @@ def wl_tokens_for_cpu(cfg, rank):
 
 
 PER_CONFIG = [  # (config, router, timed steps)
-    (2, "hash", 128), (2, "learned", 128), (3, None, 48), (4, None, 16)]
+    (2, "hash", 128), (2, "learned", 128), (3, None, 48), (4, None, 16),
+    (6, None, 32), (7, None, 4)]  # the NVFP4-style weight variant (CUDA-core GEMMs)
 
 
 def per_config(args, bqe, dev, peaks):
@@ -485,12 +487,12 @@ def per_config(args, bqe, dev, peaks):
     for ci, router, K in PER_CONFIG:
         cfg = CONFIGS[ci]
         t_start = time.time()
-        key = (cfg.shared, cfg.T if cfg.shared else 512)
+        key = (cfg.shared, cfg.T if cfg.shared else 512, cfg.wfmt)
         if layer_for != key:
             if layer is not None:
                 layer.close()
                 torch.cuda.empty_cache()
-            layer = make_layer(bqe, cfg, make_weights(cfg), dev, key[1], args.path)
+            layer = make_layer(bqe, cfg, make_weights(cfg), dev, key[1], args.path if cfg.wfmt == "mxfp4" else "auto")
             layer_for = key
         W = 3
         wl = Workload(bqe, cfg, layer, dev, min(K + W, 4), cfg.default_seed, router=router)
@@ -510,9 +512,11 @@ def per_config(args, bqe, dev, peaks):
         byts = algorithmic_bytes(cfg, avg_touched, rows)
         dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
         roof = roofline(cfg, dom, stage_ms[dom], byts, rows, peaks, mma_peak)
-        roof["kernel"] = f"{dom} GEMM (k_gemm_tc)"
+        roof["kernel"] = f"{dom} GEMM ({'k_gemm_cc, CUDA cores' if cfg.wfmt == 'nvfp4' else 'k_gemm_tc'})"
         recs.append({"workload": cfg.name if router is None else f"{cfg.name.rsplit('_', 1)[0]}_{router}",
                      "tokens_per_step": cfg.T, "router": router or cfg.router, "shared_expert": cfg.shared,
+                     "weights": "NVFP4-style e2m1 + e4m3 /16 + fp32 per matrix (CUDA-core GEMMs)"
+                     if cfg.wfmt == "nvfp4" else "MXFP4 e2m1 + UE8M0 /32",
                      "value": job_rate(1, K * cfg.T, ms), "unit": UNIT, "steps": K, "warmup": W,
                      "ms_per_step": round(ms / K, 6), "experts_touched_per_step": avg_touched,
                      "stage_ms_untimed_pass": {k: round(v, 5) for k, v in stage_ms.items()},
