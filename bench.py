@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--config", type=int, default=1, choices=[1, 2, 3, 4])
     ap.add_argument("--path", choices=["auto", "cc", "tc"], default="auto")
     ap.add_argument("--graph-chunk", type=int, default=256, help="steps per CUDA graph")
+    ap.add_argument("--decode-kernel", type=int, default=0, choices=[0, 1, 2],
+                    help="one-token calls: 0 automatic, 1 the CUDA-core GEMV kernel, 2 the tcgen05 kernel")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-per-config", action="store_true",
@@ -107,6 +109,8 @@ def config_json(cfg, args, world):
             "top_k": cfg.k, "tokens_per_step": cfg.T, "router": cfg.router,
             "shared_expert": cfg.shared, "weights": "MXFP4 e2m1 + UE8M0 /32",
             "activations": "MXFP8 e4m3 + UE8M0 /32", "gemm_path": args.path,
+            **({"decode_kernel": {0: "auto", 1: "gemv", 2: "tcgen05"}[args.decode_kernel]}
+               if cfg.T == 1 else {}),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
             "l2": "inputs larger than L2 (3.4 GB expert set; fresh tokens each step)",
             **({"route_prune": {"keep": args.prune_t[0], "min_w": args.prune_t[1], "rho": args.prune_t[2]}}
@@ -192,7 +196,7 @@ def _upload_weights(w, dev):
             if getattr(w, n, None) is not None}
 
 
-def make_layer(bqe, cfg, w, dev, max_tokens, path="auto", prune=None):
+def make_layer(bqe, cfg, w, dev, max_tokens, path="auto", prune=None, decode_kernel=0):
     import torch
     dw = _upload_weights(w, dev)
     mc = bqe.MoeConfig(cfg.H, cfg.I, cfg.E, cfg.k, max_tokens, cfg.shared, cfg.w_scale,
@@ -201,6 +205,8 @@ def make_layer(bqe, cfg, w, dev, max_tokens, path="auto", prune=None):
     torch.cuda.synchronize(dev)
     del dw
     bqe.moe_set_gemm_path(layer, {"auto": 0, "cc": 1, "tc": 2}[path])
+    if decode_kernel:
+        bqe.moe_set_decode_kernel(layer, decode_kernel)
     if prune:
         bqe.moe_set_route_prune(layer, *prune)
     return layer
@@ -392,7 +398,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     W = max(W, 3)
 
     w = make_weights(cfg)
-    layer = make_layer(bqe, cfg, w, dev, cfg.T, args.path, args.prune_t)
+    layer = make_layer(bqe, cfg, w, dev, cfg.T, args.path, args.prune_t, args.decode_kernel)
+    decode_kind = bqe.moe_decode_info(layer) if cfg.T == 1 else 0
     # distinct inputs: one token per step for decode, else a few batches cycled
     S = (K + W) if cfg.T == 1 else min(K + W, 4)
     wl = Workload(bqe, cfg, layer, dev, S, rank_seed(cfg, rank))
@@ -422,14 +429,14 @@ def run_ours(args, cfg, rank, world, local_rank):
         # duration is the timed region over the K calls
         dom, kernel_ms, stage_ms = "layer", ms / K, None
         byts["layer"] = step_bytes
-        kernel = "whole-layer decode kernel (k_decode)"
+        kernel = DECODE_KERNELS[decode_kind]
     else:
         stage_ms = stage_times(bqe, layer, wl.step, W + K, min(K, 32), stream)
         dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
         kernel_ms, kernel = stage_ms[dom], f"{dom} GEMM"
     roof = roofline(cfg, dom, kernel_ms, byts, rows, peaks)
     roof["kernel"] = kernel
-    roof["traffic"] = profiled_traffic(cfg, dom) if not args.prune_t else None
+    roof["traffic"] = profiled_traffic(cfg, dom, decode_kind) if not args.prune_t else None
     roof["hbm_frac_whole_step"] = round(step_bytes / (ms / K * 1e-3) / 1e9 / roof["peak"], 4) \
         if roof["unit"] == "GB/s" else None
 
@@ -530,29 +537,35 @@ def per_config(args, bqe, dev, peaks):
     return recs
 
 
-# DRAM bytes per launch of the decode kernel from a committed ncu capture,
-# valid only for the kernel sources it was taken on
-PROFILE_COUNTERS = os.path.join(ROOT, "profiles", "decode_t1_k_decode_counters.json")
-KERNEL_SOURCES = ["gemm_tc.cu", "common.cuh", "tc_ptx.cuh", "route.cuh", "layer.h"]
+# The whole-layer decode kernels (moe_decode_info codes), and for each the
+# committed ncu capture of its DRAM bytes per launch with the sources it is
+# valid for
+DECODE_KERNELS = {1: "whole-layer decode kernel, CUDA-core GEMV (k_decode_gemv)",
+                  2: "whole-layer decode kernel, tcgen05 (k_decode)"}
+PROFILE_COUNTERS = {1: ("decode_t1_k_decode_gemv_counters.json",
+                        ["decode_gemv.cu", "common.cuh", "tc_ptx.cuh", "route.cuh", "layer.h"]),
+                    2: ("decode_t1_k_decode_counters.json",
+                        ["gemm_tc.cu", "common.cuh", "tc_ptx.cuh", "route.cuh", "layer.h"])}
 
 
-def kernel_sources_sha256():
+def kernel_sources_sha256(sources):
     import hashlib
     h = hashlib.sha256()
-    for name in sorted(KERNEL_SOURCES):
+    for name in sorted(sources):
         with open(os.path.join(ROOT, "block_quantized_expert_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()
 
 
-def profiled_traffic(cfg, dom):
-    if dom != "layer" or cfg.index != 1:
+def profiled_traffic(cfg, dom, decode_kind):
+    if dom != "layer" or cfg.index != 1 or decode_kind not in PROFILE_COUNTERS:
         return None
+    fname, sources = PROFILE_COUNTERS[decode_kind]
     try:
-        rec = json.load(open(PROFILE_COUNTERS))
+        rec = json.load(open(os.path.join(ROOT, "profiles", fname)))
     except (OSError, ValueError):
         return None
-    if rec.get("kernel_sources_sha256") != kernel_sources_sha256():
+    if rec.get("kernel_sources_sha256") != kernel_sources_sha256(sources):
         return None  # the kernel changed since the counters were taken
     return int(rec["dram_bytes_per_launch"])
 

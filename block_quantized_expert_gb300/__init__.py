@@ -24,7 +24,8 @@ EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_perm
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
            "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace", "moe_route_forward",
-           "moe_set_route_prune", "moe_set_wait_limit", "moe_test_stall_next_decode")
+           "moe_set_route_prune", "moe_set_wait_limit", "moe_test_stall_next_decode",
+           "moe_set_decode_kernel", "moe_decode_info")
 
 
 class MoeError(RuntimeError):
@@ -85,6 +86,8 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_set_route_prune": ([vp, i, f, f], i),
         "moe_set_wait_limit": ([vp, C.c_double], i),
         "moe_test_stall_next_decode": ([vp], i),
+        "moe_set_decode_kernel": ([vp, i], i),
+        "moe_decode_info": ([vp, C.POINTER(C.c_int)], i),
     }
     for name, (args, res) in sigs.items():
         fn = getattr(L, name)
@@ -202,6 +205,18 @@ def moe_destroy(layer: Layer):
 
 def moe_set_gemm_path(layer: Layer, path: int):
     _check(load_library().moe_set_gemm_path(layer.ptr, int(path)), layer.ptr)
+
+
+def moe_set_decode_kernel(layer: Layer, kind: int):
+    """One-token calls: 0 automatic, 1 the CUDA-core GEMV kernel, 2 the tcgen05 kernel."""
+    _check(load_library().moe_set_decode_kernel(layer.ptr, int(kind)), layer.ptr)
+
+
+def moe_decode_info(layer: Layer) -> int:
+    """The whole-layer kernel a one-token call takes: 0 none, 1 CUDA-core GEMV, 2 tcgen05."""
+    kind = C.c_int(0)
+    _check(load_library().moe_decode_info(layer.ptr, C.byref(kind)), layer.ptr)
+    return kind.value
 
 
 def moe_set_route_prune(layer: Layer, keep: int, min_w: float = 0.0, rho: float = 0.0):

@@ -94,6 +94,7 @@ size_t workspace_bytes(const moe_config& c) {
     // split-tile counters, decode flags and partial accumulators (sized for up to 256 SMs)
     b += (size_t)((4 * 256 + 32) + (2 + 8 * 256 + 128 + 32)) * 4 + (size_t)256 * 2 * 2 * 128 * 128 * 4;
     b += (size_t)128 * 256 * 8;                  // decode down outputs with their epoch
+    b += (size_t)moe::gv_words_count(c, 256) * 4;  // CUDA-core decode kernel: flags, launch counts (<= 256 SMs)
     return b;
 }
 
@@ -111,7 +112,8 @@ void free_all(moe_layer* L) {
                     L->row_dst, L->row_pos, L->pos_row, L->sh_desc, L->perm_cnt, L->xq, L->xs, L->xq_tok,
                     L->xs_tok, L->hq, L->hs, L->hq_sh, L->hs_sh, L->y, L->y_sh, L->x_stage,
                     L->logits_stage, L->out_stage, L->ids_stage, L->w_stage, L->d_err,
-                    L->sk_counters, L->sk_partials, L->dec_yw, L->gate_g, L->up_g, L->down_g};
+                    L->sk_counters, L->sk_partials, L->dec_yw, L->gate_g, L->up_g, L->down_g,
+                    L->gv_words, L->gv_rows};
     for (void* p : ptrs)
         if (p) cudaFree(p);
     moe::tc_free(L);
@@ -132,6 +134,23 @@ void set_thread_error(const char* msg) { snprintf(g_tls_error, sizeof(g_tls_erro
 
 namespace {
 
+// The whole-layer kernel a one-token call takes: 0 none (the grouped
+// kernels), 1 the CUDA-core GEMV kernel, 2 the tcgen05 kernel.  Automatic:
+// the CUDA-core kernel where its shape allows, else the tcgen05 one.
+int decode_kind(const moe_layer* L) {
+    if (L->gemm_path != 0) return 0;
+    const bool gv = moe::gemv::supported(L), tcd = L->tc != nullptr && moe::decode_supported(L);
+    if (L->decode_kernel == 1) return gv ? 1 : 0;
+    if (L->decode_kernel == 2) return tcd ? 2 : 0;
+    return gv ? 1 : (tcd ? 2 : 0);
+}
+
+cudaError_t launch_decode_kind(moe_layer* L, int kind, const float* logits, const uint16_t* x, int32_t* ids,
+                               float* w, float* out, cudaStream_t s, bool x_in_host) {
+    return kind == 1 ? moe::gemv::launch(L, logits, x, ids, w, out, s, x_in_host)
+                     : moe::launch_decode(L, logits, x, ids, w, out, s, x_in_host);
+}
+
 // The kernels of one layer call.  Small batches (T <= kFrontMaxT) run the
 // routing (when logits are given), the counting sort and the quantisation in
 // one CTA; on the tensor-core path without a shared expert the combine is
@@ -144,12 +163,13 @@ cudaError_t forward_kernels(moe_layer* L, const float* logits, const uint16_t* x
     const bool tc = L->gemm_path != 1 && L->tc != nullptr;  // automatic: tensor cores
     const bool fuse_combine = tc && small && !L->cfg.has_shared && T <= moe::kFusedCombineMaxT;
     cudaError_t e = M(0, cudaSuccess);
-    if (tc && L->gemm_path == 0 && logits && T == 1 && moe::decode_supported(L)) {
+    const int dk = logits && T == 1 ? decode_kind(L) : 0;
+    if (dk) {
         // one token: the whole layer in one cooperative kernel (the stage
         // marks before it are empty and its time shows as the gate/up stage)
         if (e == cudaSuccess) e = M(1, cudaSuccess);
         if (e == cudaSuccess) e = M(2, cudaSuccess);
-        if (e == cudaSuccess) e = moe::launch_decode(L, logits, x, ids, w, out, s);
+        if (e == cudaSuccess) e = launch_decode_kind(L, dk, logits, x, ids, w, out, s, false);
         if (e == cudaSuccess) e = M(3, cudaSuccess);
         if (e == cudaSuccess) e = M(4, cudaSuccess);
         if (e == cudaSuccess) e = M(5, cudaSuccess);
@@ -254,6 +274,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     A(&L->sk_counters, (size_t)moe::kSkCounters(L) * 4);
     A(&L->sk_partials, (size_t)L->num_sms * 2 * 2 * 128 * 128 * 4);
     A(&L->dec_yw, (size_t)128 * 256 * 8);
+    A(&L->gv_words, moe::gv_words_count(c, L->num_sms) * 4);
     if (a != cudaSuccess) {
         cudaGetLastError();
         free_all(L);
@@ -296,10 +317,10 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     }
     // a defined workspace: padding rows of the activation buffers read as zero
     // (and the epoch-tagged decode words start at epoch 0, which no launch uses)
-    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters, L->dec_yw};
+    void* zero[] = {L->xq, L->xs, L->hq, L->hs, L->d_err, L->pos_row, L->sk_counters, L->dec_yw, L->gv_words};
     size_t zn[] = {z.Rp * H, z.Rp * H / 32, z.Rp * I, z.Rp * I / 32, 256, z.Rp * 4,
-                   (size_t)moe::kSkCounters(L) * 4, (size_t)128 * 256 * 8};
-    for (int i = 0; i < 8 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
+                   (size_t)moe::kSkCounters(L) * 4, (size_t)128 * 256 * 8, moe::gv_words_count(c, L->num_sms) * 4};
+    for (int i = 0; i < 9 && a == cudaSuccess; ++i) a = cudaMemsetAsync(zero[i], 0, zn[i], s);
     if (c.has_shared) {
         void* zs[] = {L->xq_tok, L->xs_tok, L->hq_sh, L->hs_sh};
         size_t zsn[] = {z.Tpad * H, z.Tpad * H / 32, z.Tpad * I, z.Tpad * I / 32};
@@ -309,6 +330,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
     if (a == cudaSuccess) a = moe::kernels_init();
     if (a == cudaSuccess) a = moe::cc_init();
     if (a == cudaSuccess) a = moe::tc_init(L);
+    if (a == cudaSuccess) a = moe::gemv::init(L);
     if (a != cudaSuccess) {
         moe_status st = cuda_fail(nullptr, a, "moe_create");
         cudaGetLastError();
@@ -317,6 +339,7 @@ moe_status moe_create(const moe_config* cfg, const moe_weights* w, moe_stream_t 
         return st;
     }
     L->gemm_path = 0;
+    L->decode_kernel = 0;
     L->wait_ns = 2000000000ull;
     L->stall_next_decode = 0;
     L->prune_keep = L->cfg.top_k;
@@ -383,8 +406,26 @@ moe_status moe_set_wait_limit(moe_layer* L, double seconds) {
 
 moe_status moe_test_stall_next_decode(moe_layer* L) {
     if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
-    if (!moe::decode_supported(L)) return fail(L, MOE_ERR_UNSUPPORTED, "the layer has no whole-layer decode kernel");
+    if (!moe::gemv::supported(L) && !(L->tc != nullptr && moe::decode_supported(L)))
+        return fail(L, MOE_ERR_UNSUPPORTED, "the layer has no whole-layer decode kernel");
     L->stall_next_decode = 1;
+    return MOE_OK;
+}
+
+moe_status moe_set_decode_kernel(moe_layer* L, int kind) {
+    if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
+    if (kind < 0 || kind > 2) return fail(L, MOE_ERR_INVALID_ARG, "kind must be 0, 1 or 2");
+    if (kind == 1 && !moe::gemv::supported(L))
+        return fail(L, MOE_ERR_UNSUPPORTED, "the layer's shape has no CUDA-core decode kernel");
+    if (kind == 2 && !(L->tc != nullptr && moe::decode_supported(L)))
+        return fail(L, MOE_ERR_UNSUPPORTED, "the layer's shape has no tcgen05 decode kernel");
+    L->decode_kernel = kind;
+    return MOE_OK;
+}
+
+moe_status moe_decode_info(const moe_layer* L, int* kind) {
+    if (!L || !kind) return fail(nullptr, MOE_ERR_INVALID_ARG, "NULL pointer");
+    *kind = decode_kind(L);
     return MOE_OK;
 }
 
@@ -480,14 +521,15 @@ moe_status moe_forward_host(moe_layer* L, const uint16_t* x, const float* logits
     // one token on the one-kernel decode path with page-locked buffers: the
     // kernel reads x and the logits and writes out in host memory directly
     // (mapped), so no copy is enqueued at all
-    if (L->gemm_path == 0 && L->tc != nullptr && T == 1 && moe::decode_supported(L)) {
+    const int dk = T == 1 ? decode_kind(L) : 0;
+    if (dk) {
         const void *dx = nullptr, *dl = nullptr, *dout = nullptr;
         if (mapped_host(x, &dx) && mapped_host(logits, &dl) && mapped_host(out, &dout) && aligned(dx, 16) &&
             aligned(dout, 16)) {
             L->stage_ev_set = 0;
-            cudaError_t e = moe::launch_decode(L, static_cast<const float*>(dl), static_cast<const uint16_t*>(dx),
-                                               L->ids_stage, L->w_stage, static_cast<float*>(const_cast<void*>(dout)),
-                                               s, true);
+            cudaError_t e = launch_decode_kind(L, dk, static_cast<const float*>(dl),
+                                               static_cast<const uint16_t*>(dx), L->ids_stage, L->w_stage,
+                                               static_cast<float*>(const_cast<void*>(dout)), s, true);
             L->trace = nullptr;
             return e == cudaSuccess ? MOE_OK : cuda_fail(L, e, "moe_forward_host");
         }

@@ -157,10 +157,10 @@ __global__ void __launch_bounds__(kCCThreads) k_gemm_cc(CCArgs a) {
                     }
                 }
             }
-#pragma unroll
             // kind 2: the matrix scales multiply the finished dot products
             const float g1 = kWKind == 2 ? __ldg(a.w1_g + e) : 1.f;
             const float g2 = (kWKind == 2 && kGateUp) ? __ldg(a.w2_g + e) : 1.f;
+#pragma unroll
             for (int n = 0; n < kChunk; ++n) {
                 const float g = warp_sum(acc1[n]) * g1;
                 if (kGateUp) {

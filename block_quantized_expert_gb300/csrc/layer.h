@@ -65,6 +65,13 @@ struct moe_layer {
     int32_t* sk_counters; // [4][num_sms] arrival counters of split tiles (zeroed per forward)
     float* sk_partials;   // [num_sms][2][2][128][128] partial accumulators of split tiles
     unsigned long long* dec_yw;  // [128 tiles][256] decode down outputs: launch epoch << 32 | fp32 bits
+    // the CUDA-core decode kernel: its words (the staged-x flag, the h-block
+    // flags [8][I/32], the CTAs' launch counts), its shared memory and work
+    // bounds (gv_smem 0: the kernel is not available)
+    uint32_t* gv_words;
+    int32_t* gv_rows;  // its down-row cuts: [k][num_sms + 1] for each kept count 1 .. k
+    int gv_smem, gv_nbmax, gv_dmax;
+    int decode_kernel;  // one-token calls: 0 automatic, 1 the CUDA-core kernel, 2 the tcgen05 kernel
 
     void* tc;             // tensor-core kernel state (tensor maps), or null
     unsigned long long launches;  // kernels enqueued so far
@@ -97,6 +104,16 @@ inline int kSkZeroed(const moe_layer* L) { return 4 * L->num_sms + 32; }
 // the staged-x flag (+ spare)
 inline int kDecWords(const moe_layer* L) { return 2 + 8 * L->num_sms + 128 + 32; }
 inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L); }
+
+// 32-bit words of the CUDA-core decode kernel, zeroed at creation: spare
+// [0, 2), staged-x flag [2], spare [3], the CTAs' launch counts [num_sms] from
+// kGvCountOff, then (8-byte aligned) the published h: [8 kept experts][I/32
+// blocks][9] 64-bit epoch-tagged words
+constexpr int kGvCountOff = 4;
+inline size_t gv_hword_off(int num_sms) { return ((size_t)kGvCountOff + num_sms + 1) / 2 * 2; }
+inline size_t gv_words_count(const moe_config& c, int num_sms) {
+    return gv_hword_off(num_sms) + (size_t)2 * 8 * (c.inter / 32) * 9;
+}
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
 // stream; the kernels synchronise on it with pdl_wait().
@@ -152,6 +169,14 @@ bool decode_supported(const moe_layer* L);
 cudaError_t launch_decode(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w,
                           float* out, cudaStream_t s, bool x_in_host = false);
 void tc_free(moe_layer* L);
+
+// The one-token layer as a split-K GEMV on the CUDA cores (decode_gemv.cu).
+namespace gemv {
+cudaError_t init(moe_layer* L);      // sets gv_smem / gv_nbmax / gv_dmax (0: not available)
+bool supported(const moe_layer* L);  // shape, weight format, no shared expert, init succeeded
+cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w, float* out,
+                   cudaStream_t s, bool x_in_host);
+}  // namespace gemv
 // cmb_ids != null: fuse the combine into the down GEMM (out = sum over the
 // token's experts in ascending order of w * y); requires no shared expert.
 cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid, const int32_t* cmb_ids,

@@ -223,7 +223,12 @@ moe_status moe_set_stage_events(moe_layer* layer, void* const* events, int n);
  * data, MMA ns waiting for the accumulator, epilogue ns waiting for the
  * accumulator, epilogue ns working, K-stages issued, ns when the wait for the
  * previous kernel ended]; the one-CTA front kernel of small batches writes
- * [entry, wait end, exit] at buf + 4 * num_sms * 12.  entries >= 4 * num_sms
+ * [entry, wait end, exit] at buf + 4 * num_sms * 12; the CUDA-core decode
+ * kernel writes per CTA [entry, -, publisher done, first h gathered, first
+ * copy issued, final barrier] ns at buf + 8 * cta and, for CTAs 0, 1, 80 and
+ * num_sms - 1 (t = 0 .. 3), event times at buf + 8 * num_sms + 256 * t + i
+ * (i = 128 + stage: copy issued; 192 + j, 200 + j: h block j computed,
+ * published; 208 + s: kept expert s's h gathered).  entries >= 4 * num_sms
  * * 12 + 4.  One-shot, like moe_set_stage_events.                        */
 moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entries);
 
@@ -239,6 +244,28 @@ unsigned long long moe_kernel_launches(const moe_layer* layer);
  * kernels only (never the decode kernel).  All compute the same layer; the
  * choice only affects speed and the order of fp32 additions.               */
 moe_status moe_set_gemm_path(moe_layer* layer, int path);
+
+/* Which whole-layer kernel a one-token call on the automatic GEMM path
+ * (moe_route_forward / moe_forward_host with T = 1) takes.  kind 0 =
+ * automatic: the CUDA-core split-K GEMV kernel where the shape allows it
+ * (MXFP4 experts, H and I multiples of 1024 with H / 1024 and I / 1024
+ * dividing 16, H >= 2048, I <= 4096, no shared expert), else the tcgen05
+ * kernel (H <=
+ * 4096, I <= 2048, no shared expert), else the grouped kernels; 1 = the
+ * CUDA-core kernel; 2 = the tcgen05 kernel.  Both compute the layer for a
+ * single decode token (guide, section 2.A: one token, the MUL_MAT_ID of its
+ * top-k experts), with the combine in ascending expert order; they differ
+ * only in the order of fp32 additions.
+ * MOE_ERR_UNSUPPORTED if the layer's shape has no such kernel,
+ * MOE_ERR_INVALID_ARG for another kind; the setting is then unchanged.
+ * Not part of the method: a switch for benchmarks and tests.             */
+moe_status moe_set_decode_kernel(moe_layer* layer, int kind);
+
+/* The whole-layer kernel a one-token call of this layer takes with its
+ * current settings: *kind = 0 none (the grouped kernels), 1 the CUDA-core
+ * GEMV kernel, 2 the tcgen05 kernel (the codes of moe_set_decode_kernel).
+ * A diagnostic for benchmarks and tests.                                  */
+moe_status moe_decode_info(const moe_layer* layer, int* kind);
 
 /* Tail pruning of the learned router (guide, section 3.2 item 3: top-k
  * below the layer's k and the adaptive tail, with L2-quadrature rescaling;

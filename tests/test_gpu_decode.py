@@ -1,7 +1,10 @@
-"""The whole-layer decode kernel (one token through moe_route_forward on the
+"""The whole-layer decode kernels (one token through moe_route_forward on the
 automatic path: route, quantise, gate/up, down and combine in one
 cooperative launch) against the fp64 oracle and against the grouped
-tensor-core kernels, eagerly and replayed from a CUDA graph."""
+tensor-core kernels, eagerly and replayed from a CUDA graph.  The decode
+shape runs every test on both kernels: the CUDA-core split-K GEMV (kind 1,
+the automatic choice) and the tcgen05 kernel (kind 2); the tiny shape has
+only the tcgen05 one."""
 import numpy as np
 import pytest
 import torch
@@ -15,10 +18,20 @@ pytestmark = pytest.mark.gpu
 
 
 @pytest.fixture(scope="module")
-def decode_layer():
+def decode_layer_base():
     cfg = CONFIGS[1]
     w = G.weights_np(1)
     return cfg, w, G.make_layer(cfg, w, max_tokens=64)
+
+
+@pytest.fixture(params=[1, 2], ids=["gemv", "tcgen05"])
+def decode_layer(request, decode_layer_base):
+    cfg, w, layer = decode_layer_base
+    bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_decode_kernel(layer, request.param)
+    assert bqe.moe_decode_info(layer) == request.param
+    yield cfg, w, layer
+    bqe.moe_set_decode_kernel(layer, 0)
 
 
 @pytest.fixture(scope="module")
@@ -211,3 +224,48 @@ def test_two_layers_interleaved_in_one_graph(decode_layer, tiny_layer):
         torch.cuda.synchronize()
         assert torch.equal(ids, ids1) and torch.equal(w, w1)
         assert out.cpu().numpy().tobytes() == out1.cpu().numpy().tobytes()
+
+
+def test_decode_kernel_choice(decode_layer_base, tiny_layer):
+    """The automatic choice: the CUDA-core kernel where its shape rules allow
+    (H, I multiples of 1024), else the tcgen05 kernel; an explicit choice the
+    shape does not allow is refused and leaves the setting unchanged."""
+    _, _, layer = decode_layer_base
+    _, _, tiny = tiny_layer
+    bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_gemm_path(tiny, 0)
+    assert bqe.moe_decode_info(layer) == 1
+    assert bqe.moe_decode_info(tiny) == 2
+    with pytest.raises(bqe.MoeError) as ei:
+        bqe.moe_set_decode_kernel(tiny, 1)
+    assert ei.value.status == bqe.MOE_ERR_UNSUPPORTED
+    assert bqe.moe_decode_info(tiny) == 2
+    for bad in (-1, 3):
+        with pytest.raises(bqe.MoeError) as ei:
+            bqe.moe_set_decode_kernel(layer, bad)
+        assert ei.value.status == bqe.MOE_ERR_INVALID_ARG
+    bqe.moe_set_gemm_path(layer, 2)   # the tcgen05-only GEMM path has no decode kernel
+    assert bqe.moe_decode_info(layer) == 0
+    bqe.moe_set_gemm_path(layer, 0)
+
+
+def test_decode_kernels_agree(decode_layer_base):
+    """The two decode kernels on the same tokens: the same routing bit for bit,
+    outputs within the oracle tolerance of each other, and the CUDA-core
+    kernel's output repeatable bit for bit (fixed reduction order)."""
+    cfg, _, layer = decode_layer_base
+    bqe.moe_set_gemm_path(layer, 0)
+    tk = G.tokens(1, n=6)
+    for t in range(6):
+        res = {}
+        for kind in (1, 2):
+            bqe.moe_set_decode_kernel(layer, kind)
+            res[kind] = _route_forward(layer, tk.logits[t:t + 1], tk.x_bits[t:t + 1], 0)
+        bqe.moe_set_decode_kernel(layer, 1)
+        again = _route_forward(layer, tk.logits[t:t + 1], tk.x_bits[t:t + 1], 0)
+        bqe.moe_set_decode_kernel(layer, 0)
+        (i1, w1, o1, _), (i2, w2, o2, _) = res[1], res[2]
+        assert torch.equal(i1, i2) and torch.equal(w1, w2)
+        a, b = o1.cpu().numpy().astype(np.float64), o2.cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(a - b) <= G.NORM_TOL * np.linalg.norm(b)
+        assert o1.cpu().numpy().tobytes() == again[2].cpu().numpy().tobytes()

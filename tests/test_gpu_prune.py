@@ -117,10 +117,12 @@ def test_layer_with_pruned_routing(decode_layer, path, T):
     bqe.moe_set_gemm_path(layer, 0)
 
 
-def test_decode_kernel_pruned_equals_grouped(decode_layer):
-    """The decode kernel and the grouped tcgen05 kernels choose the same
+@pytest.mark.parametrize("kind", [1, 2], ids=["gemv", "tcgen05"])
+def test_decode_kernel_pruned_equals_grouped(decode_layer, kind):
+    """Each decode kernel and the grouped tcgen05 kernels choose the same
     experts and weights bit for bit under pruning."""
     cfg, wts, layer = decode_layer
+    bqe.moe_set_decode_kernel(layer, kind)
     tk = G.tokens(1, n=6)
     for setting in SETTINGS:
         bqe.moe_set_route_prune(layer, *setting)
@@ -140,6 +142,7 @@ def test_decode_kernel_pruned_equals_grouped(decode_layer):
             assert np.linalg.norm(o1 - o2) <= G.NORM_TOL * np.linalg.norm(o2)
     bqe.moe_set_route_prune(layer, cfg.k)
     bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_decode_kernel(layer, 0)
 
 
 def test_hash_route_is_never_pruned(decode_layer):
@@ -166,12 +169,14 @@ def test_prune_setter_validates(decode_layer):
     bqe.moe_set_route_prune(layer, 99)  # more than k: no count limit
 
 
-def test_decode_graph_replay_with_varying_kept_counts(decode_layer):
-    """The decode kernel replayed from one CUDA graph over tokens whose kept
-    expert counts differ (an adaptive threshold): the stream-K split changes
+@pytest.mark.parametrize("kind", [1, 2], ids=["gemv", "tcgen05"])
+def test_decode_graph_replay_with_varying_kept_counts(decode_layer, kind):
+    """Each decode kernel replayed from one CUDA graph over tokens whose kept
+    expert counts differ (an adaptive threshold): the work split changes
     from launch to launch, and every replay gives the bytes of the eager call."""
     cfg, _, layer = decode_layer
     bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_decode_kernel(layer, kind)
     bqe.moe_set_route_prune(layer, 6, 0.245, 0.0)
     tk = G.tokens(1, n=8)
     ids0, w0 = orc.route_learned(tk.logits, cfg.k, cfg.w_scale)
@@ -206,3 +211,4 @@ def test_decode_graph_replay_with_varying_kept_counts(decode_layer):
             assert out.cpu().numpy().tobytes() == out_e.cpu().numpy().tobytes()
     finally:
         bqe.moe_set_route_prune(layer, cfg.k)
+        bqe.moe_set_decode_kernel(layer, 0)

@@ -4,7 +4,8 @@ that no CTA ever writes (plain global-memory flags; no hardware barrier is
 given a wrong count), with the wait limit set to a few milliseconds.  Every
 CTA's wait then runs out, the kernel frees its tensor memory and exits, the
 call reports MOE_ERR_TIMEOUT through moe_check, and the next calls on the
-same layer and context are correct again."""
+same layer and context are correct again.  Both whole-layer decode kernels
+(the CUDA-core GEMV and the tcgen05 one) take the hook."""
 import time
 
 import numpy as np
@@ -53,9 +54,11 @@ def test_wait_limit_arguments(decode_layer):
     bqe.moe_set_wait_limit(layer, 2.0)
 
 
-def test_stalled_decode_times_out_and_layer_recovers(decode_layer):
+@pytest.mark.parametrize("kind", [1, 2], ids=["gemv", "tcgen05"])
+def test_stalled_decode_times_out_and_layer_recovers(decode_layer, kind):
     cfg, wts, layer = decode_layer
     bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_decode_kernel(layer, kind)
     tk = G.tokens(1, n=4)
     ids, _, out = _call(layer, tk, 0)       # a normal call first
     bqe.moe_check(layer)
@@ -88,3 +91,4 @@ def test_stalled_decode_times_out_and_layer_recovers(decode_layer):
     bqe.moe_check(layer)
     _check_oracle(cfg, wts, tk, 1, ids, out)
     bqe.moe_set_gemm_path(layer, 0)
+    bqe.moe_set_decode_kernel(layer, 0)
