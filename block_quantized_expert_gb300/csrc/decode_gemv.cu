@@ -84,11 +84,15 @@ constexpr int kStageBytes = kStageCodes + kStageScales;
 constexpr int kStages = 5;
 constexpr int kMaxK = kMaxTopK;
 constexpr int kMaxI = 4096;                   // h of every kept expert resident as f16
-// A published h block (32 features): 8 words of 4 e4m3 codes and one word of
-// its scale byte, each 64-bit word tagged with the launch's epoch in its upper
-// half (single-copy atomic: a reader that sees the epoch sees the payload).
-constexpr int kHWords = 9;
-constexpr int kGatherWords = 9;              // words a gather lane has in flight
+// A published h block (32 features): 6 64-bit words, word w holding e4m3 codes
+// 6w .. 6w + 5 in bytes 0 .. 5 (the last word: codes 30, 31 and the block's
+// scale byte in byte 2) and the low 8 bits of the launch's epoch in byte 7
+// (a single-copy atomic store: a reader that sees the tag sees the payload).
+// Every launch writes every block of the k kept positions -- published, or
+// (positions >= m) overwritten with a payload no reader uses -- so a word
+// older than the launch carries the previous launch's tag, never this one's.
+constexpr int kHWords = 6;
+constexpr int kGatherWords = 12;             // words a gather lane has in flight
 
 struct Args {
     const float* logits;  // [E]
@@ -149,7 +153,7 @@ __host__ __device__ inline Split down_rows(int c, int G, int m, int H, int I) {
 
 // Shared-memory layout (bytes), the same on the host and the device.
 struct Layout {
-    int ring, route, lg, bars, pgu, pdn, h16, hsc, total;
+    int ring, route, lg, bars, pgu, pdn, hraw, total;
     __host__ __device__ Layout(int H, int I, int nbmax, int dmax) {
         const int NQ = H / kSeg, NQd = I / kSeg;
         ring = 0;                                     // [kStages][kStageBytes]
@@ -158,9 +162,8 @@ struct Layout {
         bars = lg + 4096 + 2048;  // full [kStages], empty [kStages], blk [nbmax], h_ready [kMaxK]
         pgu = bars + ((8 * (2 * kStages + nbmax + kMaxK) + 15) / 16) * 16;  // [nbmax][NQ][64] f32
         pdn = pgu + nbmax * NQ * 64 * 4;              // [kMaxK][NQd][dmax] f32
-        h16 = pdn + ((kMaxK * NQd * dmax * 4 + 15) / 16) * 16;  // [kMaxK][I] f16 values of h's codes
-        hsc = h16 + kMaxK * I * 2;                    // [kMaxK][I/32] u8
-        total = hsc + kMaxK * (I / 32);
+        hraw = pdn + ((kMaxK * NQd * dmax * 4 + 15) / 16) * 16;  // [kMaxK][I/32][kHWords] h words as published
+        total = hraw + kMaxK * (I / 32) * kHWords * 8;
     }
 };
 // words of the route area
@@ -245,8 +248,8 @@ __device__ __forceinline__ uint32_t flag_get(const uint32_t* f) {
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(f) : "memory");
     return v;
 }
-__device__ __forceinline__ void st_tagged(unsigned long long* p, uint32_t payload, uint32_t epoch) {
-    const unsigned long long v = ((unsigned long long)epoch << 32) | payload;
+__device__ __forceinline__ void st_tagged(unsigned long long* p, unsigned long long payload, uint32_t epoch) {
+    const unsigned long long v = ((unsigned long long)(epoch & 0xFFu) << 56) | payload;
     asm volatile("st.relaxed.gpu.global.b64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
 }
 __device__ __forceinline__ unsigned long long ld_tagged(const unsigned long long* p) {
@@ -348,11 +351,16 @@ __device__ void publish_block(const Args& a, const float* pgu, int j, int b, int
     const float h = silu_mul(g, u);
     const int ex = mxfp8_exponent(warp_max(fabsf(h)));
     const uint32_t code = f32x2_to_e4m3x2(scale_pow2(h, ex), 0.f) & 0xFFu;
-    const uint32_t c1 = __shfl_down_sync(0xFFFFFFFFu, code, 1), c2 = __shfl_down_sync(0xFFFFFFFFu, code, 2),
-                   c3 = __shfl_down_sync(0xFFFFFFFFu, code, 3);
+    // lane 6w collects codes 6w .. 6w + 5 (lane 30: codes 30, 31 and the scale)
+    unsigned long long word = code;
+#pragma unroll
+    for (int i = 1; i < 6; ++i) {
+        const unsigned long long ci = __shfl_down_sync(0xFFFFFFFFu, code, i);
+        if (lane + i < 32) word |= ci << (8 * i);
+    }
+    if (lane == 30) word |= (unsigned long long)(ex + 127) << 16;
     unsigned long long* dst = a.hw + ((size_t)s * FB + fb) * kHWords;
-    if ((lane & 3) == 0) st_tagged(dst + (lane >> 2), code | (c1 << 8) | (c2 << 16) | (c3 << 24), epoch);
-    if (lane == 0) st_tagged(dst + 8, (uint32_t)(ex + 127), epoch);
+    if (lane % 6 == 0 && lane <= 30) st_tagged(dst + lane / 6, word, epoch);
 }
 
 // 20 warps: 16 compute warps, the producer, the publisher and two gatherers
@@ -373,8 +381,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
     const uint32_t blk0 = empty0 + 8u * kStages, hrdy0 = blk0 + 8u * a.nbmax;
     float* pgu = reinterpret_cast<float*>(smem + Lo.pgu);
     float* pdn = reinterpret_cast<float*>(smem + Lo.pdn);
-    uint16_t* h16 = reinterpret_cast<uint16_t*>(smem + Lo.h16);
-    uint8_t* hsc = smem + Lo.hsc;
+    unsigned long long* hraw = reinterpret_cast<unsigned long long*>(smem + Lo.hraw);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int NQ = a.H / kSeg, NQd = a.I / kSeg, FB = a.I / 32;
@@ -572,6 +579,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         __syncthreads();  // (the routing weights)
     }
     const int m = words[W_M];
+    if (warp == kService) {
+        // blocks of the kept positions m .. k - 1 (round-robin like the
+        // published ones): their words get this launch's tag, so that no word
+        // is ever more than one launch old
+        const unsigned long long inval = 0;
+        for (int b = m * FB + ((c - m * FB) % G + G) % G; b < a.k * FB; b += G)
+            if (lane < kHWords) st_tagged(a.hw + (size_t)b * kHWords + lane, inval, epoch);
+    }
     if (m == 0) {
         // no valid routing (ERR_BAD_ID is raised): the output is zero
         for (int i = c * kThreads + threadIdx.x; i < a.H; i += G * kThreads) a.out[i] = 0.f;
@@ -603,55 +618,61 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         if (lane == 0) stamp(a, 2);
     } else if (warp == kGather || warp == kGather + 1) {
         // ------------------------------------------------------ gatherers
-        // every kept expert's h, in order: its tagged words (gatherer gi the
-        // words [lo, hi), each lane lo + lane, lo + lane + 32, ..; the stale
-        // ones re-read until all carry this launch's epoch), the codes as f16
-        // and the scale bytes into shared memory; every lane arrives on the
-        // expert's barrier (also when a wait ran out, so that no compute warp
-        // waits on)
-        const uint32_t want = a.stall_h ? (epoch ^ 0x80000000u) : epoch;  // (stall_h: a value no CTA writes)
-        const int nw = FB * kHWords, half = (nw + 63) / 64 * 32;
-        const int lo = (warp - kGather) * half, hi = min(nw, lo + half);
+        // the kept experts' h, P experts a pass: the pass's words (positions
+        // s0 .. s0 + np - 1, contiguous) are read by gatherer gi as words
+        // (2 k2 + gi) 32 + lane, k2 < kGatherWords; the stale ones are re-read
+        // until all carry this launch's tag, and go to shared memory as they
+        // are (the compute warps unpack their blocks).  A lane arrives on an expert's
+        // barrier once its words of that expert are in (its k2 in
+        // [klo(e), klo(e + 1))); every lane arrives for every expert, also when
+        // a wait ran out, so that no compute warp waits on.
+        const uint32_t want = a.stall_h ? 0x100u : (epoch & 0xFFu);  // (stall_h: a tag no CTA writes)
+        const int gi = warp - kGather, nwe = FB * kHWords;
+        const int P = max(1, 64 * kGatherWords / nwe);  // (nwe <= 64 kGatherWords: I <= kMaxI)
+        auto klo = [&](int e) { return min(kGatherWords, max(0, (e * nwe - 32 * gi - lane + 63) / 64)); };
         bool ok = true;
-        for (int s = 0; s < m; ++s) {
-            const unsigned long long* src = a.hw + (size_t)s * nw;
+        for (int s0 = 0; s0 < m; s0 += P) {
+            const int np = min(P, m - s0), nf = np * nwe;
+            const unsigned long long* src = a.hw + (size_t)s0 * nwe;
+            unsigned long long* dst = hraw + (size_t)s0 * nwe;
+            uint32_t todo = 0, left = (1u << np) - 1u;
+#pragma unroll
+            for (int k2 = 0; k2 < kGatherWords; ++k2)
+                if ((2 * k2 + gi) * 32 + lane < nf) todo |= 1u << k2;
             const uint64_t t0 = globaltimer();
-            for (int base = lo; ok && base < hi; base += 32 * kGatherWords) {
-                uint32_t todo = 0;
-#pragma unroll
-                for (int k2 = 0; k2 < kGatherWords; ++k2)
-                    if (base + 32 * k2 + lane < hi) todo |= 1u << k2;
-                while (todo) {
-                    unsigned long long v[kGatherWords];
-#pragma unroll
-                    for (int k2 = 0; k2 < kGatherWords; ++k2)
-                        if ((todo >> k2) & 1u) v[k2] = ld_tagged(src + base + 32 * k2 + lane);
-#pragma unroll
-                    for (int k2 = 0; k2 < kGatherWords; ++k2) {
-                        if (((todo >> k2) & 1u) && (uint32_t)(v[k2] >> 32) == want) {
-                            const int wi = base + 32 * k2 + lane, fb = wi / kHWords, w = wi - fb * kHWords;
-                            const uint32_t pl = (uint32_t)v[k2];
-                            if (w < 8)
-                                *reinterpret_cast<uint2*>(h16 + (size_t)s * a.I + 32 * fb + 4 * w) =
-                                    make_uint2(e4m3x2_to_f16x2(pl), e4m3x2_to_f16x2(pl >> 16));
-                            else
-                                hsc[s * FB + fb] = (uint8_t)pl;
-                            todo &= ~(1u << k2);
+            while (true) {
+                for (int e = 0; e < np; ++e) {
+                    const uint32_t em = (1u << klo(e + 1)) - (1u << klo(e));
+                    if (((left >> e) & 1u) && (!ok || !(todo & em))) {
+                        mbar_arrive(hrdy0 + 8u * (s0 + e));
+                        left &= ~(1u << e);
+                        if (lane == 0 && gi == 0) {
+                            trace_event(a, 208 + s0 + e);
+                            if (s0 + e == 0) stamp(a, 3);
                         }
                     }
-                    if (todo && (globaltimer() - t0 > a.wait_ns || *abort_flag)) ok = false;
-                    if (!ok) break;
                 }
+                if (!todo || !ok) break;
+                unsigned long long v[kGatherWords];
+#pragma unroll
+                for (int k2 = 0; k2 < kGatherWords; ++k2)
+                    if ((todo >> k2) & 1u) v[k2] = ld_tagged(src + (2 * k2 + gi) * 32 + lane);
+#pragma unroll
+                for (int k2 = 0; k2 < kGatherWords; ++k2) {
+                    if (((todo >> k2) & 1u) && (uint32_t)(v[k2] >> 56) == want) {
+                        dst[(2 * k2 + gi) * 32 + lane] = v[k2];
+                        todo &= ~(1u << k2);
+                    }
+                }
+                if (todo && (globaltimer() - t0 > a.wait_ns || *abort_flag)) ok = false;
             }
-            ok = __all_sync(0xFFFFFFFFu, ok);
-            if (!ok && lane == 0) {
-                *abort_flag = 1;
-                raise_flag(a.err, ERR_TIMEOUT);
-            }
-            mbar_arrive(hrdy0 + 8u * s);
-            if (lane == 0 && warp == kGather) {
-                trace_event(a, 208 + s);
-                if (s == 0) stamp(a, 3);
+            if (!ok) {
+                if (lane == 0) {
+                    *abort_flag = 1;
+                    raise_flag(a.err, ERR_TIMEOUT);
+                }
+                for (int sp = s0 + np; sp < m; ++sp) mbar_arrive(hrdy0 + 8u * sp);
+                break;
             }
         }
     } else if (warp < kComputeWarps) {
@@ -729,16 +750,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                             ok = false;
                             break;
                         }
-                        const uint4* hp = reinterpret_cast<const uint4*>(h16 + (size_t)s * a.I + qh * kSeg + 32 * lane);
+                        // this lane's block of h (qh 32 + lane): its 6 words,
+                        // the codes as f16 pairs, the scale from the last word
+                        const unsigned long long* hp = hraw + ((size_t)s * FB + qh * 32 + lane) * kHWords;
 #pragma unroll
-                        for (int k2 = 0; k2 < 4; ++k2) {
-                            const uint4 hv = hp[k2];
-                            op[4 * k2] = hv.x;
-                            op[4 * k2 + 1] = hv.y;
-                            op[4 * k2 + 2] = hv.z;
-                            op[4 * k2 + 3] = hv.w;
+                        for (int w = 0; w < 5; ++w) {
+                            const unsigned long long hv = hp[w];
+                            op[3 * w] = e4m3x2_to_f16x2((uint32_t)hv);
+                            op[3 * w + 1] = e4m3x2_to_f16x2((uint32_t)(hv >> 16));
+                            op[3 * w + 2] = e4m3x2_to_f16x2((uint32_t)(hv >> 32));
                         }
-                        opsf = ue8m0_to_f32(hsc[s * FB + qh * 32 + lane]);
+                        const unsigned long long h5 = hp[5];
+                        op[15] = e4m3x2_to_f16x2((uint32_t)h5);
+                        opsf = ue8m0_to_f32((uint32_t)(h5 >> 16) & 0xFFu);
                         cur = s;
                     }
                 }

@@ -108,11 +108,11 @@ inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L);
 // 32-bit words of the CUDA-core decode kernel, zeroed at creation: spare
 // [0, 2), staged-x flag [2], spare [3], the CTAs' launch counts [num_sms] from
 // kGvCountOff, then (8-byte aligned) the published h: [8 kept experts][I/32
-// blocks][9] 64-bit epoch-tagged words
+// blocks][6] 64-bit tagged words
 constexpr int kGvCountOff = 4;
 inline size_t gv_hword_off(int num_sms) { return ((size_t)kGvCountOff + num_sms + 1) / 2 * 2; }
 inline size_t gv_words_count(const moe_config& c, int num_sms) {
-    return gv_hword_off(num_sms) + (size_t)2 * 8 * (c.inter / 32) * 9;
+    return gv_hword_off(num_sms) + (size_t)2 * 8 * (c.inter / 32) * 6;
 }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
