@@ -436,14 +436,19 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             cv[chk * a.k + r] = v;
         }
     }
-    // (compute warps) the token's segment qx as f16 (MXFP8: its 32-block's
-    // scale, e4m3 codes), one 32-block per lane, from a device x (a host x
-    // is staged by CTA 0 after the routing)
+    // (padding) the candidate slots up to a multiple of 4 are empty
+    if (threadIdx.x < (-nc & 3)) {
+        ci[nc + threadIdx.x] = -1;
+        cv[nc + threadIdx.x] = __int_as_float(0x7FC00000);
+    }
+    // (compute warps) the token's segment qx, one 32-block per lane, from a
+    // device x: loaded now, quantised once the copies are issued (a host x is
+    // staged by CTA 0 after the routing)
     uint32_t op[16];
     float opsf = 0.f;
+    uint32_t xw[16];
     if (warp < kComputeWarps && !a.x_stage) {
         const uint4* xp = reinterpret_cast<const uint4*>(a.x + qx * kSeg + 32 * lane);
-        uint32_t xw[16];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint4 v = __ldg(xp + i);
@@ -452,18 +457,23 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             xw[4 * i + 2] = v.z;
             xw[4 * i + 3] = v.w;
         }
-        quantize_token(xw, op, opsf);
     }
     __syncthreads();
-    // second round: thread t ranks candidate t among all candidates
+    // second round: thread t ranks candidate t among all candidates (four at
+    // a time; empty slots hold NaN: never counted)
     for (int t = threadIdx.x; t < nc; t += kThreads) {
         const int e = ci[t];
         if (e < 0) continue;
         const float v = cv[t];
         int r = 0;
-        for (int t2 = 0; t2 < nc; ++t2) {  // empty slots hold NaN: never counted
-            const float u = cv[t2];
-            r += (int)(u > v) | ((int)(u == v) & (int)(ci[t2] < e));
+#pragma unroll 4
+        for (int t2 = 0; t2 < nc; t2 += 4) {
+            const float4 u = *reinterpret_cast<const float4*>(cv + t2);
+            const int4 ie = *reinterpret_cast<const int4*>(ci + t2);
+            r += (int)(u.x > v) | ((int)(u.x == v) & (int)(ie.x < e));
+            r += (int)(u.y > v) | ((int)(u.y == v) & (int)(ie.y < e));
+            r += (int)(u.z > v) | ((int)(u.z == v) & (int)(ie.z < e));
+            r += (int)(u.w > v) | ((int)(u.w == v) & (int)(ie.w < e));
         }
         if (r < a.k) sel[r] = e;
     }
@@ -524,6 +534,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         }
         __syncwarp();
     } else {
+        if (warp < kComputeWarps && !a.x_stage) quantize_token(xw, op, opsf);
         if (warp == kService) {
             // the routing weights (the arithmetic of route_token: w_j =
             // w_scale * s_j / (s_0 + .. + s_{k-1}), s = sqrt(softplus(logit)),
