@@ -508,25 +508,36 @@ def per_config(args, bqe, dev, peaks):
             wl.step(i)
         bqe.moe_check(layer)
         stream = torch.cuda.Stream(device=dev)
+        launches0 = bqe.moe_kernel_launches(layer)
         graphs = capture(wl.step, W, K, K, stream)
+        launches = bqe.moe_kernel_launches(layer) - launches0
         (ms, _, w0, w1), clocks = clocked(lambda: timed_replay(graphs, K, K, stream, dev, 1))
         del graphs
         mma_peak = None
         if cfg.index == 4:
             mma_peak = pk.mma_mx_tflops(iters=60000, reps=3)
-        stage_ms = stage_times(bqe, layer, wl.step, W + K, min(K, 16), stream)
-        bqe.moe_check(layer)
         byts = algorithmic_bytes(cfg, avg_touched, rows)
-        dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
-        roof = roofline(cfg, dom, stage_ms[dom], byts, rows, peaks, mma_peak)
-        roof["kernel"] = f"{dom} GEMM ({'k_gemm_cc, CUDA cores' if cfg.wfmt == 'nvfp4' else 'k_gemm_tc'})"
+        if launches == K:
+            # one whole-layer decode kernel per step: its average duration is the
+            # timed region over the K steps
+            stage_ms = None
+            byts["layer"] = byts["gateup"] + byts["down"]
+            roof = roofline(cfg, "layer", ms / K, byts, rows, peaks, mma_peak)
+            roof["kernel"] = DECODE_KERNELS[bqe.moe_decode_info(layer)]
+        else:
+            stage_ms = stage_times(bqe, layer, wl.step, W + K, min(K, 16), stream)
+            dom = max(("gateup", "down"), key=lambda n: stage_ms[n])
+            roof = roofline(cfg, dom, stage_ms[dom], byts, rows, peaks, mma_peak)
+            roof["kernel"] = f"{dom} GEMM ({'k_gemm_cc, CUDA cores' if cfg.wfmt == 'nvfp4' else 'k_gemm_tc'})"
+        bqe.moe_check(layer)
         recs.append({"workload": cfg.name if router is None else f"{cfg.name.rsplit('_', 1)[0]}_{router}",
                      "tokens_per_step": cfg.T, "router": router or cfg.router, "shared_expert": cfg.shared,
-                     "weights": "NVFP4-style e2m1 + e4m3 /16 + fp32 per matrix (CUDA-core GEMMs)"
+                     "weights": "NVFP4-style e2m1 + e4m3 /16 + fp32 per matrix (CUDA cores)"
                      if cfg.wfmt == "nvfp4" else "MXFP4 e2m1 + UE8M0 /32",
                      "value": job_rate(1, K * cfg.T, ms), "unit": UNIT, "steps": K, "warmup": W,
                      "ms_per_step": round(ms / K, 6), "experts_touched_per_step": avg_touched,
-                     "stage_ms_untimed_pass": {k: round(v, 5) for k, v in stage_ms.items()},
+                     **({"stage_ms_untimed_pass": {k: round(v, 5) for k, v in stage_ms.items()}} if stage_ms else {}),
+                     "gpu_launches": int(launches),
                      "roofline": roof, "clocks": clocks,
                      "l2": "weights of the touched experts larger than L2; 4 input batches cycled",
                      "wall_s": round(time.time() - t_start, 1)})

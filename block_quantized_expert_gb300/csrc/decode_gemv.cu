@@ -79,8 +79,10 @@ constexpr int kThreads = 32 * (kComputeWarps + 4);
 constexpr int kSeg = 1024;                    // K elements of one warp step (32 lanes x one 32-block)
 constexpr int kRun = 4;                       // consecutive rows of a compute warp in a stage
 constexpr int kStageCodes = 512 * kRun * kComputeWarps;  // bytes of codes per stage (32 KB)
-constexpr int kStageScales = kStageCodes / 16;           // the rows' scale bytes
-constexpr int kStageBytes = kStageCodes + kStageScales;
+// the rows' scale bytes of a stage: one per 32-block (MXFP4: UE8M0), two
+// (NVFP4: an e4m3 scale per 16 elements)
+__host__ __device__ constexpr int stage_scales(bool nv) { return kStageCodes / (nv ? 8 : 16); }
+__host__ __device__ constexpr int stage_bytes(bool nv) { return kStageCodes + stage_scales(nv); }
 constexpr int kStages = 5;
 constexpr int kMaxK = kMaxTopK;
 constexpr int kMaxI = 4096;                   // h of every kept expert resident as f16
@@ -104,10 +106,11 @@ struct Args {
     float* w_out;      // [k]
     float* out;        // [H]
     const uint8_t* gu_q;    // [E][I/128][gate 128 rows, up 128 rows][H/2]
-    const uint8_t* gate_s;  // [E][I][H/32]
-    const uint8_t* up_s;    // [E][I][H/32]
+    const uint8_t* gate_s;  // [E][I][H/32] (NVFP4: [E][I][H/16] e4m3)
+    const uint8_t* up_s;    // [E][I][H/32] (NVFP4: [E][I][H/16] e4m3)
     const uint8_t* down_q;  // [E][H][I/2]
-    const uint8_t* down_s;  // [E][H][I/32]
+    const uint8_t* down_s;  // [E][H][I/32] (NVFP4: [E][H][I/16] e4m3)
+    const float *gate_g, *up_g, *down_g;  // NVFP4: the per-expert matrix scales [E]
     unsigned long long* hw;  // [kMaxK][I/32][kHWords]: h by kept position, epoch-tagged words
     uint32_t* launches;     // [G]: launches CTA c has completed (its epoch - 1)
     uint16_t* x_stage;      // CTA 0's device copy of a host x, or null
@@ -154,10 +157,10 @@ __host__ __device__ inline Split down_rows(int c, int G, int m, int H, int I) {
 // Shared-memory layout (bytes), the same on the host and the device.
 struct Layout {
     int ring, route, lg, bars, pgu, pdn, hraw, total;
-    __host__ __device__ Layout(int H, int I, int nbmax, int dmax) {
+    __host__ __device__ Layout(int H, int I, int nbmax, int dmax, bool nv) {
         const int NQ = H / kSeg, NQd = I / kSeg;
-        ring = 0;                                     // [kStages][kStageBytes]
-        route = ring + kStages * kStageBytes;         // sel, w_t, seg_e, seg_w, prod_e [8] each; words [16]
+        ring = 0;                                     // [kStages][stage_bytes(nv)]
+        route = ring + kStages * stage_bytes(nv);     // sel, w_t, seg_e, seg_w, prod_e [8] each; words [16]
         lg = route + 256;                             // the logits [E <= 1024], candidates [256] x 2
         bars = lg + 4096 + 2048;  // full [kStages], empty [kStages], blk [nbmax], h_ready [kMaxK]
         pgu = bars + ((8 * (2 * kStages + nbmax + kMaxK) + 15) / 16) * 16;  // [nbmax][NQ][64] f32
@@ -195,8 +198,9 @@ __device__ __forceinline__ float dot2_f16_f32(uint32_t a, uint32_t b, float acc)
 }
 // The block's dot product: 16 bytes of e2m1 codes against op (f16x2 of the
 // block's 32 operand values, elements 2j, 2j + 1 in op[j]); four partial
-// sums over the block's four 8-element quarters, then (q0 + q1) + (q2 + q3).
-__device__ __forceinline__ float block_dot(const uint4& w, const uint32_t (&op)[16]) {
+// sums over the block's four 8-element quarters, returned as the two
+// 16-element halves' sums (q0 + q1, q2 + q3).
+__device__ __forceinline__ float2 block_dot_halves(const uint4& w, const uint32_t (&op)[16]) {
     const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
     float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -206,7 +210,23 @@ __device__ __forceinline__ float block_dot(const uint4& w, const uint32_t (&op)[
 #pragma unroll
         for (int j = 0; j < 4; ++j) acc[i] = dot2_f16_f32(h[j], op[4 * i + j], acc[i]);
     }
-    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+    return make_float2(acc[0] + acc[1], acc[2] + acc[3]);
+}
+// Two e4m3 scale bytes (the first in the low byte) -> fp32.
+__device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2((__nv_fp8x2_storage_t)(two & 0xFFFFu), __NV_E4M3);
+    return make_float2(__half2float(__half(__half_raw{h.x})), __half2float(__half(__half_raw{h.y})));
+}
+// A row's 32-block value times its weight scale(s): MXFP4 (one UE8M0 byte in
+// sv) (lo + hi) * 2^s; NVFP4 (two e4m3 bytes) lo * s0 + hi * s1.
+template <bool kNv>
+__device__ __forceinline__ float scaled_block(const uint4& w, const uint32_t (&op)[16], uint32_t sv) {
+    const float2 d = block_dot_halves(w, op);
+    if (kNv) {
+        const float2 sc = e4m3x2_to_f32x2(sv);
+        return fmaf(d.y, sc.y, d.x * sc.x);
+    }
+    return (d.x + d.y) * ue8m0_to_f32(sv);
 }
 // One lane's 32-block of the token (16 words of bf16 pairs) -> MXFP8 (the
 // block's scale 2^ex from its amax, e4m3 codes rounded to nearest even) ->
@@ -310,26 +330,28 @@ __device__ __forceinline__ void make_plan(Plan& p, const Args& a, int c, int G, 
 // (producer) The copies of stage i into the ring buffer at dst, completing on
 // the barrier fb: one contiguous run of codes and one of scale bytes per
 // expert the stage's rows belong to.
+template <bool kNv>
 __device__ __forceinline__ void issue_stage(const Args& a, const Plan& p, const int* seg_e, int i, uint8_t* dst,
                                             uint32_t fb) {
+    constexpr int SB = kNv ? 16 : 32;  // elements per scale byte
     if (i < p.ngu) {
         const int j = i / p.spb, row0 = (i - j * p.spb) * p.RG;
         const int b = p.c + j * p.G, s = b / p.FB, fb32 = b - s * p.FB;
         const int e = seg_e[s], f = 32 * fb32 + (row0 & 31), up = row0 >> 5;
         const size_t grow = ((size_t)e * (p.I / 128) + (f >> 7)) * 256 + up * 128 + (f & 127);
-        const uint32_t cb = (uint32_t)(p.RG * (p.H / 2)), sb = (uint32_t)(p.RG * (p.H / 32));
+        const uint32_t cb = (uint32_t)(p.RG * (p.H / 2)), sb = (uint32_t)(p.RG * (p.H / SB));
         mbar_arrive_expect_tx(fb, cb + sb);
         bulk_load(smem_u32(dst), a.gu_q + grow * (p.H / 2), cb, fb);
-        bulk_load(smem_u32(dst + kStageCodes), (up ? a.up_s : a.gate_s) + ((size_t)e * p.I + f) * (p.H / 32), sb, fb);
+        bulk_load(smem_u32(dst + kStageCodes), (up ? a.up_s : a.gate_s) + ((size_t)e * p.I + f) * (p.H / SB), sb, fb);
     } else {
         const int u0 = (i - p.ngu) * p.RD, u1 = min(u0 + p.RD, p.m * p.d);
-        mbar_arrive_expect_tx(fb, (uint32_t)(u1 - u0) * (uint32_t)(p.I / 2 + p.I / 32));
+        mbar_arrive_expect_tx(fb, (uint32_t)(u1 - u0) * (uint32_t)(p.I / 2 + p.I / SB));
         for (int u = u0; u < u1;) {
             const int s = u / p.d, o = u - s * p.d, n = min(u1 - u, p.d - o);
             const size_t drow = (size_t)seg_e[s] * p.H + p.r0 + o;
             bulk_load(smem_u32(dst + (u - u0) * (p.I / 2)), a.down_q + drow * (p.I / 2), (uint32_t)(n * (p.I / 2)), fb);
-            bulk_load(smem_u32(dst + kStageCodes + (u - u0) * (p.I / 32)), a.down_s + drow * (p.I / 32),
-                      (uint32_t)(n * (p.I / 32)), fb);
+            bulk_load(smem_u32(dst + kStageCodes + (u - u0) * (p.I / SB)), a.down_s + drow * (p.I / SB),
+                      (uint32_t)(n * (p.I / SB)), fb);
             u += n;
         }
     }
@@ -340,13 +362,18 @@ __device__ __forceinline__ void issue_stage(const Args& a, const Plan& p, const 
 // order, h = SiLU(g) * u, MXFP8 over the 32 features (lane f: feature
 // 32 fb + f), then the block's tagged words: lane 4w stores codes 4w .. 4w + 3
 // (the first in the low byte), lane 0 the scale byte.
-__device__ void publish_block(const Args& a, const float* pgu, int j, int b, int FB, int NQ, uint32_t epoch,
-                              int lane) {
+template <bool kNv>
+__device__ void publish_block(const Args& a, const float* pgu, const int* seg_e, int j, int b, int FB, int NQ,
+                              uint32_t epoch, int lane) {
     const int s = b / FB, fb = b - s * FB;
     float g = 0.f, u = 0.f;
     for (int q = 0; q < NQ; ++q) {
         g += pgu[(j * NQ + q) * 64 + lane];
         u += pgu[(j * NQ + q) * 64 + 32 + lane];
+    }
+    if (kNv) {  // the matrix scales multiply the finished dot products
+        g *= __ldg(a.gate_g + seg_e[s]);
+        u *= __ldg(a.up_g + seg_e[s]);
     }
     const float h = silu_mul(g, u);
     const int ex = mxfp8_exponent(warp_max(fabsf(h)));
@@ -365,9 +392,11 @@ __device__ void publish_block(const Args& a, const float* pgu, int j, int b, int
 
 // 20 warps: 16 compute warps, the producer, the publisher and two gatherers
 // (at most 96 registers a thread: 5 warps on one SM quarter).
+template <bool kNv>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_constant__ Args a) {
+    constexpr int kStageBytes = stage_bytes(kNv), kSB = kNv ? 16 : 32;  // (kSB: elements per scale byte)
     extern __shared__ __align__(128) uint8_t smem[];
-    const Layout Lo(a.H, a.I, a.nbmax, a.dmax);
+    const Layout Lo(a.H, a.I, a.nbmax, a.dmax, kNv);
     int* sel = reinterpret_cast<int*>(smem + Lo.route);  // [8] the router's selection, in router order
     float* w_t = reinterpret_cast<float*>(sel + 8);
     int* seg_e = reinterpret_cast<int*>(w_t + 8);         // [8] the kept experts, ascending
@@ -501,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                 make_plan(p, a, c, G, m, cuts);
                 i0 = min(p.n, kStages);
                 if (lane < i0) {
-                    issue_stage(a, p, prod_e, lane, smem + Lo.ring + lane * kStageBytes, full0 + 8u * lane);
+                    issue_stage<kNv>(a, p, prod_e, lane, smem + Lo.ring + lane * kStageBytes, full0 + 8u * lane);
                     trace_event(a, 128 + lane);
                 }
                 if (lane == 0) stamp(a, 4);
@@ -524,7 +553,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                     break;
                 }
                 if (i == 0) stamp(a, 4);
-                issue_stage(a, p, prod_e, i, smem + Lo.ring + slot * kStageBytes, full0 + 8u * slot);
+                issue_stage<kNv>(a, p, prod_e, i, smem + Lo.ring + slot * kStageBytes, full0 + 8u * slot);
                 trace_event(a, 128 + i);
                 if (++slot == kStages) {
                     slot = 0;
@@ -619,7 +648,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                 break;
             }
             if (lane == 0) trace_event(a, 192 + j);
-            publish_block(a, pgu, j, c + j * G, FB, NQ, epoch, lane);
+            publish_block<kNv>(a, pgu, seg_e, j, c + j * G, FB, NQ, epoch, lane);
             if (lane == 0) trace_event(a, 200 + j);
         }
         if (!ok && lane == 0) {
@@ -702,9 +731,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         {
             // gate/up: block j's rows row0 .. row0 + RG (gate rows 0 .. 31,
             // up rows 32 .. 63 of the block) per stage, the token as operand
-            const int rowb = a.H / 2, scb = a.H / 32, g = warp / NQ;
+            const int rowb = a.H / 2, scb = a.H / kSB, g = warp / NQ;
             const uint8_t* wb = smem + Lo.ring + kRun * g * rowb + qx * 512 + lane * 16;
-            const uint8_t* sb = smem + Lo.ring + kStageCodes + kRun * g * scb + qx * 32 + lane;
+            const uint8_t* sb = smem + Lo.ring + kStageCodes + kRun * g * scb + (qx * 32 + lane) * (32 / kSB);
             float* pw = pgu + qx * 64 + kRun * g + t4;
             int row0 = 0, j = 0;
             for (int i = 0; i < p.ngu; ++i) {
@@ -717,13 +746,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
 #pragma unroll
                 for (int t = 0; t < kRun; ++t) {
                     wv[t] = *reinterpret_cast<const uint4*>(w + t * rowb);
-                    sv[t] = sp[t * scb];
+                    sv[t] = kNv ? *reinterpret_cast<const uint16_t*>(sp + t * scb) : sp[t * scb];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8u * slot);
                 float v[kRun];
 #pragma unroll
-                for (int t = 0; t < kRun; ++t) v[t] = block_dot(wv[t], op) * ue8m0_to_f32(sv[t]) * opsf;
+                for (int t = 0; t < kRun; ++t) v[t] = scaled_block<kNv>(wv[t], op, sv[t]) * opsf;
                 const float r = warp_sum4(v[0], v[1], v[2], v[3], lane);
                 if (writer) pw[j * NQ * 64 + row0] = r;
                 if (++slot == kStages) {
@@ -744,9 +773,9 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             // down: the CTA's (kept expert s, row o) pairs as the flat list
             // u = s d + o, RD a stage; the warp's run starts at u, the operand
             // is expert s's h (K segment qh), switched when s changes
-            const int rowb = a.I / 2, scb = a.I / 32, g = warp / NQd, md = m * p.d;
+            const int rowb = a.I / 2, scb = a.I / kSB, g = warp / NQd, md = m * p.d;
             const uint8_t* wb = smem + Lo.ring + kRun * g * rowb + qh * 512 + lane * 16;
-            const uint8_t* sb = smem + Lo.ring + kStageCodes + kRun * g * scb + qh * 32 + lane;
+            const uint8_t* sb = smem + Lo.ring + kStageCodes + kRun * g * scb + (qh * 32 + lane) * (32 / kSB);
             int u = kRun * g, s = 0, sbase = 0, cur = -1;
             for (int i = p.ngu; i < p.n; ++i, u += p.RD) {
                 const bool live = u < md;
@@ -786,14 +815,14 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
 #pragma unroll
                 for (int t = 0; t < kRun; ++t) {
                     wv[t] = *reinterpret_cast<const uint4*>(w + t * rowb);
-                    sv[t] = sp[t * scb];
+                    sv[t] = kNv ? *reinterpret_cast<const uint16_t*>(sp + t * scb) : sp[t * scb];
                 }
                 __syncwarp();
                 if (lane == 0) mbar_arrive(empty0 + 8u * slot);
                 if (live) {
                     float v[kRun];
 #pragma unroll
-                    for (int t = 0; t < kRun; ++t) v[t] = block_dot(wv[t], op) * ue8m0_to_f32(sv[t]) * opsf;
+                    for (int t = 0; t < kRun; ++t) v[t] = scaled_block<kNv>(wv[t], op, sv[t]) * opsf;
                     const float r = warp_sum4(v[0], v[1], v[2], v[3], lane);
                     if (writer) pdn[(s * NQd + qh) * a.dmax + (u - sbase) + t4] = r;
                 }
@@ -823,6 +852,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         for (int s = 0; s < m; ++s) {
             float y = 0.f;
             for (int q = 0; q < NQd; ++q) y += pdn[(s * NQd + q) * a.dmax + i];
+            if (kNv) y *= __ldg(a.down_g + seg_e[s]);  // the matrix scale of the finished dot product
             o += seg_w[s] * y;
         }
         a.out[p.r0 + i] = o;
@@ -835,8 +865,8 @@ bool supported(const moe_layer* L) {
     const int NQ = c.hidden / kSeg, NQd = c.inter / kSeg;
     (void)NQ;
     (void)NQd;
-    return c.weight_format == MOE_WEIGHTS_MXFP4 && !c.has_shared && c.top_k <= kMaxK && c.n_experts <= 1024 &&
-           L->gv_smem > 0;
+    return (c.weight_format == MOE_WEIGHTS_MXFP4 || c.weight_format == MOE_WEIGHTS_NVFP4) && !c.has_shared &&
+           c.top_k <= kMaxK && c.n_experts <= 1024 && L->gv_smem > 0;
 }
 
 // The largest h-block count and down range of a CTA over the kept counts
@@ -850,7 +880,7 @@ int smem_bytes(const moe_config& c, int G, int* nbmax, int* dmax) {
             const Split s = down_rows(x, G, m, c.hidden, c.inter);
             if (s.r1 - s.r0 > *dmax) *dmax = s.r1 - s.r0;
         }
-    const Layout Lo(c.hidden, c.inter, *nbmax, *dmax);
+    const Layout Lo(c.hidden, c.inter, *nbmax, *dmax, c.weight_format == MOE_WEIGHTS_NVFP4);
     return Lo.total <= 227 * 1024 ? Lo.total : 0;
 }
 
@@ -866,10 +896,13 @@ cudaError_t init(moe_layer* L) {
     int nbmax = 0, dmax = 0;
     const int bytes = smem_bytes(c, L->num_sms, &nbmax, &dmax);
     if (bytes == 0) return cudaSuccess;
-    cudaError_t e = cudaFuncSetAttribute(k_decode_gemv, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
+    const void* kern = nv ? reinterpret_cast<const void*>(k_decode_gemv<true>)
+                          : reinterpret_cast<const void*>(k_decode_gemv<false>);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess) return e;
     int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, k_decode_gemv, kThreads, bytes);
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, bytes);
     if (e != cudaSuccess) return e;
     if (per_sm < 1) return cudaSuccess;
     // the down-row cuts of every kept count 1 .. k (the same on every call)
@@ -910,6 +943,9 @@ cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t
     a.up_s = L->up_s;
     a.down_q = L->down_q;
     a.down_s = L->down_s;
+    a.gate_g = L->gate_g;
+    a.up_g = L->up_g;
+    a.down_g = L->down_g;
     a.hw = reinterpret_cast<unsigned long long*>(L->gv_words + gv_hword_off(L->num_sms));
     a.launches = L->gv_words + kGvCountOff;
     a.x_flag = L->gv_words + 2;
@@ -940,7 +976,8 @@ cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     L->launches += 1;
-    return cudaLaunchKernelEx(&cfg, k_decode_gemv, a);
+    return L->cfg.weight_format == MOE_WEIGHTS_NVFP4 ? cudaLaunchKernelEx(&cfg, k_decode_gemv<true>, a)
+                                                     : cudaLaunchKernelEx(&cfg, k_decode_gemv<false>, a);
 }
 
 }  // namespace gemv

@@ -83,7 +83,9 @@ typedef struct {
  * matrix, element = e2m1 * e4m3 scale * matrix scale.  The tcgen05
  * block-scaled MMAs take UE8M0 scales per 32 elements only, so an NVFP4
  * layer runs its GEMMs on the CUDA cores (moe_set_gemm_path 2 returns
- * MOE_ERR_UNSUPPORTED and a one-token call takes the grouped path).        */
+ * MOE_ERR_UNSUPPORTED); a one-token call takes the CUDA-core whole-layer
+ * decode kernel where its shape rules hold (moe_set_decode_kernel), else
+ * the grouped CUDA-core path.                                              */
 enum { MOE_WEIGHTS_MXFP4 = 0, MOE_WEIGHTS_NVFP4 = 1 };
 
 /* Device pointers to the weights, in the canonical shipping layout:
@@ -248,11 +250,11 @@ moe_status moe_set_gemm_path(moe_layer* layer, int path);
 /* Which whole-layer kernel a one-token call on the automatic GEMM path
  * (moe_route_forward / moe_forward_host with T = 1) takes.  kind 0 =
  * automatic: the CUDA-core split-K GEMV kernel where the shape allows it
- * (MXFP4 experts, H and I multiples of 1024 with H / 1024 and I / 1024
- * dividing 16, H >= 2048, I <= 4096, no shared expert), else the tcgen05
- * kernel (H <=
- * 4096, I <= 2048, no shared expert), else the grouped kernels; 1 = the
- * CUDA-core kernel; 2 = the tcgen05 kernel.  Both compute the layer for a
+ * (MXFP4 or NVFP4 experts, H and I multiples of 1024 with H / 1024 and
+ * I / 1024 dividing 16, H >= 2048, I <= 4096, no shared expert), else the
+ * tcgen05 kernel (MXFP4, H <= 4096, I <= 2048, no shared expert), else the
+ * grouped kernels; 1 = the CUDA-core kernel; 2 = the tcgen05 kernel.  Both
+ * compute the layer for a
  * single decode token (guide, section 2.A: one token, the MUL_MAT_ID of its
  * top-k experts), with the combine in ascending expert order; they differ
  * only in the order of fp32 additions.

@@ -2,10 +2,11 @@
 quantization scheme study", row "E2M1 + E4M3 b16": e2m1 codes, an e4m3 scale
 per 16 elements, an fp32 scale per matrix) through the C ABI, against the
 fp64 oracle run end to end on its own routing: the tiny layer, one-token
-decode calls and pp512 at full size.  The layer's GEMMs run on the CUDA
-cores (the block-scaled tensor-core MMAs take UE8M0 scales per 32 elements
-only); routing, sort, quantisation and combine are the MXFP4 layer's
-kernels.  Same tolerances as the MXFP4 parity tests."""
+decode calls (grouped path and the whole-layer CUDA-core decode kernel) and
+pp512 at full size.  The layer's GEMMs run on the CUDA cores (the
+block-scaled tensor-core MMAs take UE8M0 scales per 32 elements only);
+routing, sort, quantisation and combine are the MXFP4 layer's kernels.  Same
+tolerances as the MXFP4 parity tests."""
 import numpy as np
 import pytest
 import torch
@@ -82,12 +83,47 @@ def test_nvfp4_tiny(tiny, n):
 
 
 def test_nvfp4_decode_calls(full):
+    """One-token calls on the grouped CUDA-core path (moe_set_gemm_path 1),
+    with the requantised h checked too."""
     w, layer = full
     cfg = CONFIGS[6]
     tk = G.tokens(6, n=6)
-    for t in range(6):
+    bqe.moe_set_gemm_path(layer, 1)
+    try:
+        for t in range(6):
+            one = type(tk)(x_bits=tk.x_bits[t:t + 1], logits=tk.logits[t:t + 1], token_ids=None)
+            _check(cfg, w, layer, one, 1, np.array([0], np.int32), "decode_nvfp4")
+    finally:
+        bqe.moe_set_gemm_path(layer, 0)
+
+
+def test_nvfp4_decode_kernel(full):
+    """One-token calls on the automatic path: the CUDA-core whole-layer decode
+    kernel (one launch), the NVFP4 block dot product taking an e4m3 scale per
+    16-element half and the matrix scales on the finished dot products;
+    routing bit for bit and the output against the oracle end to end, and
+    within the oracle tolerance of the grouped path's output."""
+    w, layer = full
+    cfg = CONFIGS[6]
+    assert bqe.moe_decode_info(layer) == 1
+    tk = G.tokens(6, n=8)
+    for t in range(8):
         one = type(tk)(x_bits=tk.x_bits[t:t + 1], logits=tk.logits[t:t + 1], token_ids=None)
-        _check(cfg, w, layer, one, 1, np.array([0], np.int32), "decode_nvfp4")
+        n0 = bqe.moe_kernel_launches(layer)
+        ids, wt, out = _run(layer, cfg, one, 1)
+        assert bqe.moe_kernel_launches(layer) - n0 == 1
+        rid, rw = orc.route_learned(one.logits, cfg.k, cfg.w_scale)
+        assert np.array_equal(ids.cpu().numpy(), rid)
+        ref = orc.layer_forward(w, one.x_bits, rid, rw)
+        norm, elem = G.compare_out(out.cpu().numpy(), ref)
+        assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (t, norm, elem)
+        bqe.moe_set_gemm_path(layer, 1)
+        try:
+            _, _, out2 = _run(layer, cfg, one, 1)
+        finally:
+            bqe.moe_set_gemm_path(layer, 0)
+        a, b = out.cpu().numpy().astype(np.float64), out2.cpu().numpy().astype(np.float64)
+        assert np.linalg.norm(a - b) <= G.NORM_TOL * np.linalg.norm(b)
 
 
 def test_nvfp4_prefill_pp512(full):
