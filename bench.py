@@ -339,6 +339,24 @@ def clocked(fn):
     return r, clocks
 
 
+def gemv_alu(cfg, touched, kernel_ms, clocks):
+    """The CUDA-core decode kernel against its arithmetic ceiling: weight
+    elements per SM clock (the touched experts' 3 H I elements over the
+    kernel's duration at the median SM clock of the timed region) beside the
+    e2m1 dot-product rate measured here (libmoe_peaks)."""
+    import torch
+    from block_quantized_expert_gb300 import peaks as pk
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    mhz = clocks.get("sm_mhz") or 2070.0
+    elems = touched * 3.0 * cfg.H * cfg.I
+    achieved = elems / (kernel_ms * 1e-3 * mhz * 1e6 * sms)
+    peak = pk.dot_e2m1_el_per_clk()
+    return {"unit": "weight elements per SM clock", "achieved": round(achieved, 1), "peak": round(peak, 1),
+            "frac": round(achieved / peak, 4), "sm_mhz": mhz,
+            "peak_source": "e2m1 x f16 -> fp32 block dot products on the CUDA cores (libmoe_peaks "
+                           "peak_dot_e2m1) measured in this run, of measured"}
+
+
 def load_peaks():
     try:
         return json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json")))
@@ -437,6 +455,8 @@ def run_ours(args, cfg, rank, world, local_rank):
     roof = roofline(cfg, dom, kernel_ms, byts, rows, peaks)
     roof["kernel"] = kernel
     roof["traffic"] = profiled_traffic(cfg, dom, decode_kind) if not args.prune_t else None
+    if dom == "layer" and decode_kind == 1:
+        roof["alu"] = gemv_alu(cfg, avg_touched, roof["kernel_ms"], clocks)
     roof["hbm_frac_whole_step"] = round(step_bytes / (ms / K * 1e-3) / 1e9 / roof["peak"], 4) \
         if roof["unit"] == "GB/s" else None
 
@@ -524,6 +544,8 @@ def per_config(args, bqe, dev, peaks):
             byts["layer"] = byts["gateup"] + byts["down"]
             roof = roofline(cfg, "layer", ms / K, byts, rows, peaks, mma_peak)
             roof["kernel"] = DECODE_KERNELS[bqe.moe_decode_info(layer)]
+            if bqe.moe_decode_info(layer) == 1:
+                roof["alu"] = gemv_alu(cfg, avg_touched, ms / K, clocks)
         else:
             stage_ms = stage_times(bqe, layer, wl.step, W + K, min(K, 16), stream)
             dom = max(("gateup", "down"), key=lambda n: stage_ms[n])

@@ -5,6 +5,9 @@
 * mma_mx_tflops(): block-scaled tcgen05 MMAs of the shape the grouped GEMMs
   issue (kind::mxf8f6f4, M 128, N 256, K 32, e4m3 x e2m1, UE8M0 / 32), one
   issuing thread per SM on resident operands -- the bound of prefill.
+* dot_e2m1_el_per_clk(): the CUDA-core decode kernel's block dot products
+  (e2m1 codes -> f16 by the hardware converter, times f16 operands, fp32
+  sums) in elements per SM clock -- its arithmetic ceiling.
 
 Both run on the current CUDA device and return figures from CUDA events.
 ``python -m block_quantized_expert_gb300.peaks [--out FILE]`` prints (and
@@ -27,6 +30,7 @@ def load(build: bool = True):
         L = C.CDLL(str(path))
         L.peak_read_stream.argtypes = [C.c_void_p, C.c_longlong, C.c_int, C.c_void_p, C.POINTER(C.c_float)]
         L.peak_mma_mx.argtypes = [C.c_int, C.c_int, C.c_void_p, C.POINTER(C.c_float)]
+        L.peak_dot_e2m1.argtypes = [C.c_int, C.c_int, C.c_void_p, C.c_void_p, C.c_void_p, C.POINTER(C.c_float)]
         _lib = L
     return _lib
 
@@ -69,6 +73,30 @@ def mma_mx_tflops(iters: int = 200000, reps: int = 3) -> float:
     return best
 
 
+def dot_e2m1_el_per_clk(iters: int = 4096, reps: int = 3) -> float:
+    """Elements per SM clock of the decode kernel's e2m1 x f16 -> fp32 block
+    dot products on the CUDA cores (one CTA of 16 warps per SM, operands in
+    shared memory), the median CTA of the best of `reps` runs."""
+    import torch
+
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    g = torch.Generator().manual_seed(12345)
+    seed = torch.randint(0, 2 ** 31 - 1, (1024,), generator=g, dtype=torch.int64).to(torch.int32).cuda()
+    out = torch.empty(sms * 512, dtype=torch.float32, device="cuda")
+    cyc = torch.zeros(sms, dtype=torch.int64, device="cuda")
+    best = 0.0
+    for r in range(reps + 1):  # the first is a warm-up
+        ms = C.c_float(0.0)
+        rc = load().peak_dot_e2m1(sms, iters if r else 64, seed.data_ptr(), out.data_ptr(), cyc.data_ptr(),
+                                  C.byref(ms))
+        if rc:
+            raise RuntimeError(f"peak_dot_e2m1 failed ({rc})")
+        if r:
+            c = float(cyc.cpu().median().item())
+            best = max(best, iters * 16 * 4 * 1024 / c)
+    return best
+
+
 def main():
     import argparse
     import subprocess
@@ -89,6 +117,8 @@ def main():
            "hbm_read_gbs": round(hbm_read_gbs(), 1),
            "mma_mxf8f6f4_tflops": round(mma_mx_tflops(), 1),
            "mma_shape": "kind::mxf8f6f4 block_scale scale_vec::1X, M128 N256 K32, e4m3 x e2m1",
+           "dot_e2m1_el_per_clk_per_sm": round(dot_e2m1_el_per_clk(), 1),
+           "dot_e2m1": "cvt.rn.f16x2.e2m1x2 + fma.rn.f32.f16, 16 warps x 4 32-blocks per iteration, operands in shared memory",
            "read_stream": "16-byte evict-first loads, 4 GiB, grid 4 x SMs x 512 threads, best of 5"}
     smi.terminate()
     smi.wait()

@@ -1,8 +1,9 @@
-// peaks.cu -- the two denominators of the layer's rooflines, measured on the
-// GPU the layer runs on: a plain HBM read stream (the decode and pp512
-// kernels are weight-read streams) and a loop of block-scaled tcgen05 MMAs
-// of the kind and shape the grouped GEMMs issue (kind::mxf8f6f4, M = 128,
-// N = 256, K = 32, e4m3 A x e2m1 B, one UE8M0 scale per 32 elements).
+// peaks.cu -- the denominators of the layer's rooflines, measured on the GPU
+// the layer runs on: a plain HBM read stream (the decode and pp512 kernels
+// are weight-read streams), a loop of block-scaled tcgen05 MMAs of the kind
+// and shape the grouped GEMMs issue (kind::mxf8f6f4, M = 128, N = 256,
+// K = 32, e4m3 A x e2m1 B, one UE8M0 scale per 32 elements), and the CUDA-core
+// decode kernel's e2m1 dot-product rate (its arithmetic ceiling).
 // Built into its own library (libmoe_peaks.so); the layer never calls it.
 #include <cuda_runtime.h>
 #include <cstdint>
@@ -79,6 +80,70 @@ __global__ void __launch_bounds__(64, 1) k_mma_loop(int iters, int* ok_out) {
     }
 }
 
+// ---- the CUDA-core decode kernel's arithmetic on one 32-block: 16 bytes of
+// e2m1 codes -> f16 pairs by the hardware converter, times f16 operand values
+// with fp32 accumulation (four partial sums of 8).
+__device__ __forceinline__ void cvt_e2m1x8(uint32_t w, uint32_t (&o)[4]) {
+    asm("{\n.reg .b8 b0, b1, b2, b3;\nmov.b32 {b0, b1, b2, b3}, %4;\n"
+        "cvt.rn.f16x2.e2m1x2 %0, b0;\ncvt.rn.f16x2.e2m1x2 %1, b1;\n"
+        "cvt.rn.f16x2.e2m1x2 %2, b2;\ncvt.rn.f16x2.e2m1x2 %3, b3;\n}"
+        : "=r"(o[0]), "=r"(o[1]), "=r"(o[2]), "=r"(o[3])
+        : "r"(w));
+}
+__device__ __forceinline__ float fma2_f16_f32(uint32_t a, uint32_t b, float acc) {
+    asm("{\n.reg .b16 al, ah, bl, bh;\nmov.b32 {al, ah}, %1;\nmov.b32 {bl, bh}, %2;\n"
+        "fma.rn.f32.f16 %0, al, bl, %0;\nfma.rn.f32.f16 %0, ah, bh, %0;\n}"
+        : "+f"(acc)
+        : "r"(a), "r"(b));
+    return acc;
+}
+__device__ __forceinline__ float dot_block(const uint4& w, const uint32_t (&op)[16]) {
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        uint32_t h[4];
+        cvt_e2m1x8(ws[i], h);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i] = fma2_f16_f32(h[j], op[4 * i + j], acc[i]);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+
+constexpr int kDotWarps = 16;
+constexpr int kDotSmem = 32768;
+
+// 16 warps per CTA; each iteration a warp takes 4 distinct 512-byte chunks of
+// a 32 KB shared-memory buffer (one 32-block per lane each, the chunks move
+// every iteration and shared memory is declared clobbered, so no load or
+// product carries over), as the decode kernel's compute warps do per stage.
+// cyc[c]: clock cycles of CTA c's loop.
+__global__ void __launch_bounds__(32 * kDotWarps, 1) k_dot_loop(const uint32_t* seed, int iters, float* out,
+                                                               long long* cyc) {
+    extern __shared__ __align__(16) uint8_t smd[];
+    for (int i = threadIdx.x; i < kDotSmem / 4; i += blockDim.x)
+        reinterpret_cast<uint32_t*>(smd)[i] = seed[i & 1023];
+    __syncthreads();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t op[16];
+    for (int i = 0; i < 16; ++i) op[i] = seed[(lane * 16 + i) & 1023] & 0x3BFF3BFFu;  // finite f16 pairs
+    float tot = 0.f;
+    const long long c0 = clock64();
+    for (int it = 0; it < iters; ++it) {
+        asm volatile("" ::: "memory");
+        float v[4];
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+            const int chunk = (warp * 4 + t + 4 * it) & 63;
+            v[t] = dot_block(*reinterpret_cast<const uint4*>(smd + chunk * 512 + lane * 16), op);
+        }
+        tot += (v[0] + v[1]) + (v[2] + v[3]);
+    }
+    const long long c1 = clock64();
+    out[blockIdx.x * blockDim.x + threadIdx.x] = tot;
+    if (threadIdx.x == 0) cyc[blockIdx.x] = c1 - c0;
+}
+
 }  // namespace
 
 extern "C" {
@@ -120,6 +185,31 @@ int peak_mma_mx(int grid, int iters, int* ok, float* ms) {
     }
     cudaEventRecord(e0, 0);
     k_mma_loop<<<grid, 64, kSmem>>>(iters, ok);
+    cudaEventRecord(e1, 0);
+    int rc = (int)cudaDeviceSynchronize();
+    if (rc == 0) rc = (int)cudaGetLastError();
+    cudaEventElapsedTime(ms, e0, e1);
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    return rc;
+}
+
+// `grid` CTAs of 16 warps each run `iters` iterations of 4 e2m1 32-block dot
+// products per warp (4 x 1024 elements); seed: 1024 device words (the codes
+// and operands), out: grid x 512 floats, cyc: grid int64 (each CTA's loop in
+// clock cycles).  *ms = the kernel's duration.
+int peak_dot_e2m1(int grid, int iters, const unsigned int* seed, float* out, long long* cyc, float* ms) {
+    if (grid < 1 || iters < 1 || !seed || !out || !cyc || !ms) return (int)cudaErrorInvalidValue;
+    cudaError_t e = cudaFuncSetAttribute(k_dot_loop, cudaFuncAttributeMaxDynamicSharedMemorySize, kDotSmem);
+    if (e != cudaSuccess) return (int)e;
+    cudaEvent_t e0, e1;
+    if (cudaEventCreate(&e0) != cudaSuccess) return (int)cudaErrorUnknown;
+    if (cudaEventCreate(&e1) != cudaSuccess) {
+        cudaEventDestroy(e0);
+        return (int)cudaErrorUnknown;
+    }
+    cudaEventRecord(e0, 0);
+    k_dot_loop<<<grid, 32 * kDotWarps, kDotSmem>>>(seed, iters, out, cyc);
     cudaEventRecord(e1, 0);
     int rc = (int)cudaDeviceSynchronize();
     if (rc == 0) rc = (int)cudaGetLastError();
