@@ -251,7 +251,10 @@ moe_status moe_set_gemm_path(moe_layer* layer, int path);
  * (moe_route_forward / moe_forward_host with T = 1) takes.  kind 0 =
  * automatic: the CUDA-core split-K GEMV kernel where the shape allows it
  * (MXFP4 or NVFP4 experts, H and I multiples of 1024 with H / 1024 and
- * I / 1024 dividing 16, H >= 2048, I <= 4096, no shared expert), else the
+ * I / 1024 dividing 16, H >= 2048, no shared expert, and its shared-memory
+ * layout -- a 5-stage weight ring, the h of top_k experts, the CTA's
+ * partial sums -- within 227 KB: e.g. I <= 2048 for top_k <= 8, not
+ * I = 4096 with 6 experts), else the
  * tcgen05 kernel (MXFP4, H <= 4096, I <= 2048, no shared expert), else the
  * grouped kernels; 1 = the CUDA-core kernel; 2 = the tcgen05 kernel.  Both
  * compute the layer for a
