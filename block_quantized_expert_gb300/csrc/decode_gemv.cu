@@ -6,45 +6,48 @@
 // SwiGLU + MXFP8 requantisation of h, down and the fixed-order combine.
 //
 // Why the CUDA cores.  With one token the tensor-core MMA does 1/128 useful
-// work, and on one SM the weight copies into shared memory and the MMAs that
-// read them do not overlap: the coupled stream runs at ~0.5 us per 16 KB
-// stage per SM (4.7 TB/s over 152 SMs).  The e2m1 -> f16x2 converter and the
-// mixed f16 x f16 + f32 FMA, with 16 warps of 4 independent 32-blocks each,
-// decode and multiply ~80 elements per clock per SM (~12 TB/s of codes over
-// 152 SMs), so the copies set the pace.
+// work, and the tcgen05 kernel's stream of weight copies and MMAs runs at
+// ~0.5 us per 16 KB stage per SM.  The e2m1 -> f16x2 converter and the mixed
+// f16 x f16 + f32 FMA (half rate) do ~59 elements per clock per SM (the
+// peak_dot_e2m1 measurement), about 1.4 times what HBM delivers per SM, so a
+// lean stage loop keeps up with the copies.
 //
 // Arithmetic of one 32-block (the block-scaled dot product of the method):
 // the e2m1 weight values and the e4m3 values of the token (or of h) are
 // exact in f16, so each product is exact in fp32; the block's 32 products are
 // summed in fp32 (four partial sums of 8), the sum is multiplied by the two
 // UE8M0 block scales (powers of two), and the blocks' values of a row are
-// summed across the lanes of the warp.
+// summed across the lanes of the warp.  NVFP4-style weights: each 16-element
+// half's sum is multiplied by its own e4m3 scale, and the matrix scales
+// multiply the finished dot products.
 //
 // Work split (the same in every CTA, from the kept count m and the grid G):
 //  * gate/up: the m * I / 32 "h blocks" (32 consecutive features of one
 //    expert: 32 gate rows + the 32 matching up rows, K = H) go to the CTAs
 //    round-robin, block b to CTA b mod G.  A CTA owns whole blocks, so it
 //    forms h = SiLU(g) * u and its MXFP8 requantisation (32 features share
-//    a scale) itself and publishes the codes and the scale byte with a flag.
+//    a scale) itself.
 //  * down: each CTA owns a contiguous range of d output rows (a multiple of
 //    4) for every kept expert, so out[o] = sum over experts (ascending) of
 //    w_s * y_s[o] is formed in the CTA that computed the y_s[o]: no combine
 //    pass, no atomics.  The ranges are sized so that every CTA streams about
 //    the same bytes (gate/up blocks + down rows).
-//  * a CTA streams its work as stages of 32 KB of codes (+ their rows' 2 KB
-//    of scale bytes): RG = 65536 / H rows of a block's gate or up half, or
-//    RD = 65536 / I down rows, the CTA's (expert, row) pairs in order -- a
-//    stage may span experts, in runs of 4 rows.  A producer warp
-//    bulk-copies them into a ring of kStages buffers; 16 compute warps each
-//    take 4 consecutive rows of one K segment (4 x 512 bytes: one 32-block
-//    per lane), whose operand (the token, or h) they hold in registers as
-//    f16.  The down weights do not depend on h: the producer streams on
-//    while h is exchanged, and starts before the routing weights are known
-//    when the kept count does not depend on them.
-//  * a publisher warp routes the token's weights and publishes the CTA's h
-//    blocks as the compute warps finish them; a gather warp fetches each
-//    kept expert's h (its flags, then its codes, as f16 in shared memory)
-//    for the down stages, from the start on.
+//  * a CTA streams its work as stages of 32 KB of codes (+ their rows' scale
+//    bytes): RG = 65536 / H rows of a block's gate or up half, or RD = 65536 /
+//    I down rows, the CTA's (expert, row) pairs in order -- a stage may span
+//    experts, in runs of 4 rows.  A producer warp bulk-copies them into a
+//    ring of kStages buffers; 16 compute warps each take 4 consecutive rows
+//    of one K segment (4 x 512 bytes: one 32-block per lane), whose operand
+//    (the token, or h) they hold in registers as f16.  The down weights do
+//    not depend on h: the producer streams on while h is exchanged, and
+//    starts before the routing weights are known when the kept count does
+//    not depend on them.
+//  * h exchange: a publisher warp (which first computes the routing
+//    weights) publishes each of the CTA's h blocks once the compute warps'
+//    partial sums of it are in, as 6 64-bit words tagged with the launch's
+//    epoch (a reader that sees the tag sees the payload: one L2 round trip,
+//    no flags); two gatherer warps poll the kept experts' words, two experts
+//    a pass, and copy them into shared memory for the compute warps.
 // Cross-CTA hand-offs carry the launch's epoch: CTA c counts its own
 // launches in a word of its own (read at the start, advanced at the exit;
 // every CTA of a grid runs once per launch, so all hold the same count), so
