@@ -24,7 +24,7 @@ EXPORTS = ("moe_create", "moe_destroy", "moe_route", "moe_route_hash", "moe_perm
            "moe_quantize", "moe_forward", "moe_forward_host", "moe_hidden", "moe_check",
            "moe_workspace_bytes", "moe_last_error", "moe_set_gemm_path", "moe_set_stage_events",
            "moe_kernel_launches", "moe_permute_noalloc", "moe_set_trace", "moe_route_forward",
-           "moe_set_route_prune", "moe_set_wait_limit", "moe_test_stall_next_decode",
+           "moe_set_route_prune", "moe_set_wait_limit", "moe_test_stall_next_decode", "moe_test_decode_split",
            "moe_set_decode_kernel", "moe_decode_info")
 
 
@@ -86,6 +86,7 @@ def load_library(build: bool = True) -> C.CDLL:
         "moe_set_route_prune": ([vp, i, f, f], i),
         "moe_set_wait_limit": ([vp, C.c_double], i),
         "moe_test_stall_next_decode": ([vp], i),
+        "moe_test_decode_split": ([C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.c_int, C.POINTER(C.c_int)], i),
         "moe_set_decode_kernel": ([vp, i], i),
         "moe_decode_info": ([vp, C.POINTER(C.c_int)], i),
     }
@@ -229,6 +230,14 @@ def moe_set_route_prune(layer: Layer, keep: int, min_w: float = 0.0, rho: float 
 def moe_set_wait_limit(layer: Layer, seconds: float):
     """Wall-time limit of the layer's device-side waits (default 2 s)."""
     _check(load_library().moe_set_wait_limit(layer.ptr, float(seconds)), layer.ptr)
+
+
+def moe_test_decode_split(num_sms: int, kept: int, hidden: int, inter: int, nvfp4: bool = False,
+                          shared: bool = False) -> list:
+    """The CUDA-core decode kernel's down-row cuts (host computation, no GPU)."""
+    cut = (C.c_int * (num_sms + 1))()
+    _check(load_library().moe_test_decode_split(num_sms, kept, hidden, inter, int(nvfp4), int(shared), cut))
+    return list(cut)
 
 
 def moe_test_stall_next_decode(layer: Layer):

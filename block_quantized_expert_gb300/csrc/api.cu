@@ -412,6 +412,14 @@ moe_status moe_test_stall_next_decode(moe_layer* L) {
     return MOE_OK;
 }
 
+moe_status moe_test_decode_split(int num_sms, int kept, int hidden, int inter, int nvfp4, int shared, int* cut) {
+    if (num_sms < 1 || kept < 1 || hidden < 1024 || inter < 1024 || hidden % 1024 || inter % 1024 ||
+        hidden > 8192 || inter > 8192 || !cut)
+        return fail(nullptr, MOE_ERR_INVALID_ARG, "invalid split arguments");
+    moe::gemv::split_table(num_sms, kept, hidden, inter, nvfp4 != 0, shared != 0, cut);
+    return MOE_OK;
+}
+
 moe_status moe_set_decode_kernel(moe_layer* L, int kind) {
     if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
     if (kind < 0 || kind > 2) return fail(L, MOE_ERR_INVALID_ARG, "kind must be 0, 1 or 2");

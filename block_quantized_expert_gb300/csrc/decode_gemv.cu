@@ -88,6 +88,8 @@ __host__ __device__ constexpr int stage_scales(bool nv) { return kStageCodes / (
 __host__ __device__ constexpr int stage_bytes(bool nv) { return kStageCodes + stage_scales(nv); }
 constexpr int kStages = 5;
 constexpr int kMaxK = kMaxTopK;
+constexpr int kMaxPos = kMaxK + 1;            // kept positions: the routed experts, then the shared expert
+constexpr int kRunS = 2;                      // rows of a compute warp in a stage of fp8 (shared-expert) rows
 constexpr int kMaxI = 4096;                   // h of every kept expert resident as f16
 // A published h block (32 features): 6 64-bit words, word w holding e4m3 codes
 // 6w .. 6w + 5 in bytes 0 .. 5 (the last word: codes 30, 31 and the block's
@@ -114,7 +116,11 @@ struct Args {
     const uint8_t* down_q;  // [E][H][I/2]
     const uint8_t* down_s;  // [E][H][I/32] (NVFP4: [E][H][I/16] e4m3)
     const float *gate_g, *up_g, *down_g;  // NVFP4: the per-expert matrix scales [E]
-    unsigned long long* hw;  // [kMaxK][I/32][kHWords]: h by kept position, epoch-tagged words
+    // the shared expert (sh set): e4m3 codes, gate/up interleaved per 128
+    // features [I/128][256][H], down [H][I]; UE8M0 scales per 128 x 128 tile
+    int sh;
+    const uint8_t *sh_gu_q, *sh_gate_s, *sh_up_s, *sh_down_q, *sh_down_s;
+    unsigned long long* hw;  // [kMaxPos][I/32][kHWords]: h by kept position, epoch-tagged words
     uint32_t* launches;     // [G]: launches CTA c has completed (its epoch - 1)
     uint16_t* x_stage;      // CTA 0's device copy of a host x, or null
     uint32_t* x_flag;       // x_stage written (the launch's epoch)
@@ -123,53 +129,57 @@ struct Args {
     int stall_h;            // test hook: the h waits expect a value no CTA writes
     int nbmax, dmax;        // the largest h-block count and down range of a CTA (smem sizing)
     int RG, RD, spb;        // rows per gate/up and per down stage, stages per h block
+    int RGs, RDs, spbs;     // the same for the shared expert's fp8 rows
     const int32_t* rows;    // [k][G + 1]: CTA c's down rows [rows[c], rows[c + 1]) for m = 1 .. k kept
     unsigned long long* trace;  // [G][8] ns stamps (+ CTA 0's stages [64][3]), or null
 };
 
 // ------------------------------------------------------------- work split --
-// Output rows [r0, r1) of CTA c: the CTAs' stream bytes are about equal.
-// Gate/up block b goes to CTA b mod G; a CTA with n blocks has the capacity
-// max(0, W / G - n * Wgu) for down rows (W = all bytes), the H rows are cut in
-// proportion to the capacities (prefix sums, so the ranges tile [0, H) in CTA
-// order), and every cut is rounded to a multiple of 4 rows (H is one).
-struct Split {
-    int r0, r1;
-};
-__host__ __device__ inline int cut_rows(long long c, long long G, int m, int H, int I) {
-    const long long FB = I / 32, NB = (long long)m * FB;
-    const long long q0 = NB / G, rr = NB % G;
-    const long long Wgu = 64LL * (H / 2 + H / 32), Wdn = (long long)m * (I / 2 + I / 32);
-    const long long Wg = (NB * Wgu + (long long)H * Wdn) / G;
-    const long long capA = Wg > (q0 + 1) * Wgu ? Wg - (q0 + 1) * Wgu : 0;  // CTAs c < rr
-    const long long capB = Wg > q0 * Wgu ? Wg - q0 * Wgu : 0;
-    auto cap = [&](long long x) { return (x < rr ? x : rr) * capA + (x > rr ? x - rr : 0) * capB; };
-    const long long total = cap(G);
-    const long long r = total <= 0 ? c * H / G : H * cap(c) / total;
-    return (int)((r + 2) / 4 * 4);
-}
-__host__ __device__ inline Split down_rows(int c, int G, int m, int H, int I) {
-    Split s;
-    s.r0 = cut_rows(c, G, m, H, I);
-    s.r1 = c + 1 == G ? H : cut_rows(c + 1, G, m, H, I);
-    if (s.r1 > H) s.r1 = H;
-    if (s.r0 > s.r1) s.r0 = s.r1;
-    return s;
+// Output rows [cut[x], cut[x + 1]) of CTA x (x = 0 .. G - 1), so that the
+// CTAs' stream bytes are about equal.  The h blocks -- m * I / 32 routed ones,
+// then I / 32 of the shared expert -- go to CTA b mod G; a CTA's capacity for
+// down rows is max(0, W / G - its gate/up bytes) (W = all bytes), the H rows
+// are cut in proportion to the capacities (prefix sums, so the ranges tile
+// [0, H) in CTA order), and every cut is rounded to a multiple of 4 rows (H is
+// one).  Host only: the kernel reads the table.
+inline void split_rows(int G, int m, int H, int I, bool nv, bool sh, int* cut) {
+    const long long sb = nv ? 16 : 32;  // elements per weight scale byte
+    const long long FB = I / 32, NBr = (long long)m * FB, NB = NBr + (sh ? FB : 0);
+    const long long Wr = 64LL * (H / 2 + H / sb), Ws = 64LL * H;  // a routed / the shared expert's h block
+    const long long Wdn = (long long)m * (I / 2 + I / sb) + (sh ? I : 0);  // one output row of every expert
+    const long long Wg = (NBr * Wr + (NB - NBr) * Ws + (long long)H * Wdn) / G;
+    auto cap = [&](long long x) {
+        const long long nr = x < NBr ? (NBr - 1 - x) / G + 1 : 0, nt = x < NB ? (NB - 1 - x) / G + 1 : 0;
+        const long long gu = nr * Wr + (nt - nr) * Ws;
+        return Wg > gu ? Wg - gu : 0;
+    };
+    long long total = 0;
+    for (long long x = 0; x < G; ++x) total += cap(x);
+    long long pre = 0;
+    for (long long x = 0; x < G; ++x) {
+        const long long r = total <= 0 ? x * H / G : H * pre / total;
+        cut[x] = (int)((r + 2) / 4 * 4);
+        if (cut[x] > H) cut[x] = H;
+        pre += cap(x);
+    }
+    cut[G] = H;
 }
 
 // Shared-memory layout (bytes), the same on the host and the device.
 struct Layout {
-    int ring, route, lg, bars, pgu, pdn, hraw, total;
-    __host__ __device__ Layout(int H, int I, int nbmax, int dmax, bool nv) {
+    int ring, route, lg, bars, pgu, pdn, hraw, shs, total;
+    __host__ __device__ Layout(int H, int I, int nbmax, int dmax, bool nv, bool sh) {
         const int NQ = H / kSeg, NQd = I / kSeg;
         ring = 0;                                     // [kStages][stage_bytes(nv)]
         route = ring + kStages * stage_bytes(nv);     // sel, w_t, seg_e, seg_w, prod_e [8] each; words [16]
         lg = route + 256;                             // the logits [E <= 1024], candidates [256] x 2
-        bars = lg + 4096 + 2048;  // full [kStages], empty [kStages], blk [nbmax], h_ready [kMaxK]
-        pgu = bars + ((8 * (2 * kStages + nbmax + kMaxK) + 15) / 16) * 16;  // [nbmax][NQ][64] f32
-        pdn = pgu + nbmax * NQ * 64 * 4;              // [kMaxK][NQd][dmax] f32
-        hraw = pdn + ((kMaxK * NQd * dmax * 4 + 15) / 16) * 16;  // [kMaxK][I/32][kHWords] h words as published
-        total = hraw + kMaxK * (I / 32) * kHWords * 8;
+        const int np = sh ? kMaxPos : kMaxK;          // positions with h: the kept experts (+ the shared one)
+        bars = lg + 4096 + 2048;  // full [kStages], empty [kStages], blk [nbmax], h_ready [kMaxPos]
+        pgu = bars + ((8 * (2 * kStages + nbmax + kMaxPos) + 15) / 16) * 16;  // [nbmax][NQ][64] f32
+        pdn = pgu + nbmax * NQ * 64 * 4;              // [np][NQd][dmax] f32
+        hraw = pdn + ((np * NQd * dmax * 4 + 15) / 16) * 16;  // [np][I/32][kHWords] h words as published
+        shs = hraw + np * (I / 32) * kHWords * 8;     // the shared expert's tile scales: gate, up, down
+        total = shs + (sh ? ((3 * (I / 128) * (H / 128) + 15) / 16) * 16 : 0);
     }
 };
 // words of the route area
@@ -214,6 +224,32 @@ __device__ __forceinline__ float2 block_dot_halves(const uint4& w, const uint32_
         for (int j = 0; j < 4; ++j) acc[i] = dot2_f16_f32(h[j], op[4 * i + j], acc[i]);
     }
     return make_float2(acc[0] + acc[1], acc[2] + acc[3]);
+}
+// The block's dot product for e4m3 weight codes (the shared expert): 32
+// bytes (two 16-byte loads) against op, four partial sums of 8.
+__device__ __forceinline__ float block_dot_fp8(const uint4& w0, const uint4& w1, const uint32_t (&op)[16]) {
+    const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+    float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        acc[i >> 1] = dot2_f16_f32(e4m3x2_to_f16x2(ws[i]), op[2 * i], acc[i >> 1]);
+        acc[i >> 1] = dot2_f16_f32(e4m3x2_to_f16x2(ws[i] >> 16), op[2 * i + 1], acc[i >> 1]);
+    }
+    return (acc[0] + acc[1]) + (acc[2] + acc[3]);
+}
+// The operand of a down run: a lane's published h block (6 tagged words): its
+// codes as f16 pairs, its scale from the last word.
+__device__ __forceinline__ void load_h(const unsigned long long* hp, uint32_t (&op)[16], float& opsf) {
+#pragma unroll
+    for (int w = 0; w < 5; ++w) {
+        const unsigned long long hv = hp[w];
+        op[3 * w] = e4m3x2_to_f16x2((uint32_t)hv);
+        op[3 * w + 1] = e4m3x2_to_f16x2((uint32_t)(hv >> 16));
+        op[3 * w + 2] = e4m3x2_to_f16x2((uint32_t)(hv >> 32));
+    }
+    const unsigned long long h5 = hp[5];
+    op[15] = e4m3x2_to_f16x2((uint32_t)h5);
+    opsf = ue8m0_to_f32((uint32_t)(h5 >> 16) & 0xFFu);
 }
 // Two e4m3 scale bytes (the first in the low byte) -> fp32.
 __device__ __forceinline__ float2 e4m3x2_to_f32x2(uint32_t two) {
@@ -310,10 +346,11 @@ __device__ __forceinline__ void trace_event(const Args& a, int i) {
 // rows of every kept expert, as the flat list u = s * d + o (s ascending, o
 // the row in [r0, r0 + d)), RD rows a stage.
 struct Plan {
-    int c, G, FB, H, I, m, nb, r0, d;
-    int RG, RD, spb;  // rows per gate/up and per down stage, stages per h block
-    int ngu, n;       // gate/up stages, all stages
+    int c, G, FB, H, I, m, nb, nbr, r0, d;
+    int RG, RD, spb, RGs, RDs, spbs;  // rows per gate/up and per down stage, stages per h block (routed, shared)
+    int ngur, ngu, ndr, n;            // stages: routed gate/up, all gate/up, + routed down, all
 };
+template <bool kSh>
 __device__ __forceinline__ void make_plan(Plan& p, const Args& a, int c, int G, int m, const int32_t* cuts) {
     p.c = c;
     p.G = G;
@@ -321,23 +358,45 @@ __device__ __forceinline__ void make_plan(Plan& p, const Args& a, int c, int G, 
     p.H = a.H;
     p.I = a.I;
     p.m = m;
-    p.nb = c < m * p.FB ? (m * p.FB - c + G - 1) / G : 0;  // this CTA's h blocks: c, c + G, ...
+    const int NBr = m * p.FB, NB = NBr + (kSh ? p.FB : 0);
+    p.nbr = c < NBr ? (NBr - c + G - 1) / G : 0;  // this CTA's h blocks: c, c + G, .. (routed first)
+    p.nb = c < NB ? (NB - c + G - 1) / G : 0;
     p.r0 = cuts[2 * (m - 1)];
     p.d = cuts[2 * (m - 1) + 1] - p.r0;
     p.RG = a.RG;
     p.RD = a.RD;
     p.spb = a.spb;
-    p.ngu = p.nb * p.spb;
-    p.n = p.ngu + (m * p.d + p.RD - 1) / p.RD;
+    p.RGs = a.RGs;
+    p.RDs = a.RDs;
+    p.spbs = a.spbs;
+    p.ngur = p.nbr * p.spb;
+    p.ngu = p.ngur + (p.nb - p.nbr) * p.spbs;
+    p.ndr = p.ngu + (m * p.d + p.RD - 1) / p.RD;
+    p.n = p.ndr + (kSh ? (p.d + p.RDs - 1) / p.RDs : 0);
 }
 // (producer) The copies of stage i into the ring buffer at dst, completing on
 // the barrier fb: one contiguous run of codes and one of scale bytes per
 // expert the stage's rows belong to.
-template <bool kNv>
+template <bool kNv, bool kSh>
 __device__ __forceinline__ void issue_stage(const Args& a, const Plan& p, const int* seg_e, int i, uint8_t* dst,
                                             uint32_t fb) {
     constexpr int SB = kNv ? 16 : 32;  // elements per scale byte
-    if (i < p.ngu) {
+    if (kSh && i >= p.ngur && i < p.ngu) {
+        // a shared-expert gate/up stage: RGs fp8 rows of block j (scales: in shared memory)
+        const int i2 = i - p.ngur, j2 = i2 / p.spbs, row0 = (i2 - j2 * p.spbs) * p.RGs;
+        const int fb32 = p.c + (p.nbr + j2) * p.G - p.m * p.FB;
+        const int f = 32 * fb32 + (row0 & 31), up = row0 >> 5;
+        const size_t grow = (size_t)(f >> 7) * 256 + up * 128 + (f & 127);
+        const uint32_t cb = (uint32_t)(p.RGs * p.H);
+        mbar_arrive_expect_tx(fb, cb);
+        bulk_load(smem_u32(dst), a.sh_gu_q + grow * p.H, cb, fb);
+    } else if (kSh && i >= p.ndr) {
+        // a shared-expert down stage: up to RDs fp8 rows of the CTA's range
+        const int u0 = (i - p.ndr) * p.RDs, u1 = min(u0 + p.RDs, p.d);
+        const uint32_t cb = (uint32_t)((u1 - u0) * p.I);
+        mbar_arrive_expect_tx(fb, cb);
+        bulk_load(smem_u32(dst), a.sh_down_q + (size_t)(p.r0 + u0) * p.I, cb, fb);
+    } else if (i < p.ngur) {
         const int j = i / p.spb, row0 = (i - j * p.spb) * p.RG;
         const int b = p.c + j * p.G, s = b / p.FB, fb32 = b - s * p.FB;
         const int e = seg_e[s], f = 32 * fb32 + (row0 & 31), up = row0 >> 5;
@@ -347,7 +406,7 @@ __device__ __forceinline__ void issue_stage(const Args& a, const Plan& p, const 
         bulk_load(smem_u32(dst), a.gu_q + grow * (p.H / 2), cb, fb);
         bulk_load(smem_u32(dst + kStageCodes), (up ? a.up_s : a.gate_s) + ((size_t)e * p.I + f) * (p.H / SB), sb, fb);
     } else {
-        const int u0 = (i - p.ngu) * p.RD, u1 = min(u0 + p.RD, p.m * p.d);
+        const int u0 = (i - p.ngu) * p.RD, u1 = min(u0 + p.RD, p.m * p.d);  // (routed down)
         mbar_arrive_expect_tx(fb, (uint32_t)(u1 - u0) * (uint32_t)(p.I / 2 + p.I / SB));
         for (int u = u0; u < u1;) {
             const int s = u / p.d, o = u - s * p.d, n = min(u1 - u, p.d - o);
@@ -366,15 +425,15 @@ __device__ __forceinline__ void issue_stage(const Args& a, const Plan& p, const 
 // 32 fb + f), then the block's tagged words: lane 4w stores codes 4w .. 4w + 3
 // (the first in the low byte), lane 0 the scale byte.
 template <bool kNv>
-__device__ void publish_block(const Args& a, const float* pgu, const int* seg_e, int j, int b, int FB, int NQ,
-                              uint32_t epoch, int lane) {
+__device__ void publish_block(const Args& a, const float* pgu, const int* seg_e, int m, int j, int b, int FB,
+                              int NQ, uint32_t epoch, int lane) {
     const int s = b / FB, fb = b - s * FB;
     float g = 0.f, u = 0.f;
     for (int q = 0; q < NQ; ++q) {
         g += pgu[(j * NQ + q) * 64 + lane];
         u += pgu[(j * NQ + q) * 64 + 32 + lane];
     }
-    if (kNv) {  // the matrix scales multiply the finished dot products
+    if (kNv && b < m * FB) {  // (routed) the matrix scales multiply the finished dot products
         g *= __ldg(a.gate_g + seg_e[s]);
         u *= __ldg(a.up_g + seg_e[s]);
     }
@@ -395,11 +454,11 @@ __device__ void publish_block(const Args& a, const float* pgu, const int* seg_e,
 
 // 20 warps: 16 compute warps, the producer, the publisher and two gatherers
 // (at most 96 registers a thread: 5 warps on one SM quarter).
-template <bool kNv>
+template <bool kNv, bool kSh>
 __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_constant__ Args a) {
     constexpr int kStageBytes = stage_bytes(kNv), kSB = kNv ? 16 : 32;  // (kSB: elements per scale byte)
     extern __shared__ __align__(128) uint8_t smem[];
-    const Layout Lo(a.H, a.I, a.nbmax, a.dmax, kNv);
+    const Layout Lo(a.H, a.I, a.nbmax, a.dmax, kNv, kSh);
     int* sel = reinterpret_cast<int*>(smem + Lo.route);  // [8] the router's selection, in router order
     float* w_t = reinterpret_cast<float*>(sel + 8);
     int* seg_e = reinterpret_cast<int*>(w_t + 8);         // [8] the kept experts, ascending
@@ -414,6 +473,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
     float* pgu = reinterpret_cast<float*>(smem + Lo.pgu);
     float* pdn = reinterpret_cast<float*>(smem + Lo.pdn);
     unsigned long long* hraw = reinterpret_cast<unsigned long long*>(smem + Lo.hraw);
+    uint8_t* shs = smem + Lo.shs;  // the shared expert's tile scales: gate, up [I/128][H/128], down [H/128][I/128]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int G = gridDim.x, c = blockIdx.x;
     const int NQ = a.H / kSeg, NQd = a.I / kSeg, FB = a.I / 32;
@@ -425,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             mbar_init(empty0 + 8u * st, kComputeWarps);
         }
         for (int j = 0; j < a.nbmax; ++j) mbar_init(blk0 + 8u * j, kComputeWarps);
-        for (int s = 0; s < kMaxK; ++s) mbar_init(hrdy0 + 8u * s, 64);
+        for (int s = 0; s < kMaxPos; ++s) mbar_init(hrdy0 + 8u * s, 64);
         *abort_flag = 0;
         tc::fence_mbar_init();
     }
@@ -433,6 +493,11 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
     pdl_launch_dependents();
     pdl_wait();
     stamp(a, 0);
+    if (kSh) {  // the shared expert's tile scales (3 x (I/128)(H/128) bytes), in place before the routing barrier
+        const int nt = (a.I / 128) * (a.H / 128);
+        for (int i = threadIdx.x; i < 3 * nt; i += kThreads)
+            shs[i] = i < nt ? __ldg(a.sh_gate_s + i) : i < 2 * nt ? __ldg(a.sh_up_s + i - nt) : __ldg(a.sh_down_s + i - 2 * nt);
+    }
     // (producer lanes j < k) CTA c's down-row cuts for j + 1 kept experts,
     // in flight during the routing
     if (warp == kProducer && lane < a.k) {
@@ -530,10 +595,10 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             if (lane < m) prod_e[pos] = e;
             __syncwarp();
             if (m > 0) {
-                make_plan(p, a, c, G, m, cuts);
+                make_plan<kSh>(p, a, c, G, m, cuts);
                 i0 = min(p.n, kStages);
                 if (lane < i0) {
-                    issue_stage<kNv>(a, p, prod_e, lane, smem + Lo.ring + lane * kStageBytes, full0 + 8u * lane);
+                    issue_stage<kNv, kSh>(a, p, prod_e, lane, smem + Lo.ring + lane * kStageBytes, full0 + 8u * lane);
                     trace_event(a, 128 + lane);
                 }
                 if (lane == 0) stamp(a, 4);
@@ -544,7 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             m = words[W_M];
             if (lane < m) prod_e[lane] = seg_e[lane];
             __syncwarp();
-            if (m > 0) make_plan(p, a, c, G, m, cuts);
+            if (m > 0) make_plan<kSh>(p, a, c, G, m, cuts);
         }
         if (m > 0 && lane == 0) {
             int slot = i0 % kStages;
@@ -556,7 +621,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                     break;
                 }
                 if (i == 0) stamp(a, 4);
-                issue_stage<kNv>(a, p, prod_e, i, smem + Lo.ring + slot * kStageBytes, full0 + 8u * slot);
+                issue_stage<kNv, kSh>(a, p, prod_e, i, smem + Lo.ring + slot * kStageBytes, full0 + 8u * slot);
                 trace_event(a, 128 + i);
                 if (++slot == kStages) {
                     slot = 0;
@@ -622,12 +687,13 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         __syncthreads();  // (the routing weights)
     }
     const int m = words[W_M];
+    const int mp = m > 0 ? m + (kSh ? 1 : 0) : 0;  // positions with h this launch: the kept experts, then the shared one
     if (warp == kService) {
-        // blocks of the kept positions m .. k - 1 (round-robin like the
+        // blocks of the positions mp .. k + sh - 1 (round-robin like the
         // published ones): their words get this launch's tag, so that no word
         // is ever more than one launch old
         const unsigned long long inval = 0;
-        for (int b = m * FB + ((c - m * FB) % G + G) % G; b < a.k * FB; b += G)
+        for (int b = mp * FB + ((c - mp * FB) % G + G) % G; b < (a.k + (kSh ? 1 : 0)) * FB; b += G)
             if (lane < kHWords) st_tagged(a.hw + (size_t)b * kHWords + lane, inval, epoch);
     }
     if (m == 0) {
@@ -638,7 +704,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         return;
     }
     Plan p;
-    make_plan(p, a, c, G, m, cuts);
+    make_plan<kSh>(p, a, c, G, m, cuts);
 
     if (warp == kService) {
         // ------------------------------------------------------ publisher
@@ -651,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                 break;
             }
             if (lane == 0) trace_event(a, 192 + j);
-            publish_block<kNv>(a, pgu, seg_e, j, c + j * G, FB, NQ, epoch, lane);
+            publish_block<kNv>(a, pgu, seg_e, m, j, c + j * G, FB, NQ, epoch, lane);
             if (lane == 0) trace_event(a, 200 + j);
         }
         if (!ok && lane == 0) {
@@ -674,8 +740,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         const int P = max(1, 64 * kGatherWords / nwe);  // (nwe <= 64 kGatherWords: I <= kMaxI)
         auto klo = [&](int e) { return min(kGatherWords, max(0, (e * nwe - 32 * gi - lane + 63) / 64)); };
         bool ok = true;
-        for (int s0 = 0; s0 < m; s0 += P) {
-            const int np = min(P, m - s0), nf = np * nwe;
+        for (int s0 = 0; s0 < mp; s0 += P) {
+            const int np = min(P, mp - s0), nf = np * nwe;
             const unsigned long long* src = a.hw + (size_t)s0 * nwe;
             unsigned long long* dst = hraw + (size_t)s0 * nwe;
             uint32_t todo = 0, left = (1u << np) - 1u;
@@ -714,7 +780,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                     *abort_flag = 1;
                     raise_flag(a.err, ERR_TIMEOUT);
                 }
-                for (int sp = s0 + np; sp < m; ++sp) mbar_arrive(hrdy0 + 8u * sp);
+                for (int sp = s0 + np; sp < mp; ++sp) mbar_arrive(hrdy0 + 8u * sp);
                 break;
             }
         }
@@ -728,6 +794,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
         // is a multiple of 4).  After warp_sum4 lane 8 t holds row t's sum.
         const int t4 = 2 * ((lane >> 4) & 1) + ((lane >> 3) & 1);
         const bool writer = (lane & 7) == 0;
+        const int nt = (a.I / 128) * (a.H / 128);  // tiles of a shared-expert matrix
         int slot = 0;
         uint32_t par = 0;
         bool ok = true;
@@ -738,8 +805,8 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             const uint8_t* wb = smem + Lo.ring + kRun * g * rowb + qx * 512 + lane * 16;
             const uint8_t* sb = smem + Lo.ring + kStageCodes + kRun * g * scb + (qx * 32 + lane) * (32 / kSB);
             float* pw = pgu + qx * 64 + kRun * g + t4;
-            int row0 = 0, j = 0;
-            for (int i = 0; i < p.ngu; ++i) {
+            int row0 = 0, j = 0;  // h block j of this CTA, its rows row0 .. in the current stage
+            for (int i = 0; i < p.ngur; ++i) {
                 ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8u * slot, par, a.wait_ns, abort_flag));
                 if (!ok) break;
                 const uint8_t* w = wb + slot * kStageBytes;
@@ -772,6 +839,42 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                 }
             }
         }
+        if (kSh && ok && p.ngu > p.ngur) {
+            // the shared expert's gate/up blocks: e4m3 rows of H bytes, RGs a
+            // stage, this warp rows 2 g, 2 g + 1 (two 16-byte loads a row per
+            // lane); one UE8M0 scale per 128 x 128 tile, in shared memory
+            const int g = warp / NQ;
+            const uint8_t* wb = smem + Lo.ring + kRunS * g * a.H + qx * 1024 + lane * 32;
+            float* pw = pgu + qx * 64 + kRunS * g + t4;
+            int row0 = 0, j = p.nbr;  // (the shared expert's blocks follow the routed ones)
+            for (int i = p.ngur; i < p.ngu; ++i) {
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8u * slot, par, a.wait_ns, abort_flag));
+                if (!ok) break;
+                const uint8_t* w = wb + slot * kStageBytes;
+                const uint4 w00 = *reinterpret_cast<const uint4*>(w), w01 = *reinterpret_cast<const uint4*>(w + 16);
+                const uint4 w10 = *reinterpret_cast<const uint4*>(w + a.H);
+                const uint4 w11 = *reinterpret_cast<const uint4*>(w + a.H + 16);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+                const int f = 32 * (c + j * G - m * FB);  // the block's first feature
+                const float sc = ue8m0_to_f32(shs[(row0 < 32 ? 0 : nt) + (f >> 7) * (a.H / 128) + qx * 8 + (lane >> 2)]);
+                const float v0 = block_dot_fp8(w00, w01, op) * sc * opsf;
+                const float v1 = block_dot_fp8(w10, w11, op) * sc * opsf;
+                const float r = warp_sum4(v0, v1, 0.f, 0.f, lane);
+                if (writer && t4 < kRunS) pw[j * NQ * 64 + row0] = r;
+                if (++slot == kStages) {
+                    slot = 0;
+                    par ^= 1u;
+                }
+                row0 += p.RGs;
+                if (row0 == 64) {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(blk0 + 8u * j);
+                    row0 = 0;
+                    ++j;
+                }
+            }
+        }
         if (ok) {
             // down: the CTA's (kept expert s, row o) pairs as the flat list
             // u = s d + o, RD a stage; the warp's run starts at u, the operand
@@ -780,7 +883,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             const uint8_t* wb = smem + Lo.ring + kRun * g * rowb + qh * 512 + lane * 16;
             const uint8_t* sb = smem + Lo.ring + kStageCodes + kRun * g * scb + (qh * 32 + lane) * (32 / kSB);
             int u = kRun * g, s = 0, sbase = 0, cur = -1;
-            for (int i = p.ngu; i < p.n; ++i, u += p.RD) {
+            for (int i = p.ngu; i < p.ndr; ++i, u += p.RD) {
                 const bool live = u < md;
                 if (live) {
                     while (u >= sbase + p.d) {
@@ -793,19 +896,7 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                             ok = false;
                             break;
                         }
-                        // this lane's block of h (qh 32 + lane): its 6 words,
-                        // the codes as f16 pairs, the scale from the last word
-                        const unsigned long long* hp = hraw + ((size_t)s * FB + qh * 32 + lane) * kHWords;
-#pragma unroll
-                        for (int w = 0; w < 5; ++w) {
-                            const unsigned long long hv = hp[w];
-                            op[3 * w] = e4m3x2_to_f16x2((uint32_t)hv);
-                            op[3 * w + 1] = e4m3x2_to_f16x2((uint32_t)(hv >> 16));
-                            op[3 * w + 2] = e4m3x2_to_f16x2((uint32_t)(hv >> 32));
-                        }
-                        const unsigned long long h5 = hp[5];
-                        op[15] = e4m3x2_to_f16x2((uint32_t)h5);
-                        opsf = ue8m0_to_f32((uint32_t)(h5 >> 16) & 0xFFu);
+                        load_h(hraw + ((size_t)s * FB + qh * 32 + lane) * kHWords, op, opsf);
                         cur = s;
                     }
                 }
@@ -828,6 +919,38 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
                     for (int t = 0; t < kRun; ++t) v[t] = scaled_block<kNv>(wv[t], op, sv[t]) * opsf;
                     const float r = warp_sum4(v[0], v[1], v[2], v[3], lane);
                     if (writer) pdn[(s * NQd + qh) * a.dmax + (u - sbase) + t4] = r;
+                }
+                if (++slot == kStages) {
+                    slot = 0;
+                    par ^= 1u;
+                }
+            }
+        }
+        if (kSh && ok && p.n > p.ndr) {
+            // the shared expert's down rows: e4m3 rows of I bytes, RDs a stage
+            // (this warp rows u, u + 1 of the CTA's range), h of position m
+            ok = __all_sync(0xFFFFFFFFu, mbar_wait(hrdy0 + 8u * m, 0, a.wait_ns, abort_flag));
+            if (ok && *abort_flag) ok = false;
+            if (ok) load_h(hraw + ((size_t)m * FB + qh * 32 + lane) * kHWords, op, opsf);
+            const int g = warp / NQd;
+            const uint8_t* wb = smem + Lo.ring + kRunS * g * a.I + qh * 1024 + lane * 32;
+            int u = kRunS * g;
+            for (int i = p.ndr; ok && i < p.n; ++i, u += p.RDs) {
+                ok = __all_sync(0xFFFFFFFFu, mbar_wait(full0 + 8u * slot, par, a.wait_ns, abort_flag));
+                if (!ok) break;
+                const uint8_t* w = wb + slot * kStageBytes;
+                const uint4 w00 = *reinterpret_cast<const uint4*>(w), w01 = *reinterpret_cast<const uint4*>(w + 16);
+                const uint4 w10 = *reinterpret_cast<const uint4*>(w + a.I);
+                const uint4 w11 = *reinterpret_cast<const uint4*>(w + a.I + 16);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(empty0 + 8u * slot);
+                if (u < p.d) {  // (rows u, u + 1: d is even; one 128-row tile, u and r0 being even)
+                    const int row = p.r0 + u;
+                    const float sc = ue8m0_to_f32(shs[2 * nt + (row >> 7) * (a.I / 128) + qh * 8 + (lane >> 2)]);
+                    const float v0 = block_dot_fp8(w00, w01, op) * sc * opsf;
+                    const float v1 = block_dot_fp8(w10, w11, op) * sc * opsf;
+                    const float r = warp_sum4(v0, v1, 0.f, 0.f, lane);
+                    if (writer && t4 < kRunS) pdn[(m * NQd + qh) * a.dmax + u + t4] = r;
                 }
                 if (++slot == kStages) {
                     slot = 0;
@@ -858,33 +981,47 @@ __global__ void __launch_bounds__(kThreads, 1) k_decode_gemv(const __grid_consta
             if (kNv) y *= __ldg(a.down_g + seg_e[s]);  // the matrix scale of the finished dot product
             o += seg_w[s] * y;
         }
+        if (kSh) {  // the shared expert, unweighted, last
+            float y = 0.f;
+            for (int q = 0; q < NQd; ++q) y += pdn[(m * NQd + q) * a.dmax + i];
+            o += y;
+        }
         a.out[p.r0 + i] = o;
     }
 }
 
 // ------------------------------------------------------------------- host --
+void split_table(int G, int m, int H, int I, bool nv, bool sh, int* cut) { split_rows(G, m, H, I, nv, sh, cut); }
+
 bool supported(const moe_layer* L) {
     const moe_config& c = L->cfg;
-    const int NQ = c.hidden / kSeg, NQd = c.inter / kSeg;
-    (void)NQ;
-    (void)NQd;
-    return (c.weight_format == MOE_WEIGHTS_MXFP4 || c.weight_format == MOE_WEIGHTS_NVFP4) && !c.has_shared &&
-           c.top_k <= kMaxK && c.n_experts <= 1024 && L->gv_smem > 0;
+    return (c.weight_format == MOE_WEIGHTS_MXFP4 || c.weight_format == MOE_WEIGHTS_NVFP4) && c.top_k <= kMaxK &&
+           c.n_experts <= 1024 && L->gv_smem > 0;
 }
 
-// The largest h-block count and down range of a CTA over the kept counts
-// 1 .. k, and the shared memory they need (0: more than a CTA has).
-int smem_bytes(const moe_config& c, int G, int* nbmax, int* dmax) {
-    const int FB = c.inter / 32;
-    *nbmax = (c.top_k * FB + G - 1) / G;
+// The down-row cuts of every kept count 1 .. k ([k][G + 1]), the largest h-block
+// count and down range of a CTA over them, and the shared memory they need
+// (0: more than a CTA has).
+int smem_bytes(const moe_config& c, int G, int32_t* tab, int* nbmax, int* dmax) {
+    const int FB = c.inter / 32, sh = c.has_shared ? 1 : 0;
+    const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
+    *nbmax = ((c.top_k + sh) * FB + G - 1) / G;
     *dmax = 4;
-    for (int m = 1; m <= c.top_k; ++m)
-        for (int x = 0; x < G; ++x) {
-            const Split s = down_rows(x, G, m, c.hidden, c.inter);
-            if (s.r1 - s.r0 > *dmax) *dmax = s.r1 - s.r0;
-        }
-    const Layout Lo(c.hidden, c.inter, *nbmax, *dmax, c.weight_format == MOE_WEIGHTS_NVFP4);
+    for (int m = 1; m <= c.top_k; ++m) {
+        int32_t* cut = tab + (size_t)(m - 1) * (G + 1);
+        split_rows(G, m, c.hidden, c.inter, nv, sh != 0, cut);
+        for (int x = 0; x < G; ++x)
+            if (cut[x + 1] - cut[x] > *dmax) *dmax = cut[x + 1] - cut[x];
+    }
+    const Layout Lo(c.hidden, c.inter, *nbmax, *dmax, nv, sh != 0);
     return Lo.total <= 227 * 1024 ? Lo.total : 0;
+}
+
+static const void* kernel_for(bool nv, bool sh) {
+    return nv ? (sh ? reinterpret_cast<const void*>(k_decode_gemv<true, true>)
+                    : reinterpret_cast<const void*>(k_decode_gemv<true, false>))
+              : (sh ? reinterpret_cast<const void*>(k_decode_gemv<false, true>)
+                    : reinterpret_cast<const void*>(k_decode_gemv<false, false>));
 }
 
 cudaError_t init(moe_layer* L) {
@@ -896,26 +1033,25 @@ cudaError_t init(moe_layer* L) {
     if (c.hidden % kSeg || c.inter % kSeg || c.inter > kMaxI || c.hidden < 2 * kSeg ||
         kComputeWarps % (c.hidden / kSeg) || kComputeWarps % (c.inter / kSeg))
         return cudaSuccess;
-    int nbmax = 0, dmax = 0;
-    const int bytes = smem_bytes(c, L->num_sms, &nbmax, &dmax);
-    if (bytes == 0) return cudaSuccess;
-    const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
-    const void* kern = nv ? reinterpret_cast<const void*>(k_decode_gemv<true>)
-                          : reinterpret_cast<const void*>(k_decode_gemv<false>);
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
-    if (e != cudaSuccess) return e;
-    int per_sm = 0;
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, bytes);
-    if (e != cudaSuccess) return e;
-    if (per_sm < 1) return cudaSuccess;
-    // the down-row cuts of every kept count 1 .. k (the same on every call)
     const int G = L->num_sms;
     int32_t* tab = new (std::nothrow) int32_t[(size_t)c.top_k * (G + 1)];
     if (!tab) return cudaErrorMemoryAllocation;
-    for (int m = 1; m <= c.top_k; ++m) {
-        for (int x = 0; x < G; ++x) tab[(size_t)(m - 1) * (G + 1) + x] = down_rows(x, G, m, c.hidden, c.inter).r0;
-        tab[(size_t)(m - 1) * (G + 1) + G] = c.hidden;
+    int nbmax = 0, dmax = 0;
+    const int bytes = smem_bytes(c, G, tab, &nbmax, &dmax);
+    if (bytes == 0) {
+        delete[] tab;
+        return cudaSuccess;
     }
+    const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
+    const void* kern = kernel_for(nv, c.has_shared != 0);
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    int per_sm = 0;
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, bytes);
+    if (e != cudaSuccess || per_sm < 1) {
+        delete[] tab;
+        return e;
+    }
+    // the down-row cuts of every kept count 1 .. k (the same on every call)
     e = cudaMalloc(&L->gv_rows, (size_t)c.top_k * (G + 1) * sizeof(int32_t));
     if (e == cudaSuccess)
         e = cudaMemcpy(L->gv_rows, tab, (size_t)c.top_k * (G + 1) * sizeof(int32_t), cudaMemcpyHostToDevice);
@@ -949,6 +1085,12 @@ cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t
     a.gate_g = L->gate_g;
     a.up_g = L->up_g;
     a.down_g = L->down_g;
+    a.sh = L->cfg.has_shared ? 1 : 0;
+    a.sh_gu_q = L->sh_gu_q;
+    a.sh_gate_s = L->sh_gate_s;
+    a.sh_up_s = L->sh_up_s;
+    a.sh_down_q = L->sh_down_q;
+    a.sh_down_s = L->sh_down_s;
     a.hw = reinterpret_cast<unsigned long long*>(L->gv_words + gv_hword_off(L->num_sms));
     a.launches = L->gv_words + kGvCountOff;
     a.x_flag = L->gv_words + 2;
@@ -962,6 +1104,9 @@ cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t
     a.RG = kStageCodes / (a.H / 2);
     a.RD = kStageCodes / (a.I / 2);
     a.spb = 64 / a.RG;
+    a.RGs = kStageCodes / a.H;
+    a.RDs = kStageCodes / a.I;
+    a.spbs = 64 / a.RGs;
     a.rows = L->gv_rows;
     a.trace = L->trace;
     cudaLaunchConfig_t cfg = {};
@@ -979,8 +1124,11 @@ cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t
     cfg.attrs = attr;
     cfg.numAttrs = 2;
     L->launches += 1;
-    return L->cfg.weight_format == MOE_WEIGHTS_NVFP4 ? cudaLaunchKernelEx(&cfg, k_decode_gemv<true>, a)
-                                                     : cudaLaunchKernelEx(&cfg, k_decode_gemv<false>, a);
+    const bool nv = L->cfg.weight_format == MOE_WEIGHTS_NVFP4, sh = L->cfg.has_shared != 0;
+    return nv ? (sh ? cudaLaunchKernelEx(&cfg, k_decode_gemv<true, true>, a)
+                    : cudaLaunchKernelEx(&cfg, k_decode_gemv<true, false>, a))
+              : (sh ? cudaLaunchKernelEx(&cfg, k_decode_gemv<false, true>, a)
+                    : cudaLaunchKernelEx(&cfg, k_decode_gemv<false, false>, a));
 }
 
 }  // namespace gemv

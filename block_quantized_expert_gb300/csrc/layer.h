@@ -107,12 +107,12 @@ inline int kSkCounters(const moe_layer* L) { return kSkZeroed(L) + kDecWords(L);
 
 // 32-bit words of the CUDA-core decode kernel, zeroed at creation: spare
 // [0, 2), staged-x flag [2], spare [3], the CTAs' launch counts [num_sms] from
-// kGvCountOff, then (8-byte aligned) the published h: [8 kept experts][I/32
-// blocks][6] 64-bit tagged words
+// kGvCountOff, then (8-byte aligned) the published h: [9 positions: up to 8
+// kept experts, then the shared expert][I/32 blocks][6] 64-bit tagged words
 constexpr int kGvCountOff = 4;
 inline size_t gv_hword_off(int num_sms) { return ((size_t)kGvCountOff + num_sms + 1) / 2 * 2; }
 inline size_t gv_words_count(const moe_config& c, int num_sms) {
-    return gv_hword_off(num_sms) + (size_t)2 * 8 * (c.inter / 32) * 6;
+    return gv_hword_off(num_sms) + (size_t)2 * 9 * (c.inter / 32) * 6;
 }
 
 // Launch with a programmatic (early-launch) edge to the previous kernel of the
@@ -173,7 +173,9 @@ void tc_free(moe_layer* L);
 // The one-token layer as a split-K GEMV on the CUDA cores (decode_gemv.cu).
 namespace gemv {
 cudaError_t init(moe_layer* L);      // sets gv_smem / gv_nbmax / gv_dmax (0: not available)
-bool supported(const moe_layer* L);  // shape, weight format, no shared expert, init succeeded
+bool supported(const moe_layer* L);  // shape, weight format, init succeeded
+// rows [cut[x], cut[x + 1]) of CTA x of G for m kept experts (cut: G + 1 entries)
+void split_table(int G, int m, int H, int I, bool nv, bool sh, int* cut);
 cudaError_t launch(moe_layer* L, const float* logits, const uint16_t* x, int32_t* ids, float* w, float* out,
                    cudaStream_t s, bool x_in_host);
 }  // namespace gemv

@@ -308,8 +308,23 @@ moe_status moe_set_wait_limit(moe_layer* layer, double seconds);
  * value no CTA ever writes, so every CTA's wait runs out after the wait
  * limit and the call ends with MOE_ERR_TIMEOUT at the next moe_check().
  * One-shot: the call after it runs normally.  MOE_ERR_UNSUPPORTED if the
- * layer has no decode kernel (shape, shared expert, or not an sm_103 GPU).  */
+ * layer has no decode kernel (shape, or not an sm_103 GPU).               */
 moe_status moe_test_stall_next_decode(moe_layer* layer);
+
+/* Host-side view of the CUDA-core decode kernel's work split, for tests (no
+ * GPU needed): cut[x], x = 0 .. num_sms, receives the first output row of
+ * CTA x of num_sms for `kept` kept experts of a layer with this hidden and
+ * inter size, NVFP4 (nvfp4 != 0) or MXFP4 weights and a shared expert
+ * (shared != 0) or none; CTA x owns rows [cut[x], cut[x + 1]) of every
+ * expert.  The h blocks (kept * inter / 32 routed ones, then the shared
+ * expert's inter / 32) go to CTA b mod num_sms; the rows are cut in
+ * proportion to what each CTA has left of an equal share of the stream
+ * bytes, every cut rounded to a multiple of 4.  cut (host, num_sms + 1
+ * ints) is caller-owned.  MOE_ERR_INVALID_ARG for num_sms < 1, kept < 1,
+ * hidden or inter not positive multiples of 1024 or above 8192, or a NULL
+ * cut.                                                                     */
+moe_status moe_test_decode_split(int num_sms, int kept, int hidden, int inter, int nvfp4, int shared,
+                                 int* cut);
 
 /* Token -> expert grouping without a layer and without any allocation.
  * The method's description has no counterpart: this entry point exists for callers that

@@ -2,7 +2,9 @@
 admit, against the fp64 oracle end to end: hidden sizes of 2048 .. 8192
 (2 .. 8 K segments of 1024 per gate/up row, so 32 .. 8 rows per gate/up
 stage), intermediate sizes of 1024 and 2048 (one or two K segments per down
-row), top-k from 1 to 8 over 8 .. 64 experts, MXFP4 and NVFP4-style weights.
+row), top-k from 1 to 8 over 8 .. 64 experts, MXFP4 and NVFP4-style weights,
+with and without the always-on shared expert (fp8 e4m3 rows with a UE8M0
+scale per 128 x 128 tile, added to the routed output unweighted, last).
 Each shape also runs on the grouped CUDA-core path, whose output it must
 match within the oracle tolerance."""
 import dataclasses
@@ -18,20 +20,23 @@ from workloads import CONFIGS, make_tokens, make_weights
 
 pytestmark = pytest.mark.gpu
 
-# (H, I, E, k, weight format)
+# (H, I, E, k, weight format, shared expert)
 SHAPES = [
-    (2048, 1024, 64, 8, "mxfp4"),
-    (4096, 1024, 32, 8, "mxfp4"),
-    (8192, 2048, 8, 6, "mxfp4"),
-    (8192, 1024, 8, 2, "mxfp4"),
-    (2048, 1024, 16, 1, "mxfp4"),
-    (2048, 2048, 16, 4, "nvfp4"),
+    (2048, 1024, 64, 8, "mxfp4", False),
+    (4096, 1024, 32, 8, "mxfp4", False),
+    (8192, 2048, 8, 6, "mxfp4", False),
+    (8192, 1024, 8, 2, "mxfp4", False),
+    (2048, 1024, 16, 1, "mxfp4", False),
+    (2048, 2048, 16, 4, "nvfp4", False),
+    (4096, 2048, 32, 6, "mxfp4", True),
+    (8192, 1024, 8, 8, "mxfp4", True),
+    (2048, 1024, 16, 3, "nvfp4", True),
 ]
 
 
-def _cfg(i, H, I, E, k, wfmt):
-    return dataclasses.replace(CONFIGS[1], index=60 + i, name=f"decode_shape_{H}x{I}x{E}k{k}_{wfmt}", H=H, I=I,
-                               E=E, k=k, T=1, steps=4, wfmt=wfmt)
+def _cfg(i, H, I, E, k, wfmt, shared):
+    return dataclasses.replace(CONFIGS[1], index=60 + i, name=f"decode_shape_{H}x{I}x{E}k{k}_{wfmt}_{shared}",
+                               H=H, I=I, E=E, k=k, T=1, steps=4, wfmt=wfmt, shared=shared)
 
 
 def _call(layer, cfg, lg, xb):
@@ -45,7 +50,8 @@ def _call(layer, cfg, lg, xb):
     return ids, w, out, bqe.moe_kernel_launches(layer) - n0
 
 
-@pytest.mark.parametrize("i", range(len(SHAPES)), ids=[f"{h}x{i}_E{e}_k{k}_{f}" for h, i, e, k, f in SHAPES])
+@pytest.mark.parametrize("i", range(len(SHAPES)),
+                         ids=[f"{h}x{i}_E{e}_k{k}_{f}{'_shared' if sh else ''}" for h, i, e, k, f, sh in SHAPES])
 def test_decode_kernel_shape(i):
     cfg = _cfg(i, *SHAPES[i])
     w = make_weights(cfg, seed=2000 + i, cache=False)
