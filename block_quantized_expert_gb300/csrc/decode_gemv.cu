@@ -90,14 +90,15 @@ constexpr int kStages = 5;
 constexpr int kMaxK = kMaxTopK;
 constexpr int kMaxPos = kMaxK + 1;            // kept positions: the routed experts, then the shared expert
 constexpr int kRunS = 2;                      // rows of a compute warp in a stage of fp8 (shared-expert) rows
-constexpr int kMaxI = 4096;                   // h of every kept expert resident as f16
+constexpr int kMaxI = 4096;                   // (the h words of every position are resident in shared memory)
 // A published h block (32 features): 6 64-bit words, word w holding e4m3 codes
 // 6w .. 6w + 5 in bytes 0 .. 5 (the last word: codes 30, 31 and the block's
 // scale byte in byte 2) and the low 8 bits of the launch's epoch in byte 7
 // (a single-copy atomic store: a reader that sees the tag sees the payload).
-// Every launch writes every block of the k kept positions -- published, or
-// (positions >= m) overwritten with a payload no reader uses -- so a word
-// older than the launch carries the previous launch's tag, never this one's.
+// Every launch writes every block of its k (+ 1 with the shared expert)
+// positions -- published, or (positions after the m kept ones and the shared
+// one) overwritten with a payload no reader uses -- so a word older than the
+// launch carries the previous launch's tag, never this one's.
 constexpr int kHWords = 6;
 constexpr int kGatherWords = 12;             // words a gather lane has in flight
 
@@ -131,7 +132,7 @@ struct Args {
     int RG, RD, spb;        // rows per gate/up and per down stage, stages per h block
     int RGs, RDs, spbs;     // the same for the shared expert's fp8 rows
     const int32_t* rows;    // [k][G + 1]: CTA c's down rows [rows[c], rows[c + 1]) for m = 1 .. k kept
-    unsigned long long* trace;  // [G][8] ns stamps (+ CTA 0's stages [64][3]), or null
+    unsigned long long* trace;  // diagnostics (see stamp / trace_event), or null
 };
 
 // ------------------------------------------------------------- work split --
