@@ -99,3 +99,38 @@ def test_decode_kernel_declines_shapes_it_cannot_hold():
     finally:
         layer.close()
         torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("setting", [(4, 0.0, 0.0), (6, 0.245, 0.3), (1, 0.0, 0.0)])
+def test_decode_kernel_shared_expert_with_pruning(setting):
+    """Tail pruning with the shared expert: the kept count m varies per
+    token, so the shared expert's position (m) and the down split move; the
+    output against the oracle on its own pruned routing (tokens whose keep
+    decision sits within fp32 reach of the threshold are skipped)."""
+    cfg = _cfg(20, 4096, 2048, 32, 6, "mxfp4", True)
+    w = make_weights(cfg, seed=2200, cache=False)
+    layer = G.make_layer(cfg, w, max_tokens=1)
+    try:
+        bqe.moe_set_route_prune(layer, *setting)
+        assert bqe.moe_decode_info(layer) == 1
+        tk = make_tokens(cfg, n=6)
+        keep, min_w, rho = setting
+        checked = 0
+        for t in range(6):
+            lg, xb = tk.logits[t:t + 1], tk.x_bits[t:t + 1]
+            rid, rw = orc.route_learned(lg, cfg.k, cfg.w_scale)
+            if min_w > 0 and not (np.abs(rw - min_w) > 1e-5).all():
+                continue
+            pid, pw = orc.route_prune(rid, rw, keep, min_w, rho)
+            ids, _, out, n = _call(layer, cfg, lg, xb)
+            assert n == 1
+            assert np.array_equal(ids.cpu().numpy(), pid)
+            ref = orc.layer_forward(w, xb, pid, pw)
+            norm, elem = G.compare_out(out.cpu().numpy(), ref)
+            assert norm <= G.NORM_TOL and elem <= G.ELEM_TOL, (t, norm, elem)
+            checked += 1
+        assert checked >= 4
+    finally:
+        bqe.moe_set_route_prune(layer, cfg.k)
+        layer.close()
+        torch.cuda.empty_cache()
