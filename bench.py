@@ -608,7 +608,7 @@ def trace_report(bqe, layer, step, i, dev):
     import torch
     sms = torch.cuda.get_device_properties(dev).multi_processor_count
     n_tr = 3  # the last three calls of the graph are traced
-    bufs = [torch.zeros(4 * sms * 12 + 4, dtype=torch.int64, device=dev) for _ in range(n_tr)]
+    bufs = [torch.zeros(max(48 * sms + 4, 8 * sms + 1024), dtype=torch.int64, device=dev) for _ in range(n_tr)]
     stream = torch.cuda.Stream(device=dev)
     g = torch.cuda.CUDAGraph()
     with torch.cuda.stream(stream):

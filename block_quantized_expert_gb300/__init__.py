@@ -377,7 +377,7 @@ def moe_check(layer: Layer, stream=None) -> int:
 
 
 def moe_set_trace(layer: Layer, buf):
-    """buf: CUDA int64 tensor of >= 4 * num_sms * 12 + 4 entries, or None."""
+    """buf: CUDA int64 tensor of >= max(48 * num_sms + 4, 8 * num_sms + 1024) entries, or None."""
     import torch
     if buf is None:
         _check(load_library().moe_set_trace(layer.ptr, None, 0), layer.ptr)

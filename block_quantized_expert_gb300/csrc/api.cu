@@ -372,8 +372,11 @@ unsigned long long moe_kernel_launches(const moe_layer* L) { return L ? L->launc
 
 moe_status moe_set_trace(moe_layer* L, unsigned long long* buf, size_t entries) {
     if (!L) return fail(nullptr, MOE_ERR_INVALID_ARG, "layer is NULL");
-    if (buf && entries < (size_t)4 * L->num_sms * 12 + 4)
-        return fail(L, MOE_ERR_INVALID_ARG, "trace buffer needs 4 * num_sms * 12 + 4 entries");
+    // the GEMMs' and front kernel's counters, and the CUDA-core decode kernel's
+    // per-CTA stamps followed by 4 x 256 event times
+    const size_t ng = (size_t)48 * L->num_sms + 4, nd = (size_t)8 * L->num_sms + 1024;
+    const size_t need = ng > nd ? ng : nd;
+    if (buf && entries < need) return fail(L, MOE_ERR_INVALID_ARG, "trace buffer needs %zu entries", need);
     L->trace = buf;
     return MOE_OK;
 }

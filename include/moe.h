@@ -230,8 +230,9 @@ moe_status moe_set_stage_events(moe_layer* layer, void* const* events, int n);
  * copy issued, final barrier] ns at buf + 8 * cta and, for CTAs 0, 1, 80 and
  * num_sms - 1 (t = 0 .. 3), event times at buf + 8 * num_sms + 256 * t + i
  * (i = 128 + stage: copy issued; 192 + j, 200 + j: h block j computed,
- * published; 208 + s: kept expert s's h gathered).  entries >= 4 * num_sms
- * * 12 + 4.  One-shot, like moe_set_stage_events.                        */
+ * published; 208 + s: kept expert s's h gathered).  entries >=
+ * max(48 * num_sms + 4, 8 * num_sms + 1024), else MOE_ERR_INVALID_ARG.
+ * One-shot, like moe_set_stage_events.                                    */
 moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entries);
 
 /* Number of CUDA kernels this layer has enqueued since moe_create (a launch
@@ -240,10 +241,10 @@ moe_status moe_set_trace(moe_layer* layer, unsigned long long* buf, size_t entri
 unsigned long long moe_kernel_launches(const moe_layer* layer);
 
 /* Kernel path of the GEMM steps: 0 = automatic (tcgen05 when the device is
- * sm_103, and moe_route_forward of one token as the single whole-layer
- * decode kernel when the shape allows: H <= 4096, I <= 2048, no shared
- * expert), 1 = CUDA-core kernels, 2 = tcgen05 block-scaled tensor-core
- * kernels only (never the decode kernel).  All compute the same layer; the
+ * sm_103, and a one-token moe_route_forward / moe_forward_host as a single
+ * whole-layer decode kernel where the shape allows one: see
+ * moe_set_decode_kernel), 1 = CUDA-core kernels, 2 = tcgen05 block-scaled
+ * tensor-core kernels only (never a decode kernel).  All compute the same layer; the
  * choice only affects speed and the order of fp32 additions.               */
 moe_status moe_set_gemm_path(moe_layer* layer, int path);
 
@@ -251,10 +252,10 @@ moe_status moe_set_gemm_path(moe_layer* layer, int path);
  * (moe_route_forward / moe_forward_host with T = 1) takes.  kind 0 =
  * automatic: the CUDA-core split-K GEMV kernel where the shape allows it
  * (MXFP4 or NVFP4 experts, H and I multiples of 1024 with H / 1024 and
- * I / 1024 dividing 16, H >= 2048, no shared expert, and its shared-memory
- * layout -- a 5-stage weight ring, the h of top_k experts, the CTA's
- * partial sums -- within 227 KB: e.g. I <= 2048 for top_k <= 8, not
- * I = 4096 with 6 experts), else the
+ * I / 1024 dividing 16, H >= 2048, with or without the shared expert, and
+ * its shared-memory layout -- a 5-stage weight ring, the h of the kept
+ * experts (and the shared one), the CTA's partial sums -- within 227 KB:
+ * e.g. I <= 2048 for top_k <= 8, not I = 4096 with 6 experts), else the
  * tcgen05 kernel (MXFP4, H <= 4096, I <= 2048, no shared expert), else the
  * grouped kernels; 1 = the CUDA-core kernel; 2 = the tcgen05 kernel.  Both
  * compute the layer for a
