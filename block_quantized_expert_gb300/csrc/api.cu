@@ -9,6 +9,7 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "stage_event.h"
 
 namespace {
 
@@ -489,12 +490,8 @@ moe_status moe_forward(moe_layer* L, const uint16_t* x, int T, const int32_t* id
     cudaStream_t s = (cudaStream_t)stream;
     const bool ev = L->stage_ev_set != 0;
     L->stage_ev_set = 0;
-    // external records: inside a stream capture they become timestamped
-    // event nodes of the graph (not capture-internal dependencies)
     std::function<cudaError_t(int, cudaError_t)> mark = [&](int i, cudaError_t e) {
-        return (ev && e == cudaSuccess)
-                   ? cudaEventRecordWithFlags(L->stage_ev[i], s, cudaEventRecordExternal)
-                   : e;
+        return (ev && e == cudaSuccess) ? moe::record_stage(L->stage_ev[i], s) : e;
     };
     cudaError_t e = forward_kernels(L, nullptr, x, T, const_cast<int32_t*>(ids), const_cast<float*>(w),
                                     out, s, ev ? mark : std::function<cudaError_t(int, cudaError_t)>());
@@ -513,9 +510,7 @@ moe_status moe_route_forward(moe_layer* L, const float* logits, const uint16_t* 
     L->stage_ev_set = 0;
     cudaStream_t s = (cudaStream_t)stream;
     std::function<cudaError_t(int, cudaError_t)> mark = [&](int i, cudaError_t e) {
-        return (ev && e == cudaSuccess)
-                   ? cudaEventRecordWithFlags(L->stage_ev[i], s, cudaEventRecordExternal)
-                   : e;
+        return (ev && e == cudaSuccess) ? moe::record_stage(L->stage_ev[i], s) : e;
     };
     cudaError_t e = forward_kernels(L, logits, x, T, ids, w, out, s,
                                     ev ? mark : std::function<cudaError_t(int, cudaError_t)>());

@@ -16,6 +16,7 @@
 // requantisation of h (guide, section 4); down writes fp32 rows.
 #include "common.cuh"
 #include "layer.h"
+#include "stage_event.h"
 
 namespace moe {
 
@@ -225,7 +226,7 @@ cudaError_t launch_gemm_cc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid)
     a.hq = L->hq; a.hs = L->hs;
     const bool nv = c.weight_format == MOE_WEIGHTS_NVFP4;
     cudaError_t err = nv ? cc_launch<2, true>(L, a, s) : cc_launch<0, true>(L, a, s);
-    if (err == cudaSuccess && mid) err = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
+    if (err == cudaSuccess && mid) err = record_stage(mid, s);
     if (err != cudaSuccess) return err;
     CCArgs d = a;
     d.w1_q = L->down_q; d.w1_s = L->down_s; d.w2_q = nullptr; d.w2_s = nullptr;

@@ -36,6 +36,7 @@
 
 #include "common.cuh"
 #include "layer.h"
+#include "stage_event.h"
 #include "route.cuh"
 #include "tc_ptx.cuh"
 
@@ -1452,7 +1453,7 @@ cudaError_t launch_gemm_tc(moe_layer* L, int T, cudaStream_t s, cudaEvent_t mid,
     g.sk_cnt = L->sk_counters;
     g.trace = L->trace;
     cudaError_t e = tc_launch<true, kFmtE2M1>(L, st->gu, st->xq, g, s);
-    if (e == cudaSuccess && mid) e = cudaEventRecordWithFlags(mid, s, cudaEventRecordExternal);
+    if (e == cudaSuccess && mid) e = record_stage(mid, s);
     if (e != cudaSuccess) return e;
     TcArgs d = g;
     d.K = c.inter;
